@@ -1,0 +1,248 @@
+"""Seeded synthetic inputs for the quantized lightning indexer.
+
+This module only draws random inputs and lays them out in the documented
+shapes; it holds none of the indexer's arithmetic, so both the CPU oracle and
+the CUDA path can be fed from it.
+
+Shapes and value distributions follow the Ascend ``VllmQuantLightningIndexer``
+README (single-operator call example and parameter table):
+
+* query   BSND ``[B, S1, 64, 128]`` or TND ``[T, 64, 128]``, int8 or fp8-e4m3
+* key     PA_BSND pool ``[num_blocks, block_size, 1, 128]``
+* k_scale ``[num_blocks, block_size, 1]``; q_scale / weights ``[..., 64]``
+* block_table ``[B, max_blocks_per_seq]`` int32
+
+int8 values are drawn the way the README's example does: a float64 uniform on
+[-128, 127) converted to int8 by truncation toward zero.  fp8 values are a
+float normal times 4 cast to ``float8_e4m3fn`` (round to nearest even);
+codes that decode to NaN are never produced at these magnitudes.
+
+The key pool is sized for the number of compressed keys each batch holds,
+``ceil(S_k / cmp_ratio)``: the fifth workload spells that length out.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional
+
+import numpy as np
+
+NUM_HEADS_Q = 64
+NUM_HEADS_K = 1
+HEAD_DIM = 128
+
+INT8 = "int8"
+FP8 = "fp8_e4m3"
+F16 = "f16"
+F32 = "f32"
+
+
+@dataclasses.dataclass
+class Case:
+    """One indexer invocation: every input array (numpy, host) and the attributes."""
+
+    name: str
+    layout_q: str                 # "BSND" or "TND"
+    qk_dtype: str                 # INT8 or FP8 (FP8 arrays hold the raw e4m3 codes as uint8)
+    scale_dtype: str              # F16 or F32 (weights, q_scale and k_scale share it)
+    batch: int
+    s1: int                       # BSND query rows per batch (0 for TND)
+    total_q: int                  # TND rows T (0 for BSND)
+    block_size: int
+    num_blocks: int
+    max_blocks_per_seq: int
+    sparse_count: int
+    sparse_mode: int
+    cmp_ratio: int
+    query: np.ndarray             # int8 / uint8 codes
+    key: np.ndarray               # int8 / uint8 codes
+    weights: np.ndarray
+    q_scale: np.ndarray
+    k_scale: np.ndarray
+    seq_lens_q: Optional[np.ndarray]  # int32 [B] (TND: prefix sums) or None
+    seq_lens_k: np.ndarray        # int32 [B], original (uncompressed) key tokens
+    block_table: np.ndarray       # int32 [B, max_blocks_per_seq]
+
+    @property
+    def rows(self) -> int:
+        return self.batch * self.s1 if self.layout_q == "BSND" else self.total_q
+
+    @property
+    def max_seqlen_k(self) -> int:
+        return int(self.seq_lens_k.max()) if self.batch else 0
+
+    @property
+    def max_seqlen_q(self) -> int:
+        if self.layout_q == "BSND":
+            return int(self.seq_lens_q.max()) if self.seq_lens_q is not None and self.batch else self.s1
+        if self.batch == 0:
+            return 0
+        cum = np.concatenate([[0], self.seq_lens_q.astype(np.int64)])
+        return int(np.diff(cum).max())
+
+
+def _int8_like_readme(draw: np.ndarray) -> np.ndarray:
+    # float -> int8 by truncation toward zero, as torch's .to(torch.int8) does
+    return np.trunc(draw).astype(np.int8)
+
+
+def _fp8_codes(x: np.ndarray) -> np.ndarray:
+    import torch  # the float8 cast is a library routine; only used here for input drawing
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    codes = t.view(torch.uint8).numpy().copy()
+    assert not np.any((codes & 0x7F) == 0x7F), "NaN code drawn"
+    return codes
+
+
+def _scale_cast(x: np.ndarray, scale_dtype: str) -> np.ndarray:
+    return x.astype(np.float16) if scale_dtype == F16 else x.astype(np.float32)
+
+
+def _pages_for(seq_lens_k, cmp_ratio, block_size) -> List[int]:
+    out = []
+    for s in seq_lens_k:
+        compressed = -(-int(s) // cmp_ratio)
+        out.append(-(-compressed // block_size))
+    return out
+
+
+def paged_layout(seq_lens_k, cmp_ratio, block_size, rng, permute=True, extra_pages=0, width=None):
+    """Allocate pages for each batch and build the block_table.
+
+    Returns (num_blocks, block_table).  Pages are handed out as one seeded
+    random permutation of the whole pool (or in order when ``permute`` is
+    false); unused table slots hold -1.
+    """
+    pages = _pages_for(seq_lens_k, cmp_ratio, block_size)
+    total = sum(pages) + extra_pages
+    w = max(pages) if pages else 0
+    if width is not None:
+        w = max(w, width)
+    w = max(w, 1)
+    perm = rng.permutation(total).astype(np.int32) if permute else np.arange(total, dtype=np.int32)
+    table = np.full((len(pages), w), -1, dtype=np.int32)
+    pos = 0
+    for b, p in enumerate(pages):
+        table[b, :p] = perm[pos:pos + p]
+        pos += p
+    return max(total, 1), table
+
+
+def make_case(name, *, layout_q="BSND", qk_dtype=INT8, scale_dtype=F16, batch=1, s1=1,
+              q_lens=None, seq_lens_k=(256,), block_size=128, sparse_count=64, sparse_mode=0,
+              cmp_ratio=1, seed=0, permute=True, pass_seq_lens_q=False, extra_pages=0,
+              table_width=None) -> Case:
+    """General seeded case.
+
+    BSND: ``batch`` x ``s1`` query rows; ``q_lens`` (optional) gives
+    actual_seq_lengths_query per batch.  TND: ``q_lens`` is the per-sequence
+    query length list; the passed tensor holds its prefix sums.
+    """
+    rng = np.random.default_rng(seed)
+    seq_lens_k = np.asarray(seq_lens_k, dtype=np.int32)
+    B = len(seq_lens_k) if layout_q == "TND" else batch
+    assert len(seq_lens_k) == B
+    num_blocks, table = paged_layout(seq_lens_k, cmp_ratio, block_size, rng, permute,
+                                     extra_pages, table_width)
+    if layout_q == "BSND":
+        rows_shape = (B, s1, NUM_HEADS_Q)
+        if q_lens is not None:
+            seq_lens_q = np.asarray(q_lens, dtype=np.int32)
+        elif pass_seq_lens_q:
+            seq_lens_q = np.full(B, s1, dtype=np.int32)
+        else:
+            seq_lens_q = None
+        total_q = 0
+    else:
+        q_lens = np.asarray(q_lens, dtype=np.int64)
+        seq_lens_q = np.cumsum(q_lens).astype(np.int32)
+        total_q = int(seq_lens_q[-1]) if B else 0
+        rows_shape = (total_q, NUM_HEADS_Q)
+        s1 = 0
+    q_shape = rows_shape + (HEAD_DIM,)
+    k_shape = (num_blocks, block_size, NUM_HEADS_K, HEAD_DIM)
+    if qk_dtype == INT8:
+        key = _int8_like_readme(rng.uniform(-128, 127, k_shape))
+        query = _int8_like_readme(rng.uniform(-128, 127, q_shape))
+    else:
+        key = _fp8_codes(rng.standard_normal(k_shape) * 4.0)
+        query = _fp8_codes(rng.standard_normal(q_shape) * 4.0)
+    k_scale = _scale_cast(rng.uniform(0, 10, (num_blocks, block_size, NUM_HEADS_K)), scale_dtype)
+    q_scale = _scale_cast(rng.uniform(0, 10, rows_shape), scale_dtype)
+    weights = _scale_cast(rng.uniform(0, 0.01, rows_shape), scale_dtype)
+    return Case(name=name, layout_q=layout_q, qk_dtype=qk_dtype, scale_dtype=scale_dtype,
+                batch=B, s1=s1, total_q=total_q, block_size=block_size, num_blocks=num_blocks,
+                max_blocks_per_seq=table.shape[1], sparse_count=sparse_count,
+                sparse_mode=sparse_mode, cmp_ratio=cmp_ratio, query=query, key=key,
+                weights=weights, q_scale=q_scale, k_scale=k_scale, seq_lens_q=seq_lens_q,
+                seq_lens_k=seq_lens_k, block_table=table)
+
+
+# ----------------------------------------------------------------------------------------------
+# The five named workloads
+# ----------------------------------------------------------------------------------------------
+
+def tiny_decode() -> Case:
+    """B=1, one query token, S_k=256 in two 128-key pages, table [[0,1]], k=64, mode 0."""
+    return make_case("tiny_decode", batch=1, s1=1, seq_lens_k=[256], block_size=128,
+                     sparse_count=64, sparse_mode=0, cmp_ratio=1, seed=0, permute=False)
+
+
+def page_decode() -> Case:
+    """The README's single-operator example, drawn in its order from ``np.random.seed(0)``.
+
+    B=24, S1=4, S_k=512 in 4 pages of 128 per batch, identity block_table,
+    k=512, sparse_mode 0, cmp_ratio 1.
+    """
+    b, s1, s2, bs, n1, n2, d = 24, 4, 512, 128, NUM_HEADS_Q, NUM_HEADS_K, HEAD_DIM
+    np.random.seed(0)
+    mb = (s2 + bs - 1) // bs
+    table = np.arange(b * mb, dtype=np.int32).reshape(b, -1)
+    key = _int8_like_readme(np.random.uniform(-128, 127, (b * mb, bs, n2, d)))
+    k_scale = np.random.uniform(0, 10, (b * mb, bs, n2)).astype(np.float16)
+    query = _int8_like_readme(np.random.uniform(-128, 127, (b, s1, n1, d)))
+    q_scale = np.random.uniform(0, 10, (b, s1, n1)).astype(np.float16)
+    weights = np.random.uniform(0, 0.01, (b, s1, n1)).astype(np.float16)
+    seq_lens_q = np.random.uniform(s1, s1, (b,)).astype(np.int32)
+    seq_lens_k = np.random.uniform(s2, s2, (b,)).astype(np.int32)
+    return Case(name="page_decode", layout_q="BSND", qk_dtype=INT8, scale_dtype=F16, batch=b,
+                s1=s1, total_q=0, block_size=bs, num_blocks=b * mb, max_blocks_per_seq=mb,
+                sparse_count=512, sparse_mode=0, cmp_ratio=1, query=query, key=key,
+                weights=weights, q_scale=q_scale, k_scale=k_scale, seq_lens_q=seq_lens_q,
+                seq_lens_k=seq_lens_k, block_table=table)
+
+
+def long_decode(seed: int = 3, batch: int = 32) -> Case:
+    """B=32, one query token each, S_k ~ U{8192..32768}, 64-key pages, k=2048, causal."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(8192, 32768, size=batch, endpoint=True).astype(np.int32)
+    return make_case("long_decode", batch=batch, s1=1, seq_lens_k=lens, block_size=64,
+                     sparse_count=2048, sparse_mode=3, cmp_ratio=1, seed=seed + 100,
+                     permute=True, pass_seq_lens_q=True)
+
+
+def fp8_compressed_decode(seed: int = 4, batch: int = 16) -> Case:
+    """B=16, S1=2, fp8 q/k, S_k ~ U{16384..65536} compressed 4x, 128-key pages, fp32 scales."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(16384, 65536, size=batch, endpoint=True).astype(np.int32)
+    return make_case("fp8_compressed_decode", batch=batch, s1=2, qk_dtype=FP8, scale_dtype=F32,
+                     seq_lens_k=lens, block_size=128, sparse_count=2048, sparse_mode=3,
+                     cmp_ratio=4, seed=seed + 100, permute=True, pass_seq_lens_q=True)
+
+
+def varlen_prefill(seed: int = 5, lens=(1024, 2048, 4096, 8192)) -> Case:
+    """TND prefill: sequences of the given lengths, key length = query length, causal."""
+    return make_case("varlen_prefill", layout_q="TND", q_lens=list(lens), seq_lens_k=list(lens),
+                     block_size=128, sparse_count=2048, sparse_mode=3, cmp_ratio=1, seed=seed,
+                     permute=True)
+
+
+WORKLOADS = {
+    "tiny_decode": tiny_decode,
+    "page_decode": page_decode,
+    "long_decode": long_decode,
+    "fp8_compressed_decode": fp8_compressed_decode,
+    "varlen_prefill": varlen_prefill,
+}
