@@ -1,0 +1,162 @@
+/*
+ * qli.h -- C ABI of the GB300 (sm_103a) quantized lightning indexer.
+ *
+ * The operation (Ascend "VllmQuantLightningIndexer" README, function section, the formula
+ * out = Top-k{ 1_{1 x g} @ [ (W @ 1_{1 x Sk}) (.) ReLU( (Scale_Q @ Scale_K^T) (.) (Q @ K^T) ) ] }):
+ * for every query token with g = 64 quantized heads of dim 128 and one shared quantized key head,
+ *
+ *     score[j] = sum_h W[h] * ReLU( ScaleQ[h] * ScaleK[j] * (Q_h . K_j) )
+ *
+ * over the token's visible compressed keys j, and the int32 indices of the sparse_count largest
+ * scores (score descending, ties by index ascending), padded with -1.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller; the library never allocates,
+ *     frees or retains them past the call.  Host structs are read during the call only.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Calls only
+ *     enqueue work; none synchronises except qli_get_device_error.  No call reads device data on
+ *     the host, so the enqueueing calls can be captured into a CUDA graph.
+ *   - Arguments that are wrong on their face (shape, dtype, attribute, size, alignment, null) are
+ *     rejected synchronously with a status and nothing is enqueued.
+ *   - Faults only the device data can reveal (a length beyond the declared maxima or the
+ *     block_table's capacity, non-monotone TND prefix sums, a block_table entry outside the pool)
+ *     never trap: every output row of the affected batch (all rows, for bad TND prefix sums) is
+ *     written as -1 and a bit is set in the workspace's sticky device error word, which
+ *     qli_get_device_error reports.
+ *
+ * Layouts (README parameter table and layout constraints):
+ *   query        BSND [B, S1, 64, 128] or TND [T, 64, 128]; int8 or float8_e4m3fn codes
+ *   key          PA_BSND pool [num_blocks, block_size, 1, 128], same dtype as query, contiguous
+ *   weights      [B, S1, 64] / [T, 64]     float16 or float32 (one dtype shared by the three
+ *   q_scale      [B, S1, 64] / [T, 64]       float inputs), contiguous
+ *   k_scale      [num_blocks, block_size, 1]
+ *   seq_lens_q   int32 [B]: BSND query tokens per batch (optional, default S1);
+ *                TND prefix sums (required)
+ *   seq_lens_k   int32 [B]: original key tokens per batch (required); the batch holds
+ *                ceil(seq_lens_k / cmp_ratio) compressed keys, key j at
+ *                key[block_table[b][j / block_size]][j % block_size]
+ *   block_table  int32 [B, max_blocks_per_seq]
+ *   sparse_indices int32 [B, S1, 1, sparse_count] / [T, 1, sparse_count]: compressed-key indices
+ *                within the row's batch
+ */
+#ifndef QLI_H
+#define QLI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QLI_OK = 0,
+    QLI_ERR_INVALID_ARG = 1,          /* argument wrong on its face; nothing enqueued */
+    QLI_ERR_UNSUPPORTED = 2,          /* valid per the README but not implemented (return_value) */
+    QLI_ERR_WORKSPACE_TOO_SMALL = 3,  /* metadata or workspace buffer below the required size */
+    QLI_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
+    QLI_ERR_DEVICE_BAD_INPUT = 5,     /* (qli_get_device_error) device data was invalid */
+    QLI_ERR_DEVICE_TIMEOUT = 6,       /* (qli_get_device_error) a bounded device wait gave up */
+    QLI_ERR_NO_DEVICE = 7             /* no sm_100-family GPU with tensor memory is current */
+} qli_status;
+
+typedef enum { QLI_INT8 = 0, QLI_FP8_E4M3 = 1 } qli_qk_dtype;    /* README: INT8, FLOAT8_e4m3fn */
+typedef enum { QLI_F16 = 0, QLI_F32 = 1 } qli_scale_dtype;       /* README: FLOAT16, FLOAT32 */
+typedef enum { QLI_BSND = 0, QLI_TND = 1 } qli_q_layout;         /* README layout_query */
+
+/*
+ * Every attribute of one call (README parameter table).  Fields are plain ints so the struct has
+ * the same layout for every caller.
+ */
+typedef struct {
+    int32_t batch;              /* B; for TND the number of entries of seq_lens_q */
+    int32_t max_q_tokens;       /* BSND: S1 (rows per batch in query/output); ignored for TND */
+    int32_t total_q_tokens;     /* TND: T (rows of query/output); ignored for BSND */
+    int32_t num_heads_q;        /* must be 64 (README constraint on query's N axis) */
+    int32_t num_heads_k;        /* must be 1 (README constraint on key's N axis) */
+    int32_t head_dim;           /* must be 128 (README constraint on the D axis) */
+    int32_t qk_dtype;           /* qli_qk_dtype of query and key */
+    int32_t scale_dtype;        /* qli_scale_dtype of weights, q_scale and k_scale */
+    int32_t layout_q;           /* qli_q_layout; the key layout is always PA_BSND */
+    int32_t num_blocks;         /* pages in the key pool */
+    int32_t block_size;         /* keys per page: a multiple of 16, at most 1024 */
+    int32_t max_blocks_per_seq; /* block_table row length: >= ceil(ceil(max_seqlen_k/cmp)/bs) */
+    int32_t sparse_count;       /* k, in [1, 2048] */
+    int32_t sparse_mode;        /* 0 = defaultMask, 3 = rightDownCausal */
+    int32_t cmp_ratio;          /* key compression multiple: 1, 2, 4, ..., 128 */
+    int32_t query_quant_mode;   /* must be 0 (per-token-head) */
+    int32_t key_quant_mode;     /* must be 0 (per-token-head) */
+    int32_t return_value;       /* must be 0: sparse_values output not supported */
+    int64_t pre_tokens;         /* reserved by the README: must be INT64_MAX */
+    int64_t next_tokens;        /* reserved by the README: must be INT64_MAX */
+    int32_t max_seqlen_q;       /* host-known bound on per-batch query tokens (>= every one) */
+    int32_t max_seqlen_k;       /* host-known bound on seq_lens_k (>= every entry) */
+} qli_problem;
+
+/* Fill `p` with the README's defaults (BSND, int8, fp16, mode 0, cmp 1, k 2048, reserved fields
+ * at their only accepted values).  The caller then sets the sizes. */
+void qli_problem_init(qli_problem* p);
+
+/* Check `p` on the host without touching the device.  QLI_OK or QLI_ERR_INVALID_ARG /
+ * QLI_ERR_UNSUPPORTED; `why` (optional, may be NULL) receives a static message. */
+qli_status qli_validate(const qli_problem* p, const char** why);
+
+/* Number of int32 words the metadata buffer needs for `p` (at least 1024, the README's size).
+ * 0 if `p` is invalid. */
+size_t qli_metadata_words(const qli_problem* p);
+
+/* Bytes of device scratch qli_score_topk needs for `p` (256-byte aligned start required).
+ * 0 if `p` is invalid. */
+size_t qli_workspace_size(const qli_problem* p);
+
+/*
+ * Work-split scheduler (README: metadata parameter of the indexer and its companion
+ * VllmQuantLightningIndexerMetadata call: cores used, block size and each core's start points).
+ * Reads the device lengths and writes, into `metadata` (int32[metadata_words], device, caller-
+ * owned), the per-batch row/key extents and a balanced split of every live query group's key
+ * tiles over the GPU's SMs.  One kernel, enqueued on `stream`.  The result depends only on the
+ * lengths and `p`, so one metadata buffer serves every call that shares them (e.g. all layers of a
+ * step).  seq_lens_q may be NULL for BSND.
+ */
+qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                        int32_t* metadata, size_t metadata_words, void* stream);
+
+/*
+ * The indexer (README: the indexer call and its formula).  Scores every visible (query token,
+ * compressed key) pair on the tensor cores and writes the top-sparse_count indices per row into
+ * sparse_indices.  `metadata` must come from qli_metadata with the same `p` and lengths.
+ * `workspace` is caller-owned device scratch of at least qli_workspace_size(p) bytes, 256-byte
+ * aligned, zeroed once after allocation (qli_workspace_init); calls sharing a workspace must be
+ * ordered on one stream.  sparse_values must be NULL (README: return_value unsupported).
+ * query, key and k_scale must be 16-byte aligned.
+ */
+qli_status qli_score_topk(const qli_problem* p, const void* query, const void* key,
+                          const void* weights, const void* q_scale, const void* k_scale,
+                          const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                          const int32_t* block_table, const int32_t* metadata,
+                          size_t metadata_words, void* workspace, size_t workspace_bytes,
+                          int32_t* sparse_indices, float* sparse_values, void* stream);
+
+/* Zero the workspace's device error word (enqueued on `stream`).  Call once after allocating a
+ * workspace, before its first qli_score_topk. */
+qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, read and clear the workspace's sticky device error word.  QLI_OK,
+ * QLI_ERR_DEVICE_BAD_INPUT (a length or block_table entry was invalid; the affected rows are -1),
+ * QLI_ERR_DEVICE_TIMEOUT (a bounded wait inside a kernel gave up), or QLI_ERR_CUDA.
+ * `bits` (optional) receives the raw word: 1 length, 2 page, 4 timeout, 8 metadata mismatch.
+ */
+qli_status qli_get_device_error(void* workspace, void* stream, uint32_t* bits);
+
+/* Static, human-readable name of a status. */
+const char* qli_status_string(qli_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int qli_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLI_H */

@@ -60,7 +60,7 @@ def lib():
             vp = ctypes.c_void_p
             L.qlio_score_topk.restype = ctypes.c_int
             L.qlio_score_topk.argtypes = [ctypes.POINTER(Problem), vp, vp, vp, vp, vp, vp, vp, vp,
-                                          vp, vp, ctypes.c_int64, ctypes.c_int]
+                                          vp, vp, ctypes.c_int64, vp, ctypes.c_int]
             _lib = L
     return _lib
 
@@ -101,26 +101,31 @@ def max_compressed_len(case) -> int:
 
 
 def score_topk(case, with_scores: bool = False, nthreads: int | None = None,
-               complete_blocks_only: bool = False):
+               complete_blocks_only: bool = False, rows=None):
     """Run the oracle.  Returns ``(indices[rows, k] int32, scores or None, error_mask)``.
 
     ``scores`` (when requested) is float32 ``[rows, max Lc]`` holding each visible key's fp32 score
-    and NaN elsewhere.
+    and NaN elsewhere.  ``rows`` (optional iterable of row numbers) limits the work to those rows;
+    every other output row is -1.
     """
     L = lib()
     p = problem_of(case, complete_blocks_only)
-    rows = int(L.qlio_rows(ctypes.byref(p)))
+    rows_total = int(L.qlio_rows(ctypes.byref(p)))
     k = case.sparse_count
-    out = np.empty((max(rows, 0), k), dtype=np.int32)
+    out = np.empty((max(rows_total, 0), k), dtype=np.int32)
     ld = max(1, max_compressed_len(case))
-    scores = np.full((max(rows, 0), ld), np.nan, dtype=np.float32) if with_scores else None
+    scores = np.full((max(rows_total, 0), ld), np.nan, dtype=np.float32) if with_scores else None
     arrs = [np.ascontiguousarray(a) for a in (case.query, case.key, case.weights, case.q_scale,
                                                case.k_scale)]
     slq = None if case.seq_lens_q is None else np.ascontiguousarray(case.seq_lens_q, np.int32)
     slk = np.ascontiguousarray(case.seq_lens_k, np.int32)
     bt = np.ascontiguousarray(case.block_table, np.int32)
+    mask = None
+    if rows is not None:
+        mask = np.zeros(max(rows_total, 1), dtype=np.uint8)
+        mask[np.asarray(list(rows), dtype=np.int64)] = 1
     if nthreads is None:
         nthreads = os.cpu_count() or 1
     err = L.qlio_score_topk(ctypes.byref(p), *[_ptr(a) for a in arrs], _ptr(slq), _ptr(slk),
-                            _ptr(bt), _ptr(out), _ptr(scores), ld, int(nthreads))
+                            _ptr(bt), _ptr(out), _ptr(scores), ld, _ptr(mask), int(nthreads))
     return out, scores, int(err)

@@ -29,7 +29,8 @@
  *     are padded with -1; BSND rows r >= actual_seq_lengths_query[b] are all -1.
  *   - Indices are the logical compressed-key positions 0..Lc-1 of the row's own batch.
  *   - Invalid inputs that only the data can reveal (a length out of range, a block_table entry
- *     outside the pool) make every row of that batch -1 and set a bit in the returned error mask.
+ *     outside the pool) make every row of that batch -1 and set a bit in the returned error mask;
+ *     invalid TND prefix sums make every row of the call -1.
  */
 #include <math.h>
 #include <pthread.h>
@@ -209,6 +210,7 @@ typedef struct {
     int32_t* out;
     float* scores;       /* optional [rows, ld] */
     int64_t ld;
+    const uint8_t* row_mask; /* optional: only rows with a non-zero entry are computed */
     int64_t rows;
     int64_t* row_batch;  /* batch of each global row, -1 if none */
     int32_t* batch_ok;   /* per batch: lengths and pages valid */
@@ -249,6 +251,8 @@ static void run_row(job* J, int64_t row, scored_key* buf)
         out[i] = -1;
     int64_t b = J->row_batch[row];
     if (b < 0 || !J->batch_ok[b])
+        return;
+    if (J->row_mask && !J->row_mask[row])
         return;
     int64_t first_row, rows_alloc;
     int32_t sq;
@@ -313,13 +317,14 @@ int64_t qlio_rows(const qlio_problem* p)
 /*
  * The whole operator.  Inputs are host arrays in the README's layouts (see the module header);
  * `out` is int32 [rows, sparse_count].  `scores` (optional, may be NULL) receives the fp32 score of
- * every visible key at [row * ld + j]; other entries are left untouched.  Returns the error mask
- * (0 when every batch was valid).  `nthreads` worker threads split the rows.
+ * every visible key at [row * ld + j]; other entries are left untouched.  `row_mask` (optional)
+ * restricts the work to the rows whose entry is non-zero; the others are written as -1.  Returns
+ * the error mask (0 when every batch was valid).  `nthreads` worker threads split the rows.
  */
 int qlio_score_topk(const qlio_problem* p, const void* query, const void* key, const void* weights,
                     const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
                     const int32_t* seq_lens_k, const int32_t* block_table, int32_t* out,
-                    float* scores, int64_t ld, int nthreads)
+                    float* scores, int64_t ld, const uint8_t* row_mask, int nthreads)
 {
     job J;
     pthread_once(&e4m3_once, fill_e4m3_table);
@@ -336,6 +341,7 @@ int qlio_score_topk(const qlio_problem* p, const void* query, const void* key, c
     J.out = out;
     J.scores = scores;
     J.ld = ld;
+    J.row_mask = row_mask;
     J.rows = qlio_rows(p);
     J.next_row = 0;
     int err = 0;
@@ -344,10 +350,21 @@ int qlio_score_topk(const qlio_problem* p, const void* query, const void* key, c
     J.batch_sq = (int32_t*)malloc(sizeof(int32_t) * (size_t)(p->batch > 0 ? p->batch : 1));
     for (int64_t i = 0; i < J.rows; ++i)
         J.row_batch[i] = -1;
+    /* TND prefix sums that are negative, decreasing or beyond T leave no consistent row ranges:
+     * then every batch counts as invalid */
+    int tnd_bad = 0;
+    if (p->layout_tnd) {
+        for (int b = 0; b < p->batch; ++b) {
+            int64_t fr, ra;
+            int32_t sq;
+            if (!batch_rows(p, seq_lens_q, b, &fr, &ra, &sq))
+                tnd_bad = 1;
+        }
+    }
     for (int b = 0; b < p->batch; ++b) {
         int64_t first_row, rows_alloc;
         int32_t sq;
-        int ok = batch_rows(p, seq_lens_q, b, &first_row, &rows_alloc, &sq);
+        int ok = batch_rows(p, seq_lens_q, b, &first_row, &rows_alloc, &sq) && !tnd_bad;
         int32_t sk = seq_lens_k[b];
         if (sk < 0)
             ok = 0;

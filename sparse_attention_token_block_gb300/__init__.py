@@ -1,0 +1,234 @@
+"""Thin Python binding of ``libqli.so``, the GB300 quantized lightning indexer.
+
+Every function here only marshals arguments to the C ABI declared in ``include/qli.h`` (same
+names without the ``qli_`` prefix); all computation runs in the library's CUDA kernels.  Tensors
+are torch CUDA tensors; the current torch stream is passed to the library.  The shared library is
+loaded on first use; if it has not been built, that first use raises ImportError: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqli.so")
+
+QLI_OK = 0
+STATUS_NAMES = {0: "QLI_OK", 1: "QLI_ERR_INVALID_ARG", 2: "QLI_ERR_UNSUPPORTED",
+                3: "QLI_ERR_WORKSPACE_TOO_SMALL", 4: "QLI_ERR_CUDA", 5: "QLI_ERR_DEVICE_BAD_INPUT",
+                6: "QLI_ERR_DEVICE_TIMEOUT", 7: "QLI_ERR_NO_DEVICE"}
+INT8, FP8_E4M3 = 0, 1
+F16, F32 = 0, 1
+BSND, TND = 0, 1
+INT64_MAX = (1 << 63) - 1
+
+# symbols include/qli.h declares
+EXPORTS = ("qli_problem_init", "qli_validate", "qli_metadata_words", "qli_workspace_size",
+           "qli_metadata", "qli_score_topk", "qli_workspace_init", "qli_get_device_error",
+           "qli_status_string", "qli_version")
+
+
+class QliError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__("%s: %s (%d)" % (what, STATUS_NAMES.get(status, "?"), status))
+
+
+class Problem(ctypes.Structure):
+    """Mirror of ``qli_problem``."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "max_q_tokens", "total_q_tokens", "num_heads_q", "num_heads_k", "head_dim",
+        "qk_dtype", "scale_dtype", "layout_q", "num_blocks", "block_size", "max_blocks_per_seq",
+        "sparse_count", "sparse_mode", "cmp_ratio", "query_quant_mode", "key_quant_mode",
+        "return_value")] + [("pre_tokens", ctypes.c_int64), ("next_tokens", ctypes.c_int64),
+                            ("max_seqlen_q", ctypes.c_int32), ("max_seqlen_k", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libqli.so is not built (run __graft_entry__.build() or "
+                          "python sparse_attention_token_block_gb300/build.py)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
+    P = ctypes.POINTER(Problem)
+    L.qli_problem_init.argtypes = [P]
+    L.qli_problem_init.restype = None
+    L.qli_validate.argtypes = [P, ctypes.POINTER(ctypes.c_char_p)]
+    L.qli_validate.restype = ctypes.c_int
+    L.qli_metadata_words.argtypes = [P]
+    L.qli_metadata_words.restype = sz
+    L.qli_workspace_size.argtypes = [P]
+    L.qli_workspace_size.restype = sz
+    L.qli_metadata.argtypes = [P, i32p, i32p, i32p, sz, vp]
+    L.qli_metadata.restype = ctypes.c_int
+    L.qli_score_topk.argtypes = [P, vp, vp, vp, vp, vp, i32p, i32p, i32p, i32p, sz, vp, sz, i32p,
+                                 vp, vp]
+    L.qli_score_topk.restype = ctypes.c_int
+    L.qli_workspace_init.argtypes = [vp, sz, vp]
+    L.qli_workspace_init.restype = ctypes.c_int
+    L.qli_get_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.qli_get_device_error.restype = ctypes.c_int
+    L.qli_status_string.argtypes = [ctypes.c_int]
+    L.qli_status_string.restype = ctypes.c_char_p
+    L.qli_version.argtypes = []
+    L.qli_version.restype = ctypes.c_int
+    return L
+
+
+_lib_handle = None
+
+
+def _get_lib():
+    global _lib_handle
+    if _lib_handle is None:
+        _lib_handle = _load()
+    return _lib_handle
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _get_lib()
+    raise AttributeError(name)
+
+
+# ------------------------------------------------------------------------------------ marshalling
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def problem_init() -> Problem:
+    p = Problem()
+    _get_lib().qli_problem_init(ctypes.byref(p))
+    return p
+
+
+def validate(p: Problem):
+    why = ctypes.c_char_p()
+    st = _get_lib().qli_validate(ctypes.byref(p), ctypes.byref(why))
+    return st, why.value.decode() if why.value else ""
+
+
+def metadata_words(p: Problem) -> int:
+    return int(_get_lib().qli_metadata_words(ctypes.byref(p)))
+
+
+def workspace_size(p: Problem) -> int:
+    return int(_get_lib().qli_workspace_size(ctypes.byref(p)))
+
+
+def metadata(p: Problem, seq_lens_q, seq_lens_k, meta, stream=None) -> int:
+    return _get_lib().qli_metadata(ctypes.byref(p), _ptr(seq_lens_q), _ptr(seq_lens_k), _ptr(meta),
+                            meta.numel() if meta is not None else 0, _stream(stream))
+
+
+def score_topk(p: Problem, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k,
+               block_table, meta, workspace, sparse_indices, sparse_values=None, stream=None) -> int:
+    return _get_lib().qli_score_topk(ctypes.byref(p), _ptr(query), _ptr(key), _ptr(weights),
+                              _ptr(q_scale), _ptr(k_scale), _ptr(seq_lens_q), _ptr(seq_lens_k),
+                              _ptr(block_table), _ptr(meta), meta.numel(), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(sparse_indices),
+                              _ptr(sparse_values), _stream(stream))
+
+
+def workspace_init(workspace, stream=None) -> int:
+    return _get_lib().qli_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+
+
+def get_device_error(workspace, stream=None):
+    bits = ctypes.c_uint32(0)
+    st = _get_lib().qli_get_device_error(_ptr(workspace), _stream(stream), ctypes.byref(bits))
+    return st, int(bits.value)
+
+
+def status_string(st: int) -> str:
+    return _get_lib().qli_status_string(st).decode()
+
+
+def version() -> int:
+    return _get_lib().qli_version()
+
+
+def check(st: int, what: str = "qli"):
+    if st != QLI_OK:
+        raise QliError(st, what)
+
+
+# ------------------------------------------------------------------------------------ convenience
+def make_problem(*, batch, layout_q=BSND, max_q_tokens=0, total_q_tokens=0, qk_dtype=INT8,
+                 scale_dtype=F16, num_blocks, block_size, max_blocks_per_seq, sparse_count,
+                 sparse_mode, cmp_ratio, max_seqlen_q, max_seqlen_k) -> Problem:
+    p = problem_init()
+    p.batch = batch
+    p.layout_q = layout_q
+    p.max_q_tokens = max_q_tokens
+    p.total_q_tokens = total_q_tokens
+    p.qk_dtype = qk_dtype
+    p.scale_dtype = scale_dtype
+    p.num_blocks = num_blocks
+    p.block_size = block_size
+    p.max_blocks_per_seq = max_blocks_per_seq
+    p.sparse_count = sparse_count
+    p.sparse_mode = sparse_mode
+    p.cmp_ratio = cmp_ratio
+    p.max_seqlen_q = max_seqlen_q
+    p.max_seqlen_k = max_seqlen_k
+    return p
+
+
+class Indexer:
+    """Owns the metadata, workspace and output buffers of one problem shape.
+
+    ``run`` enqueues qli_metadata (when ``refresh_metadata``) and qli_score_topk on the current
+    stream and returns the int32 ``sparse_indices`` tensor ([rows, sparse_count]).
+    """
+
+    def __init__(self, p: Problem, device="cuda"):
+        import torch
+        st, why = validate(p)
+        if st != QLI_OK:
+            raise QliError(st, "problem: " + why)
+        self.p = p
+        self.meta = torch.zeros(metadata_words(p), dtype=torch.int32, device=device)
+        nbytes = workspace_size(p)
+        self.workspace = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=device)
+        check(workspace_init(self.workspace), "workspace_init")
+        rows = p.batch * p.max_q_tokens if p.layout_q == BSND else p.total_q_tokens
+        self.rows = rows
+        self.out = torch.empty((rows, p.sparse_count), dtype=torch.int32, device=device)
+
+    def run(self, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
+            refresh_metadata=True, out=None):
+        if refresh_metadata:
+            check(metadata(self.p, seq_lens_q, seq_lens_k, self.meta), "metadata")
+        o = self.out if out is None else out
+        check(score_topk(self.p, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k,
+                         block_table, self.meta, self.workspace, o), "score_topk")
+        return o
+
+    def device_error(self):
+        return get_device_error(self.workspace)
+
+    def score_lines(self):
+        """The last call's per-row ordered score codes decoded to float32 ([rows, ld]); entries of
+        keys that were not visible hold stale values.  Debug/test aid."""
+        import torch
+        lc = -(-self.p.max_seqlen_k // self.p.cmp_ratio)
+        ld = max(128, -(-lc // 128) * 128)
+        codes = self.workspace.view(torch.uint8)[256:256 + self.rows * ld * 4].view(torch.int32)
+        codes = codes.view(self.rows, ld).to(torch.int64) & 0xFFFFFFFF
+        neg = codes < 0x80000000
+        bits = torch.where(neg, (~codes) & 0xFFFFFFFF, codes & 0x7FFFFFFF)
+        return bits.to(torch.int32).view(torch.float32).reshape(self.rows, ld)

@@ -1,0 +1,311 @@
+// qli_api.cu -- host side of the C ABI: argument validation (README parameter table and
+// constraints), buffer sizing, the key pool's TMA descriptor, and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstring>
+#include <mutex>
+
+#include "qli_internal.cuh"
+
+namespace qli {
+
+MetaLayout meta_layout(int64_t batch, int64_t max_groups)
+{
+    MetaLayout m;
+    m.batch_off = kMhWords;
+    m.cta_off = m.batch_off + batch * kBatchWords;
+    m.group_off = m.cta_off + kMaxCtas + 1;
+    m.unit_off = m.group_off + max_groups + 1;
+    m.max_groups = max_groups;
+    m.max_units = max_groups + kMaxCtas;
+    m.total_words = m.unit_off + m.max_units * kUnitWords;
+    if (m.total_words < 1024) m.total_words = 1024;
+    return m;
+}
+
+namespace {
+
+bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+qli_status check(const qli_problem* p, const char** why)
+{
+#define QLI_REJECT(cond, msg, st)       \
+    do {                                \
+        if (cond) {                     \
+            if (why) *why = msg;        \
+            return st;                  \
+        }                               \
+    } while (0)
+    QLI_REJECT(p == nullptr, "problem is NULL", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->num_heads_q != kHeads, "num_heads_q must be 64", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->num_heads_k != 1, "num_heads_k must be 1", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->head_dim != kDim, "head_dim must be 128", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->qk_dtype != QLI_INT8 && p->qk_dtype != QLI_FP8_E4M3, "qk_dtype must be int8 or fp8 e4m3", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->scale_dtype != QLI_F16 && p->scale_dtype != QLI_F32, "scale_dtype must be f16 or f32", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->layout_q != QLI_BSND && p->layout_q != QLI_TND, "layout_q must be BSND or TND", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->batch < 0, "batch must be >= 0", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->layout_q == QLI_BSND && p->max_q_tokens < 0, "max_q_tokens must be >= 0", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->layout_q == QLI_TND && p->total_q_tokens < 0, "total_q_tokens must be >= 0", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->block_size < 16 || p->block_size > 1024 || p->block_size % 16 != 0,
+               "block_size must be a multiple of 16 in [16, 1024]", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->num_blocks < 1, "num_blocks must be >= 1", QLI_ERR_INVALID_ARG);
+    QLI_REJECT((int64_t)p->num_blocks * p->block_size >= INT32_MAX, "key pool too large", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->sparse_count < 1 || p->sparse_count > kMaxSparse, "sparse_count must be in [1, 2048]", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->sparse_mode != 0 && p->sparse_mode != 3, "sparse_mode must be 0 or 3", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(!is_pow2(p->cmp_ratio) || p->cmp_ratio > 128, "cmp_ratio must be 1, 2, 4, ..., 128", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->query_quant_mode != 0 || p->key_quant_mode != 0, "quant modes must be 0 (per-token-head)", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->pre_tokens != INT64_MAX || p->next_tokens != INT64_MAX, "pre_tokens/next_tokens must be 2^63-1", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->max_seqlen_k < 0 || p->max_seqlen_q < 0, "max_seqlen_q/k must be >= 0", QLI_ERR_INVALID_ARG);
+    const int64_t max_lc = compressed_keys(p->max_seqlen_k, p->cmp_ratio);
+    QLI_REJECT(p->max_blocks_per_seq < 0 || (int64_t)p->max_blocks_per_seq * p->block_size < max_lc,
+               "max_blocks_per_seq too small for max_seqlen_k", QLI_ERR_INVALID_ARG);
+    const int64_t rows = p->layout_q == QLI_BSND ? (int64_t)p->batch * p->max_q_tokens : p->total_q_tokens;
+    QLI_REJECT(rows >= INT32_MAX, "too many query rows", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(rows * ceil_div64(max_lc, kTileKeys) >= INT32_MAX, "problem too large for one call", QLI_ERR_UNSUPPORTED);
+    QLI_REJECT(p->return_value != 0, "return_value (sparse_values) is not supported", QLI_ERR_UNSUPPORTED);
+#undef QLI_REJECT
+    if (why) *why = "ok";
+    return QLI_OK;
+}
+
+int64_t max_groups_of(const qli_problem* p)
+{
+    if (p->layout_q == QLI_BSND) return (int64_t)p->batch * ceil_div64(p->max_q_tokens, kGroupTokens);
+    return ceil_div64(p->total_q_tokens, kGroupTokens) + p->batch;
+}
+
+Params params_of(const qli_problem* q)
+{
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.batch = q->batch;
+    p.s1 = q->layout_q == QLI_BSND ? q->max_q_tokens : 0;
+    p.total_q = q->layout_q == QLI_TND ? q->total_q_tokens : 0;
+    p.layout_tnd = q->layout_q == QLI_TND;
+    p.qk_fp8 = q->qk_dtype == QLI_FP8_E4M3;
+    p.scale_f32 = q->scale_dtype == QLI_F32;
+    p.num_blocks = q->num_blocks;
+    p.block_size = q->block_size;
+    p.max_blocks_per_seq = q->max_blocks_per_seq;
+    p.sparse_count = q->sparse_count;
+    p.sparse_mode = q->sparse_mode;
+    p.cmp_ratio = q->cmp_ratio;
+    p.max_seqlen_q = q->max_seqlen_q;
+    p.max_seqlen_k = q->max_seqlen_k;
+    int box = 128;
+    while (q->block_size % box != 0) box >>= 1;
+    p.box_rows = box;
+    p.rows = (int32_t)(p.layout_tnd ? (int64_t)p.total_q : (int64_t)p.batch * p.s1);
+    const int64_t max_lc = compressed_keys(q->max_seqlen_k, q->cmp_ratio);
+    int64_t ld = ceil_div64(max_lc, kTileKeys) * kTileKeys;
+    p.ld = ld > 0 ? ld : kTileKeys;
+    p.meta = meta_layout(p.batch, max_groups_of(q));
+    p.hash = problem_hash(p);
+    return p;
+}
+
+WsLayout ws_layout(const Params& p)
+{
+    WsLayout w;
+    w.scores_off = kWsHeaderBytes;
+    w.ld = p.ld;
+    w.total = w.scores_off + (size_t)p.rows * (size_t)p.ld * sizeof(uint32_t);
+    return w;
+}
+
+// SM count of the current device, cached per device
+int device_sms(int* dev_out)
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev_out) *dev_out = dev;
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int sms = 0, major = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return -1;
+    if (major != 10) return 0;  // tensor memory and tcgen05: sm_100 family only
+    if (dev < 64) cache[dev] = sms;
+    return sms;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link needed)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// Key pool viewed as a 2-D byte matrix [num_blocks * block_size rows, 128 B]; the box is
+// box_rows x 128 B with the 128-byte swizzle the score kernel reads back.
+bool encode_key_map(CUtensorMap* tm, const void* key, const Params& p)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)p.num_blocks * (cuuint64_t)p.block_size};
+    cuuint64_t strides[1] = {(cuuint64_t)kDim};
+    cuuint32_t box[2] = {(cuuint32_t)kDim, (cuuint32_t)p.box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(key), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+}  // namespace
+}  // namespace qli
+
+using namespace qli;
+
+extern "C" {
+
+void qli_problem_init(qli_problem* p)
+{
+    if (!p) return;
+    std::memset(p, 0, sizeof(*p));
+    p->num_heads_q = kHeads;
+    p->num_heads_k = 1;
+    p->head_dim = kDim;
+    p->qk_dtype = QLI_INT8;
+    p->scale_dtype = QLI_F16;
+    p->layout_q = QLI_BSND;
+    p->block_size = 128;
+    p->num_blocks = 1;
+    p->sparse_count = kMaxSparse;
+    p->sparse_mode = 0;
+    p->cmp_ratio = 1;
+    p->pre_tokens = INT64_MAX;
+    p->next_tokens = INT64_MAX;
+}
+
+qli_status qli_validate(const qli_problem* p, const char** why) { return check(p, why); }
+
+size_t qli_metadata_words(const qli_problem* p)
+{
+    if (check(p, nullptr) != QLI_OK) return 0;
+    return (size_t)params_of(p).meta.total_words;
+}
+
+size_t qli_workspace_size(const qli_problem* p)
+{
+    if (check(p, nullptr) != QLI_OK) return 0;
+    return ws_layout(params_of(p)).total;
+}
+
+qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                        int32_t* metadata, size_t metadata_words, void* stream)
+{
+    qli_status s = check(p, nullptr);
+    if (s != QLI_OK) return s;
+    const Params P = params_of(p);
+    if (!metadata) return QLI_ERR_INVALID_ARG;
+    if (metadata_words < (size_t)P.meta.total_words) return QLI_ERR_WORKSPACE_TOO_SMALL;
+    if (P.batch > 0 && !seq_lens_k) return QLI_ERR_INVALID_ARG;     // PA_BSND needs key lengths
+    if (P.batch > 0 && P.layout_tnd && !seq_lens_q) return QLI_ERR_INVALID_ARG;  // TND needs prefix sums
+    int sms = device_sms(nullptr);
+    if (sms < 0) return QLI_ERR_CUDA;
+    if (sms == 0) return QLI_ERR_NO_DEVICE;
+    cudaError_t e = launch_metadata(P, seq_lens_q, seq_lens_k, metadata, sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
+qli_status qli_score_topk(const qli_problem* p, const void* query, const void* key, const void* weights,
+                          const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
+                          const int32_t* seq_lens_k, const int32_t* block_table, const int32_t* metadata,
+                          size_t metadata_words, void* workspace, size_t workspace_bytes,
+                          int32_t* sparse_indices, float* sparse_values, void* stream)
+{
+    qli_status s = check(p, nullptr);
+    if (s != QLI_OK) return s;
+    if (sparse_values) return QLI_ERR_UNSUPPORTED;
+    const Params P = params_of(p);
+    const WsLayout W = ws_layout(P);
+    if (metadata_words < (size_t)P.meta.total_words || workspace_bytes < W.total) return QLI_ERR_WORKSPACE_TOO_SMALL;
+    if (!metadata || !workspace || !aligned(workspace, 256)) return QLI_ERR_INVALID_ARG;
+    if (P.rows == 0) return QLI_OK;
+    if (!sparse_indices) return QLI_ERR_INVALID_ARG;
+    if (P.batch > 0) {
+        if (!query || !key || !weights || !q_scale || !k_scale || !seq_lens_k || !block_table) return QLI_ERR_INVALID_ARG;
+        if (P.layout_tnd && !seq_lens_q) return QLI_ERR_INVALID_ARG;
+        if (!aligned(query, 16) || !aligned(key, 16) || !aligned(k_scale, 16) || !aligned(weights, 16) ||
+            !aligned(q_scale, 16))
+            return QLI_ERR_INVALID_ARG;
+    }
+    int sms = device_sms(nullptr);
+    if (sms < 0) return QLI_ERR_CUDA;
+    if (sms == 0) return QLI_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+    uint32_t* scores = reinterpret_cast<uint32_t*>(ws + W.scores_off);
+    if (P.batch > 0) {
+        CUtensorMap tm;
+        if (!encode_key_map(&tm, key, P)) return QLI_ERR_CUDA;
+        const int grid = sms < kMaxCtas ? sms : kMaxCtas;
+        cudaError_t e = launch_score(P, &tm, query, key, weights, q_scale, k_scale, block_table, metadata, scores,
+                                     err, grid, st);
+        if (e != cudaSuccess) return QLI_ERR_CUDA;
+    }
+    cudaError_t e = launch_topk(P, block_table, metadata, scores, err, sparse_indices, st);
+    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
+qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (!workspace || workspace_bytes < kWsHeaderBytes || !aligned(workspace, 256)) return QLI_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kWsHeaderBytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
+qli_status qli_get_device_error(void* workspace, void* stream, uint32_t* bits)
+{
+    if (!workspace) return QLI_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return QLI_ERR_CUDA;
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return QLI_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof(word), st) != cudaSuccess) return QLI_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return QLI_ERR_CUDA;
+    if (bits) *bits = word;
+    if (word & kErrTimeout) return QLI_ERR_DEVICE_TIMEOUT;
+    if (word) return QLI_ERR_DEVICE_BAD_INPUT;
+    return QLI_OK;
+}
+
+const char* qli_status_string(qli_status s)
+{
+    switch (s) {
+    case QLI_OK: return "ok";
+    case QLI_ERR_INVALID_ARG: return "invalid argument";
+    case QLI_ERR_UNSUPPORTED: return "unsupported";
+    case QLI_ERR_WORKSPACE_TOO_SMALL: return "metadata or workspace buffer too small";
+    case QLI_ERR_CUDA: return "CUDA error";
+    case QLI_ERR_DEVICE_BAD_INPUT: return "device data invalid (affected rows written as -1)";
+    case QLI_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case QLI_ERR_NO_DEVICE: return "no sm_100-family device current";
+    }
+    return "unknown status";
+}
+
+int qli_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,135 @@
+// qli_internal.cuh -- layouts shared by the host code and the kernels of the CUDA library, plus
+// thin wrappers over the sm_100-family PTX the kernels use (mbarrier, TMA, tcgen05).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qli.h"
+
+namespace qli {
+
+// ------------------------------------------------------------------------------------------------
+// Fixed shape of the method (README constraints: N_q = 64, N_k = 1, D = 128)
+// ------------------------------------------------------------------------------------------------
+constexpr int kHeads = 64;
+constexpr int kDim = 128;
+constexpr int kMaxSparse = 2048;
+
+// Score kernel tiling: a tile is 128 consecutive compressed keys of one batch (one TMEM lane per
+// key); a query group is up to kGroupTokens consecutive query tokens of one batch scored together
+// (MMA N = 64 * tokens).
+constexpr int kTileKeys = 128;
+constexpr int kGroupTokens = 2;
+constexpr int kMaxCtas = 1024;            // bound on the split's CTA count (GB300 has 152 SMs)
+
+// Device error bits (sticky word at the start of the workspace)
+constexpr uint32_t kErrLength = 1u;       // a length beyond its bound / non-monotone prefix sums
+constexpr uint32_t kErrPage = 2u;         // a block_table entry outside [0, num_blocks)
+constexpr uint32_t kErrTimeout = 4u;      // a bounded wait gave up
+constexpr uint32_t kErrMetadata = 8u;     // metadata buffer not written for this problem
+
+// ------------------------------------------------------------------------------------------------
+// Metadata buffer (int32 words), written by qli_metadata, read by qli_score_topk
+// ------------------------------------------------------------------------------------------------
+constexpr int32_t kMetaMagic = 0x514C4931;  // "QLI1"
+enum MetaHeader {
+    kMhMagic = 0,
+    kMhCtas = 1,        // G: CTAs the split was made for
+    kMhUnits = 2,       // units written
+    kMhTiles = 3,       // total key tiles over all groups
+    kMhErr = 4,         // error bits found while reading the lengths
+    kMhBatch = 5,
+    kMhRows = 6,        // output rows (B * S1 or T)
+    kMhGroups = 7,      // live query groups
+    kMhLayoutHash = 8,  // hash of the problem fields the split depends on
+    kMhWords = 16
+};
+constexpr int kBatchWords = 8;
+enum BatchEntry {
+    kBeSq = 0,          // live query rows Sq_b
+    kBeSk = 1,          // original key tokens Sk_b
+    kBeLc = 2,          // compressed keys Lc_b
+    kBeFirstRow = 3,    // first output row of the batch
+    kBeOk = 4,          // 1 when the lengths are valid
+    kBeGroups = 5,      // query groups ceil(Sq_b / kGroupTokens) (0 if invalid)
+    kBeGroupBase = 6,   // index of the batch's first group
+};
+constexpr int kUnitWords = 4;   // {batch, first row within batch, key_begin, key_end}
+
+struct MetaLayout {
+    int64_t batch_off, cta_off, group_off, unit_off, total_words;
+    int64_t max_groups, max_units;
+};
+
+// ------------------------------------------------------------------------------------------------
+// Workspace (bytes): header (error word ...), then the per-row score lines
+// ------------------------------------------------------------------------------------------------
+constexpr size_t kWsHeaderBytes = 256;
+
+struct WsLayout {
+    size_t scores_off;     // uint32 ordered scores [rows, ld]
+    int64_t ld;            // row stride in elements (max Lc rounded up to a tile)
+    size_t total;
+};
+
+// ------------------------------------------------------------------------------------------------
+// Kernel parameter block (host-validated problem plus derived sizes)
+// ------------------------------------------------------------------------------------------------
+struct Params {
+    int32_t batch, s1, total_q, layout_tnd, qk_fp8, scale_f32;
+    int32_t num_blocks, block_size, max_blocks_per_seq;
+    int32_t sparse_count, sparse_mode, cmp_ratio;
+    int32_t max_seqlen_q, max_seqlen_k;
+    int32_t box_rows;      // TMA box height (largest power of two <= 128 dividing block_size)
+    int32_t rows;          // output rows
+    int32_t meta_ctas;     // G
+    int32_t hash;
+    int64_t ld;            // score line stride
+    MetaLayout meta;
+};
+
+// ---------------------------------------------------------------------------- shared helpers
+__host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Compressed keys of a batch with sk original tokens
+__host__ __device__ inline int64_t compressed_keys(int64_t sk, int cmp) { return ceil_div64(sk, cmp); }
+
+// Visible compressed keys of live row r (0 <= r < sq); mode 3 counts the compressed blocks that
+// have started at or before the row's right-aligned original position.
+__host__ __device__ inline int64_t visible_keys(int mode, int cmp, int64_t sq, int64_t sk, int64_t lc,
+                                                int64_t r)
+{
+    if (r < 0 || r >= sq) return 0;
+    if (mode == 0) return lc;
+    int64_t pos = sk - sq + r;
+    if (pos < 0) return 0;
+    int64_t n = ceil_div64(pos + 1, cmp);
+    return n < lc ? n : lc;
+}
+
+// Problem fields the metadata depends on, folded into one word to catch mismatched buffers
+__host__ __device__ inline int32_t problem_hash(const Params& p)
+{
+    uint32_t h = 2166136261u;
+    const int32_t f[] = {p.batch, p.s1, p.total_q, p.layout_tnd, p.sparse_mode, p.cmp_ratio,
+                         p.max_seqlen_q, p.max_seqlen_k, p.block_size, p.max_blocks_per_seq};
+    for (int i = 0; i < 10; ++i) { h ^= (uint32_t)f[i]; h *= 16777619u; }
+    return (int32_t)(h & 0x7fffffff);
+}
+
+MetaLayout meta_layout(int64_t batch, int64_t max_groups);
+
+// Launchers (defined in the kernel translation units)
+cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                            int32_t* meta, int num_sms, cudaStream_t st);
+cudaError_t launch_score(const Params& p, const void* tmap_key, const void* query, const void* key,
+                         const void* weights, const void* q_scale, const void* k_scale,
+                         const int32_t* block_table, const int32_t* meta, uint32_t* scores,
+                         uint32_t* err_word, int grid, cudaStream_t st);
+cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
+                        const uint32_t* scores, uint32_t* err_word, int32_t* out,
+                        cudaStream_t st);
+
+}  // namespace qli

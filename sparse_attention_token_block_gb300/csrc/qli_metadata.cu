@@ -1,0 +1,221 @@
+// qli_metadata.cu -- the work-split scheduler (README: the metadata input of the indexer and its
+// companion metadata call, "number of cores used, block size, and each core's start point").
+//
+// One CTA reads the device lengths and writes, into the caller's int32 buffer:
+//   * the header (magic, CTA count G, unit count, total tiles, error bits, problem hash);
+//   * per batch: live query rows Sq_b, key tokens Sk_b, compressed keys Lc_b, first output row,
+//     validity, query-group count and first group index;
+//   * per query group (kGroupTokens consecutive live rows of one batch): the prefix sum of its key
+//     tile counts, where a group needs ceil(n_last / 128) tiles and n_last is the visible-key count
+//     of its last row (the largest in the group under either mask);
+//   * the split: the concatenated tile sequence of all groups is cut into G equal ranges, one per
+//     CTA of the score kernel; each range becomes the list of (batch, first row, key_begin,
+//     key_end) units it overlaps, stored CTA by CTA with offsets.
+#include "qli_internal.cuh"
+
+namespace qli {
+
+namespace {
+
+constexpr int kMetaThreads = 1024;
+
+// Block-wide exclusive scan of one int64 per thread; returns the exclusive prefix and the total.
+__device__ int64_t block_exclusive_scan(int64_t v, int64_t* total, int64_t* sh /* [32] */)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        sh[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int64_t warp_excl = warp > 0 ? sh[warp - 1] : 0;
+    *total = sh[(blockDim.x >> 5) - 1];
+    __syncthreads();
+    return warp_excl + x - v;
+}
+
+// Largest i in [0, n) with a[i] <= key, for non-decreasing a (a[0] <= key assumed)
+__device__ int64_t upper_index(const int32_t* a, int64_t n, int64_t key)
+{
+    int64_t lo = 0, hi = n - 1;
+    while (lo < hi) {
+        int64_t mid = (lo + hi + 1) >> 1;
+        if (a[mid] <= key) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ int64_t batch_of_group(const int32_t* meta, const Params& p, int64_t g)
+{
+    // largest b whose first group index <= g (batch entries are kBatchWords apart)
+    int64_t lo = 0, hi = p.batch - 1;
+    const int32_t* be = meta + p.meta.batch_off;
+    while (lo < hi) {
+        int64_t mid = (lo + hi + 1) >> 1;
+        if (be[mid * kBatchWords + kBeGroupBase] <= g) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kMetaThreads, 1)
+    metadata_kernel(Params p, const int32_t* __restrict__ seq_lens_q,
+                    const int32_t* __restrict__ seq_lens_k, int32_t* __restrict__ meta, int G)
+{
+    __shared__ int64_t scan_sh[32];
+    __shared__ uint32_t s_err;
+    __shared__ int s_tnd_bad;
+    __shared__ int64_t s_total;
+    const int tid = threadIdx.x;
+    int32_t* be = meta + p.meta.batch_off;
+    int32_t* cta_off = meta + p.meta.cta_off;
+    int32_t* gpre = meta + p.meta.group_off;
+    int32_t* units = meta + p.meta.unit_off;
+    if (tid == 0) { s_err = 0; s_tnd_bad = 0; }
+    __syncthreads();
+
+    // ---- per-batch extents and validity
+    for (int b = tid; b < p.batch; b += blockDim.x) {
+        int64_t sq = 0, first = 0;
+        bool ok = true;
+        if (!p.layout_tnd) {
+            first = (int64_t)b * p.s1;
+            int64_t v = seq_lens_q ? seq_lens_q[b] : p.s1;
+            ok = v >= 0 && v <= p.s1;
+            sq = ok ? v : 0;
+        } else {
+            int64_t lo = b > 0 ? seq_lens_q[b - 1] : 0, hi = seq_lens_q[b];
+            ok = lo >= 0 && hi >= lo && hi <= p.total_q;
+            if (!ok) atomicOr(&s_tnd_bad, 1);
+            first = lo < 0 ? 0 : lo;
+            sq = ok ? hi - lo : 0;
+        }
+        int64_t sk = seq_lens_k[b];
+        ok = ok && sk >= 0 && sk <= p.max_seqlen_k;
+        int64_t lc = ok ? compressed_keys(sk, p.cmp_ratio) : 0;
+        ok = ok && lc <= (int64_t)p.max_blocks_per_seq * p.block_size;
+        if (!ok) atomicOr(&s_err, kErrLength);
+        int32_t* e = be + (int64_t)b * kBatchWords;
+        e[kBeSq] = (int32_t)sq;
+        e[kBeSk] = (int32_t)(ok ? sk : 0);
+        e[kBeLc] = (int32_t)lc;
+        e[kBeFirstRow] = (int32_t)first;
+        e[kBeOk] = ok ? 1 : 0;
+    }
+    __syncthreads();
+
+    // ---- query groups per batch (bad TND prefix sums invalidate every batch) and their prefix
+    int64_t running = 0;
+    for (int base = 0; base < p.batch; base += blockDim.x) {
+        int b = base + tid;
+        int64_t groups = 0;
+        if (b < p.batch) {
+            int32_t* e = be + (int64_t)b * kBatchWords;
+            if (s_tnd_bad) e[kBeOk] = 0;
+            groups = e[kBeOk] ? ceil_div64(e[kBeSq], kGroupTokens) : 0;
+            e[kBeGroups] = (int32_t)groups;
+        }
+        int64_t tot;
+        int64_t ex = block_exclusive_scan(groups, &tot, scan_sh);
+        if (b < p.batch) be[(int64_t)b * kBatchWords + kBeGroupBase] = (int32_t)(running + ex);
+        running += tot;
+    }
+    const int64_t total_groups = running;
+    __syncthreads();
+
+    // ---- tiles per group, then their exclusive prefix (gpre[g]; gpre[total_groups] = total)
+    running = 0;
+    for (int64_t base = 0; base < total_groups; base += blockDim.x) {
+        int64_t g = base + tid;
+        int64_t tiles = 0;
+        if (g < total_groups) {
+            int64_t b = batch_of_group(meta, p, g);
+            const int32_t* e = be + b * kBatchWords;
+            int64_t r0 = (g - e[kBeGroupBase]) * kGroupTokens;
+            int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)e[kBeSq]) - 1;
+            int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], e[kBeLc], rl);
+            tiles = ceil_div64(n, kTileKeys);
+        }
+        int64_t tot;
+        int64_t ex = block_exclusive_scan(tiles, &tot, scan_sh);
+        if (g < total_groups) gpre[g] = (int32_t)(running + ex);
+        running += tot;
+    }
+    const int64_t T = running;
+    if (tid == 0) gpre[total_groups] = (int32_t)T;
+    __syncthreads();
+
+    // ---- split the tile sequence over G CTAs: count units per CTA, scan, then write them
+    running = 0;
+    for (int cbase = 0; cbase <= G; cbase += blockDim.x) {
+        int c = cbase + tid;
+        int64_t cnt = 0;
+        if (c < G && T > 0 && total_groups > 0) {
+            int64_t t0 = (T * c) / G, t1 = (T * (c + 1)) / G;
+            if (t1 > t0) {
+                for (int64_t g = upper_index(gpre, total_groups, t0); g < total_groups && gpre[g] < t1; ++g)
+                    if (gpre[g + 1] > gpre[g]) ++cnt;
+            }
+        }
+        int64_t tot;
+        int64_t ex = block_exclusive_scan(cnt, &tot, scan_sh);
+        if (c <= G) cta_off[c] = (int32_t)(running + ex);
+        if (c < G && cnt > 0) {
+            int64_t t0 = (T * c) / G, t1 = (T * (c + 1)) / G;
+            int64_t u = running + ex;
+            for (int64_t g = upper_index(gpre, total_groups, t0); g < total_groups && gpre[g] < t1; ++g) {
+                if (gpre[g + 1] <= gpre[g]) continue;
+                int64_t b = batch_of_group(meta, p, g);
+                const int32_t* e = be + b * kBatchWords;
+                int64_t r0 = (g - e[kBeGroupBase]) * kGroupTokens;
+                int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)e[kBeSq]) - 1;
+                int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], e[kBeLc], rl);
+                int64_t tb = max(t0, (int64_t)gpre[g]) - gpre[g];
+                int64_t te = min(t1, (int64_t)gpre[g + 1]) - gpre[g];
+                int32_t* w = units + u * kUnitWords;
+                w[0] = (int32_t)b;
+                w[1] = (int32_t)r0;
+                w[2] = (int32_t)(tb * kTileKeys);
+                w[3] = (int32_t)min(te * kTileKeys, n);
+                ++u;
+            }
+        }
+        running += tot;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        meta[kMhMagic] = kMetaMagic;
+        meta[kMhCtas] = G;
+        meta[kMhUnits] = (int32_t)running;
+        meta[kMhTiles] = (int32_t)T;
+        meta[kMhErr] = (int32_t)s_err;
+        meta[kMhBatch] = p.batch;
+        meta[kMhRows] = p.rows;
+        meta[kMhGroups] = (int32_t)total_groups;
+        meta[kMhLayoutHash] = p.hash;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                            int32_t* meta, int num_sms, cudaStream_t st)
+{
+    int G = num_sms < kMaxCtas ? num_sms : kMaxCtas;
+    metadata_kernel<<<1, kMetaThreads, 0, st>>>(p, seq_lens_q, seq_lens_k, meta, G);
+    return cudaGetLastError();
+}
+
+}  // namespace qli

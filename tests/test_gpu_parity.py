@@ -1,0 +1,185 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI (needs a GB300)."""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from checker import check, check_scores, visible_counts
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qli():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_attention_token_block_gb300 import build as B
+    B.build()
+    import sparse_attention_token_block_gb300 as Q
+    return Q
+
+
+def run_gpu(Q, case, repeat=1):
+    import torch
+    p = Q.make_problem(**W.problem_kwargs(case))
+    ix = Q.Indexer(p)
+    d = W.to_device(case)
+    for _ in range(repeat):
+        out = ix.run(**d)
+    torch.cuda.synchronize()
+    st, bits = ix.device_error()
+    return out.cpu().numpy(), ix.score_lines().cpu().numpy(), st, bits
+
+
+def assert_parity(Q, case, rows=None, scores=True):
+    gpu_idx, gpu_scores, st, bits = run_gpu(Q, case)
+    ora_idx, ora_scores, err = oracle.score_topk(case, with_scores=True, rows=rows)
+    assert err == 0 and st == 0, (err, st, bits)
+    vis = visible_counts(case, oracle)
+    exact, checked, fails = check(gpu_idx, ora_idx, ora_scores, vis, case.sparse_count, rows=rows)
+    assert not fails, fails[:5]
+    if scores:
+        worst = check_scores(gpu_scores, ora_scores, vis, rows=rows)
+        assert worst <= 1.0, worst
+    return exact, checked
+
+
+# ---------------------------------------------------------------------------- the named workloads
+
+@pytest.mark.parametrize("name", ["tiny_decode", "page_decode"])
+def test_small_workloads(qli, name):
+    exact, checked = assert_parity(qli, W.WORKLOADS[name]())
+    assert checked > 0
+
+
+def test_long_decode_full_size(qli):
+    case = W.long_decode()
+    assert_parity(qli, case)
+
+
+def test_fp8_compressed_decode_full_size(qli):
+    case = W.fp8_compressed_decode()
+    assert_parity(qli, case)
+
+
+def test_varlen_prefill_sampled_rows(qli):
+    case = W.varlen_prefill()
+    rng = np.random.default_rng(0)
+    cum = np.concatenate([[0], case.seq_lens_q])
+    rows = set(rng.choice(case.rows, 48, replace=False).tolist())
+    for b in range(case.batch):                       # each sequence's first, k-th and last rows
+        rows |= {int(cum[b]), int(min(cum[b] + 2047, cum[b + 1] - 1)), int(cum[b + 1] - 1)}
+    assert_parity(qli, case, rows=sorted(rows))
+
+
+# ---------------------------------------------------------------------------- seeded small shapes
+
+SMALL = [
+    # (name, kwargs)
+    ("bs16_c1_m0", dict(batch=2, s1=1, seq_lens_k=[300, 17], block_size=16, sparse_count=64)),
+    ("bs32_c2_m3", dict(batch=3, s1=3, seq_lens_k=[257, 1, 640], block_size=32, sparse_count=7,
+                        sparse_mode=3, cmp_ratio=2)),
+    ("bs64_c4_m3", dict(batch=2, s1=2, seq_lens_k=[1000, 129], block_size=64, sparse_count=100,
+                        sparse_mode=3, cmp_ratio=4)),
+    ("bs128_c8", dict(batch=2, s1=4, seq_lens_k=[4096, 385], block_size=128, sparse_count=512,
+                      sparse_mode=3, cmp_ratio=8)),
+    ("bs256_c16", dict(batch=1, s1=2, seq_lens_k=[8000], block_size=256, sparse_count=2048,
+                       sparse_mode=0, cmp_ratio=16)),
+    ("bs1024_c128", dict(batch=2, s1=1, seq_lens_k=[70000, 129], block_size=1024,
+                         sparse_count=33, sparse_mode=3, cmp_ratio=128)),
+    ("bs48_odd", dict(batch=2, s1=3, seq_lens_k=[700, 95], block_size=48, sparse_count=64,
+                      sparse_mode=3)),
+    ("bs80_c32", dict(batch=2, s1=1, seq_lens_k=[9000, 33], block_size=80, sparse_count=64,
+                      sparse_mode=3, cmp_ratio=32)),
+    ("sq_gt_sk", dict(batch=2, s1=4, seq_lens_k=[2, 130], block_size=16, sparse_count=16,
+                      sparse_mode=3)),
+    ("k1", dict(batch=2, s1=2, seq_lens_k=[500, 4000], block_size=64, sparse_count=1,
+                sparse_mode=3)),
+    ("sk0", dict(batch=3, s1=1, seq_lens_k=[0, 128, 127], block_size=64, sparse_count=8)),
+    ("qlens", dict(batch=3, s1=4, q_lens=[4, 0, 1], seq_lens_k=[600, 600, 129], block_size=64,
+                   sparse_count=200, sparse_mode=3)),
+    ("fp8_f32", dict(batch=2, s1=2, qk_dtype=W.FP8, scale_dtype=W.F32, seq_lens_k=[3000, 257],
+                     block_size=128, sparse_count=256, sparse_mode=3, cmp_ratio=4)),
+    ("fp8_f16", dict(batch=2, s1=1, qk_dtype=W.FP8, scale_dtype=W.F16, seq_lens_k=[1500, 64],
+                     block_size=32, sparse_count=100)),
+    ("int8_f32", dict(batch=2, s1=1, scale_dtype=W.F32, seq_lens_k=[1500, 64], block_size=32,
+                      sparse_count=100)),
+    ("tnd_mixed", dict(layout_q="TND", q_lens=[5, 1, 0, 9], seq_lens_k=[300, 40, 10, 600],
+                       block_size=32, sparse_count=64, sparse_mode=3)),
+    ("tnd_mode0", dict(layout_q="TND", q_lens=[3, 2], seq_lens_k=[200, 1000], block_size=64,
+                       sparse_count=128, sparse_mode=0, cmp_ratio=2)),
+    ("k_ge_n", dict(batch=2, s1=2, seq_lens_k=[200, 2048], block_size=128, sparse_count=2048,
+                    sparse_mode=3)),
+    ("identity_table", dict(batch=3, s1=2, seq_lens_k=[513, 1, 256], block_size=128,
+                            sparse_count=300, permute=False)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=[s[0] for s in SMALL])
+def test_small_shapes(qli, name, kw):
+    case = W.make_case(name, seed=zlib.crc32(name.encode()) % 1000, **kw)
+    assert_parity(qli, case)
+
+
+def test_negative_scales_and_weights(qli):
+    case = W.make_case("neg", batch=2, s1=2, seq_lens_k=[700, 300], block_size=64,
+                       sparse_count=100, sparse_mode=3, seed=5, scale_dtype=W.F32)
+    rng = np.random.default_rng(1)
+    case.q_scale *= np.where(rng.random(case.q_scale.shape) < 0.3, -1, 1).astype(np.float32)
+    case.k_scale *= np.where(rng.random(case.k_scale.shape) < 0.3, -1, 1).astype(np.float32)
+    case.weights *= np.where(rng.random(case.weights.shape) < 0.2, -1, 1).astype(np.float32)
+    assert_parity(qli, case)
+
+
+def test_int8_extremes_exact(qli):
+    """All -128 / 127 codes: dots of +-2^21 and +-2^14 * 127 * ... must come out exact."""
+    case = W.make_case("ext", batch=1, s1=1, seq_lens_k=[256], block_size=128, sparse_count=256,
+                       seed=2, scale_dtype=W.F32)
+    rng = np.random.default_rng(3)
+    case.query[:] = np.where(rng.random(case.query.shape) < 0.5, -128, 127).astype(np.int8)
+    case.key[:] = np.where(rng.random(case.key.shape) < 0.5, -128, 127).astype(np.int8)
+    case.q_scale[:] = 1.0
+    case.k_scale[:] = 1.0
+    case.weights[:] = 0.0
+    case.weights[0, 0, 0] = 1.0
+    gpu_idx, gpu_scores, st, _ = run_gpu(qli, case)
+    ora_idx, ora_scores, _ = oracle.score_topk(case, with_scores=True)
+    assert st == 0
+    assert np.array_equal(gpu_scores[0, :256], ora_scores[0, :256])   # integer dots, exact
+    assert np.array_equal(gpu_idx, ora_idx)
+
+
+def test_repeat_calls_same_result(qli):
+    case = W.make_case("rep", batch=3, s1=2, seq_lens_k=[900, 5, 300], block_size=64,
+                       sparse_count=64, sparse_mode=3, seed=8)
+    a, _, _, _ = run_gpu(qli, case, repeat=1)
+    b, _, _, _ = run_gpu(qli, case, repeat=3)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------- device-side faults
+
+def test_bad_page_blanks_batch_and_reports(qli):
+    case = W.make_case("badpage", batch=2, s1=1, seq_lens_k=[300, 300], block_size=64,
+                       sparse_count=16, seed=4)
+    case.block_table[1, 1] = case.num_blocks + 5
+    gpu_idx, _, st, bits = run_gpu(qli, case)
+    ora_idx, _, err = oracle.score_topk(case)
+    assert err & oracle.ERR_PAGE
+    assert st == 5 and bits & 2
+    assert (gpu_idx[1] == -1).all()
+    assert np.array_equal(gpu_idx, ora_idx)
+
+
+def test_bad_lengths_blank_batch_and_report(qli):
+    case = W.make_case("badlen", batch=2, s1=2, q_lens=[2, 2], seq_lens_k=[300, 300],
+                       block_size=64, sparse_count=16, seed=4)
+    case.seq_lens_q = np.array([2, 3], np.int32)        # 3 > S1
+    gpu_idx, _, st, bits = run_gpu(qli, case)
+    ora_idx, _, err = oracle.score_topk(case)
+    assert err & oracle.ERR_LENGTH
+    assert st == 5 and bits & 1
+    assert np.array_equal(gpu_idx, ora_idx)

@@ -1,0 +1,79 @@
+"""Host-side checks of the C-ABI library that need no GPU: it loads, exports every symbol the
+header declares, and rejects invalid problems synchronously."""
+import ctypes
+import re
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def Q():
+    from sparse_attention_token_block_gb300 import build as B
+    B.build()
+    import sparse_attention_token_block_gb300 as Q
+    return Q
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "qli.h")).read()
+    return sorted(set(re.findall(r"\b(qli_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(Q):
+    names = declared_symbols()
+    assert set(names) == set(Q.EXPORTS)
+    for n in names:
+        assert hasattr(Q.lib, n), n
+
+
+def _ok_problem(Q, **kw):
+    args = dict(batch=2, max_q_tokens=1, num_blocks=8, block_size=64, max_blocks_per_seq=4,
+                sparse_count=64, sparse_mode=3, cmp_ratio=1, max_seqlen_q=1, max_seqlen_k=256)
+    args.update(kw)
+    return Q.make_problem(**args)
+
+
+def test_validate_accepts_readme_example(Q):
+    p = _ok_problem(Q, batch=24, max_q_tokens=4, num_blocks=96, block_size=128,
+                    max_blocks_per_seq=4, sparse_count=512, sparse_mode=0, max_seqlen_q=4,
+                    max_seqlen_k=512)
+    st, why = Q.validate(p)
+    assert st == 0, why
+    assert Q.metadata_words(p) >= 1024
+    assert Q.workspace_size(p) >= 256 + 96 * 512 * 4
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("num_heads_q", 32, 1), ("num_heads_k", 2, 1), ("head_dim", 64, 1), ("block_size", 24, 1),
+    ("block_size", 2048, 1), ("sparse_count", 0, 1), ("sparse_count", 2049, 1),
+    ("sparse_mode", 1, 1), ("cmp_ratio", 3, 1), ("cmp_ratio", 256, 1), ("query_quant_mode", 1, 1),
+    ("key_quant_mode", 1, 1), ("pre_tokens", 5, 1), ("next_tokens", 0, 1), ("qk_dtype", 2, 1),
+    ("scale_dtype", 7, 1), ("layout_q", 2, 1), ("max_blocks_per_seq", 3, 1),
+    ("return_value", 1, 2), ("num_blocks", 0, 1), ("batch", -1, 1),
+])
+def test_validate_rejects(Q, field, value, status):
+    p = _ok_problem(Q)
+    setattr(p, field, value)
+    st, why = Q.validate(p)
+    assert st == status, (field, why)
+    assert Q.metadata_words(p) == 0 and Q.workspace_size(p) == 0
+
+
+def test_invalid_calls_enqueue_nothing(Q):
+    # rejected before any CUDA call, so these work without a GPU
+    p = _ok_problem(Q)
+    p.sparse_count = 0
+    assert Q.lib.qli_metadata(ctypes.byref(p), None, None, None, 0, None) == 1
+    assert Q.lib.qli_score_topk(ctypes.byref(p), *([None] * 9), 0, None, 0, None, None, None) == 1
+    p = _ok_problem(Q)
+    assert Q.lib.qli_metadata(ctypes.byref(p), None, None, None, 0, None) == 1      # no buffer
+    assert Q.lib.qli_metadata(ctypes.byref(p), None, None, 16, 10, None) == 3       # too small
+    assert Q.lib.qli_score_topk(ctypes.byref(p), *([None] * 9), 0, None, 0, None, None,
+                                None) == 3
+    assert Q.lib.qli_score_topk(ctypes.byref(p), *([None] * 9), 1 << 20, None, 1 << 30, None,
+                                1024, None) == 2                                       # values
+    assert Q.status_string(6) == "device wait timed out"
+    assert Q.version() >= 100

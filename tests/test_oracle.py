@@ -299,3 +299,13 @@ def test_bad_lengths_blank_the_batch():
     case.seq_lens_k = np.array([300, 10 ** 6], np.int32)   # beyond the block_table's capacity
     idx, _, err = oracle.score_topk(case)
     assert err & oracle.ERR_LENGTH and (idx[3:6] == -1).all()
+
+
+def test_bad_tnd_prefix_sums_blank_every_row():
+    case = W.make_case("tndbad", layout_q="TND", q_lens=[3, 4], seq_lens_k=[40, 40],
+                       block_size=16, sparse_count=8, sparse_mode=3, seed=9)
+    idx, _, err = oracle.score_topk(case)
+    assert err == 0 and (idx != -1).any()
+    case.seq_lens_q = np.array([5, 3], np.int32)     # decreasing
+    idx, _, err = oracle.score_topk(case)
+    assert err & oracle.ERR_LENGTH and (idx == -1).all()

@@ -246,3 +246,37 @@ WORKLOADS = {
     "fp8_compressed_decode": fp8_compressed_decode,
     "varlen_prefill": varlen_prefill,
 }
+
+
+# ----------------------------------------------------------------------------------------------
+# Marshalling for the CUDA library (torch device tensors and the problem attributes)
+# ----------------------------------------------------------------------------------------------
+
+def problem_kwargs(case: Case) -> dict:
+    """Attributes of ``case`` as keyword arguments of the binding's ``make_problem``."""
+    return dict(batch=case.batch, layout_q=0 if case.layout_q == "BSND" else 1,
+                max_q_tokens=case.s1, total_q_tokens=case.total_q,
+                qk_dtype=0 if case.qk_dtype == INT8 else 1,
+                scale_dtype=0 if case.scale_dtype == F16 else 1, num_blocks=case.num_blocks,
+                block_size=case.block_size, max_blocks_per_seq=case.max_blocks_per_seq,
+                sparse_count=case.sparse_count, sparse_mode=case.sparse_mode,
+                cmp_ratio=case.cmp_ratio, max_seqlen_q=case.max_seqlen_q,
+                max_seqlen_k=case.max_seqlen_k)
+
+
+def to_device(case: Case, device="cuda") -> dict:
+    """Copy every input array of ``case`` to ``device`` as a torch tensor (codes keep their bytes)."""
+    import torch
+
+    def t(a, dtype=None):
+        if a is None:
+            return None
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype is not None:
+            x = x.view(dtype)
+        return x.to(device)
+
+    return dict(query=t(case.query.view(np.uint8)), key=t(case.key.view(np.uint8)),
+                weights=t(case.weights), q_scale=t(case.q_scale), k_scale=t(case.k_scale),
+                seq_lens_q=t(case.seq_lens_q), seq_lens_k=t(case.seq_lens_k),
+                block_table=t(case.block_table))
