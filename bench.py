@@ -1,0 +1,412 @@
+"""Benchmark of the quantized lightning indexer on one or more GB300s.
+
+A step is one pass of the whole hot path over one batch of synthetic input: the work split
+(qli_metadata), the scoring kernel (qli_score: paged key gather, tensor-core Q.K^T, fused
+dequant/ReLU/head-sum/mask epilogue) and the top-k (qli_topk).  The default workload is the
+long-context decode: 32 sequences, one query token each, 64 int8 heads of dim 128, key lengths
+uniform in [8192, 32768] in 64-key pages under a random block_table, sparse_count 2048, causal.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the launching
+stream with an L2 flush (a 512 MB write) between steps, outside the events; barrier +
+synchronize around the timed region; the maximum over ranks.  SM clocks and throttle reasons are
+sampled with nvidia-smi over ~1.5 s of identical untimed load steps ending where the timed steps
+begin, and through the timed steps.  Printed: one JSON line.
+
+``--impl reference`` times the CPU oracle instead (the reference arm): the plain C implementation
+run on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+OPS_PER_PAIR = 2 * 64 * 128          # 64 heads x 128-dim dot, multiply + add
+METRIC = "indexer GOPS (algorithmic: 16384 ops per visible query-key pair)"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "score_kernel_long_decode.md")
+SCORE_SOURCES = ["qli_score.cu", "qli_ptx.cuh", "qli_internal.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_decode", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
+    ap.add_argument("--flush-mb", type=int, default=512)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="skip the clock-sampling load window")
+    return ap.parse_args()
+
+
+def make_workload(name, batch, rank):
+    fn = W.WORKLOADS[name]
+    if name == "long_decode":
+        return fn(seed=3 + 1000 * rank, batch=batch or 32)
+    if name == "fp8_compressed_decode":
+        return fn(seed=4 + 1000 * rank, batch=batch or 16)
+    return fn()
+
+
+def visible_pairs(case):
+    """Visible (query row, compressed key) pairs of the workload: Lc = ceil(S_k / cmp_ratio) keys
+    per sequence; under sparse_mode 3 row r of Sq sees min(Lc, ceil((S_k - Sq + r + 1) / cmp))."""
+    c = case.cmp_ratio
+    total = 0
+    lo = 0
+    for b in range(case.batch):
+        sk = int(case.seq_lens_k[b])
+        if case.layout_q == "BSND":
+            sq = case.s1 if case.seq_lens_q is None else int(case.seq_lens_q[b])
+        else:
+            hi = int(case.seq_lens_q[b])
+            sq, lo = hi - lo, hi
+        lc = -(-sk // c)
+        for r in range(sq):
+            if case.sparse_mode == 0:
+                total += lc
+            else:
+                pos = sk - sq + r
+                total += 0 if pos < 0 else min(lc, -(-(pos + 1) // c))
+    return total
+
+
+def workload_stats(case):
+    """Visible pairs, keys read (once per sequence) and algorithmic bytes of the scoring stage."""
+    pairs = visible_pairs(case)
+    esz = 2 if case.scale_dtype == W.F16 else 4
+    lc = [-(-int(s) // case.cmp_ratio) for s in case.seq_lens_k]
+    keys = int(sum(lc))
+    pages = int(sum(-(-x // case.block_size) for x in lc))
+    rows = case.rows
+    score_bytes = keys * (128 + esz) + rows * 64 * (128 + 2 * esz) + pages * 4
+    total_bytes = score_bytes + rows * case.sparse_count * 4 + case.batch * 8
+    return dict(pairs=pairs, keys=keys, rows=rows, score_bytes=score_bytes,
+                total_bytes=total_bytes)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the scoring kernel from the committed ncu summary, if that summary
+    was taken on the current kernel source (else None)."""
+    try:
+        text = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None, None
+    h = hashlib.sha256()
+    for s in SCORE_SOURCES:
+        with open(os.path.join(ROOT, "sparse_attention_token_block_gb300", "csrc", s), "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()[:16]
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha") != sha:
+        return None, sha
+    try:
+        return float(vals["traffic_bytes_per_launch"]), sha
+    except (KeyError, ValueError):
+        return None, sha
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_baseline(case, budget_s=15.0):
+    """Time the oracle (as it stands) on a bounded sample of the workload: whole sequences, as
+    many as fit in about ``budget_s`` of wall time on the host cores."""
+    import oracle
+    nthreads = os.cpu_count() or 1
+    oracle.build()
+    if case.layout_q != "BSND":
+        take, sub = case.batch, case
+    else:
+        t0 = time.perf_counter()
+        oracle.score_topk(subcase(case, [0]), nthreads=nthreads)
+        one = max(time.perf_counter() - t0, 1e-3)
+        take = int(max(1, min(case.batch, budget_s / one)))
+        sub = subcase(case, list(range(take)))
+    t0 = time.perf_counter()
+    oracle.score_topk(sub, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    pairs = visible_pairs(sub)
+    return {"value": pairs * OPS_PER_PAIR / dt / 1e9, "unit": "GOPS", "cores": nthreads,
+            "kind": "oracle", "seconds": dt,
+            "sample": "%d of %d sequences of the workload (%d visible pairs); full oracle: exact "
+                      "dots, fp32 scaling and head sum, stable sort" % (take, case.batch, pairs)}
+
+
+def subcase(case, batches):
+    """The workload restricted to some of its sequences (BSND decode workloads)."""
+    b = np.asarray(batches, dtype=np.int64)
+    rows = case.query[b]
+    return W.Case(**{**case.__dict__, "batch": len(b), "query": rows, "weights": case.weights[b],
+                     "q_scale": case.q_scale[b],
+                     "seq_lens_q": None if case.seq_lens_q is None else case.seq_lens_q[b],
+                     "seq_lens_k": case.seq_lens_k[b], "block_table": case.block_table[b]})
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    case = make_workload(args.workload, args.batch, 0)
+    import oracle
+    oracle.build()
+    nthreads = os.cpu_count() or 1
+    take = max(1, min(case.batch, 2)) if case.layout_q == "BSND" else None
+    sub = subcase(case, list(range(take))) if take else case
+    pairs = visible_pairs(sub)
+    for _ in range(args.warmup):
+        oracle.score_topk(sub, nthreads=nthreads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.score_topk(sub, nthreads=nthreads)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = pairs * OPS_PER_PAIR * args.steps / total / 1e9
+    sample = ("%d of %d sequences per step (%d visible pairs)" % (take, case.batch, pairs)
+              if take else "whole workload")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic", "config": config_of(case, args, world),
+            "cpu_baseline": {"value": value, "unit": "GOPS", "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def config_of(case, args, world):
+    return {"workload": "%s: B=%d, S1=%d, %s q/k, %s scales, S_k %d..%d, block_size %d, "
+                        "sparse_count %d, sparse_mode %d, cmp_ratio %d" % (
+                            case.name, case.batch, case.s1 or 0, case.qk_dtype, case.scale_dtype,
+                            int(case.seq_lens_k.min()), int(case.seq_lens_k.max()),
+                            case.block_size, case.sparse_count, case.sparse_mode, case.cmp_ratio),
+            "global_batch": case.batch * world, "parallelism": "independent sequences per rank",
+            "l2": "flushed between timed steps (%d MB write, outside the events)" % args.flush_mb}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    import sparse_attention_token_block_gb300 as Q
+    from sparse_attention_token_block_gb300 import build as B
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    case = make_workload(args.workload, args.batch, rank)
+    stats = workload_stats(case)
+    p = Q.make_problem(**W.problem_kwargs(case))
+    ix = Q.Indexer(p, device=dev)
+    d = W.to_device(case, dev)
+    flush = torch.empty(args.flush_mb * (1 << 20) // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        Q.check(Q.metadata(p, d["seq_lens_q"], d["seq_lens_k"], ix.meta), "metadata")
+        if evs:
+            evs[1].record(stream)
+        Q.check(Q.score(p, d["query"], d["key"], d["weights"], d["q_scale"], d["k_scale"],
+                        d["seq_lens_q"], d["seq_lens_k"], d["block_table"], ix.meta,
+                        ix.workspace), "score")
+        if evs:
+            evs[2].record(stream)
+        Q.check(Q.topk(p, d["block_table"], ix.meta, ix.workspace, ix.out), "topk")
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st, bits = ix.device_error()
+    Q.check(st, "device error after warm-up (bits %d)" % bits)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # nvidia-smi samples every 100 ms: keep the GPU on the same load for ~1.5 s of untimed steps
+    # right before the timed ones so the samples describe the clocks the timed steps ran at
+    clocks = Clocks(local)
+    if not args.no_clocks:
+        clocks.start()
+    t_end = time.perf_counter() + (0 if args.no_clocks else 1.5)
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            flush.fill_(2)
+            step()
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i)
+        step(evs[i])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    meta_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    score_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    topk_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ops = stats["pairs"] * OPS_PER_PAIR * args.steps * world
+    value = ops / (total_ms * 1e-3) / 1e9
+
+    # end to end through the public call with host buffers: pinned host inputs copied in, the
+    # indices copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in d.items()}
+        out_h = torch.empty(ix.out.shape, dtype=torch.int32).pin_memory()
+        dd = {k: (torch.empty_like(v) if v is not None else None) for k, v in d.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = out_h.numel() * 4
+
+        def e2e_step():
+            for k, v in host.items():
+                if v is not None:
+                    dd[k].copy_(v, non_blocking=True)
+            out = ix.run(**dd)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i)
+            ev[i][0].record(stream)
+            e2e_step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = sum(a.elapsed_time(b) for a, b in ev)
+        if dist:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": ops / (e_ms * 1e-3) / 1e9, "unit": "GOPS", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps}
+
+    st, bits = ix.device_error()
+    Q.check(st, "device error after timing (bits %d)" % bits)
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    score_avg = sum(score_ms) / len(score_ms)
+    achieved = stats["score_bytes"] / (score_avg * 1e-3) / 1e9
+    traffic, _ = recorded_traffic()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8" if case.qk_dtype == W.INT8 else "fp8_e4m3",
+        "data": "synthetic", "config": config_of(case, args, world),
+        "keys_scored_per_s": stats["pairs"] * args.steps * world / (total_ms * 1e-3),
+        "us_per_call": 1e3 * total_ms / args.steps,
+        "stage_us": {"metadata": 1e3 * statistics.mean(meta_ms),
+                     "score": 1e3 * score_avg, "topk": 1e3 * statistics.mean(topk_ms)},
+        "roofline": {"kernel": "score_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": stats["score_bytes"], "traffic": traffic},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

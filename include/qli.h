@@ -137,6 +137,23 @@ qli_status qli_score_topk(const qli_problem* p, const void* query, const void* k
                           size_t metadata_words, void* workspace, size_t workspace_bytes,
                           int32_t* sparse_indices, float* sparse_values, void* stream);
 
+/*
+ * The two stages of qli_score_topk, for callers that time or reuse them separately.  Same
+ * arguments, rules and errors as qli_score_topk; calling qli_score then qli_topk on one stream with
+ * one workspace gives exactly what qli_score_topk gives.
+ *   qli_score: README steps 1-2 and the weighted head sum -- every visible key's score, kept in the
+ *              workspace (one line per query row);
+ *   qli_topk:  README step 3 -- the top-sparse_count indices of each row's score line, padded
+ *              with -1, into sparse_indices.
+ */
+qli_status qli_score(const qli_problem* p, const void* query, const void* key, const void* weights,
+                     const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
+                     const int32_t* seq_lens_k, const int32_t* block_table, const int32_t* metadata,
+                     size_t metadata_words, void* workspace, size_t workspace_bytes, void* stream);
+qli_status qli_topk(const qli_problem* p, const int32_t* block_table, const int32_t* metadata,
+                    size_t metadata_words, void* workspace, size_t workspace_bytes,
+                    int32_t* sparse_indices, void* stream);
+
 /* Zero the workspace's device error word (enqueued on `stream`).  Call once after allocating a
  * workspace, before its first qli_score_topk. */
 qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

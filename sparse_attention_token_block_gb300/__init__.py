@@ -25,7 +25,8 @@ INT64_MAX = (1 << 63) - 1
 
 # symbols include/qli.h declares
 EXPORTS = ("qli_problem_init", "qli_validate", "qli_metadata_words", "qli_workspace_size",
-           "qli_metadata", "qli_score_topk", "qli_workspace_init", "qli_get_device_error",
+           "qli_metadata", "qli_score_topk", "qli_score", "qli_topk", "qli_workspace_init",
+           "qli_get_device_error",
            "qli_status_string", "qli_version")
 
 
@@ -65,6 +66,10 @@ def _load():
     L.qli_score_topk.argtypes = [P, vp, vp, vp, vp, vp, i32p, i32p, i32p, i32p, sz, vp, sz, i32p,
                                  vp, vp]
     L.qli_score_topk.restype = ctypes.c_int
+    L.qli_score.argtypes = [P, vp, vp, vp, vp, vp, i32p, i32p, i32p, i32p, sz, vp, sz, vp]
+    L.qli_score.restype = ctypes.c_int
+    L.qli_topk.argtypes = [P, i32p, i32p, sz, vp, sz, i32p, vp]
+    L.qli_topk.restype = ctypes.c_int
     L.qli_workspace_init.argtypes = [vp, sz, vp]
     L.qli_workspace_init.restype = ctypes.c_int
     L.qli_get_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -140,6 +145,20 @@ def score_topk(p: Problem, query, key, weights, q_scale, k_scale, seq_lens_q, se
                               _ptr(block_table), _ptr(meta), meta.numel(), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _ptr(sparse_indices),
                               _ptr(sparse_values), _stream(stream))
+
+
+def score(p: Problem, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
+          meta, workspace, stream=None) -> int:
+    return _get_lib().qli_score(ctypes.byref(p), _ptr(query), _ptr(key), _ptr(weights),
+                                _ptr(q_scale), _ptr(k_scale), _ptr(seq_lens_q), _ptr(seq_lens_k),
+                                _ptr(block_table), _ptr(meta), meta.numel(), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def topk(p: Problem, block_table, meta, workspace, sparse_indices, stream=None) -> int:
+    return _get_lib().qli_topk(ctypes.byref(p), _ptr(block_table), _ptr(meta), meta.numel(),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _ptr(sparse_indices), _stream(stream))
 
 
 def workspace_init(workspace, stream=None) -> int:

@@ -228,6 +228,70 @@ qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const i
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
 
+namespace {
+
+// Shared argument checks of the score and top-k stages
+qli_status check_call(const qli_problem* p, const int32_t* metadata, size_t metadata_words, void* workspace,
+                      size_t workspace_bytes, Params* P, WsLayout* W, int* sms)
+{
+    qli_status s = check(p, nullptr);
+    if (s != QLI_OK) return s;
+    *P = params_of(p);
+    *W = ws_layout(*P);
+    if (metadata_words < (size_t)P->meta.total_words || workspace_bytes < W->total) return QLI_ERR_WORKSPACE_TOO_SMALL;
+    if (!metadata || !workspace || !aligned(workspace, 256)) return QLI_ERR_INVALID_ARG;
+    *sms = device_sms(nullptr);
+    if (*sms < 0) return QLI_ERR_CUDA;
+    if (*sms == 0) return QLI_ERR_NO_DEVICE;
+    return QLI_OK;
+}
+
+}  // namespace
+
+qli_status qli_score(const qli_problem* p, const void* query, const void* key, const void* weights,
+                     const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
+                     const int32_t* seq_lens_k, const int32_t* block_table, const int32_t* metadata,
+                     size_t metadata_words, void* workspace, size_t workspace_bytes, void* stream)
+{
+    Params P;
+    WsLayout W;
+    int sms = 0;
+    qli_status s = check_call(p, metadata, metadata_words, workspace, workspace_bytes, &P, &W, &sms);
+    if (s != QLI_OK) return s;
+    if (P.rows == 0 || P.batch == 0) return QLI_OK;
+    if (!query || !key || !weights || !q_scale || !k_scale || !seq_lens_k || !block_table) return QLI_ERR_INVALID_ARG;
+    if (P.layout_tnd && !seq_lens_q) return QLI_ERR_INVALID_ARG;
+    if (!aligned(query, 16) || !aligned(key, 16) || !aligned(k_scale, 16) || !aligned(weights, 16) ||
+        !aligned(q_scale, 16))
+        return QLI_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    CUtensorMap tm;
+    if (!encode_key_map(&tm, key, P)) return QLI_ERR_CUDA;
+    const int grid = sms < kMaxCtas ? sms : kMaxCtas;
+    cudaError_t e = launch_score(P, &tm, query, key, weights, q_scale, k_scale, block_table, metadata,
+                                 reinterpret_cast<uint32_t*>(ws + W.scores_off), reinterpret_cast<uint32_t*>(ws),
+                                 grid, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
+qli_status qli_topk(const qli_problem* p, const int32_t* block_table, const int32_t* metadata,
+                    size_t metadata_words, void* workspace, size_t workspace_bytes, int32_t* sparse_indices,
+                    void* stream)
+{
+    Params P;
+    WsLayout W;
+    int sms = 0;
+    qli_status s = check_call(p, metadata, metadata_words, workspace, workspace_bytes, &P, &W, &sms);
+    if (s != QLI_OK) return s;
+    if (P.rows == 0) return QLI_OK;
+    if (!sparse_indices) return QLI_ERR_INVALID_ARG;
+    if (P.batch > 0 && !block_table) return QLI_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaError_t e = launch_topk(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),
+                                reinterpret_cast<uint32_t*>(ws), sparse_indices, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
 qli_status qli_score_topk(const qli_problem* p, const void* query, const void* key, const void* weights,
                           const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
                           const int32_t* seq_lens_k, const int32_t* block_table, const int32_t* metadata,
@@ -237,36 +301,16 @@ qli_status qli_score_topk(const qli_problem* p, const void* query, const void* k
     qli_status s = check(p, nullptr);
     if (s != QLI_OK) return s;
     if (sparse_values) return QLI_ERR_UNSUPPORTED;
-    const Params P = params_of(p);
-    const WsLayout W = ws_layout(P);
-    if (metadata_words < (size_t)P.meta.total_words || workspace_bytes < W.total) return QLI_ERR_WORKSPACE_TOO_SMALL;
-    if (!metadata || !workspace || !aligned(workspace, 256)) return QLI_ERR_INVALID_ARG;
-    if (P.rows == 0) return QLI_OK;
-    if (!sparse_indices) return QLI_ERR_INVALID_ARG;
-    if (P.batch > 0) {
-        if (!query || !key || !weights || !q_scale || !k_scale || !seq_lens_k || !block_table) return QLI_ERR_INVALID_ARG;
-        if (P.layout_tnd && !seq_lens_q) return QLI_ERR_INVALID_ARG;
-        if (!aligned(query, 16) || !aligned(key, 16) || !aligned(k_scale, 16) || !aligned(weights, 16) ||
-            !aligned(q_scale, 16))
-            return QLI_ERR_INVALID_ARG;
+    {
+        const Params P = params_of(p);
+        if (P.rows > 0 && !sparse_indices &&
+            metadata_words >= (size_t)P.meta.total_words && workspace_bytes >= ws_layout(P).total)
+            return QLI_ERR_INVALID_ARG;   // validate everything before enqueueing the first stage
     }
-    int sms = device_sms(nullptr);
-    if (sms < 0) return QLI_ERR_CUDA;
-    if (sms == 0) return QLI_ERR_NO_DEVICE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    uint32_t* err = reinterpret_cast<uint32_t*>(ws);
-    uint32_t* scores = reinterpret_cast<uint32_t*>(ws + W.scores_off);
-    if (P.batch > 0) {
-        CUtensorMap tm;
-        if (!encode_key_map(&tm, key, P)) return QLI_ERR_CUDA;
-        const int grid = sms < kMaxCtas ? sms : kMaxCtas;
-        cudaError_t e = launch_score(P, &tm, query, key, weights, q_scale, k_scale, block_table, metadata, scores,
-                                     err, grid, st);
-        if (e != cudaSuccess) return QLI_ERR_CUDA;
-    }
-    cudaError_t e = launch_topk(P, block_table, metadata, scores, err, sparse_indices, st);
-    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+    s = qli_score(p, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table, metadata,
+                  metadata_words, workspace, workspace_bytes, stream);
+    if (s != QLI_OK) return s;
+    return qli_topk(p, block_table, metadata, metadata_words, workspace, workspace_bytes, sparse_indices, stream);
 }
 
 qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream)
