@@ -154,6 +154,27 @@ qli_status qli_topk(const qli_problem* p, const int32_t* block_table, const int3
                     size_t metadata_words, void* workspace, size_t workspace_bytes,
                     int32_t* sparse_indices, void* stream);
 
+/*
+ * qli_score_topk without a caller-provided workspace.  The README has no counterpart: this entry
+ * point exists for callers that cannot allocate device memory -- a plugin whose host framework
+ * owns every allocation and forbids cudaMalloc, a runtime with a fixed memory budget set aside at
+ * start-up, or latency-critical code that must not call cudaMalloc because it can synchronise
+ * the device.  The scratch lives in one 16 MiB array inside the library, reserved on every GPU
+ * that loads the library until the process exits; a problem whose qli_workspace_size exceeds
+ * 16 MiB is rejected with QLI_ERR_WORKSPACE_TOO_SMALL.  Inputs, metadata and sparse_indices are
+ * as for qli_score_topk; `device_error` (optional device pointer to one uint32) receives this
+ * call's device error word (bits as for qli_get_device_error).  The first call on a device looks
+ * up the array's address with that device current; make it before any stream capture.  All
+ * calls share the array: calls that overlap on the GPU race, so order them on one stream.  No
+ * allocating call is made.
+ */
+qli_status qli_score_topk_static(const qli_problem* p, const void* query, const void* key,
+                                 const void* weights, const void* q_scale, const void* k_scale,
+                                 const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                                 const int32_t* block_table, const int32_t* metadata,
+                                 size_t metadata_words, int32_t* sparse_indices,
+                                 uint32_t* device_error, void* stream);
+
 /* Zero the workspace's device error word (enqueued on `stream`).  Call once after allocating a
  * workspace, before its first qli_score_topk. */
 qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

@@ -25,8 +25,8 @@ INT64_MAX = (1 << 63) - 1
 
 # symbols include/qli.h declares
 EXPORTS = ("qli_problem_init", "qli_validate", "qli_metadata_words", "qli_workspace_size",
-           "qli_metadata", "qli_score_topk", "qli_score", "qli_topk", "qli_workspace_init",
-           "qli_get_device_error",
+           "qli_metadata", "qli_score_topk", "qli_score", "qli_topk", "qli_score_topk_static",
+           "qli_workspace_init", "qli_get_device_error",
            "qli_status_string", "qli_version")
 
 
@@ -70,6 +70,9 @@ def _load():
     L.qli_score.restype = ctypes.c_int
     L.qli_topk.argtypes = [P, i32p, i32p, sz, vp, sz, i32p, vp]
     L.qli_topk.restype = ctypes.c_int
+    L.qli_score_topk_static.argtypes = [P, vp, vp, vp, vp, vp, i32p, i32p, i32p, i32p, sz, i32p,
+                                        vp, vp]
+    L.qli_score_topk_static.restype = ctypes.c_int
     L.qli_workspace_init.argtypes = [vp, sz, vp]
     L.qli_workspace_init.restype = ctypes.c_int
     L.qli_get_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -159,6 +162,15 @@ def topk(p: Problem, block_table, meta, workspace, sparse_indices, stream=None) 
     return _get_lib().qli_topk(ctypes.byref(p), _ptr(block_table), _ptr(meta), meta.numel(),
                                _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _ptr(sparse_indices), _stream(stream))
+
+
+def score_topk_static(p: Problem, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k,
+                      block_table, meta, sparse_indices, device_error=None, stream=None) -> int:
+    """qli_score_topk_static: no workspace argument; the library's own fixed scratch is used."""
+    return _get_lib().qli_score_topk_static(
+        ctypes.byref(p), _ptr(query), _ptr(key), _ptr(weights), _ptr(q_scale), _ptr(k_scale),
+        _ptr(seq_lens_q), _ptr(seq_lens_k), _ptr(block_table), _ptr(meta), meta.numel(),
+        _ptr(sparse_indices), _ptr(device_error), _stream(stream))
 
 
 def workspace_init(workspace, stream=None) -> int:
