@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/qli.h"
+#include "qli.h"
 
 namespace qli {
 
@@ -93,19 +93,30 @@ struct Params {
 // ---------------------------------------------------------------------------- shared helpers
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Compressed keys of a batch with sk original tokens
-__host__ __device__ inline int64_t compressed_keys(int64_t sk, int cmp) { return ceil_div64(sk, cmp); }
+// log2 of a power-of-two cmp_ratio (validated on the host)
+__host__ __device__ inline int log2_pow2(int v)
+{
+    int s = 0;
+    while ((1 << s) < v) ++s;
+    return s;
+}
+
+// Compressed keys of a batch with sk original tokens: ceil(sk / cmp)
+__host__ __device__ inline int64_t compressed_keys(int64_t sk, int cmp)
+{
+    return (sk + cmp - 1) >> log2_pow2(cmp);
+}
 
 // Visible compressed keys of live row r (0 <= r < sq); mode 3 counts the compressed blocks that
-// have started at or before the row's right-aligned original position.
+// have started at or before the row's right-aligned original position: ceil((pos + 1) / cmp).
 __host__ __device__ inline int64_t visible_keys(int mode, int cmp, int64_t sq, int64_t sk, int64_t lc,
                                                 int64_t r)
 {
     if (r < 0 || r >= sq) return 0;
     if (mode == 0) return lc;
-    int64_t pos = sk - sq + r;
+    const int64_t pos = sk - sq + r;
     if (pos < 0) return 0;
-    int64_t n = ceil_div64(pos + 1, cmp);
+    const int64_t n = (pos + cmp) >> log2_pow2(cmp);
     return n < lc ? n : lc;
 }
 

@@ -17,7 +17,7 @@ namespace qli {
 
 namespace {
 
-constexpr int kMetaThreads = 1024;
+constexpr int kMetaThreads = 256;
 
 // Block-wide exclusive scan of one int64 per thread; returns the exclusive prefix and the total.
 __device__ int64_t block_exclusive_scan(int64_t v, int64_t* total, int64_t* sh /* [32] */)
@@ -47,42 +47,51 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t* total, int64_t* sh /
     return warp_excl + x - v;
 }
 
+// A strided int32 array in shared or global memory
+struct View {
+    int32_t* p;
+    int stride;
+    __device__ int32_t& operator[](int64_t i) const { return p[i * stride]; }
+};
+
 // Largest i in [0, n) with a[i] <= key, for non-decreasing a (a[0] <= key assumed)
-__device__ int64_t upper_index(const int32_t* a, int64_t n, int64_t key)
+__device__ int64_t upper_index(const View& a, int64_t n, int64_t key)
 {
     int64_t lo = 0, hi = n - 1;
     while (lo < hi) {
-        int64_t mid = (lo + hi + 1) >> 1;
+        const int64_t mid = (lo + hi + 1) >> 1;
         if (a[mid] <= key) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
 
-__device__ int64_t batch_of_group(const int32_t* meta, const Params& p, int64_t g)
-{
-    // largest b whose first group index <= g (batch entries are kBatchWords apart)
-    int64_t lo = 0, hi = p.batch - 1;
-    const int32_t* be = meta + p.meta.batch_off;
-    while (lo < hi) {
-        int64_t mid = (lo + hi + 1) >> 1;
-        if (be[mid * kBatchWords + kBeGroupBase] <= g) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
+constexpr int kSmemBatch = 2048;     // batches whose fields are staged in shared memory
+constexpr int kSmemGroups = 16384;   // groups whose tile prefix is staged in shared memory
+constexpr int kMetaSmemBytes = (5 * kSmemBatch + kSmemGroups + 1) * 4;
 
 __global__ void __launch_bounds__(kMetaThreads, 1)
     metadata_kernel(Params p, const int32_t* __restrict__ seq_lens_q,
                     const int32_t* __restrict__ seq_lens_k, int32_t* __restrict__ meta, int G)
 {
+    extern __shared__ int32_t msm[];
     __shared__ int64_t scan_sh[32];
     __shared__ uint32_t s_err;
     __shared__ int s_tnd_bad;
-    __shared__ int64_t s_total;
     const int tid = threadIdx.x;
     int32_t* be = meta + p.meta.batch_off;
     int32_t* cta_off = meta + p.meta.cta_off;
-    int32_t* gpre = meta + p.meta.group_off;
     int32_t* units = meta + p.meta.unit_off;
+    // per-batch fields and the group prefix live in shared memory when they fit, else they are
+    // read back from their home in the metadata buffer
+    const bool sb = p.batch <= kSmemBatch;
+    const bool sg = p.meta.max_groups <= kSmemGroups;
+    const View v_sq = sb ? View{msm, 1} : View{be + kBeSq, kBatchWords};
+    const View v_sk = sb ? View{msm + kSmemBatch, 1} : View{be + kBeSk, kBatchWords};
+    const View v_lc = sb ? View{msm + 2 * kSmemBatch, 1} : View{be + kBeLc, kBatchWords};
+    const View v_gb = sb ? View{msm + 3 * kSmemBatch, 1} : View{be + kBeGroupBase, kBatchWords};
+    const View v_ok = sb ? View{msm + 4 * kSmemBatch, 1} : View{be + kBeOk, kBatchWords};
+    const View v_gp = sg ? View{msm + 5 * kSmemBatch, 1} : View{meta + p.meta.group_off, 1};
+    int32_t* gpre_home = meta + p.meta.group_off;
     if (tid == 0) { s_err = 0; s_tnd_bad = 0; }
     __syncthreads();
 
@@ -92,19 +101,19 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
         bool ok = true;
         if (!p.layout_tnd) {
             first = (int64_t)b * p.s1;
-            int64_t v = seq_lens_q ? seq_lens_q[b] : p.s1;
+            const int64_t v = seq_lens_q ? seq_lens_q[b] : p.s1;
             ok = v >= 0 && v <= p.s1;
             sq = ok ? v : 0;
         } else {
-            int64_t lo = b > 0 ? seq_lens_q[b - 1] : 0, hi = seq_lens_q[b];
+            const int64_t lo = b > 0 ? seq_lens_q[b - 1] : 0, hi = seq_lens_q[b];
             ok = lo >= 0 && hi >= lo && hi <= p.total_q;
             if (!ok) atomicOr(&s_tnd_bad, 1);
             first = lo < 0 ? 0 : lo;
             sq = ok ? hi - lo : 0;
         }
-        int64_t sk = seq_lens_k[b];
+        const int64_t sk = seq_lens_k[b];
         ok = ok && sk >= 0 && sk <= p.max_seqlen_k;
-        int64_t lc = ok ? compressed_keys(sk, p.cmp_ratio) : 0;
+        const int64_t lc = ok ? compressed_keys(sk, p.cmp_ratio) : 0;
         ok = ok && lc <= (int64_t)p.max_blocks_per_seq * p.block_size;
         if (!ok) atomicOr(&s_err, kErrLength);
         int32_t* e = be + (int64_t)b * kBatchWords;
@@ -113,23 +122,32 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
         e[kBeLc] = (int32_t)lc;
         e[kBeFirstRow] = (int32_t)first;
         e[kBeOk] = ok ? 1 : 0;
+        if (sb) {
+            v_sq[b] = (int32_t)sq;
+            v_sk[b] = (int32_t)(ok ? sk : 0);
+            v_lc[b] = (int32_t)lc;
+            v_ok[b] = ok ? 1 : 0;
+        }
     }
     __syncthreads();
 
     // ---- query groups per batch (bad TND prefix sums invalidate every batch) and their prefix
     int64_t running = 0;
     for (int base = 0; base < p.batch; base += blockDim.x) {
-        int b = base + tid;
+        const int b = base + tid;
         int64_t groups = 0;
         if (b < p.batch) {
             int32_t* e = be + (int64_t)b * kBatchWords;
             if (s_tnd_bad) e[kBeOk] = 0;
-            groups = e[kBeOk] ? ceil_div64(e[kBeSq], kGroupTokens) : 0;
+            groups = (!s_tnd_bad && v_ok[b]) ? (v_sq[b] + kGroupTokens - 1) / kGroupTokens : 0;
             e[kBeGroups] = (int32_t)groups;
         }
         int64_t tot;
-        int64_t ex = block_exclusive_scan(groups, &tot, scan_sh);
-        if (b < p.batch) be[(int64_t)b * kBatchWords + kBeGroupBase] = (int32_t)(running + ex);
+        const int64_t ex = block_exclusive_scan(groups, &tot, scan_sh);
+        if (b < p.batch) {
+            be[(int64_t)b * kBatchWords + kBeGroupBase] = (int32_t)(running + ex);
+            if (sb) v_gb[b] = (int32_t)(running + ex);
+        }
         running += tot;
     }
     const int64_t total_groups = running;
@@ -138,52 +156,59 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     // ---- tiles per group, then their exclusive prefix (gpre[g]; gpre[total_groups] = total)
     running = 0;
     for (int64_t base = 0; base < total_groups; base += blockDim.x) {
-        int64_t g = base + tid;
+        const int64_t g = base + tid;
         int64_t tiles = 0;
         if (g < total_groups) {
-            int64_t b = batch_of_group(meta, p, g);
-            const int32_t* e = be + b * kBatchWords;
-            int64_t r0 = (g - e[kBeGroupBase]) * kGroupTokens;
-            int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)e[kBeSq]) - 1;
-            int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], e[kBeLc], rl);
+            const int64_t b = upper_index(v_gb, p.batch, g);
+            const int64_t r0 = (g - v_gb[b]) * kGroupTokens;
+            const int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)v_sq[b]) - 1;
+            const int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl);
             tiles = ceil_div64(n, kTileKeys);
         }
         int64_t tot;
-        int64_t ex = block_exclusive_scan(tiles, &tot, scan_sh);
-        if (g < total_groups) gpre[g] = (int32_t)(running + ex);
+        const int64_t ex = block_exclusive_scan(tiles, &tot, scan_sh);
+        if (g < total_groups) {
+            v_gp[g] = (int32_t)(running + ex);
+            if (sg) gpre_home[g] = (int32_t)(running + ex);
+        }
         running += tot;
     }
     const int64_t T = running;
-    if (tid == 0) gpre[total_groups] = (int32_t)T;
+    if (tid == 0) {
+        v_gp[total_groups] = (int32_t)T;
+        if (sg) gpre_home[total_groups] = (int32_t)T;
+    }
     __syncthreads();
 
     // ---- split the tile sequence over G CTAs: count units per CTA, scan, then write them
     running = 0;
     for (int cbase = 0; cbase <= G; cbase += blockDim.x) {
-        int c = cbase + tid;
+        const int c = cbase + tid;
         int64_t cnt = 0;
+        int64_t t0 = 0, t1 = 0, g0 = 0;
         if (c < G && T > 0 && total_groups > 0) {
-            int64_t t0 = (T * c) / G, t1 = (T * (c + 1)) / G;
+            t0 = (T * c) / G;
+            t1 = (T * (c + 1)) / G;
             if (t1 > t0) {
-                for (int64_t g = upper_index(gpre, total_groups, t0); g < total_groups && gpre[g] < t1; ++g)
-                    if (gpre[g + 1] > gpre[g]) ++cnt;
+                g0 = upper_index(v_gp, total_groups, t0);
+                for (int64_t g = g0; g < total_groups && v_gp[g] < t1; ++g)
+                    if (v_gp[g + 1] > v_gp[g]) ++cnt;
             }
         }
         int64_t tot;
-        int64_t ex = block_exclusive_scan(cnt, &tot, scan_sh);
+        const int64_t ex = block_exclusive_scan(cnt, &tot, scan_sh);
         if (c <= G) cta_off[c] = (int32_t)(running + ex);
-        if (c < G && cnt > 0) {
-            int64_t t0 = (T * c) / G, t1 = (T * (c + 1)) / G;
+        if (cnt > 0) {
             int64_t u = running + ex;
-            for (int64_t g = upper_index(gpre, total_groups, t0); g < total_groups && gpre[g] < t1; ++g) {
-                if (gpre[g + 1] <= gpre[g]) continue;
-                int64_t b = batch_of_group(meta, p, g);
-                const int32_t* e = be + b * kBatchWords;
-                int64_t r0 = (g - e[kBeGroupBase]) * kGroupTokens;
-                int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)e[kBeSq]) - 1;
-                int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], e[kBeLc], rl);
-                int64_t tb = max(t0, (int64_t)gpre[g]) - gpre[g];
-                int64_t te = min(t1, (int64_t)gpre[g + 1]) - gpre[g];
+            for (int64_t g = g0; g < total_groups && v_gp[g] < t1; ++g) {
+                const int64_t gs = v_gp[g], ge = v_gp[g + 1];
+                if (ge <= gs) continue;
+                const int64_t b = upper_index(v_gb, p.batch, g);
+                const int64_t r0 = (g - v_gb[b]) * kGroupTokens;
+                const int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)v_sq[b]) - 1;
+                const int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl);
+                const int64_t tb = max(t0, gs) - gs;
+                const int64_t te = min(t1, ge) - gs;
                 int32_t* w = units + u * kUnitWords;
                 w[0] = (int32_t)b;
                 w[1] = (int32_t)r0;
@@ -214,7 +239,10 @@ cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const in
                             int32_t* meta, int num_sms, cudaStream_t st)
 {
     int G = num_sms < kMaxCtas ? num_sms : kMaxCtas;
-    metadata_kernel<<<1, kMetaThreads, 0, st>>>(p, seq_lens_q, seq_lens_k, meta, G);
+    cudaError_t e = cudaFuncSetAttribute(metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kMetaSmemBytes);
+    if (e != cudaSuccess) return e;
+    metadata_kernel<<<1, kMetaThreads, kMetaSmemBytes, st>>>(p, seq_lens_q, seq_lens_k, meta, G);
     return cudaGetLastError();
 }
 

@@ -4,24 +4,32 @@
 //
 // One persistent CTA per SM walks the units the metadata assigned to it.  A unit is a query group
 // (up to kGroupTokens tokens of one batch, 64 heads each) and a range of its compressed keys, cut
-// into tiles of 128 keys.  Per tile:
+// into tiles of 128 keys.  Eighteen warps, four roles, connected by mbarriers (the converter and
+// epilogue roles each have two groups of four warps that take alternate tiles):
 //
-//   producer warp   TMA-loads the tile's key rows (128 B each, 128-byte swizzle) and their scales
-//                   from the pages the block_table names into a ring of shared-memory stages;
-//   4 convert warps one thread per key: read the row, convert int8 / e4m3 to fp16 exactly and
-//                   store it into tensor memory as the MMA's A operand (key = TMEM lane);
-//   MMA thread      D[128 keys x 64*tokens] = K_tile[128 x 128] . Q_group^T with tcgen05 kind::f16
-//                   (A from tensor memory, B = the group's fp16 query rows in shared memory, fp32
-//                   accumulation: int8 products and sums are integers below 2^21, exact in fp32);
-//   4 convert warps (epilogue, one tile behind) read their key's row of D and form
-//                   score = sK * sum_h (W[h]*|sQ[h]|) * relu_or_min(dot'_h), where dot' uses the
-//                   query head negated when sQ[h] < 0 -- algebraically the README's
-//                   sum_h W[h] * ReLU(sQ[h] * sK * dot_h) -- then write it as an order-preserving
-//                   uint32 into the row's score line if the key is visible under the mask.
+//   producer warp    per unit: bulk-copies the group's query codes, weights and query scales;
+//                    per tile: TMA-loads the 128 key rows (128 B each, 128-byte swizzle) from the
+//                    pages the block_table names into a 6-stage ring, and bulk-copies their scales
+//                    into an 8-slot scale ring (own barriers: the epilogue releases those slots);
+//   converter warps  (4) per unit: fold W * |sQ|, convert the query codes to fp16 (negating heads
+//                    with sQ < 0) into the MMA's B operand (K-major, 128-byte swizzle);
+//                    per tile: one thread per key reads its row, converts int8 / e4m3 to fp16
+//                    exactly and stores it into tensor memory as the MMA's A operand (key = TMEM
+//                    lane), 2 A buffers per group; the query group is converted by the group
+//                    whose parity matches the unit's;
+//   MMA thread       D[128 keys x 64*tokens] = K_tile[128 x 128] . Q_group^T, tcgen05 kind::f16,
+//                    A from tensor memory, B from shared memory, fp32 accumulation (int8 products
+//                    and sums are integers below 2^21: exact), 1 D buffer per epilogue group;
+//   epilogue warps   (4) one thread per key reads its row of D and forms
+//                    score = sK * sum_h (W[h]*|sQ[h]|) * relu_or_min(dot'_h), where dot' uses the
+//                    negated query head when sQ[h] < 0 -- algebraically the README's
+//                    sum_h W[h] * ReLU(sQ[h] * sK * dot_h) -- and writes it as an order-preserving
+//                    uint32 into the row's score line when the key is visible under the mask.
 //
-// Tensor memory: A operand double-buffered in columns [0, 128), D double-buffered in [128, 384).
-// Every wait is bounded (about two seconds of wall time); on expiry the kernel records
-// kErrTimeout, raises a CTA-wide abort flag and drains out instead of hanging.
+// Tensor memory: A buffers in columns [0, 256), D buffers in [256, 512).  Each role is its own
+// non-inlined function so that its registers are allocated for it alone.  Every wait is bounded
+// (about two seconds of wall time); on expiry the kernel records kErrTimeout, raises a CTA-wide
+// abort flag and drains out instead of hanging.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -32,34 +40,52 @@ namespace qli {
 
 namespace {
 
-constexpr int kStages = 4;                       // key ring depth
-constexpr int kConvThreads = 128;                // 4 warps, one key (TMEM lane) per thread
-constexpr int kThreads = kConvThreads + 64;      // + producer warp + MMA warp
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kStages = 6;                       // key ring depth
+constexpr int kScaleSlots = 8;                   // scale ring depth (released by the epilogue)
+constexpr int kGroups = 2;                       // converter and epilogue groups; tile i -> i % 2
+constexpr int kNumA = 4;                         // A buffers in tensor memory (2 per group)
+constexpr int kNumD = 2;                         // D buffers in tensor memory (1 per group)
+constexpr int kGroupThreads = 128;               // 4 warps, one key (TMEM lane) per thread
+constexpr int kConvWarp0 = 0;                    // converter group g: warps 4g .. 4g+3
+constexpr int kEpiWarp0 = 8;                     // epilogue group g: warps 8+4g .. 11+4g
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 576;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol0 = 0;                   // A buffers: 64 columns each (128 fp16 per lane)
-constexpr uint32_t kDcol0 = 128;                 // D buffers: 128 columns each (2 tokens x 64)
+constexpr uint32_t kDcol0 = kNumA * 64;          // D buffers: 128 columns each (2 tokens x 64)
 
 constexpr int kQbufBytes = kGroupTokens * kHeads * kDim * 2;   // fp16 B operand, 32 KB
 constexpr int kKstageBytes = kTileKeys * kDim;                 // 16 KB of key codes
-constexpr int kSstageBytes = kTileKeys * 4;                    // scales (fp32 max)
+constexpr int kSslotBytes = kTileKeys * 4;                     // scales (fp32 max)
 constexpr int kQrawBytes = kGroupTokens * kHeads * kDim;       // 16 KB of query codes
 constexpr int kVecRawBytes = kGroupTokens * kHeads * 4;        // weights / q_scale (fp32 max)
 
 // shared memory carve-up (offsets from a 1024-aligned base)
 constexpr int kOffQbuf = 0;                                        // 2 x 32 KB
 constexpr int kOffKring = kOffQbuf + 2 * kQbufBytes;               // kStages x 16 KB
-constexpr int kOffSring = kOffKring + kStages * kKstageBytes;      // kStages x 512 B
-constexpr int kOffQraw = kOffSring + kStages * kSstageBytes;       // 2 x 16 KB
+constexpr int kOffSring = kOffKring + kStages * kKstageBytes;      // kScaleSlots x 512 B
+constexpr int kOffQraw = kOffSring + kScaleSlots * kSslotBytes;    // 2 x 16 KB
 constexpr int kOffWraw = kOffQraw + 2 * kQrawBytes;                // 2 x 512 B
 constexpr int kOffSQraw = kOffWraw + 2 * kVecRawBytes;             // 2 x 512 B
 constexpr int kOffWq = kOffSQraw + 2 * kVecRawBytes;               // 2 x 128 floats
 constexpr int kOffSign = kOffWq + 2 * kGroupTokens * kHeads * 4;   // 2 x 128 words
 constexpr int kOffBars = kOffSign + 2 * kGroupTokens * kHeads * 4;
-enum { kBarKfull = 0, kBarKempty = kStages, kBarQrfull = 2 * kStages, kBarQrempty = kBarQrfull + 2,
-       kBarQfull = kBarQrempty + 2, kBarAfull = kBarQfull + 2, kBarDfull = kBarAfull + 2,
-       kBarDempty = kBarDfull + 2, kNumBars = kBarDempty + 2 };
+enum {
+    kBarKfull = 0,
+    kBarKempty = kBarKfull + kStages,
+    kBarSfull = kBarKempty + kStages,
+    kBarSempty = kBarSfull + kScaleSlots,
+    kBarQrfull = kBarSempty + kScaleSlots,
+    kBarQrempty = kBarQrfull + 2,
+    kBarQfull = kBarQrempty + 2,
+    kBarQempty = kBarQfull + 2,
+    kBarAfull = kBarQempty + 2,
+    kBarAempty = kBarAfull + kNumA,
+    kBarDfull = kBarAempty + kNumA,
+    kBarDempty = kBarDfull + kNumD,
+    kNumBars = kBarDempty + kNumD
+};
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;   // + slack to align the base to 1024
 
@@ -84,26 +110,39 @@ struct Shared {
     volatile int* abort;
 };
 
-// Bounded mbarrier wait: false when the CTA must abort (this wait expired or another did).
+extern __shared__ uint8_t smem_raw[];
+
+// The CTA's shared-memory carve-up, rebuilt from the dynamic shared memory symbol (cheaper than
+// passing it between non-inlined functions through local memory)
+__device__ __forceinline__ Shared shared_view()
+{
+    Shared S;
+    S.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    S.bars = reinterpret_cast<uint64_t*>(S.base + kOffBars);
+    S.tmem_slot = reinterpret_cast<uint32_t*>(S.base + kOffMisc);
+    S.abort = reinterpret_cast<volatile int*>(S.base + kOffMisc + 8);
+    return S;
+}
+
+// Bounded mbarrier wait: false when the CTA must abort (this wait expired or another did).  Each
+// test lets the thread sleep up to 100 us until the phase completes.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
                                          uint32_t* err)
 {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (*abort) return false;
-            if (ptx::globaltimer() - t0 > kWaitLimitNs) {
-                *abort = 1;
-                atomicOr(err, kErrTimeout);
-                return false;
-            }
+    for (;;) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        if (*abort) return false;
+        if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            atomicOr(err, kErrTimeout);
+            return false;
         }
     }
 }
 
-__device__ __forceinline__ float load_scale(const uint8_t* base, int64_t i, bool f32)
+__device__ __forceinline__ float load_scale(const uint8_t* base, int i, bool f32)
 {
     if (f32) return reinterpret_cast<const float*>(base)[i];
     return __half2float(reinterpret_cast<const __half*>(base)[i]);
@@ -113,13 +152,14 @@ __device__ __forceinline__ float load_scale(const uint8_t* base, int64_t i, bool
 __device__ __forceinline__ uint32_t ordered_code(float s)
 {
     if (s == 0.0f) s = 0.0f;
-    uint32_t u = __float_as_uint(s);
+    const uint32_t u = __float_as_uint(s);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 struct Unit {
     int32_t b, r0, kb, ke;
     int32_t q_cnt, row0, sq, sk, lc;
+    int32_t ntiles;
 };
 
 __device__ __forceinline__ Unit read_unit(const ScoreArgs& a, int64_t u)
@@ -136,21 +176,22 @@ __device__ __forceinline__ Unit read_unit(const ScoreArgs& a, int64_t u)
     x.lc = e[kBeLc];
     x.row0 = e[kBeFirstRow] + x.r0;
     x.q_cnt = min(kGroupTokens, x.sq - x.r0);
+    x.ntiles = (x.ke - x.kb + kTileKeys - 1) / kTileKeys;
     return x;
 }
 
 // ------------------------------------------------------------------------------------------------
-// Producer warp: query rows (bulk copies) and key tiles (tensor TMA + scale bulk copies)
+// Producer warp
 // ------------------------------------------------------------------------------------------------
 template <bool kScaleF32>
-__device__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, const Shared& S, int64_t ubeg,
-                         int64_t uend)
+__device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, int64_t ubeg, int64_t uend)
 {
+    const Shared S = shared_view();
     const int lane = threadIdx.x & 31;
     const Params& p = a.p;
     constexpr int esz = kScaleF32 ? 4 : 2;
-    const int R = p.box_rows;
-    const int cpt = kTileKeys / R;            // chunks (TMA boxes) per tile
+    const int R = p.box_rows;             // keys per TMA box; divides block_size and 128
+    const int bs = p.block_size;
     uint32_t tile_i = 0;
     for (int64_t u = ubeg; u < uend; ++u) {
         const int uu = (int)(u - ubeg);
@@ -169,42 +210,52 @@ __device__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, const Shar
             ptx::bulk_load(S.base + kOffSQraw + qb * kVecRawBytes,
                            a.q_scale + (int64_t)x.row0 * kHeads * esz, vbytes, bar);
         }
-        // key chunks of this unit: chunk c covers keys [kb + c*R, kb + (c+1)*R), inside one page
-        const int64_t nchunks = ceil_div64(x.ke - x.kb, R);
+        // logical page / slot of the current chunk, advanced without division; the block_table
+        // entries of 32 consecutive logical pages sit one per lane (cur), the next 32 in nxt
         const int32_t* table = a.block_table + (int64_t)x.b * p.max_blocks_per_seq;
-        auto page_of = [&](int64_t c) -> int32_t {
-            if (c >= nchunks) return 0;
-            return __ldg(table + (x.kb + c * R) / p.block_size);
-        };
-        int32_t cur = page_of(lane), nxt = page_of(32 + lane);
-        const int ntiles = (int)ceil_div64(x.ke - x.kb, kTileKeys);
-        for (int t = 0; t < ntiles; ++t, ++tile_i) {
+        const int lp_end = (x.ke + bs - 1) / bs;
+        int lp = x.kb / bs;
+        int slot = x.kb - lp * bs;
+        int wbase = lp;
+        int32_t cur = (wbase + lane < lp_end) ? __ldg(table + wbase + lane) : 0;
+        int32_t nxt = (wbase + 32 + lane < lp_end) ? __ldg(table + wbase + 32 + lane) : 0;
+        int key = x.kb;
+        for (int t = 0; t < x.ntiles; ++t, ++tile_i) {
             const int s = tile_i % kStages;
+            const int ss = tile_i % kScaleSlots;
             if (!wait_bar(&S.bars[kBarKempty + s], ((tile_i / kStages) & 1) ^ 1, S.abort, a.err)) return;
-            const int64_t c0 = (int64_t)t * cpt;
-            const int64_t c1 = min((int64_t)(c0 + cpt), nchunks);
+            if (!wait_bar(&S.bars[kBarSempty + ss], ((tile_i / kScaleSlots) & 1) ^ 1, S.abort, a.err)) return;
+            const int tile_end = min(x.kb + (t + 1) * kTileKeys, x.ke);
+            const int nchunks = (tile_end - key + R - 1) / R;
             uint64_t* bar = &S.bars[kBarKfull + s];
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(bar, (uint32_t)((c1 - c0) * R * (kDim + esz)));
-            for (int64_t c = c0; c < c1; ++c) {
-                if ((c & 31) == 0 && c > 0) {   // next window of 32 chunk pages
+            uint64_t* sbar = &S.bars[kBarSfull + ss];
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nchunks * R * kDim));
+                ptx::mbar_arrive_expect_tx(sbar, (uint32_t)(nchunks * R * esz));
+            }
+            for (int c = 0; c < nchunks; ++c) {
+                if (lp - wbase >= 32) {     // slide the page window by 32
+                    wbase += 32;
                     cur = nxt;
-                    nxt = page_of(c + 32 + lane);
+                    nxt = (wbase + 32 + lane < lp_end) ? __ldg(table + wbase + 32 + lane) : 0;
                 }
-                int32_t page = __shfl_sync(0xffffffffu, cur, (int)(c & 31));
+                int32_t page = __shfl_sync(0xffffffffu, cur, lp - wbase);
                 if (lane == 0) {
                     if (page < 0 || page >= p.num_blocks) {
                         atomicOr(a.err, kErrPage);
                         page = 0;
                     }
-                    const int64_t key0 = x.kb + c * R;
-                    const int64_t slot = key0 % p.block_size;
-                    const int64_t prow = (int64_t)page * p.block_size + slot;
-                    const int r_in_tile = (int)(c - c0) * R;
-                    ptx::tma_load_2d(S.base + kOffKring + s * kKstageBytes + r_in_tile * kDim, tmap,
-                                     0, (int32_t)prow, bar);
-                    ptx::bulk_load(S.base + kOffSring + s * kSstageBytes + r_in_tile * esz,
-                                   a.k_scale + prow * esz, (uint32_t)(R * esz), bar);
+                    const int64_t prow = (int64_t)page * bs + slot;
+                    ptx::tma_load_2d(S.base + kOffKring + s * kKstageBytes + c * R * kDim, tmap, 0,
+                                     (int32_t)prow, bar);
+                    ptx::bulk_load(S.base + kOffSring + ss * kSslotBytes + c * R * esz,
+                                   a.k_scale + prow * esz, (uint32_t)(R * esz), sbar);
+                }
+                key += R;
+                slot += R;
+                if (slot == bs) {
+                    slot = 0;
+                    ++lp;
                 }
             }
             __syncwarp();
@@ -215,9 +266,9 @@ __device__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, const Shar
 // ------------------------------------------------------------------------------------------------
 // MMA thread
 // ------------------------------------------------------------------------------------------------
-__device__ void mma_issuer(const ScoreArgs& a, const Shared& S, uint32_t tmem, int64_t ubeg,
-                           int64_t uend)
+__device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
 {
+    const Shared S = shared_view();
     uint32_t tile_i = 0;
     for (int64_t u = ubeg; u < uend; ++u) {
         const int uu = (int)(u - ubeg);
@@ -227,159 +278,112 @@ __device__ void mma_issuer(const ScoreArgs& a, const Shared& S, uint32_t tmem, i
         const uint32_t n = kHeads * x.q_cnt;
         const uint32_t idesc = ptx::idesc_f16_f32(128, n);
         const uint32_t qaddr = ptx::smem_addr(S.base + kOffQbuf + qb * kQbufBytes);
-        const int ntiles = (int)ceil_div64(x.ke - x.kb, kTileKeys);
-        for (int t = 0; t < ntiles; ++t, ++tile_i) {
-            const uint32_t ab = tile_i & 1, v = tile_i >> 1;
-            if (!wait_bar(&S.bars[kBarAfull + ab], v & 1, S.abort, a.err)) return;
-            if (!wait_bar(&S.bars[kBarDempty + ab], (v & 1) ^ 1, S.abort, a.err)) return;
+        for (int t = 0; t < x.ntiles; ++t, ++tile_i) {
+            const uint32_t ab = tile_i % kNumA, db = tile_i % kNumD;
+            if (!wait_bar(&S.bars[kBarAfull + ab], (tile_i / kNumA) & 1, S.abort, a.err)) return;
+            if (!wait_bar(&S.bars[kBarDempty + db], ((tile_i / kNumD) & 1) ^ 1, S.abort, a.err)) return;
             ptx::tc_fence_after();
-            const uint32_t d_t = tmem + kDcol0 + ab * 128;
+            const uint32_t d_t = tmem + kDcol0 + db * 128;
             const uint32_t a_t = tmem + kAcol0 + ab * 64;
 #pragma unroll
             for (int kk = 0; kk < kDim / 16; ++kk) {
-                // K step of 16 fp16 = 32 bytes inside a 128-byte swizzle row; the second half of
-                // K (dims 64..127) sits in the second block of n rows
+                // K step of 16 fp16 = 32 bytes inside a 128-byte swizzle row; dims 64..127 sit in
+                // the second block of n rows
                 const uint32_t baddr = qaddr + (kk >> 2) * (n * 128) + (kk & 3) * 32;
                 ptx::mma_f16_ts(d_t, a_t + kk * 8, ptx::sdesc_kmajor_sw128(baddr), idesc, kk > 0);
             }
-            ptx::mma_commit(&S.bars[kBarDfull + ab]);
+            ptx::mma_commit(&S.bars[kBarDfull + db]);
+            ptx::mma_commit(&S.bars[kBarAempty + ab]);
         }
     }
 }
 
 // ------------------------------------------------------------------------------------------------
-// Convert + epilogue warps
+// Converter warps: query group -> B operand; key tiles -> A operand in tensor memory
 // ------------------------------------------------------------------------------------------------
-struct TileCtx {
-    uint32_t tile_i;
-    int32_t qb, q_cnt, row0, r0, sq, sk, lc, kend, key0;
-    float sk_scale;
-};
-
-template <bool kScaleF32>
-__device__ bool epilogue(const ScoreArgs& a, const Shared& S, uint32_t tmem, const TileCtx& c)
-{
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const uint32_t ab = c.tile_i & 1, v = c.tile_i >> 1;
-    if (!wait_bar(&S.bars[kBarDfull + ab], v & 1, S.abort, a.err)) return false;
-    ptx::tc_fence_after();
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const float* wq = reinterpret_cast<const float*>(S.base + kOffWq) + c.qb * kGroupTokens * kHeads;
-    const int64_t j = c.key0 + tid;
-    const Params& p = a.p;
-    float score[kGroupTokens];
-#pragma unroll
-    for (int tt = 0; tt < kGroupTokens; ++tt) {
-        score[tt] = 0.0f;
-        if (tt < c.q_cnt) {
-            uint32_t d[64];
-            const uint32_t taddr = tmem + lane_base + kDcol0 + ab * 128 + tt * 64;
-            QLI_TMEM_LD_X32(taddr, d);
-            QLI_TMEM_LD_X32(taddr + 32, (d + 32));
-            ptx::tmem_wait_ld();
-            float acc = 0.0f;
-            const float* w = wq + tt * kHeads;
-            if (c.sk_scale >= 0.0f) {
-#pragma unroll
-                for (int h = 0; h < kHeads; ++h) acc = fmaf(w[h], fmaxf(__uint_as_float(d[h]), 0.0f), acc);
-            } else {
-#pragma unroll
-                for (int h = 0; h < kHeads; ++h) acc = fmaf(w[h], fminf(__uint_as_float(d[h]), 0.0f), acc);
-            }
-            score[tt] = c.sk_scale * acc;
-        }
-    }
-    ptx::tc_fence_before();
-    __syncwarp();
-    if ((tid & 31) == 0) ptx::mbar_arrive(&S.bars[kBarDempty + ab]);
-#pragma unroll
-    for (int tt = 0; tt < kGroupTokens; ++tt) {
-        if (tt < c.q_cnt) {
-            const int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, c.sq, c.sk, c.lc, c.r0 + tt);
-            if (j < n && j < c.kend)
-                a.scores[(int64_t)(c.row0 + tt) * p.ld + j] = ordered_code(score[tt]);
-        }
-    }
-    return true;
-}
-
 template <bool kFp8, bool kScaleF32>
-__device__ void converter(const ScoreArgs& a, const Shared& S, uint32_t tmem, int64_t ubeg,
-                          int64_t uend)
+__device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
 {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Shared S = shared_view();
+    const int gtid = threadIdx.x - kConvWarp0 * 32;
+    const int grp = gtid / kGroupThreads;
+    const int tid = gtid % kGroupThreads, lane = tid & 31, warp = tid >> 5;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     uint32_t tile_i = 0;
-    TileCtx prev;
-    bool have_prev = false;
     for (int64_t u = ubeg; u < uend; ++u) {
         const int uu = (int)(u - ubeg);
         const Unit x = read_unit(a, u);
         const int qb = uu & 1;
-        if (!wait_bar(&S.bars[kBarQrfull + qb], (uu >> 1) & 1, S.abort, a.err)) return;
-        // weights folded with |sQ|; heads with sQ < 0 get their query row negated instead
-        float* wq = reinterpret_cast<float*>(S.base + kOffWq) + qb * kGroupTokens * kHeads;
-        uint32_t* sgn = reinterpret_cast<uint32_t*>(S.base + kOffSign) + qb * kGroupTokens * kHeads;
-        const uint8_t* wraw = S.base + kOffWraw + qb * kVecRawBytes;
-        const uint8_t* sqraw = S.base + kOffSQraw + qb * kVecRawBytes;
-        if (tid < x.q_cnt * kHeads) {
-            const float w = load_scale(wraw, tid, kScaleF32);
-            const float sq = load_scale(sqraw, tid, kScaleF32);
-            wq[tid] = w * fabsf(sq);
-            sgn[tid] = sq < 0.0f ? 0x80008000u : 0u;
-        }
-        ptx::named_bar_sync(1, kConvThreads);
-        // query codes -> fp16 B operand: row n = token*64 + head, K-major, 128-byte swizzle, the
-        // K halves [0,64) and [64,128) in two blocks of n rows
-        const int nrows = x.q_cnt * kHeads;
-        const uint8_t* qraw = S.base + kOffQraw + qb * kQrawBytes;
-        uint8_t* qbuf = S.base + kOffQbuf + qb * kQbufBytes;
-        for (int item = tid; item < nrows * 8; item += kConvThreads) {
-            const int n = item >> 3, c16 = item & 7;   // 16 codes = dims [16*c16, 16*c16 + 16)
-            const uint4 raw = *reinterpret_cast<const uint4*>(qraw + n * kDim + c16 * 16);
-            const uint32_t neg = sgn[n];
-            uint32_t h[8];
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (kFp8) ptx::e4m3x4_to_f16x4(wv[q], h[2 * q], h[2 * q + 1]);
-                else ptx::int8x4_to_f16x4(wv[q], h[2 * q], h[2 * q + 1]);
-                h[2 * q] ^= neg;
-                h[2 * q + 1] ^= neg;
+        if (qb == grp) {
+            if (!wait_bar(&S.bars[kBarQrfull + qb], (uu >> 1) & 1, S.abort, a.err)) return;
+            if (!wait_bar(&S.bars[kBarQempty + qb], ((uu >> 1) & 1) ^ 1, S.abort, a.err)) return;
+            // weights folded with |sQ|; heads with sQ < 0 get their query row negated instead
+            float* wq = reinterpret_cast<float*>(S.base + kOffWq) + qb * kGroupTokens * kHeads;
+            uint32_t* sgn = reinterpret_cast<uint32_t*>(S.base + kOffSign) + qb * kGroupTokens * kHeads;
+            const uint8_t* wraw = S.base + kOffWraw + qb * kVecRawBytes;
+            const uint8_t* sqraw = S.base + kOffSQraw + qb * kVecRawBytes;
+            if (tid < x.q_cnt * kHeads) {
+                const float w = load_scale(wraw, tid, kScaleF32);
+                const float sq = load_scale(sqraw, tid, kScaleF32);
+                wq[tid] = w * fabsf(sq);
+                sgn[tid] = sq < 0.0f ? 0x80008000u : 0u;
             }
-            const int blk = c16 >> 2;                   // which 64-dim half
-            const int ch = (c16 & 3) * 2;               // first 16-byte chunk within the 128-B row
-            uint8_t* row = qbuf + blk * (nrows * 128) + n * 128;
-            *reinterpret_cast<uint4*>(row + (((ch) ^ (n & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(row + (((ch + 1) ^ (n & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::named_bar_sync(1, kConvThreads);
-        if (lane == 0) {
-            ptx::mbar_arrive(&S.bars[kBarQfull + qb]);
-            ptx::mbar_arrive(&S.bars[kBarQrempty + qb]);
-        }
-        const int ntiles = (int)ceil_div64(x.ke - x.kb, kTileKeys);
-        for (int t = 0; t < ntiles; ++t, ++tile_i) {
-            const int s = tile_i % kStages;
-            if (!wait_bar(&S.bars[kBarKfull + s], (tile_i / kStages) & 1, S.abort, a.err)) return;
-            // this thread's key row: 8 chunks of 16 B, chunk c stored at c ^ (row & 7)
-            const uint8_t* krow = S.base + kOffKring + s * kKstageBytes + tid * kDim;
-            uint4 kr[8];
+            ptx::named_bar_sync(1 + grp, kGroupThreads);
+            // query codes -> fp16 B operand: row n = token*64 + head, K-major, 128-byte swizzle,
+            // the K halves [0,64) and [64,128) in two blocks of n rows
+            const int nrows = x.q_cnt * kHeads;
+            const uint8_t* qraw = S.base + kOffQraw + qb * kQrawBytes;
+            uint8_t* qbuf = S.base + kOffQbuf + qb * kQbufBytes;
+            for (int item = tid; item < nrows * 8; item += kGroupThreads) {
+                const int n = item >> 3, c16 = item & 7;   // 16 codes = dims [16*c16, 16*c16 + 16)
+                const uint4 raw = *reinterpret_cast<const uint4*>(qraw + n * kDim + c16 * 16);
+                const uint32_t neg = sgn[n];
+                uint32_t h[8];
+                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                kr[c] = *reinterpret_cast<const uint4*>(krow + ((c ^ (tid & 7)) << 4));
-            const float sk = load_scale(S.base + kOffSring + s * kSstageBytes, tid, kScaleF32);
+                for (int q = 0; q < 4; ++q) {
+                    if (kFp8) ptx::e4m3x4_to_f16x4(wv[q], h[2 * q], h[2 * q + 1]);
+                    else ptx::int8x4_to_f16x4(wv[q], h[2 * q], h[2 * q + 1]);
+                    h[2 * q] ^= neg;
+                    h[2 * q + 1] ^= neg;
+                }
+                const int blk = c16 >> 2;                   // which 64-dim half
+                const int ch = (c16 & 3) * 2;               // first 16-byte chunk in the 128-B row
+                uint8_t* row = qbuf + blk * (nrows * 128) + n * 128;
+                *reinterpret_cast<uint4*>(row + ((ch ^ (n & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(row + (((ch + 1) ^ (n & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+            }
+            ptx::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&S.bars[kBarKempty + s]);
-            const uint32_t ab = tile_i & 1;
-            uint32_t h[32];
+            if (lane == 0) {
+                ptx::mbar_arrive(&S.bars[kBarQfull + qb]);
+                ptx::mbar_arrive(&S.bars[kBarQrempty + qb]);
+            }
+        }
+        for (int t = 0; t < x.ntiles; ++t, ++tile_i) {
+            if ((int)(tile_i % kGroups) != grp) continue;
+            const int s = tile_i % kStages;
+            const uint32_t ab = tile_i % kNumA;
+            if (!wait_bar(&S.bars[kBarKfull + s], (tile_i / kStages) & 1, S.abort, a.err)) return;
+            // this thread's key row: 8 chunks of 16 B, chunk c stored at c ^ (row & 7); converted
+            // and stored to tensor memory one 64-dim half at a time
+            const uint8_t* krow = S.base + kOffKring + s * kKstageBytes + tid * kDim;
+            if (!wait_bar(&S.bars[kBarAempty + ab], ((tile_i / kNumA) & 1) ^ 1, S.abort, a.err)) return;
+            ptx::tc_fence_after();
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
+                uint4 kr[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    kr[c] = *reinterpret_cast<const uint4*>(krow + (((half * 4 + c) ^ (tid & 7)) << 4));
+                if (half == 1) {
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&S.bars[kBarKempty + s]);
+                }
+                uint32_t h[32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint4 r = kr[half * 4 + c];
-                    const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+                    const uint32_t wv[4] = {kr[c].x, kr[c].y, kr[c].z, kr[c].w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if (kFp8) ptx::e4m3x4_to_f16x4(wv[q], h[c * 8 + 2 * q], h[c * 8 + 2 * q + 1]);
@@ -392,34 +396,130 @@ __device__ void converter(const ScoreArgs& a, const Shared& S, uint32_t tmem, in
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&S.bars[kBarAfull + ab]);
-            if (have_prev && !epilogue<kScaleF32>(a, S, tmem, prev)) return;
-            prev.tile_i = tile_i;
-            prev.qb = qb;
-            prev.q_cnt = x.q_cnt;
-            prev.row0 = x.row0;
-            prev.r0 = x.r0;
-            prev.sq = x.sq;
-            prev.sk = x.sk;
-            prev.lc = x.lc;
-            prev.kend = x.ke;
-            prev.key0 = x.kb + t * kTileKeys;
-            prev.sk_scale = sk;
-            have_prev = true;
         }
     }
-    if (have_prev) epilogue<kScaleF32>(a, S, tmem, prev);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Epilogue warps
+// ------------------------------------------------------------------------------------------------
+template <bool kScaleF32>
+__device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
+{
+    const Shared S = shared_view();
+    const int gtid = threadIdx.x - kEpiWarp0 * 32;
+    const int grp = gtid / kGroupThreads;
+    const int tid = gtid % kGroupThreads, lane = tid & 31, warp = tid >> 5;
+    // a warp reaches the TMEM lanes of its warp index modulo 4; group warps are 4-aligned
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int key_lane = tid;
+    const Params& p = a.p;
+    uint32_t tile_i = 0;
+    for (int64_t u = ubeg; u < uend; ++u) {
+        const int uu = (int)(u - ubeg);
+        const Unit x = read_unit(a, u);
+        const int qb = uu & 1;
+        if (!wait_bar(&S.bars[kBarQfull + qb], (uu >> 1) & 1, S.abort, a.err)) return;
+        const float* wq = reinterpret_cast<const float*>(S.base + kOffWq) + qb * kGroupTokens * kHeads;
+        int32_t nvis[kGroupTokens];
+#pragma unroll
+        for (int tt = 0; tt < kGroupTokens; ++tt)
+            nvis[tt] = tt < x.q_cnt
+                           ? (int32_t)min((int64_t)x.ke, visible_keys(p.sparse_mode, p.cmp_ratio, x.sq, x.sk,
+                                                                      x.lc, x.r0 + tt))
+                           : 0;
+        for (int t = 0; t < x.ntiles; ++t, ++tile_i) {
+            if ((int)(tile_i % kGroups) != grp) continue;
+            const uint32_t db = tile_i % kNumD;
+            const int ss = tile_i % kScaleSlots;
+            if (!wait_bar(&S.bars[kBarDfull + db], (tile_i / kNumD) & 1, S.abort, a.err)) return;
+            ptx::tc_fence_after();
+            if (!wait_bar(&S.bars[kBarSfull + ss], (tile_i / kScaleSlots) & 1, S.abort, a.err)) return;
+            const float sk = load_scale(S.base + kOffSring + ss * kSslotBytes, key_lane, kScaleF32);
+            const int j = x.kb + t * kTileKeys + key_lane;
+            float score[kGroupTokens];
+#pragma unroll
+            for (int tt = 0; tt < kGroupTokens; ++tt) {
+                score[tt] = 0.0f;
+                if (tt < x.q_cnt) {
+                    const float4* w4 = reinterpret_cast<const float4*>(wq + tt * kHeads);
+                    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t d[32];
+                        QLI_TMEM_LD_X32(tmem + lane_base + kDcol0 + db * 128 + tt * 64 + half * 32, d);
+                        ptx::tmem_wait_ld();
+                        if (sk >= 0.0f) {
+#pragma unroll
+                            for (int h = 0; h < 32; h += 4) {
+                                const float4 w = w4[(half * 32 + h) >> 2];
+                                a0 = fmaf(w.x, fmaxf(__uint_as_float(d[h]), 0.0f), a0);
+                                a1 = fmaf(w.y, fmaxf(__uint_as_float(d[h + 1]), 0.0f), a1);
+                                a0 = fmaf(w.z, fmaxf(__uint_as_float(d[h + 2]), 0.0f), a0);
+                                a1 = fmaf(w.w, fmaxf(__uint_as_float(d[h + 3]), 0.0f), a1);
+                            }
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < 32; h += 4) {
+                                const float4 w = w4[(half * 32 + h) >> 2];
+                                a0 = fmaf(w.x, fminf(__uint_as_float(d[h]), 0.0f), a0);
+                                a1 = fmaf(w.y, fminf(__uint_as_float(d[h + 1]), 0.0f), a1);
+                                a0 = fmaf(w.z, fminf(__uint_as_float(d[h + 2]), 0.0f), a0);
+                                a1 = fmaf(w.w, fminf(__uint_as_float(d[h + 3]), 0.0f), a1);
+                            }
+                        }
+                    }
+                    score[tt] = sk * (a0 + a1);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(&S.bars[kBarDempty + db]);
+                ptx::mbar_arrive(&S.bars[kBarSempty + ss]);
+            }
+#pragma unroll
+            for (int tt = 0; tt < kGroupTokens; ++tt)
+                if (tt < x.q_cnt && j < nvis[tt])
+                    a.scores[(int64_t)(x.row0 + tt) * p.ld + j] = ordered_code(score[tt]);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&S.bars[kBarQempty + qb]);
+    }
+}
+
+__device__ void init_barriers(const Shared& S)
+{
+    for (int i = 0; i < kStages; ++i) {
+        ptx::mbar_init(&S.bars[kBarKfull + i], 1);
+        ptx::mbar_init(&S.bars[kBarKempty + i], 4);
+    }
+    for (int i = 0; i < kScaleSlots; ++i) {
+        ptx::mbar_init(&S.bars[kBarSfull + i], 1);
+        ptx::mbar_init(&S.bars[kBarSempty + i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+        ptx::mbar_init(&S.bars[kBarQrfull + i], 1);
+        ptx::mbar_init(&S.bars[kBarQrempty + i], 4);
+        ptx::mbar_init(&S.bars[kBarQfull + i], 4);
+        ptx::mbar_init(&S.bars[kBarQempty + i], 4 * kGroups);
+    }
+    for (int i = 0; i < kNumA; ++i) {
+        ptx::mbar_init(&S.bars[kBarAfull + i], 4);
+        ptx::mbar_init(&S.bars[kBarAempty + i], 1);
+    }
+    for (int i = 0; i < kNumD; ++i) {
+        ptx::mbar_init(&S.bars[kBarDfull + i], 1);
+        ptx::mbar_init(&S.bars[kBarDempty + i], 4);
+    }
+    ptx::fence_mbar_init();
 }
 
 template <bool kFp8, bool kScaleF32>
 __global__ void __launch_bounds__(kThreads, 1)
-    score_kernel(const __grid_constant__ CUtensorMap tmap, const ScoreArgs a)
+    score_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ ScoreArgs a)
 {
-    extern __shared__ uint8_t smem_raw[];
-    Shared S;
-    S.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    S.bars = reinterpret_cast<uint64_t*>(S.base + kOffBars);
-    S.tmem_slot = reinterpret_cast<uint32_t*>(S.base + kOffMisc);
-    S.abort = reinterpret_cast<volatile int*>(S.base + kOffMisc + 8);
+    const Shared S = shared_view();
     const int tid = threadIdx.x, warp = tid >> 5;
 
     // the metadata must have been written for this problem
@@ -432,20 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = meta[kMhCtas];
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            ptx::mbar_init(&S.bars[kBarKfull + i], 1);
-            ptx::mbar_init(&S.bars[kBarKempty + i], 4);
-        }
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&S.bars[kBarQrfull + i], 1);
-            ptx::mbar_init(&S.bars[kBarQrempty + i], 4);
-            ptx::mbar_init(&S.bars[kBarQfull + i], 4);
-            ptx::mbar_init(&S.bars[kBarAfull + i], 4);
-            ptx::mbar_init(&S.bars[kBarDfull + i], 1);
-            ptx::mbar_init(&S.bars[kBarDempty + i], 4);
-        }
+        init_barriers(S);
         *S.abort = 0;
-        ptx::fence_mbar_init();
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(S.tmem_slot, kTmemCols);
@@ -460,39 +548,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = blockIdx.x; c < G; c += gridDim.x) {
         const int64_t ubeg = meta[a.p.meta.cta_off + c];
         const int64_t uend = meta[a.p.meta.cta_off + c + 1];
-        if (uend <= ubeg) continue;
-        if (warp < 4) {
-            converter<kFp8, kScaleF32>(a, S, tmem, ubeg, uend);
-        } else if (warp == kProducerWarp) {
-            producer<kScaleF32>(&tmap, a, S, ubeg, uend);
-        } else if (tid == kMmaWarp * 32) {
-            mma_issuer(a, S, tmem, ubeg, uend);
+        if (uend > ubeg) {
+            if (warp < kEpiWarp0) converter<kFp8, kScaleF32>(a, tmem, ubeg, uend);
+            else if (warp < kProducerWarp) epilogue<kScaleF32>(a, tmem, ubeg, uend);
+            else if (warp == kProducerWarp) producer<kScaleF32>(&tmap, a, ubeg, uend);
+            else if (tid == kMmaWarp * 32) mma_issuer(a, tmem, ubeg, uend);
         }
-        // each CTA-list restarts the barrier phases: only one list per CTA unless the grid is
-        // smaller than the split, so re-initialise between lists
         ptx::tc_fence_before();
         __syncthreads();
         ptx::tc_fence_after();
+        if (*S.abort) break;
         if (c + (int)gridDim.x < G) {
+            // another list follows: restart every barrier's phase
             if (tid == 0) {
-                for (int i = 0; i < kNumBars; ++i) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(ptx::smem_addr(&S.bars[i])) : "memory");
-                for (int i = 0; i < kStages; ++i) {
-                    ptx::mbar_init(&S.bars[kBarKfull + i], 1);
-                    ptx::mbar_init(&S.bars[kBarKempty + i], 4);
-                }
-                for (int i = 0; i < 2; ++i) {
-                    ptx::mbar_init(&S.bars[kBarQrfull + i], 1);
-                    ptx::mbar_init(&S.bars[kBarQrempty + i], 4);
-                    ptx::mbar_init(&S.bars[kBarQfull + i], 4);
-                    ptx::mbar_init(&S.bars[kBarAfull + i], 4);
-                    ptx::mbar_init(&S.bars[kBarDfull + i], 1);
-                    ptx::mbar_init(&S.bars[kBarDempty + i], 4);
-                }
-                ptx::fence_mbar_init();
+                for (int i = 0; i < kNumBars; ++i)
+                    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(ptx::smem_addr(&S.bars[i])) : "memory");
+                init_barriers(S);
             }
             __syncthreads();
         }
-        if (*S.abort) break;
     }
     ptx::tc_fence_before();
     __syncthreads();

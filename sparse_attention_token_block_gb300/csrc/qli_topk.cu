@@ -1,24 +1,34 @@
-// qli_topk.cu -- per-row top-k over the score lines (README function section, step 3: "select the
-// top-k indices"; parameter table: sparse_count, sparse_indices).
+// qli_topk.cu -- per-row top-k over the score lines (README function section, step 3: select the
+// top-k indices; parameter table: sparse_count, sparse_indices).
 //
-// One CTA per output row.  Each visible key j of the row carries the 64-bit code
-//     (ordered(score_j) << 32) | (0xFFFFFFFF - j),
-// which is unique and orders keys by score descending, then index ascending.  The CTA finds the
-// k-th largest code with an 8-bit-digit radix select (per-warp histograms, warp-aggregated
-// counts), gathers the k codes at or above it, sorts them descending with a bitonic network in
-// shared memory and writes their indices, then -1 up to sparse_count.  Rows with no visible key,
-// rows of an invalid batch, and rows whose batch's block_table names a page outside the pool are
-// written as all -1.
+// One 1024-thread CTA per output row.  Scores are held as order-preserving uint32 codes; a key's
+// full sort key is (code << 32) | (0xFFFFFFFF - index): score descending, then index ascending.
+//
+// 1. Candidates.  n <= kCap: every visible key.  n > kCap: a threshold code is the rank-r largest
+//    of 2048 evenly spaced keys of the row (radix select over the samples), with
+//    r = 1.15 k S / n + 4 sqrt(k S / n) + 2, which leaves between k and kCap keys at or above it
+//    with overwhelming probability; one pass gathers them.  Outside [k, kCap], an exact radix
+//    select on the 64-bit sort keys finds the k-th key and exactly k keys are gathered.
+// 2. Order.  The candidates are distributed into 2048 buckets by code (bucket 0 = highest codes;
+//    the code range is scaled to the bucket count), and each bucket is insertion-sorted by its
+//    owner thread on the full sort key.  If any bucket holds more than kBigBucket keys (heavy ties),
+//    a block-wide bitonic sort on the 64-bit sort keys is used instead.
+// 3. The first min(k, n) indices are written, then -1 up to sparse_count.  Rows with no visible
+//    key, rows of an invalid batch and rows whose batch's block_table names a page outside the pool
+//    are all -1.
 #include "qli_internal.cuh"
 
 namespace qli {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCacheKeys = 16384;                 // score lines up to this length live in smem
-constexpr int kSmemBytes = kCacheKeys * 4 + kWarps * 256 * 4 + kMaxSparse * 8 + 256 * 4;
+constexpr int kCap = 4096;                    // candidates held in shared memory
+constexpr int kSamples = 2048;
+constexpr int kBuckets = 2048;
+constexpr int kBigBucket = 48;
+constexpr int kSmemBytes = 4 * kCap * 4 + 2 * kBuckets * 4 + 256 * 4 + 64 * 4;
 
 struct TopkArgs {
     Params p;
@@ -29,23 +39,318 @@ struct TopkArgs {
     int32_t* out;
 };
 
-__device__ __forceinline__ uint64_t code_of(const uint32_t* line, int64_t j)
+struct Smem {
+    uint32_t* key;    // [kCap] candidate codes (gather order)
+    uint32_t* val;    // [kCap] candidate indices
+    uint32_t* okey;   // [kCap] ordered codes
+    uint32_t* oval;   // [kCap] ordered indices
+    uint32_t* cnt;    // [kBuckets]
+    uint32_t* off;    // [kBuckets]
+    uint32_t* hist;   // [256]
+    uint32_t* misc;   // [64]
+};
+
+__device__ __forceinline__ uint64_t sort_key(uint32_t code, uint32_t idx)
 {
-    return (static_cast<uint64_t>(line[j]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
+    return (static_cast<uint64_t>(code) << 32) | (0xFFFFFFFFu - idx);
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a)
+// Block-wide exclusive scan of one value per thread; also returns the total.
+__device__ uint32_t block_excl_scan(uint32_t v, uint32_t* total, uint32_t* sh /* >= kWarps */)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < kWarps ? sh[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kWarps) sh[lane] = w;
+    }
+    __syncthreads();
+    const uint32_t before = (warp > 0 ? sh[warp - 1] : 0) + x - v;
+    *total = sh[kWarps - 1];
+    __syncthreads();
+    return before;
+}
+
+__device__ uint32_t block_max(uint32_t v, uint32_t* sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    uint32_t r = sh[0];
+    for (int w = 1; w < kWarps; ++w) r = max(r, sh[w]);
+    __syncthreads();
+    return r;
+}
+
+// Radix select over 64-bit sort keys produced by `get(i)` for i < n: the k-th largest key
+// (one shared 256-bin histogram per 8-bit digit, counts aggregated per warp before the atomic).
+template <class Get>
+__device__ uint64_t radix_select(const Smem& S, int64_t n, int k, Get get, int top_shift)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t* s_digit = S.misc + 40;
+    uint32_t* s_rem = S.misc + 41;
+    uint32_t* s_done = S.misc + 42;
+    uint64_t prefix = 0, mask = 0;
+    uint32_t rem = (uint32_t)k;
+    for (int shift = top_shift; shift >= 0; shift -= 8) {
+        if (tid < 256) S.hist[tid] = 0;
+        __syncthreads();
+        for (int64_t i0 = 0; i0 < n; i0 += kThreads) {
+            const int64_t i = i0 + tid;
+            bool in = false;
+            uint32_t digit = 0;
+            if (i < n) {
+                const uint64_t c = get(i);
+                in = (c & mask) == prefix;
+                digit = (uint32_t)(c >> shift) & 0xFFu;
+            }
+            const unsigned act = __ballot_sync(0xffffffffu, in);
+            if (in) {
+                const unsigned peers = __match_any_sync(act, digit);
+                if (lane == __ffs(peers) - 1) atomicAdd(&S.hist[digit], (uint32_t)__popc(peers));
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t c8[8], sum = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                c8[q] = S.hist[255 - 8 * lane - q];
+                sum += c8[q];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t excl = incl - sum;
+            const unsigned hit = __ballot_sync(0xffffffffu, incl >= rem);
+            if (lane == __ffs(hit) - 1) {
+                uint32_t above = excl;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (above + c8[q] >= rem) {
+                        *s_digit = 255 - 8 * lane - q;
+                        *s_rem = rem - above;
+                        *s_done = (c8[q] == rem - above) ? 1u : 0u;
+                        break;
+                    }
+                    above += c8[q];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= (uint64_t)*s_digit << shift;
+        mask |= (uint64_t)0xFFu << shift;
+        rem = *s_rem;
+        const bool done = *s_done != 0;
+        __syncthreads();
+        if (done) break;
+    }
+    return prefix;
+}
+
+// Gather (unordered) the keys j < n whose sort key is >= t64; returns how many (only the first
+// kCap are stored).
+__device__ int gather(const Smem& S, const uint32_t* line, int64_t n, uint64_t t64)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+    uint32_t* s_cnt = S.misc + 48;
+    if (tid == 0) *s_cnt = 0;
+    __syncthreads();
+    for (int64_t j0 = 0; j0 < n; j0 += kThreads) {
+        const int64_t j = j0 + tid;
+        uint32_t c = 0;
+        bool take = false;
+        if (j < n) {
+            c = __ldg(line + j);
+            take = sort_key(c, (uint32_t)j) >= t64;
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, take);
+        if (bal) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(s_cnt, (uint32_t)__popc(bal));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (take) {
+                const uint32_t pos = base + __popc(bal & ((1u << lane) - 1u));
+                if (pos < (uint32_t)kCap) {
+                    S.key[pos] = c;
+                    S.val[pos] = (uint32_t)j;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    return (int)*s_cnt;
+}
+
+// Descending bitonic sort of kThreads * E 64-bit keys, thread t holding positions t*E .. t*E+E-1.
+template <int E>
+__device__ void bitonic_desc(uint64_t (&v)[E], uint64_t* xbuf)
+{
+    constexpr int P = kThreads * E;
+    const int tid = threadIdx.x;
+#pragma unroll 1
+    for (int k = 2; k <= P; k <<= 1) {
+#pragma unroll 1
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j < E) {
+#pragma unroll
+                for (int jj = 1; jj < E; jj <<= 1) {
+                    if (jj == j) {
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            const int pe = e ^ jj;
+                            if (pe > e) {
+                                const bool desc = ((tid * E + e) & k) == 0;
+                                const uint64_t x = v[e], y = v[pe];
+                                if (desc ? (x < y) : (x > y)) {
+                                    v[e] = y;
+                                    v[pe] = x;
+                                }
+                            }
+                        }
+                    }
+                }
+            } else if (j < 32 * E) {
+                const int lm = j / E;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = tid * E + e;
+                    const uint64_t other = __shfl_xor_sync(0xffffffffu, v[e], lm);
+                    const bool keep_max = ((i & j) == 0) == ((i & k) == 0);
+                    v[e] = keep_max ? (v[e] > other ? v[e] : other) : (v[e] < other ? v[e] : other);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) xbuf[tid * E + e] = v[e];
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = tid * E + e;
+                    const uint64_t other = xbuf[i ^ j];
+                    const bool keep_max = ((i & j) == 0) == ((i & k) == 0);
+                    v[e] = keep_max ? (v[e] > other ? v[e] : other) : (v[e] < other ? v[e] : other);
+                }
+                __syncthreads();
+            }
+        }
+    }
+}
+
+// Slow path: order key/val[0..c) with the bitonic network into oval (indices).
+template <int E>
+__device__ void bitonic_order(const Smem& S, int c)
+{
+    uint64_t v[E];
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int i = tid * E + e;
+        v[e] = i < c ? sort_key(S.key[i], S.val[i]) : 0ull;   // 0 sorts below every real key
+    }
+    __syncthreads();
+    bitonic_desc<E>(v, reinterpret_cast<uint64_t*>(S.okey));   // okey/oval double as 64-bit scratch
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int i = tid * E + e;
+        if (i < c) S.val[i] = 0xFFFFFFFFu - (uint32_t)(v[e] & 0xFFFFFFFFu);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int i = tid * E + e;
+        if (i < c) S.oval[i] = S.val[i];
+    }
+    __syncthreads();
+}
+
+// Order the c candidates (key/val) descending by sort key into oval.  lo = lower bound of codes.
+__device__ void order_candidates(const Smem& S, int c, uint32_t lo)
+{
+    const int tid = threadIdx.x;
+    uint32_t hi_local = 0;
+    for (int i = tid; i < c; i += kThreads) hi_local = max(hi_local, S.key[i]);
+    const uint32_t hi = block_max(hi_local, S.misc);
+    const uint32_t range = hi - lo;
+    int shift = 0;
+    while (shift < 32 && (range >> shift) >= (uint32_t)kBuckets) ++shift;
+    for (int b = tid; b < kBuckets; b += kThreads) S.cnt[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < c; i += kThreads) atomicAdd(&S.cnt[(hi - S.key[i]) >> shift], 1u);
+    __syncthreads();
+    // exclusive scan of the bucket counts, two buckets per thread
+    const uint32_t c0 = S.cnt[2 * tid], c1 = S.cnt[2 * tid + 1];
+    uint32_t total;
+    const uint32_t base = block_excl_scan(c0 + c1, &total, S.misc);
+    S.off[2 * tid] = base;
+    S.off[2 * tid + 1] = base + c0;
+    const bool big = c0 > (uint32_t)kBigBucket || c1 > (uint32_t)kBigBucket;
+    if (__syncthreads_or(big)) {
+        if (c <= kThreads) bitonic_order<1>(S, c);
+        else if (c <= 2 * kThreads) bitonic_order<2>(S, c);
+        else bitonic_order<4>(S, c);
+        return;
+    }
+    // scatter (filling each bucket from its end), then sort every bucket on the full key
+    for (int i = tid; i < c; i += kThreads) {
+        const uint32_t b = (hi - S.key[i]) >> shift;
+        const uint32_t pos = S.off[b] + atomicSub(&S.cnt[b], 1u) - 1u;
+        S.okey[pos] = S.key[i];
+        S.oval[pos] = S.val[i];
+    }
+    __syncthreads();
+    for (int b = tid; b < kBuckets; b += kThreads) {
+        const uint32_t s = S.off[b];
+        const uint32_t e = (b + 1 < kBuckets) ? S.off[b + 1] : (uint32_t)c;
+        for (uint32_t i = s + 1; i < e; ++i) {
+            const uint32_t kc = S.okey[i], kv = S.oval[i];
+            const uint64_t kk = sort_key(kc, kv);
+            uint32_t q = i;
+            while (q > s && sort_key(S.okey[q - 1], S.oval[q - 1]) < kk) {
+                S.okey[q] = S.okey[q - 1];
+                S.oval[q] = S.oval[q - 1];
+                --q;
+            }
+            S.okey[q] = kc;
+            S.oval[q] = kv;
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ TopkArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    uint32_t* cache = reinterpret_cast<uint32_t*>(smem);
-    uint32_t* whist = cache + kCacheKeys;                                  // [kWarps][256]
-    uint64_t* sel = reinterpret_cast<uint64_t*>(whist + kWarps * 256);     // [kMaxSparse]
-    uint32_t* hist = reinterpret_cast<uint32_t*>(sel + kMaxSparse);        // [256]
+    Smem S;
+    S.key = reinterpret_cast<uint32_t*>(smem);
+    S.val = S.key + kCap;
+    S.okey = S.val + kCap;
+    S.oval = S.okey + kCap;
+    S.cnt = S.oval + kCap;
+    S.off = S.cnt + kBuckets;
+    S.hist = S.off + kBuckets;
+    S.misc = S.hist + 256;
     __shared__ int s_bad;
-    __shared__ uint32_t s_digit, s_rem, s_done, s_cnt;
 
     const Params& p = a.p;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int k = p.sparse_count;
     const bool meta_ok = a.meta[kMhMagic] == kMetaMagic && a.meta[kMhLayoutHash] == p.hash;
     const int32_t* be = a.meta + p.meta.batch_off;
@@ -61,7 +366,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a)
             } else {
                 int64_t lo = 0, hi = p.batch - 1;
                 while (lo < hi) {
-                    int64_t mid = (lo + hi + 1) >> 1;
+                    const int64_t mid = (lo + hi + 1) >> 1;
                     if (be[mid * kBatchWords + kBeFirstRow] <= row) lo = mid; else hi = mid - 1;
                 }
                 b = lo;
@@ -80,7 +385,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a)
             const int32_t* table = a.block_table + b * p.max_blocks_per_seq;
             bool bad = false;
             for (int64_t i = tid; i < pages; i += kThreads) {
-                const int32_t pg = table[i];
+                const int32_t pg = __ldg(table + i);
                 bad |= pg < 0 || pg >= p.num_blocks;
             }
             if (bad) s_bad = 1;
@@ -94,131 +399,45 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a)
             for (int i = tid; i < k; i += kThreads) out[i] = -1;
             continue;
         }
-        const uint32_t* gline = a.scores + row * p.ld;
-        const bool cached = n <= kCacheKeys;
-        if (cached)
-            for (int64_t j = tid; j < n; j += kThreads) cache[j] = gline[j];
-        __syncthreads();
-        const uint32_t* line = cached ? cache : gline;
+        const uint32_t* line = a.scores + row * p.ld;
         const int64_t m = n < k ? n : k;
-
-        if (n <= k) {
-            for (int64_t j = tid; j < n; j += kThreads) sel[j] = code_of(line, j);
+        int count;
+        uint32_t lo = 0;
+        if (n <= kCap) {
+            uint32_t mn = 0xFFFFFFFFu;
+            for (int64_t j = tid; j < n; j += kThreads) {
+                const uint32_t c = __ldg(line + j);
+                S.key[j] = c;
+                S.val[j] = (uint32_t)j;
+                mn = min(mn, c);
+            }
+            lo = ~block_max(~mn, S.misc);
+            count = (int)n;
         } else {
-            // ---- radix select of the k-th largest code, 8 bits per pass from the top
-            uint64_t prefix = 0, mask = 0;
-            uint32_t rem = (uint32_t)k;
-            for (int shift = 56; shift >= 0; shift -= 8) {
-                for (int i = tid; i < kWarps * 256; i += kThreads) whist[i] = 0;
-                __syncthreads();
-                uint32_t* myh = whist + warp * 256;
-                for (int64_t j0 = 0; j0 < n; j0 += kThreads) {
-                    const int64_t j = j0 + tid;
-                    bool in = false;
-                    uint32_t digit = 0;
-                    if (j < n) {
-                        const uint64_t c = code_of(line, j);
-                        in = (c & mask) == prefix;
-                        digit = (uint32_t)(c >> shift) & 0xFFu;
-                    }
-                    const unsigned act = __ballot_sync(0xffffffffu, in);
-                    if (in) {
-                        const unsigned peers = __match_any_sync(act, digit);
-                        if (lane == __ffs(peers) - 1) myh[digit] += __popc(peers);
-                    }
-                }
-                __syncthreads();
-                if (tid < 256) {
-                    uint32_t s = 0;
-                    for (int w = 0; w < kWarps; ++w) s += whist[w * 256 + tid];
-                    hist[tid] = s;
-                }
-                __syncthreads();
-                if (warp == 0) {
-                    // lane l owns digits 255-8l .. 248-8l (descending order)
-                    uint32_t c8[8], sum = 0;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        c8[q] = hist[255 - 8 * lane - q];
-                        sum += c8[q];
-                    }
-                    uint32_t incl = sum;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += y;
-                    }
-                    const uint32_t excl = incl - sum;
-                    const unsigned hit = __ballot_sync(0xffffffffu, incl >= rem);
-                    if (lane == __ffs(hit) - 1) {
-                        uint32_t above = excl;
-                        for (int q = 0; q < 8; ++q) {
-                            if (above + c8[q] >= rem) {
-                                s_digit = 255 - 8 * lane - q;
-                                s_rem = rem - above;
-                                s_done = (c8[q] == rem - above) ? 1u : 0u;
-                                break;
-                            }
-                            above += c8[q];
-                        }
-                    }
-                }
-                __syncthreads();
-                prefix |= (uint64_t)s_digit << shift;
-                mask |= (uint64_t)0xFFu << shift;
-                rem = s_rem;
-                const bool done = s_done != 0;
-                __syncthreads();
-                if (done) break;
+            // ---- threshold: the rank-r largest of evenly spaced samples
+            for (int i = tid; i < kSamples; i += kThreads) {
+                const int64_t j = ((int64_t)i * n) / kSamples;
+                S.key[i] = __ldg(line + j);
             }
-            // ---- gather the k codes >= threshold (warp-aggregated slot allocation)
-            if (tid == 0) s_cnt = 0;
             __syncthreads();
-            for (int64_t j0 = 0; j0 < n; j0 += kThreads) {
-                const int64_t j = j0 + tid;
-                uint64_t c = 0;
-                bool take = false;
-                if (j < n) {
-                    c = code_of(line, j);
-                    take = c >= prefix;
-                }
-                const unsigned bal = __ballot_sync(0xffffffffu, take);
-                if (bal) {
-                    uint32_t base = 0;
-                    if (lane == 0) base = atomicAdd(&s_cnt, (uint32_t)__popc(bal));
-                    base = __shfl_sync(0xffffffffu, base, 0);
-                    if (take) {
-                        const uint32_t pos = base + __popc(bal & ((1u << lane) - 1u));
-                        if (pos < (uint32_t)kMaxSparse) sel[pos] = c;
-                    }
-                }
+            const double lam = (double)k * kSamples / (double)n;   // samples expected above the k-th
+            int rank = (int)(1.15 * lam + 4.0 * sqrt(lam) + 2.0);
+            rank = rank < 1 ? 1 : (rank > kSamples ? kSamples : rank);
+            const uint32_t* samp = S.key;
+            const uint64_t t = radix_select(
+                S, kSamples, rank, [&](int64_t i) { return static_cast<uint64_t>(samp[i]) << 32; }, 56);
+            lo = (uint32_t)(t >> 32);
+            count = gather(S, line, n, static_cast<uint64_t>(lo) << 32);
+            if (count < k || count > kCap) {
+                // ---- exact fallback: the k-th sort key of the row, then exactly k keys >= it
+                const uint64_t T = radix_select(
+                    S, n, k, [&](int64_t j) { return sort_key(__ldg(line + j), (uint32_t)j); }, 56);
+                count = min(gather(S, line, n, T), kCap);
+                lo = (uint32_t)(T >> 32);
             }
         }
-        // ---- bitonic sort of sel[0..P) descending, padded with zero codes (below every key)
-        int P = 1;
-        while (P < m) P <<= 1;
-        __syncthreads();
-        for (int64_t i = m + tid; i < P; i += kThreads) sel[i] = 0;
-        __syncthreads();
-        for (int kk = 2; kk <= P; kk <<= 1) {
-            for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-                for (int i = tid; i < P; i += kThreads) {
-                    const int l = i ^ jj;
-                    if (l > i) {
-                        const uint64_t x = sel[i], y = sel[l];
-                        const bool desc = (i & kk) == 0;
-                        if (desc ? (x < y) : (x > y)) {
-                            sel[i] = y;
-                            sel[l] = x;
-                        }
-                    }
-                }
-                __syncthreads();
-            }
-        }
-        for (int i = tid; i < k; i += kThreads)
-            out[i] = i < m ? (int32_t)(0xFFFFFFFFu - (uint32_t)(sel[i] & 0xFFFFFFFFu)) : -1;
-        __syncthreads();
+        order_candidates(S, count, lo);
+        for (int i = tid; i < k; i += kThreads) out[i] = i < m ? (int32_t)S.oval[i] : -1;
     }
 }
 

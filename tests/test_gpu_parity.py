@@ -183,3 +183,32 @@ def test_bad_lengths_blank_batch_and_report(qli):
     assert err & oracle.ERR_LENGTH
     assert st == 5 and bits & 1
     assert np.array_equal(gpu_idx, ora_idx)
+
+
+# ---------------------------------------------------------------------------- top-k paths
+
+def test_topk_all_equal_long_row(qli):
+    """Every key identical: all scores tie, the sampled threshold keeps every key (more than the
+    candidate buffer holds), so the exact fallback must pick the lowest indices."""
+    case = W.make_case("ties", batch=1, s1=1, seq_lens_k=[6000], block_size=64, sparse_count=100,
+                       seed=9)
+    case.key[:] = case.key[0, 0]
+    case.k_scale[:] = case.k_scale[0, 0]
+    gpu_idx, _, st, _ = run_gpu(qli, case)
+    assert st == 0
+    assert gpu_idx[0].tolist() == list(range(100))
+
+
+def test_topk_few_distinct_scores(qli):
+    """Keys drawn from 7 distinct rows: long runs of exact ties around the k-th score."""
+    case = W.make_case("few", batch=2, s1=1, seq_lens_k=[9000, 5000], block_size=128,
+                       sparse_count=2048, sparse_mode=3, seed=10)
+    rng = np.random.default_rng(10)
+    pick = rng.integers(0, 7, size=case.key.shape[:2])
+    protos = case.key[0, :7, 0].copy()
+    case.key[:, :, 0] = protos[pick]
+    case.k_scale[:] = np.float16(1.0)
+    gpu_idx, _, st, _ = run_gpu(qli, case)
+    ora_idx, _, _ = oracle.score_topk(case)
+    assert st == 0
+    assert np.array_equal(gpu_idx, ora_idx)     # exact ties resolve by index on both sides
