@@ -8,7 +8,9 @@ uniform in [8192, 32768] in 64-key pages under a random block_table, sparse_coun
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the launching
 stream with an L2 flush (a 512 MB write) between steps, outside the events; barrier +
-synchronize around the timed region; the maximum over ranks.  SM clocks and throttle reasons are
+synchronize around the timed region; the maximum over ranks.  A second pass of up to 50 steps
+puts events between the three kernels as well, for the per-stage times and the scoring kernel's
+roofline.  SM clocks and throttle reasons are
 sampled with nvidia-smi over ~1.5 s of identical untimed load steps ending where the timed steps
 begin, and through the timed steps.  Printed: one JSON line.
 
@@ -320,18 +322,29 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    # the timed steps: events only at step boundaries, so the three kernels may overlap their
+    # launches (programmatic dependent launch) as they do in use
     for i in range(args.steps):
         flush.fill_(i)
-        step(evs[i])
+        evs[i][0].record(stream)
+        step()
+        evs[i][3].record(stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    meta_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    score_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    topk_ms = [e[2].elapsed_time(e[3]) for e in evs]
     total_ms = sum(step_ms)
+    # per-stage pass (stage times and the score kernel's roofline): events between the kernels
+    stage_steps = max(3, min(args.steps, 50))
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(stage_steps)]
+    for i in range(stage_steps):
+        flush.fill_(i)
+        step(sev[i])
+    torch.cuda.synchronize()
+    meta_ms = [e[0].elapsed_time(e[1]) for e in sev]
+    score_ms = [e[1].elapsed_time(e[2]) for e in sev]
+    topk_ms = [e[2].elapsed_time(e[3]) for e in sev]
     if dist:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)

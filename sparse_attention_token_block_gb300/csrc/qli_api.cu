@@ -224,7 +224,8 @@ qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const i
     int sms = device_sms(nullptr);
     if (sms < 0) return QLI_ERR_CUDA;
     if (sms == 0) return QLI_ERR_NO_DEVICE;
-    cudaError_t e = launch_metadata(P, seq_lens_q, seq_lens_k, metadata, sms, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_metadata(P, seq_lens_q, seq_lens_k, metadata, sms * kScoreCtasPerSm,
+                                    static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
 
@@ -267,7 +268,7 @@ qli_status qli_score(const qli_problem* p, const void* query, const void* key, c
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     CUtensorMap tm;
     if (!encode_key_map(&tm, key, P)) return QLI_ERR_CUDA;
-    const int grid = sms < kMaxCtas ? sms : kMaxCtas;
+    const int grid = sms * kScoreCtasPerSm < kMaxCtas ? sms * kScoreCtasPerSm : kMaxCtas;
     cudaError_t e = launch_score(P, &tm, query, key, weights, q_scale, k_scale, block_table, metadata,
                                  reinterpret_cast<uint32_t*>(ws + W.scores_off), reinterpret_cast<uint32_t*>(ws),
                                  grid, static_cast<cudaStream_t>(stream));

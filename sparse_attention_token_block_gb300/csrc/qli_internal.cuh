@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "qli.h"
 
 namespace qli {
@@ -19,9 +21,11 @@ constexpr int kMaxSparse = 2048;
 
 // Score kernel tiling: a tile is 128 consecutive compressed keys of one batch (one TMEM lane per
 // key); a query group is up to kGroupTokens consecutive query tokens of one batch scored together
-// (MMA N = 64 * tokens).
+// (MMA N = 64 * tokens).  Two score CTAs share each SM: separate CTAs keep more key copies in flight
+// than one CTA with twice the resources.
 constexpr int kTileKeys = 128;
-constexpr int kGroupTokens = 2;
+constexpr int kGroupTokens = 1;
+constexpr int kScoreCtasPerSm = 2;        // score CTAs resident per SM (the split is made for this)
 constexpr int kMaxCtas = 1024;            // bound on the split's CTA count (GB300 has 152 SMs)
 
 // Device error bits (sticky word at the start of the workspace)
@@ -132,9 +136,29 @@ __host__ __device__ inline int32_t problem_hash(const Params& p)
 
 MetaLayout meta_layout(int64_t batch, int64_t max_groups);
 
+// Launch `kernel` with programmatic stream serialization: it may begin launching while the
+// previous kernel in the stream finishes; every kernel of this library calls griddepcontrol.wait
+// before touching memory another kernel writes or reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Launchers (defined in the kernel translation units)
 cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
-                            int32_t* meta, int num_sms, cudaStream_t st);
+                            int32_t* meta, int num_ctas, cudaStream_t st);
 cudaError_t launch_score(const Params& p, const void* tmap_key, const void* query, const void* key,
                          const void* weights, const void* q_scale, const void* k_scale,
                          const int32_t* block_table, const int32_t* meta, uint32_t* scores,

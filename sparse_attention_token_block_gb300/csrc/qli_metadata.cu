@@ -12,6 +12,7 @@
 //     CTA of the score kernel; each range becomes the list of (batch, first row, key_begin,
 //     key_end) units it overlaps, stored CTA by CTA with offsets.
 #include "qli_internal.cuh"
+#include "qli_ptx.cuh"
 
 namespace qli {
 
@@ -93,6 +94,10 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     const View v_gp = sg ? View{msm + 5 * kSmemBatch, 1} : View{meta + p.meta.group_off, 1};
     int32_t* gpre_home = meta + p.meta.group_off;
     if (tid == 0) { s_err = 0; s_tnd_bad = 0; }
+    // the lengths may come from the previous kernel, and the previous indexer call may still read
+    // this metadata buffer
+    ptx::pdl_wait();
+    ptx::pdl_launch_dependents();
     __syncthreads();
 
     // ---- per-batch extents and validity
@@ -236,14 +241,14 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
 }  // namespace
 
 cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
-                            int32_t* meta, int num_sms, cudaStream_t st)
+                            int32_t* meta, int num_ctas, cudaStream_t st)
 {
-    int G = num_sms < kMaxCtas ? num_sms : kMaxCtas;
+    int G = num_ctas < kMaxCtas ? num_ctas : kMaxCtas;
     cudaError_t e = cudaFuncSetAttribute(metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kMetaSmemBytes);
     if (e != cudaSuccess) return e;
-    metadata_kernel<<<1, kMetaThreads, kMetaSmemBytes, st>>>(p, seq_lens_q, seq_lens_k, meta, G);
-    return cudaGetLastError();
+    return launch_pdl(metadata_kernel, dim3(1), dim3(kMetaThreads), kMetaSmemBytes, st, p, seq_lens_q,
+                      seq_lens_k, meta, G);
 }
 
 }  // namespace qli

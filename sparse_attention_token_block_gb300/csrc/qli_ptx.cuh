@@ -74,6 +74,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
+// ------------------------------------------------------------------------------------ launch order
+// Programmatic dependent launch: wait until every grid this one depends on has completed and its
+// writes are visible (a no-op when launched without the programmatic attribute) ...
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// ... and allow the next grid in the stream to begin launching before this one exits.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
@@ -105,6 +112,23 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
             "r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Per-thread asynchronous copy of 8 or 16 bytes global -> shared (both aligned to the size)
+template <int kBytes>
+__device__ __forceinline__ void cp_async(void* dst, const void* src)
+{
+    static_assert(kBytes == 8 || kBytes == 16, "cp.async size");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "n"(kBytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed (the barrier's expected
+// arrival count includes this arrival)
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // ------------------------------------------------------------------------------------ tcgen05

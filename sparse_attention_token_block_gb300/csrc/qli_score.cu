@@ -9,8 +9,9 @@
 //
 //   producer warp    per unit: bulk-copies the group's query codes, weights and query scales;
 //                    per tile: TMA-loads the 128 key rows (128 B each, 128-byte swizzle) from the
-//                    pages the block_table names into a 6-stage ring, and bulk-copies their scales
-//                    into an 8-slot scale ring (own barriers: the epilogue releases those slots);
+//                    pages the block_table names into a 6-stage ring; its 32 lanes copy the keys'
+//                    scales with cp.async into an 8-slot scale ring (own barriers: the epilogue
+//                    releases those slots);
 //   converter warps  (4) per unit: fold W * |sQ|, convert the query codes to fp16 (negating heads
 //                    with sQ < 0) into the MMA's B operand (K-major, 128-byte swizzle);
 //                    per tile: one thread per key reads its row, converts int8 / e4m3 to fp16
@@ -40,36 +41,38 @@ namespace qli {
 
 namespace {
 
-constexpr int kStages = 6;                       // key ring depth
-constexpr int kScaleSlots = 8;                   // scale ring depth (released by the epilogue)
-constexpr int kGroups = 2;                       // converter and epilogue groups; tile i -> i % 2
-constexpr int kNumA = 4;                         // A buffers in tensor memory (2 per group)
-constexpr int kNumD = 2;                         // D buffers in tensor memory (1 per group)
+constexpr int kStages = 4;                       // key ring depth
+constexpr int kScaleSlots = 6;                   // scale ring depth (released by the epilogue)
+constexpr int kGroups = 1;                       // converter and epilogue groups; tile i -> i % groups
+constexpr int kNumA = 2;                         // A buffers in tensor memory
+constexpr int kNumD = 2;                         // D buffers in tensor memory
 constexpr int kGroupThreads = 128;               // 4 warps, one key (TMEM lane) per thread
 constexpr int kConvWarp0 = 0;                    // converter group g: warps 4g .. 4g+3
-constexpr int kEpiWarp0 = 8;                     // epilogue group g: warps 8+4g .. 11+4g
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;
-constexpr int kThreads = 576;
-constexpr uint32_t kTmemCols = 512;
+constexpr int kEpiWarp0 = 4 * kGroups;           // epilogue group g: warps kEpiWarp0 + 4g ..
+constexpr int kProducerWarp = 8 * kGroups;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr uint32_t kDcols = kHeads * kGroupTokens;           // one D buffer (fp32 per lane)
 constexpr uint32_t kAcol0 = 0;                   // A buffers: 64 columns each (128 fp16 per lane)
-constexpr uint32_t kDcol0 = kNumA * 64;          // D buffers: 128 columns each (2 tokens x 64)
+constexpr uint32_t kDcol0 = kNumA * 64;
+constexpr uint32_t kTmemCols = 256;              // two CTAs per SM share the 512 columns
+static_assert(kDcol0 + kNumD * kDcols <= kTmemCols, "tensor memory budget");
 
-constexpr int kQbufBytes = kGroupTokens * kHeads * kDim * 2;   // fp16 B operand, 32 KB
+constexpr int kQbufBytes = kGroupTokens * kHeads * kDim * 2;   // fp16 B operand
 constexpr int kKstageBytes = kTileKeys * kDim;                 // 16 KB of key codes
 constexpr int kSslotBytes = kTileKeys * 4;                     // scales (fp32 max)
-constexpr int kQrawBytes = kGroupTokens * kHeads * kDim;       // 16 KB of query codes
+constexpr int kQrawBytes = kGroupTokens * kHeads * kDim;       // query codes of one group
 constexpr int kVecRawBytes = kGroupTokens * kHeads * 4;        // weights / q_scale (fp32 max)
 
 // shared memory carve-up (offsets from a 1024-aligned base)
-constexpr int kOffQbuf = 0;                                        // 2 x 32 KB
+constexpr int kOffQbuf = 0;                                        // 2 B operands
 constexpr int kOffKring = kOffQbuf + 2 * kQbufBytes;               // kStages x 16 KB
 constexpr int kOffSring = kOffKring + kStages * kKstageBytes;      // kScaleSlots x 512 B
-constexpr int kOffQraw = kOffSring + kScaleSlots * kSslotBytes;    // 2 x 16 KB
-constexpr int kOffWraw = kOffQraw + 2 * kQrawBytes;                // 2 x 512 B
-constexpr int kOffSQraw = kOffWraw + 2 * kVecRawBytes;             // 2 x 512 B
-constexpr int kOffWq = kOffSQraw + 2 * kVecRawBytes;               // 2 x 128 floats
-constexpr int kOffSign = kOffWq + 2 * kGroupTokens * kHeads * 4;   // 2 x 128 words
+constexpr int kOffQraw = kOffSring + kScaleSlots * kSslotBytes;    // 1 raw query group
+constexpr int kOffWraw = kOffQraw + kQrawBytes;                    // 1 x weights
+constexpr int kOffSQraw = kOffWraw + kVecRawBytes;                 // 1 x q_scale
+constexpr int kOffWq = kOffSQraw + kVecRawBytes;                   // 2 x W*|sQ|
+constexpr int kOffSign = kOffWq + 2 * kGroupTokens * kHeads * 4;   // 2 x sign masks
 constexpr int kOffBars = kOffSign + 2 * kGroupTokens * kHeads * 4;
 enum {
     kBarKfull = 0,
@@ -88,6 +91,7 @@ enum {
 };
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;   // + slack to align the base to 1024
+static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM must fit in shared memory");
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -183,6 +187,9 @@ __device__ __forceinline__ Unit read_unit(const ScoreArgs& a, int64_t u)
 // ------------------------------------------------------------------------------------------------
 // Producer warp
 // ------------------------------------------------------------------------------------------------
+// The producer's 32 lanes also fetch the key scales (4 keys per lane) with per-thread cp.async
+// copies whose completion the scale slot's barrier tracks: TMA copies of a few hundred bytes would
+// double the copy operations per tile, and the TMA engine's throughput here is per operation.
 template <bool kScaleF32>
 __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, int64_t ubeg, int64_t uend)
 {
@@ -197,18 +204,17 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
         const int uu = (int)(u - ubeg);
         const Unit x = read_unit(a, u);
         const int qb = uu & 1;
-        if (!wait_bar(&S.bars[kBarQrempty + qb], ((uu >> 1) & 1) ^ 1, S.abort, a.err)) return;
+        (void)qb;
+        // one raw query buffer: unit uu's codes land after the converters took unit uu - 1's
+        if (!wait_bar(&S.bars[kBarQrempty], (uu & 1) ^ 1, S.abort, a.err)) return;
         if (lane == 0) {
             const uint32_t qbytes = x.q_cnt * kHeads * kDim;
             const uint32_t vbytes = x.q_cnt * kHeads * esz;
-            uint64_t* bar = &S.bars[kBarQrfull + qb];
+            uint64_t* bar = &S.bars[kBarQrfull];
             ptx::mbar_arrive_expect_tx(bar, qbytes + 2 * vbytes);
-            ptx::bulk_load(S.base + kOffQraw + qb * kQrawBytes,
-                           a.query + (int64_t)x.row0 * kHeads * kDim, qbytes, bar);
-            ptx::bulk_load(S.base + kOffWraw + qb * kVecRawBytes,
-                           a.weights + (int64_t)x.row0 * kHeads * esz, vbytes, bar);
-            ptx::bulk_load(S.base + kOffSQraw + qb * kVecRawBytes,
-                           a.q_scale + (int64_t)x.row0 * kHeads * esz, vbytes, bar);
+            ptx::bulk_load(S.base + kOffQraw, a.query + (int64_t)x.row0 * kHeads * kDim, qbytes, bar);
+            ptx::bulk_load(S.base + kOffWraw, a.weights + (int64_t)x.row0 * kHeads * esz, vbytes, bar);
+            ptx::bulk_load(S.base + kOffSQraw, a.q_scale + (int64_t)x.row0 * kHeads * esz, vbytes, bar);
         }
         // logical page / slot of the current chunk, advanced without division; the block_table
         // entries of 32 consecutive logical pages sit one per lane (cur), the next 32 in nxt
@@ -222,17 +228,29 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
         int key = x.kb;
         for (int t = 0; t < x.ntiles; ++t, ++tile_i) {
             const int s = tile_i % kStages;
-            const int ss = tile_i % kScaleSlots;
             if (!wait_bar(&S.bars[kBarKempty + s], ((tile_i / kStages) & 1) ^ 1, S.abort, a.err)) return;
-            if (!wait_bar(&S.bars[kBarSempty + ss], ((tile_i / kScaleSlots) & 1) ^ 1, S.abort, a.err)) return;
             const int tile_end = min(x.kb + (t + 1) * kTileKeys, x.ke);
+            // scales of this tile: lane l copies those of keys key + 4l .. key + 4l + 3 (one page,
+            // since bs % 16 == 0) into scale slot ss
+            {
+                const int ss = tile_i % kScaleSlots;
+                if (!wait_bar(&S.bars[kBarSempty + ss], ((tile_i / kScaleSlots) & 1) ^ 1, S.abort, a.err)) return;
+                const int k4 = key + 4 * lane;
+                const int off = k4 / bs - wbase;              // < 64: a tile spans <= 8 pages
+                const int32_t pc = __shfl_sync(0xffffffffu, cur, off & 31);
+                const int32_t pn = __shfl_sync(0xffffffffu, nxt, off & 31);
+                int32_t page = off < 32 ? pc : pn;
+                if (page < 0 || page >= p.num_blocks) page = 0;   // reported with the key rows
+                if (k4 < tile_end) {
+                    const int64_t e = (int64_t)page * bs + (k4 % bs);
+                    ptx::cp_async<4 * esz>(S.base + kOffSring + ss * kSslotBytes + lane * 4 * esz,
+                                           a.k_scale + e * esz);
+                }
+                ptx::cp_async_arrive_noinc(&S.bars[kBarSfull + ss]);
+            }
             const int nchunks = (tile_end - key + R - 1) / R;
             uint64_t* bar = &S.bars[kBarKfull + s];
-            uint64_t* sbar = &S.bars[kBarSfull + ss];
-            if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nchunks * R * kDim));
-                ptx::mbar_arrive_expect_tx(sbar, (uint32_t)(nchunks * R * esz));
-            }
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nchunks * R * kDim));
             for (int c = 0; c < nchunks; ++c) {
                 if (lp - wbase >= 32) {     // slide the page window by 32
                     wbase += 32;
@@ -248,8 +266,6 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
                     const int64_t prow = (int64_t)page * bs + slot;
                     ptx::tma_load_2d(S.base + kOffKring + s * kKstageBytes + c * R * kDim, tmap, 0,
                                      (int32_t)prow, bar);
-                    ptx::bulk_load(S.base + kOffSring + ss * kSslotBytes + c * R * esz,
-                                   a.k_scale + prow * esz, (uint32_t)(R * esz), sbar);
                 }
                 key += R;
                 slot += R;
@@ -283,7 +299,7 @@ __device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, int64
             if (!wait_bar(&S.bars[kBarAfull + ab], (tile_i / kNumA) & 1, S.abort, a.err)) return;
             if (!wait_bar(&S.bars[kBarDempty + db], ((tile_i / kNumD) & 1) ^ 1, S.abort, a.err)) return;
             ptx::tc_fence_after();
-            const uint32_t d_t = tmem + kDcol0 + db * 128;
+            const uint32_t d_t = tmem + kDcol0 + db * kDcols;
             const uint32_t a_t = tmem + kAcol0 + ab * 64;
 #pragma unroll
             for (int kk = 0; kk < kDim / 16; ++kk) {
@@ -314,14 +330,14 @@ __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_
         const int uu = (int)(u - ubeg);
         const Unit x = read_unit(a, u);
         const int qb = uu & 1;
-        if (qb == grp) {
-            if (!wait_bar(&S.bars[kBarQrfull + qb], (uu >> 1) & 1, S.abort, a.err)) return;
+        if (uu % kGroups == grp) {   // this group converts the unit's query group
+            if (!wait_bar(&S.bars[kBarQrfull], uu & 1, S.abort, a.err)) return;
             if (!wait_bar(&S.bars[kBarQempty + qb], ((uu >> 1) & 1) ^ 1, S.abort, a.err)) return;
             // weights folded with |sQ|; heads with sQ < 0 get their query row negated instead
             float* wq = reinterpret_cast<float*>(S.base + kOffWq) + qb * kGroupTokens * kHeads;
             uint32_t* sgn = reinterpret_cast<uint32_t*>(S.base + kOffSign) + qb * kGroupTokens * kHeads;
-            const uint8_t* wraw = S.base + kOffWraw + qb * kVecRawBytes;
-            const uint8_t* sqraw = S.base + kOffSQraw + qb * kVecRawBytes;
+            const uint8_t* wraw = S.base + kOffWraw;
+            const uint8_t* sqraw = S.base + kOffSQraw;
             if (tid < x.q_cnt * kHeads) {
                 const float w = load_scale(wraw, tid, kScaleF32);
                 const float sq = load_scale(sqraw, tid, kScaleF32);
@@ -332,7 +348,7 @@ __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_
             // query codes -> fp16 B operand: row n = token*64 + head, K-major, 128-byte swizzle,
             // the K halves [0,64) and [64,128) in two blocks of n rows
             const int nrows = x.q_cnt * kHeads;
-            const uint8_t* qraw = S.base + kOffQraw + qb * kQrawBytes;
+            const uint8_t* qraw = S.base + kOffQraw;
             uint8_t* qbuf = S.base + kOffQbuf + qb * kQbufBytes;
             for (int item = tid; item < nrows * 8; item += kGroupThreads) {
                 const int n = item >> 3, c16 = item & 7;   // 16 codes = dims [16*c16, 16*c16 + 16)
@@ -357,7 +373,7 @@ __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_
             __syncwarp();
             if (lane == 0) {
                 ptx::mbar_arrive(&S.bars[kBarQfull + qb]);
-                ptx::mbar_arrive(&S.bars[kBarQrempty + qb]);
+                ptx::mbar_arrive(&S.bars[kBarQrempty]);
             }
         }
         for (int t = 0; t < x.ntiles; ++t, ++tile_i) {
@@ -447,7 +463,7 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, int64_t
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t d[32];
-                        QLI_TMEM_LD_X32(tmem + lane_base + kDcol0 + db * 128 + tt * 64 + half * 32, d);
+                        QLI_TMEM_LD_X32(tmem + lane_base + kDcol0 + db * kDcols + tt * 64 + half * 32, d);
                         ptx::tmem_wait_ld();
                         if (sk >= 0.0f) {
 #pragma unroll
@@ -495,7 +511,7 @@ __device__ void init_barriers(const Shared& S)
         ptx::mbar_init(&S.bars[kBarKempty + i], 4);
     }
     for (int i = 0; i < kScaleSlots; ++i) {
-        ptx::mbar_init(&S.bars[kBarSfull + i], 1);
+        ptx::mbar_init(&S.bars[kBarSfull + i], 32);   // one cp.async arrival per producer lane
         ptx::mbar_init(&S.bars[kBarSempty + i], 4);
     }
     for (int i = 0; i < 2; ++i) {
@@ -516,24 +532,17 @@ __device__ void init_barriers(const Shared& S)
 }
 
 template <bool kFp8, bool kScaleF32>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kScoreCtasPerSm)
     score_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ ScoreArgs a)
 {
     const Shared S = shared_view();
     const int tid = threadIdx.x, warp = tid >> 5;
 
-    // the metadata must have been written for this problem
-    const int32_t* meta = a.meta;
-    if (meta[kMhMagic] != kMetaMagic || meta[kMhLayoutHash] != a.p.hash) {
-        if (blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrMetadata);
-        return;
-    }
-    if (blockIdx.x == 0 && tid == 0 && meta[kMhErr]) atomicOr(a.err, (uint32_t)meta[kMhErr]);
-    const int G = meta[kMhCtas];
-
+    // prologue that touches no global memory, overlapping the previous kernel's tail
     if (tid == 0) {
         init_barriers(S);
         *S.abort = 0;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(S.tmem_slot, kTmemCols);
@@ -543,6 +552,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *S.tmem_slot;
+    // the metadata comes from the previous kernel and the previous top-k may still read the score
+    // lines this kernel overwrites
+    ptx::pdl_wait();
+    ptx::pdl_launch_dependents();
+
+    // the metadata must have been written for this problem
+    const int32_t* meta = a.meta;
+    const bool meta_ok = meta[kMhMagic] == kMetaMagic && meta[kMhLayoutHash] == a.p.hash;
+    if (!meta_ok && blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrMetadata);
+    if (meta_ok && blockIdx.x == 0 && tid == 0 && meta[kMhErr]) atomicOr(a.err, (uint32_t)meta[kMhErr]);
+    const int G = meta_ok ? meta[kMhCtas] : 0;
 
     // this CTA's unit lists: CTA-lists blockIdx.x, blockIdx.x + gridDim.x, ... (normally one)
     for (int c = blockIdx.x; c < G; c += gridDim.x) {
@@ -580,8 +600,7 @@ cudaError_t launch_variant(const CUtensorMap* tmap, const ScoreArgs& a, int grid
     auto k = score_kernel<kFp8, kScaleF32>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, kSmemBytes, st>>>(*tmap, a);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(kThreads), kSmemBytes, st, *tmap, a);
 }
 
 }  // namespace

@@ -4,12 +4,14 @@
 // One 1024-thread CTA per output row.  Scores are held as order-preserving uint32 codes; a key's
 // full sort key is (code << 32) | (0xFFFFFFFF - index): score descending, then index ascending.
 //
-// 1. Candidates.  n <= kCap: every visible key.  n > kCap: a threshold code is the rank-r largest
+// 1. Candidates.  n <= kCap: every visible key.  n <= 32768: the row is held in registers and a
+//    two-level 2048-bin histogram over its code range narrows the k-th largest code to a sub-bin;
+//    every key in that sub-bin or above is a candidate.  Longer rows: a threshold code is the rank-r largest
 //    of 2048 evenly spaced keys of the row (radix select over the samples), with
 //    r = 1.15 k S / n + 4 sqrt(k S / n) + 2, which leaves between k and kCap keys at or above it
 //    with overwhelming probability; one pass gathers them.  Outside [k, kCap], an exact radix
 //    select on the 64-bit sort keys finds the k-th key and exactly k keys are gathered.
-// 2. Order.  The candidates are distributed into 2048 buckets by code (bucket 0 = highest codes;
+// 2. Order.  The candidates are distributed into 8192 buckets by code (bucket 0 = highest codes;
 //    the code range is scaled to the bucket count), and each bucket is insertion-sorted by its
 //    owner thread on the full sort key.  If any bucket holds more than kBigBucket keys (heavy ties),
 //    a block-wide bitonic sort on the 64-bit sort keys is used instead.
@@ -17,6 +19,7 @@
 //    key, rows of an invalid batch and rows whose batch's block_table names a page outside the pool
 //    are all -1.
 #include "qli_internal.cuh"
+#include "qli_ptx.cuh"
 
 namespace qli {
 
@@ -28,7 +31,9 @@ constexpr int kCap = 4096;                    // candidates held in shared memor
 constexpr int kSamples = 2048;
 constexpr int kBuckets = 2048;
 constexpr int kBigBucket = 48;
-constexpr int kSmemBytes = 4 * kCap * 4 + 2 * kBuckets * 4 + 256 * 4 + 64 * 4;
+constexpr int kOrderBuckets = 8192;           // ordering buckets (counters kept in the row cache)
+constexpr int kCacheKeys = 32768;             // score lines up to this length are cached in smem
+constexpr int kSmemBytes = kCacheKeys * 4 + 4 * kCap * 4 + 2 * kBuckets * 4 + 256 * 4 + 64 * 4 + 16;
 
 struct TopkArgs {
     Params p;
@@ -48,6 +53,8 @@ struct Smem {
     uint32_t* off;    // [kBuckets]
     uint32_t* hist;   // [256]
     uint32_t* misc;   // [64]
+    uint32_t* cache;  // [kCacheKeys] one score line
+    uint64_t* bar;    // bulk-copy barrier
 };
 
 __device__ __forceinline__ uint64_t sort_key(uint32_t code, uint32_t idx)
@@ -90,8 +97,14 @@ __device__ uint32_t block_max(uint32_t v, uint32_t* sh)
     for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
     if (lane == 0) sh[warp] = v;
     __syncthreads();
-    uint32_t r = sh[0];
-    for (int w = 1; w < kWarps; ++w) r = max(r, sh[w]);
+    if (warp == 0) {
+        uint32_t w = lane < kWarps ? sh[lane] : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, o));
+        if (lane == 0) sh[32] = w;
+    }
+    __syncthreads();
+    const uint32_t r = sh[32];
     __syncthreads();
     return r;
 }
@@ -282,26 +295,39 @@ __device__ void bitonic_order(const Smem& S, int c)
 }
 
 // Order the c candidates (key/val) descending by sort key into oval.  lo = lower bound of codes.
+// The buckets' counters live in the row cache, idle by now.
 __device__ void order_candidates(const Smem& S, int c, uint32_t lo)
 {
     const int tid = threadIdx.x;
+    uint32_t* cnt = S.cache;                       // [kOrderBuckets]
+    uint32_t* off = S.cache + kOrderBuckets;       // [kOrderBuckets]
+    constexpr int per = kOrderBuckets / kThreads;
     uint32_t hi_local = 0;
     for (int i = tid; i < c; i += kThreads) hi_local = max(hi_local, S.key[i]);
     const uint32_t hi = block_max(hi_local, S.misc);
     const uint32_t range = hi - lo;
     int shift = 0;
-    while (shift < 32 && (range >> shift) >= (uint32_t)kBuckets) ++shift;
-    for (int b = tid; b < kBuckets; b += kThreads) S.cnt[b] = 0;
+    while (shift < 32 && (range >> shift) >= (uint32_t)kOrderBuckets) ++shift;
+    for (int b = tid; b < kOrderBuckets; b += kThreads) cnt[b] = 0;
     __syncthreads();
-    for (int i = tid; i < c; i += kThreads) atomicAdd(&S.cnt[(hi - S.key[i]) >> shift], 1u);
+    for (int i = tid; i < c; i += kThreads) atomicAdd(&cnt[(hi - S.key[i]) >> shift], 1u);
     __syncthreads();
-    // exclusive scan of the bucket counts, two buckets per thread
-    const uint32_t c0 = S.cnt[2 * tid], c1 = S.cnt[2 * tid + 1];
+    // exclusive scan of the bucket counts, `per` consecutive buckets per thread
+    uint32_t mine[per], sum = 0;
+    bool big = false;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+        mine[q] = cnt[tid * per + q];
+        sum += mine[q];
+        big |= mine[q] > (uint32_t)kBigBucket;
+    }
     uint32_t total;
-    const uint32_t base = block_excl_scan(c0 + c1, &total, S.misc);
-    S.off[2 * tid] = base;
-    S.off[2 * tid + 1] = base + c0;
-    const bool big = c0 > (uint32_t)kBigBucket || c1 > (uint32_t)kBigBucket;
+    uint32_t base = block_excl_scan(sum, &total, S.misc);
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+        off[tid * per + q] = base;
+        base += mine[q];
+    }
     if (__syncthreads_or(big)) {
         if (c <= kThreads) bitonic_order<1>(S, c);
         else if (c <= 2 * kThreads) bitonic_order<2>(S, c);
@@ -311,28 +337,143 @@ __device__ void order_candidates(const Smem& S, int c, uint32_t lo)
     // scatter (filling each bucket from its end), then sort every bucket on the full key
     for (int i = tid; i < c; i += kThreads) {
         const uint32_t b = (hi - S.key[i]) >> shift;
-        const uint32_t pos = S.off[b] + atomicSub(&S.cnt[b], 1u) - 1u;
+        const uint32_t pos = off[b] + atomicSub(&cnt[b], 1u) - 1u;
         S.okey[pos] = S.key[i];
         S.oval[pos] = S.val[i];
     }
     __syncthreads();
-    for (int b = tid; b < kBuckets; b += kThreads) {
-        const uint32_t s = S.off[b];
-        const uint32_t e = (b + 1 < kBuckets) ? S.off[b + 1] : (uint32_t)c;
+#pragma unroll 1
+    for (int q = 0; q < per; ++q) {
+        const int b = tid * per + q;
+        const uint32_t s = off[b];
+        const uint32_t e = (b + 1 < kOrderBuckets) ? off[b + 1] : (uint32_t)c;
         for (uint32_t i = s + 1; i < e; ++i) {
             const uint32_t kc = S.okey[i], kv = S.oval[i];
             const uint64_t kk = sort_key(kc, kv);
-            uint32_t q = i;
-            while (q > s && sort_key(S.okey[q - 1], S.oval[q - 1]) < kk) {
-                S.okey[q] = S.okey[q - 1];
-                S.oval[q] = S.oval[q - 1];
-                --q;
+            uint32_t j = i;
+            while (j > s && sort_key(S.okey[j - 1], S.oval[j - 1]) < kk) {
+                S.okey[j] = S.okey[j - 1];
+                S.oval[j] = S.oval[j - 1];
+                --j;
             }
-            S.okey[q] = kc;
-            S.oval[q] = kv;
+            S.okey[j] = kc;
+            S.oval[j] = kv;
         }
     }
     __syncthreads();
+}
+
+// Find, from per-bin counts in S.cnt (bin 0 = highest codes), the bin where the running count
+// reaches `need`; returns it and stores the count of the bins before it in *above.
+__device__ uint32_t locate_bin(const Smem& S, uint32_t need, uint32_t* above)
+{
+    const int tid = threadIdx.x;
+    const uint32_t c0 = S.cnt[2 * tid], c1 = S.cnt[2 * tid + 1];
+    uint32_t total;
+    const uint32_t before = block_excl_scan(c0 + c1, &total, S.misc);
+    uint32_t* s_bin = S.misc + 56;
+    uint32_t* s_above = S.misc + 57;
+    if (before < need && before + c0 >= need) {
+        *s_bin = 2 * tid;
+        *s_above = before;
+    } else if (before + c0 < need && before + c0 + c1 >= need) {
+        *s_bin = 2 * tid + 1;
+        *s_above = before + c0;
+    }
+    __syncthreads();
+    const uint32_t b = *s_bin;
+    *above = *s_above;
+    __syncthreads();
+    return b;
+}
+
+// Rows of up to kCacheKeys keys: the score line is bulk-copied into shared memory (one memory
+// latency).  A 2048-bin histogram over the line's code range finds the bin holding the k-th
+// largest code; a second 2048-bin histogram over that bin alone narrows it to a sub-bin.  Every
+// key above that sub-bin's lower edge becomes a candidate (written to key/val).  Returns the
+// candidate count, or -1 if it would exceed kCap; *lo receives a lower bound of their codes.
+__device__ int select_cached(const Smem& S, const uint32_t* line, int64_t n, int k, uint32_t* lo,
+                             uint64_t* bar, uint32_t parity, uint32_t* err)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+    uint32_t* cache = S.cache;
+    // the previous row's generic reads of the cache come before this row's bulk write into it
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t bytes = (uint32_t)(((n * 4) + 15) & ~(int64_t)15);
+        ptx::mbar_arrive_expect_tx(bar, bytes);
+        ptx::bulk_load(cache, line, bytes, bar);
+    }
+    // bounded wait for the copy (a few microseconds normally)
+    {
+        const uint64_t t0 = ptx::globaltimer();
+        bool ok = true;
+        while (!ptx::mbar_try_wait(bar, parity)) {
+            if (ptx::globaltimer() - t0 > 2000000000ull) {
+                ok = false;
+                break;
+            }
+        }
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) atomicOr(err, kErrTimeout);
+            return -2;
+        }
+    }
+    uint32_t mn = 0xFFFFFFFFu, mx = 0;
+    for (int64_t j = tid; j < n; j += kThreads) {
+        const uint32_t c = cache[j];
+        mn = min(mn, c);
+        mx = max(mx, c);
+    }
+    mx = block_max(mx, S.misc);
+    mn = ~block_max(~mn, S.misc);
+    const uint32_t need = (uint32_t)((int64_t)k < n ? (int64_t)k : n);
+    // level 1: the whole range
+    int s1 = 0;
+    while (s1 < 32 && ((mx - mn) >> s1) >= (uint32_t)kBuckets) ++s1;
+    for (int b = tid; b < kBuckets; b += kThreads) S.cnt[b] = 0;
+    __syncthreads();
+    for (int64_t j = tid; j < n; j += kThreads) atomicAdd(&S.cnt[(mx - cache[j]) >> s1], 1u);
+    __syncthreads();
+    uint32_t above1;
+    const uint32_t b1 = locate_bin(S, need, &above1);
+    // level 2: inside bin b1 (offsets below mx in [b1 << s1, (b1 + 1) << s1))
+    const int s2 = s1 > 11 ? s1 - 11 : 0;
+    for (int b = tid; b < kBuckets; b += kThreads) S.cnt[b] = 0;
+    __syncthreads();
+    for (int64_t j = tid; j < n; j += kThreads) {
+        const uint32_t d = mx - cache[j];
+        if ((d >> s1) == b1) atomicAdd(&S.cnt[(d - (b1 << s1)) >> s2], 1u);
+    }
+    __syncthreads();
+    uint32_t above2;
+    const uint32_t b2 = locate_bin(S, need - above1, &above2);
+    (void)lane;
+    const uint64_t lim = (static_cast<uint64_t>(b1) << s1) + ((static_cast<uint64_t>(b2) + 1) << s2);
+    // every key with (mx - code) below the end of sub-bin b2 is a candidate: count per thread,
+    // scan, then write (thread t owns the keys t, t + kThreads, ...)
+    uint32_t mine = 0;
+    for (int64_t j = tid; j < n; j += kThreads) mine += (uint64_t)(mx - cache[j]) < lim ? 1u : 0u;
+    uint32_t total;
+    uint32_t pos = block_excl_scan(mine, &total, S.misc);
+    for (int64_t j = tid; j < n; j += kThreads) {
+        const uint32_t cj = cache[j];
+        if ((uint64_t)(mx - cj) < lim) {
+            if (pos < (uint32_t)kCap) {
+                S.key[pos] = cj;
+                S.val[pos] = (uint32_t)j;
+            }
+            ++pos;
+        }
+    }
+    uint32_t* s_cnt = S.misc + 48;
+    if (tid == 0) *s_cnt = total;
+    __syncthreads();
+    const int count = (int)*s_cnt;
+    *lo = lim > (uint64_t)(mx - mn) ? mn : (uint32_t)(mx - lim + 1);
+    __syncthreads();
+    return count > kCap ? -1 : count;
 }
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ TopkArgs a)
@@ -347,11 +488,23 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     S.off = S.cnt + kBuckets;
     S.hist = S.off + kBuckets;
     S.misc = S.hist + 256;
+    S.cache = S.misc + 64;                                    // 16-byte aligned (offsets are)
+    S.bar = reinterpret_cast<uint64_t*>(S.cache + kCacheKeys);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(S.bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    uint32_t bar_parity = 0;
     __shared__ int s_bad;
 
     const Params& p = a.p;
     const int tid = threadIdx.x;
     const int k = p.sparse_count;
+    // the score lines and metadata come from earlier kernels; the next call may overwrite them
+    // only after this grid completes (it waits too)
+    ptx::pdl_wait();
+    ptx::pdl_launch_dependents();
     const bool meta_ok = a.meta[kMhMagic] == kMetaMagic && a.meta[kMhLayoutHash] == p.hash;
     const int32_t* be = a.meta + p.meta.batch_off;
 
@@ -413,6 +566,19 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             }
             lo = ~block_max(~mn, S.misc);
             count = (int)n;
+        } else if (n <= kCacheKeys) {
+            count = select_cached(S, line, n, k, &lo, S.bar, bar_parity, a.err);
+            bar_parity ^= 1u;
+            if (count == -2) {           // the copy never landed: leave the row as -1
+                for (int i = tid; i < k; i += kThreads) out[i] = -1;
+                continue;
+            }
+            if (count < 0) {
+                const uint64_t T = radix_select(
+                    S, n, k, [&](int64_t j) { return sort_key(__ldg(line + j), (uint32_t)j); }, 56);
+                count = min(gather(S, line, n, T), kCap);
+                lo = (uint32_t)(T >> 32);
+            }
         } else {
             // ---- threshold: the rank-r largest of evenly spaced samples
             for (int i = tid; i < kSamples; i += kThreads) {
@@ -451,8 +617,7 @@ cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.rows < (1 << 30) ? p.rows : (1 << 30);
-    topk_kernel<<<grid, kThreads, kSmemBytes, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, a);
 }
 
 }  // namespace qli
