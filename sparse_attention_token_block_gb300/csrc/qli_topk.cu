@@ -30,7 +30,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 4096;                    // candidates held in shared memory
 constexpr int kSamples = 2048;
 constexpr int kBuckets = 2048;
-constexpr int kBigBucket = 48;
+constexpr int kBigBucket = 256;
 constexpr int kOrderBuckets = 8192;           // ordering buckets (counters kept in the row cache)
 constexpr int kCacheKeys = 32768;             // score lines up to this length are cached in smem
 constexpr int kSmemBytes = kCacheKeys * 4 + 4 * kCap * 4 + 2 * kBuckets * 4 + 256 * 4 + 64 * 4 + 16;
@@ -267,7 +267,7 @@ __device__ void bitonic_desc(uint64_t (&v)[E], uint64_t* xbuf)
     }
 }
 
-// Slow path: order key/val[0..c) with the bitonic network into oval (indices).
+// Slow path: order key/val[0..c) with the bitonic network; the ordered indices end in val.
 template <int E>
 __device__ void bitonic_order(const Smem& S, int c)
 {
@@ -286,16 +286,10 @@ __device__ void bitonic_order(const Smem& S, int c)
         if (i < c) S.val[i] = 0xFFFFFFFFu - (uint32_t)(v[e] & 0xFFFFFFFFu);
     }
     __syncthreads();
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const int i = tid * E + e;
-        if (i < c) S.oval[i] = S.val[i];
-    }
-    __syncthreads();
 }
 
-// Order the c candidates (key/val) descending by sort key into oval.  lo = lower bound of codes.
-// The buckets' counters live in the row cache, idle by now.
+// Order the c candidates (key/val) descending by sort key; the ordered indices end in val.
+// lo = lower bound of codes.  The buckets' counters live in the row cache, idle by now.
 __device__ void order_candidates(const Smem& S, int c, uint32_t lo)
 {
     const int tid = threadIdx.x;
@@ -334,7 +328,8 @@ __device__ void order_candidates(const Smem& S, int c, uint32_t lo)
         else bitonic_order<4>(S, c);
         return;
     }
-    // scatter (filling each bucket from its end), then sort every bucket on the full key
+    // scatter (filling each bucket from its end), then place every candidate at its bucket's start
+    // plus its rank among the bucket's keys (one thread per candidate)
     for (int i = tid; i < c; i += kThreads) {
         const uint32_t b = (hi - S.key[i]) >> shift;
         const uint32_t pos = off[b] + atomicSub(&cnt[b], 1u) - 1u;
@@ -342,23 +337,15 @@ __device__ void order_candidates(const Smem& S, int c, uint32_t lo)
         S.oval[pos] = S.val[i];
     }
     __syncthreads();
-#pragma unroll 1
-    for (int q = 0; q < per; ++q) {
-        const int b = tid * per + q;
-        const uint32_t s = off[b];
-        const uint32_t e = (b + 1 < kOrderBuckets) ? off[b + 1] : (uint32_t)c;
-        for (uint32_t i = s + 1; i < e; ++i) {
-            const uint32_t kc = S.okey[i], kv = S.oval[i];
-            const uint64_t kk = sort_key(kc, kv);
-            uint32_t j = i;
-            while (j > s && sort_key(S.okey[j - 1], S.oval[j - 1]) < kk) {
-                S.okey[j] = S.okey[j - 1];
-                S.oval[j] = S.oval[j - 1];
-                --j;
-            }
-            S.okey[j] = kc;
-            S.oval[j] = kv;
-        }
+    for (int i = tid; i < c; i += kThreads) {
+        const uint32_t kc = S.okey[i], kv = S.oval[i];
+        const uint64_t kk = sort_key(kc, kv);
+        const uint32_t b = (hi - kc) >> shift;
+        const uint32_t s0 = off[b];
+        const uint32_t e0 = (b + 1 < (uint32_t)kOrderBuckets) ? off[b + 1] : (uint32_t)c;
+        uint32_t r = 0;
+        for (uint32_t j = s0; j < e0; ++j) r += sort_key(S.okey[j], S.oval[j]) > kk ? 1u : 0u;
+        S.val[s0 + r] = kv;
     }
     __syncthreads();
 }
@@ -387,39 +374,15 @@ __device__ uint32_t locate_bin(const Smem& S, uint32_t need, uint32_t* above)
     return b;
 }
 
-// Rows of up to kCacheKeys keys: the score line is bulk-copied into shared memory (one memory
-// latency).  A 2048-bin histogram over the line's code range finds the bin holding the k-th
+// Rows of up to kCacheKeys keys, whose score line the caller bulk-copied into shared memory (one
+// memory latency).  A 2048-bin histogram over the line's code range finds the bin holding the k-th
 // largest code; a second 2048-bin histogram over that bin alone narrows it to a sub-bin.  Every
 // key above that sub-bin's lower edge becomes a candidate (written to key/val).  Returns the
 // candidate count, or -1 if it would exceed kCap; *lo receives a lower bound of their codes.
-__device__ int select_cached(const Smem& S, const uint32_t* line, int64_t n, int k, uint32_t* lo,
-                             uint64_t* bar, uint32_t parity, uint32_t* err)
+__device__ int select_cached(const Smem& S, int64_t n, int k, uint32_t* lo)
 {
     const int tid = threadIdx.x, lane = tid & 31;
-    uint32_t* cache = S.cache;
-    // the previous row's generic reads of the cache come before this row's bulk write into it
-    ptx::fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-        const uint32_t bytes = (uint32_t)(((n * 4) + 15) & ~(int64_t)15);
-        ptx::mbar_arrive_expect_tx(bar, bytes);
-        ptx::bulk_load(cache, line, bytes, bar);
-    }
-    // bounded wait for the copy (a few microseconds normally)
-    {
-        const uint64_t t0 = ptx::globaltimer();
-        bool ok = true;
-        while (!ptx::mbar_try_wait(bar, parity)) {
-            if (ptx::globaltimer() - t0 > 2000000000ull) {
-                ok = false;
-                break;
-            }
-        }
-        if (!__syncthreads_and(ok)) {
-            if (tid == 0) atomicOr(err, kErrTimeout);
-            return -2;
-        }
-    }
+    const uint32_t* cache = S.cache;
     uint32_t mn = 0xFFFFFFFFu, mx = 0;
     for (int64_t j = tid; j < n; j += kThreads) {
         const uint32_t c = cache[j];
@@ -529,9 +492,21 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             if (e[kBeOk] && r >= 0)
                 n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], e[kBeLc], r);
         }
+        const uint32_t* line = a.scores + row * p.ld;
+        // rows cached in shared memory: start the line's bulk copy now, under the page check
+        const bool cached_path = n > kCap && n <= kCacheKeys;
         // ---- every page this batch's rows can see must lie in the pool
         __syncthreads();
-        if (tid == 0) s_bad = 0;
+        if (tid == 0) {
+            s_bad = 0;
+            if (cached_path) {
+                // the previous row's generic reads of the cache came before (barrier above)
+                ptx::fence_proxy_async_smem();
+                const uint32_t bytes = (uint32_t)(((n * 4) + 15) & ~(int64_t)15);
+                ptx::mbar_arrive_expect_tx(S.bar, bytes);
+                ptx::bulk_load(S.cache, line, bytes, S.bar);
+            }
+        }
         __syncthreads();
         if (n > 0) {
             const int64_t pages = ceil_div64(be[b * kBatchWords + kBeLc], p.block_size);
@@ -544,15 +519,29 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             if (bad) s_bad = 1;
         }
         __syncthreads();
-        if (s_bad) {
+        bool copy_ok = true;
+        if (cached_path) {
+            // bounded wait for the line (also when the row turns out invalid: the copy must land
+            // before the cache is reused)
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(S.bar, bar_parity)) {
+                if (ptx::globaltimer() - t0 > 2000000000ull) {
+                    copy_ok = false;
+                    break;
+                }
+            }
+            bar_parity ^= 1u;
+            copy_ok = __syncthreads_and(copy_ok);
+            if (!copy_ok && tid == 0) atomicOr(a.err, kErrTimeout);
+        }
+        if (s_bad || !copy_ok) {
             n = 0;
-            if (tid == 0) atomicOr(a.err, kErrPage);
+            if (tid == 0 && s_bad) atomicOr(a.err, kErrPage);
         }
         if (n <= 0) {
             for (int i = tid; i < k; i += kThreads) out[i] = -1;
             continue;
         }
-        const uint32_t* line = a.scores + row * p.ld;
         const int64_t m = n < k ? n : k;
         int count;
         uint32_t lo = 0;
@@ -567,12 +556,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             lo = ~block_max(~mn, S.misc);
             count = (int)n;
         } else if (n <= kCacheKeys) {
-            count = select_cached(S, line, n, k, &lo, S.bar, bar_parity, a.err);
-            bar_parity ^= 1u;
-            if (count == -2) {           // the copy never landed: leave the row as -1
-                for (int i = tid; i < k; i += kThreads) out[i] = -1;
-                continue;
-            }
+            count = select_cached(S, n, k, &lo);
             if (count < 0) {
                 const uint64_t T = radix_select(
                     S, n, k, [&](int64_t j) { return sort_key(__ldg(line + j), (uint32_t)j); }, 56);
@@ -603,7 +587,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             }
         }
         order_candidates(S, count, lo);
-        for (int i = tid; i < k; i += kThreads) out[i] = i < m ? (int32_t)S.oval[i] : -1;
+        for (int i = tid; i < k; i += kThreads) out[i] = i < m ? (int32_t)S.val[i] : -1;
     }
 }
 
