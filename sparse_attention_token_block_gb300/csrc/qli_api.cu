@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -103,6 +104,10 @@ Params params_of(const qli_problem* q)
     p.ld = ld > 0 ? ld : kTileKeys;
     p.meta = meta_layout(p.batch, max_groups_of(q));
     p.hash = problem_hash(p);
+    // failure-detection test switch (host-set, no device fault involved): the score kernel's
+    // producer issues no copies, so every consumer wait runs out and reports a timeout
+    const char* stall = std::getenv("QLI_TEST_STALL_PRODUCER");
+    p.test_stall = (stall && stall[0] == '1') ? 1 : 0;
     return p;
 }
 

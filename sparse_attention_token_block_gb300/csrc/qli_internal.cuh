@@ -90,6 +90,7 @@ struct Params {
     int32_t rows;          // output rows
     int32_t meta_ctas;     // G
     int32_t hash;
+    int32_t test_stall;    // test switch: the score kernel's producer issues nothing (waits expire)
     int64_t ld;            // score line stride
     MetaLayout meta;
 };

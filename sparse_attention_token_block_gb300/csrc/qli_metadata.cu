@@ -10,7 +10,8 @@
 //     of its last row (the largest in the group under either mask);
 //   * the split: the concatenated tile sequence of all groups is cut into G equal ranges, one per
 //     CTA of the score kernel; each range becomes the list of (batch, first row, key_begin,
-//     key_end) units it overlaps, stored CTA by CTA with offsets.
+//     key_end) units it overlaps, stored CTA by CTA with offsets (computed in parallel over
+//     groups).
 #include "qli_internal.cuh"
 #include "qli_ptx.cuh"
 
@@ -18,7 +19,7 @@ namespace qli {
 
 namespace {
 
-constexpr int kMetaThreads = 256;
+constexpr int kMetaThreads = 1024;
 
 // Block-wide exclusive scan of one int64 per thread; returns the exclusive prefix and the total.
 __device__ int64_t block_exclusive_scan(int64_t v, int64_t* total, int64_t* sh /* [32] */)
@@ -185,45 +186,55 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     }
     __syncthreads();
 
-    // ---- split the tile sequence over G CTAs: count units per CTA, scan, then write them
+    // ---- split the tile sequence over G CTAs.  CTA c owns tiles [T c / G, T (c + 1) / G); a unit is
+    // a (CTA, group) pair whose tile ranges meet.  Both partitions are ordered, so listing units
+    // CTA by CTA lists them group by group too: a unit's index is the prefix over groups of their
+    // unit counts plus its CTA's offset inside the group.  Work runs in parallel over groups.
+    const int64_t Gl = G;
+    auto cta_of = [&](int64_t t) -> int64_t {     // largest c with floor(T c / G) <= t
+        int64_t c = ((t + 1) * Gl + T - 1) / T - 1;
+        return c < 0 ? 0 : (c >= Gl ? Gl - 1 : c);
+    };
+    if (T == 0)
+        for (int c = tid; c <= G; c += blockDim.x) cta_off[c] = 0;
     running = 0;
-    for (int cbase = 0; cbase <= G; cbase += blockDim.x) {
-        const int c = cbase + tid;
-        int64_t cnt = 0;
-        int64_t t0 = 0, t1 = 0, g0 = 0;
-        if (c < G && T > 0 && total_groups > 0) {
-            t0 = (T * c) / G;
-            t1 = (T * (c + 1)) / G;
-            if (t1 > t0) {
-                g0 = upper_index(v_gp, total_groups, t0);
-                for (int64_t g = g0; g < total_groups && v_gp[g] < t1; ++g)
-                    if (v_gp[g + 1] > v_gp[g]) ++cnt;
+    for (int64_t base = 0; base < total_groups; base += blockDim.x) {
+        const int64_t g = base + tid;
+        int64_t nu = 0, A = 0, Bt = 0, c0 = 0;
+        if (g < total_groups && T > 0) {
+            A = v_gp[g];
+            Bt = v_gp[g + 1];
+            if (Bt > A) {
+                c0 = cta_of(A);
+                nu = cta_of(Bt - 1) - c0 + 1;
             }
         }
         int64_t tot;
-        const int64_t ex = block_exclusive_scan(cnt, &tot, scan_sh);
-        if (c <= G) cta_off[c] = (int32_t)(running + ex);
-        if (cnt > 0) {
-            int64_t u = running + ex;
-            for (int64_t g = g0; g < total_groups && v_gp[g] < t1; ++g) {
-                const int64_t gs = v_gp[g], ge = v_gp[g + 1];
-                if (ge <= gs) continue;
-                const int64_t b = upper_index(v_gb, p.batch, g);
-                const int64_t r0 = (g - v_gb[b]) * kGroupTokens;
-                const int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)v_sq[b]) - 1;
-                const int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl);
-                const int64_t tb = max(t0, gs) - gs;
-                const int64_t te = min(t1, ge) - gs;
+        const int64_t ex = block_exclusive_scan(nu, &tot, scan_sh);
+        if (nu > 0) {
+            const int64_t b = upper_index(v_gb, p.batch, g);
+            const int64_t r0 = (g - v_gb[b]) * kGroupTokens;
+            const int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)v_sq[b]) - 1;
+            const int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl);
+            for (int64_t q = 0; q < nu; ++q) {
+                const int64_t c = c0 + q;
+                const int64_t t0 = (T * c) / Gl, t1 = (T * (c + 1)) / Gl;
+                const int64_t u = running + ex + q;
                 int32_t* w = units + u * kUnitWords;
                 w[0] = (int32_t)b;
                 w[1] = (int32_t)r0;
-                w[2] = (int32_t)(tb * kTileKeys);
-                w[3] = (int32_t)min(te * kTileKeys, n);
-                ++u;
+                w[2] = (int32_t)((max(t0, A) - A) * kTileKeys);
+                w[3] = (int32_t)min((min(t1, Bt) - A) * kTileKeys, n);
+                if (t0 >= A && t0 < Bt) {
+                    // the CTA's first unit; CTAs before it with an empty range (T < G) start here too
+                    cta_off[c] = (int32_t)u;
+                    for (int64_t ce = c - 1; ce >= 0 && (T * ce) / Gl == t0; --ce) cta_off[ce] = (int32_t)u;
+                }
             }
         }
         running += tot;
     }
+    if (tid == 0) cta_off[G] = (int32_t)running;
     __syncthreads();
     if (tid == 0) {
         meta[kMhMagic] = kMetaMagic;
@@ -247,7 +258,9 @@ cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const in
     cudaError_t e = cudaFuncSetAttribute(metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kMetaSmemBytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(metadata_kernel, dim3(1), dim3(kMetaThreads), kMetaSmemBytes, st, p, seq_lens_q,
+    // few groups: fewer warps make each block-wide step cheaper; many groups: more lanes per pass
+    const int threads = p.meta.max_groups <= 4096 && p.batch <= 4096 ? 256 : kMetaThreads;
+    return launch_pdl(metadata_kernel, dim3(1), dim3(threads), kMetaSmemBytes, st, p, seq_lens_q,
                       seq_lens_k, meta, G);
 }
 

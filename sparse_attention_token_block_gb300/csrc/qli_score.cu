@@ -199,6 +199,7 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
     constexpr int esz = kScaleF32 ? 4 : 2;
     const int R = p.box_rows;             // keys per TMA box; divides block_size and 128
     const int bs = p.block_size;
+    if (p.test_stall) return;     // test switch: nothing arrives, the consumers' waits run out
     uint32_t tile_i = 0;
     for (int64_t u = ubeg; u < uend; ++u) {
         const int uu = (int)(u - ubeg);
