@@ -103,6 +103,22 @@ def workload_stats(case):
                 total_bytes=total_bytes)
 
 
+def max_over_ranks(x, dist, device):
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gops(pairs_per_rank, steps, world, total_ms):
+    """Algorithmic GOPS of the whole job: every rank scores its own workload (weak scaling), the
+    time is the slowest rank's."""
+    return pairs_per_rank * OPS_PER_PAIR * steps * world / (total_ms * 1e-3) / 1e9
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -334,7 +350,7 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     # per-stage pass (stage times and the score kernel's roofline): events between the kernels
     stage_steps = max(3, min(args.steps, 50))
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(stage_steps)]
@@ -345,12 +361,8 @@ def main():
     meta_ms = [e[0].elapsed_time(e[1]) for e in sev]
     score_ms = [e[1].elapsed_time(e[2]) for e in sev]
     topk_ms = [e[2].elapsed_time(e[3]) for e in sev]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     ops = stats["pairs"] * OPS_PER_PAIR * args.steps * world
-    value = ops / (total_ms * 1e-3) / 1e9
+    value = whole_job_gops(stats["pairs"], args.steps, world, total_ms)
 
     # end to end through the public call with host buffers: pinned host inputs copied in, the
     # indices copied out, every step
@@ -380,11 +392,7 @@ def main():
             e2e_step()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = sum(a.elapsed_time(b) for a, b in ev)
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dist, dev)
         e2e = {"value": ops / (e_ms * 1e-3) / 1e9, "unit": "GOPS", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps}
 
