@@ -113,10 +113,10 @@ size_t qli_workspace_size(const qli_problem* p);
  * Work-split scheduler (README: metadata parameter of the indexer and its companion
  * VllmQuantLightningIndexerMetadata call: cores used, block size and each core's start points).
  * Reads the device lengths and writes, into `metadata` (int32[metadata_words], device, caller-
- * owned), the per-batch row/key extents and a balanced split of every live query group's key
- * tiles over the GPU's SMs.  One kernel, enqueued on `stream`.  The result depends only on the
- * lengths and `p`, so one metadata buffer serves every call that shares them (e.g. all layers of a
- * step).  seq_lens_q may be NULL for BSND.
+ * owned, 16-byte aligned), the per-batch row/key extents and a balanced split of every live query
+ * group's key tiles over the GPU's SMs.  One kernel, enqueued on `stream`.  The result depends
+ * only on the lengths and `p`, so one metadata buffer serves every call that shares them (e.g. all
+ * layers of a step).  seq_lens_q may be NULL for BSND.
  */
 qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                         int32_t* metadata, size_t metadata_words, void* stream);

@@ -18,7 +18,8 @@ MetaLayout meta_layout(int64_t batch, int64_t max_groups)
     m.batch_off = kMhWords;
     m.cta_off = m.batch_off + batch * kBatchWords;
     m.group_off = m.cta_off + kMaxCtas + 1;
-    m.unit_off = m.group_off + max_groups + 1;
+    m.ufirst_off = m.group_off + max_groups + 1;                    // first unit of each group
+    m.unit_off = (m.ufirst_off + max_groups + 1 + 3) & ~int64_t(3);  // 16-byte aligned units
     m.max_groups = max_groups;
     m.max_units = max_groups + kMaxCtas;
     m.total_words = m.unit_off + m.max_units * kUnitWords;
@@ -27,6 +28,8 @@ MetaLayout meta_layout(int64_t batch, int64_t max_groups)
 }
 
 namespace {
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
 
@@ -174,7 +177,6 @@ bool encode_key_map(CUtensorMap* tm, const void* key, const Params& p)
     return r == CUDA_SUCCESS;
 }
 
-bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 }  // namespace
 }  // namespace qli
@@ -222,7 +224,7 @@ qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const i
     qli_status s = check(p, nullptr);
     if (s != QLI_OK) return s;
     const Params P = params_of(p);
-    if (!metadata) return QLI_ERR_INVALID_ARG;
+    if (!metadata || !aligned(metadata, 16)) return QLI_ERR_INVALID_ARG;
     if (metadata_words < (size_t)P.meta.total_words) return QLI_ERR_WORKSPACE_TOO_SMALL;
     if (P.batch > 0 && !seq_lens_k) return QLI_ERR_INVALID_ARG;     // PA_BSND needs key lengths
     if (P.batch > 0 && P.layout_tnd && !seq_lens_q) return QLI_ERR_INVALID_ARG;  // TND needs prefix sums

@@ -63,7 +63,7 @@ enum BatchEntry {
 constexpr int kUnitWords = 4;   // {batch, first row within batch, key_begin, key_end}
 
 struct MetaLayout {
-    int64_t batch_off, cta_off, group_off, unit_off, total_words;
+    int64_t batch_off, cta_off, group_off, ufirst_off, unit_off, total_words;
     int64_t max_groups, max_units;
 };
 

@@ -21,30 +21,31 @@ namespace {
 
 constexpr int kMetaThreads = 1024;
 
-// Block-wide exclusive scan of one int64 per thread; returns the exclusive prefix and the total.
-__device__ int64_t block_exclusive_scan(int64_t v, int64_t* total, int64_t* sh /* [32] */)
+// Block-wide exclusive scan of one value per thread; returns the exclusive prefix and the total.
+__device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* total, uint32_t* sh /* [32] */)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int64_t x = v;
+    const int nwarps = (int)(blockDim.x >> 5);
+    uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) sh[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int64_t w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+        uint32_t w = lane < nwarps ? sh[lane] : 0u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
         sh[lane] = w;  // inclusive over warps
     }
     __syncthreads();
-    int64_t warp_excl = warp > 0 ? sh[warp - 1] : 0;
-    *total = sh[(blockDim.x >> 5) - 1];
+    const uint32_t warp_excl = warp > 0 ? sh[warp - 1] : 0u;
+    *total = sh[nwarps - 1];
     __syncthreads();
     return warp_excl + x - v;
 }
@@ -69,14 +70,14 @@ __device__ int64_t upper_index(const View& a, int64_t n, int64_t key)
 
 constexpr int kSmemBatch = 2048;     // batches whose fields are staged in shared memory
 constexpr int kSmemGroups = 16384;   // groups whose tile prefix is staged in shared memory
-constexpr int kMetaSmemBytes = (5 * kSmemBatch + kSmemGroups + 1) * 4;
+constexpr int kMetaSmemBytes = (5 * kSmemBatch + 2 * (kSmemGroups + 1)) * 4;
 
 __global__ void __launch_bounds__(kMetaThreads, 1)
     metadata_kernel(Params p, const int32_t* __restrict__ seq_lens_q,
                     const int32_t* __restrict__ seq_lens_k, int32_t* __restrict__ meta, int G)
 {
     extern __shared__ int32_t msm[];
-    __shared__ int64_t scan_sh[32];
+    __shared__ uint32_t scan_sh[32];
     __shared__ uint32_t s_err;
     __shared__ int s_tnd_bad;
     const int tid = threadIdx.x;
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     const View v_gb = sb ? View{msm + 3 * kSmemBatch, 1} : View{be + kBeGroupBase, kBatchWords};
     const View v_ok = sb ? View{msm + 4 * kSmemBatch, 1} : View{be + kBeOk, kBatchWords};
     const View v_gp = sg ? View{msm + 5 * kSmemBatch, 1} : View{meta + p.meta.group_off, 1};
+    const View v_uf = sg ? View{msm + 5 * kSmemBatch + kSmemGroups + 1, 1} : View{meta + p.meta.ufirst_off, 1};
     int32_t* gpre_home = meta + p.meta.group_off;
     if (tid == 0) { s_err = 0; s_tnd_bad = 0; }
     // the lengths may come from the previous kernel, and the previous indexer call may still read
@@ -138,18 +140,18 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     __syncthreads();
 
     // ---- query groups per batch (bad TND prefix sums invalidate every batch) and their prefix
-    int64_t running = 0;
+    uint32_t running = 0;
     for (int base = 0; base < p.batch; base += blockDim.x) {
         const int b = base + tid;
-        int64_t groups = 0;
+        uint32_t groups = 0;
         if (b < p.batch) {
             int32_t* e = be + (int64_t)b * kBatchWords;
             if (s_tnd_bad) e[kBeOk] = 0;
-            groups = (!s_tnd_bad && v_ok[b]) ? (v_sq[b] + kGroupTokens - 1) / kGroupTokens : 0;
+            groups = (!s_tnd_bad && v_ok[b]) ? (uint32_t)((v_sq[b] + kGroupTokens - 1) / kGroupTokens) : 0u;
             e[kBeGroups] = (int32_t)groups;
         }
-        int64_t tot;
-        const int64_t ex = block_exclusive_scan(groups, &tot, scan_sh);
+        uint32_t tot;
+        const uint32_t ex = block_exclusive_scan(groups, &tot, scan_sh);
         if (b < p.batch) {
             be[(int64_t)b * kBatchWords + kBeGroupBase] = (int32_t)(running + ex);
             if (sb) v_gb[b] = (int32_t)(running + ex);
@@ -159,25 +161,37 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     const int64_t total_groups = running;
     __syncthreads();
 
+    // each thread owns a contiguous run of groups, so each pass below needs one block scan
+    const int64_t per = (total_groups + blockDim.x - 1) / blockDim.x;
+    const int64_t g_lo = min((int64_t)tid * per, total_groups);
+    const int64_t g_hi = min(g_lo + per, total_groups);
+    auto group_keys = [&](int64_t g, int64_t* b_out, int64_t* r0_out) -> int64_t {
+        const int64_t b = upper_index(v_gb, p.batch, g);
+        const int64_t r0 = (g - v_gb[b]) * kGroupTokens;
+        const int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)v_sq[b]) - 1;
+        *b_out = b;
+        *r0_out = r0;
+        return visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl);
+    };
+
     // ---- tiles per group, then their exclusive prefix (gpre[g]; gpre[total_groups] = total)
-    running = 0;
-    for (int64_t base = 0; base < total_groups; base += blockDim.x) {
-        const int64_t g = base + tid;
-        int64_t tiles = 0;
-        if (g < total_groups) {
-            const int64_t b = upper_index(v_gb, p.batch, g);
-            const int64_t r0 = (g - v_gb[b]) * kGroupTokens;
-            const int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)v_sq[b]) - 1;
-            const int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl);
-            tiles = ceil_div64(n, kTileKeys);
+    {
+        uint32_t mine = 0;
+        for (int64_t g = g_lo; g < g_hi; ++g) {
+            int64_t b, r0;
+            const uint32_t tiles = (uint32_t)((group_keys(g, &b, &r0) + kTileKeys - 1) / kTileKeys);
+            v_gp[g] = (int32_t)tiles;                 // the count now, its prefix below
+            mine += tiles;
         }
-        int64_t tot;
-        const int64_t ex = block_exclusive_scan(tiles, &tot, scan_sh);
-        if (g < total_groups) {
-            v_gp[g] = (int32_t)(running + ex);
-            if (sg) gpre_home[g] = (int32_t)(running + ex);
+        uint32_t tot;
+        uint32_t pre = block_exclusive_scan(mine, &tot, scan_sh);
+        for (int64_t g = g_lo; g < g_hi; ++g) {
+            const uint32_t tiles = (uint32_t)v_gp[g];
+            v_gp[g] = (int32_t)pre;
+            if (sg) gpre_home[g] = (int32_t)pre;
+            pre += tiles;
         }
-        running += tot;
+        running = tot;
     }
     const int64_t T = running;
     if (tid == 0) {
@@ -191,49 +205,64 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     // CTA by CTA lists them group by group too: a unit's index is the prefix over groups of their
     // unit counts plus its CTA's offset inside the group.  Work runs in parallel over groups.
     const int64_t Gl = G;
+    const bool narrow = T * (Gl + 1) < (int64_t(1) << 32);  // (t + 1) G + T - 1 fits 32 bits
     auto cta_of = [&](int64_t t) -> int64_t {     // largest c with floor(T c / G) <= t
-        int64_t c = ((t + 1) * Gl + T - 1) / T - 1;
+        int64_t c = narrow ? (int64_t)(((uint32_t)(t + 1) * (uint32_t)G + (uint32_t)(T - 1)) / (uint32_t)T) - 1
+                           : ((t + 1) * Gl + T - 1) / T - 1;
         return c < 0 ? 0 : (c >= Gl ? Gl - 1 : c);
+    };
+    // floor(T c / G) without a 64-bit division per CTA: c * floor(T / G) + floor(c * (T mod G) / G)
+    const uint32_t t_div = (uint32_t)(T / (Gl > 0 ? Gl : 1)), t_mod = (uint32_t)(T % (Gl > 0 ? Gl : 1));
+    auto cta_start = [&](int64_t c) -> int64_t {
+        return (int64_t)c * t_div + (uint32_t)((uint32_t)c * t_mod / (uint32_t)G);
     };
     if (T == 0)
         for (int c = tid; c <= G; c += blockDim.x) cta_off[c] = 0;
-    running = 0;
-    for (int64_t base = 0; base < total_groups; base += blockDim.x) {
-        const int64_t g = base + tid;
-        int64_t nu = 0, A = 0, Bt = 0, c0 = 0;
-        if (g < total_groups && T > 0) {
-            A = v_gp[g];
-            Bt = v_gp[g + 1];
-            if (Bt > A) {
-                c0 = cta_of(A);
-                nu = cta_of(Bt - 1) - c0 + 1;
-            }
+    // With T >= G every CTA owns at least one tile and a group's units are the CTAs from the one
+    // holding its first tile to the one holding its last.  With T < G some CTAs own nothing, the
+    // others exactly one tile each, and a group has one unit per tile.
+    const bool dense = T >= Gl;
+    auto group_units = [&](int64_t A, int64_t Bt) -> uint32_t {
+        if (Bt <= A) return 0u;
+        return dense ? (uint32_t)(cta_of(Bt - 1) - cta_of(A) + 1) : (uint32_t)(Bt - A);
+    };
+    // units per group and the index of each group's first unit
+    {
+        uint32_t mine = 0;
+        for (int64_t g = g_lo; g < g_hi && T > 0; ++g) mine += group_units(v_gp[g], v_gp[g + 1]);
+        uint32_t tot;
+        uint32_t u = block_exclusive_scan(mine, &tot, scan_sh);
+        for (int64_t g = g_lo; g < g_hi; ++g) {
+            v_uf[g] = (int32_t)u;
+            if (T > 0) u += group_units(v_gp[g], v_gp[g + 1]);
         }
-        int64_t tot;
-        const int64_t ex = block_exclusive_scan(nu, &tot, scan_sh);
-        if (nu > 0) {
-            const int64_t b = upper_index(v_gb, p.batch, g);
-            const int64_t r0 = (g - v_gb[b]) * kGroupTokens;
-            const int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)v_sq[b]) - 1;
-            const int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl);
-            for (int64_t q = 0; q < nu; ++q) {
-                const int64_t c = c0 + q;
-                const int64_t t0 = (T * c) / Gl, t1 = (T * (c + 1)) / Gl;
-                const int64_t u = running + ex + q;
-                int32_t* w = units + u * kUnitWords;
-                w[0] = (int32_t)b;
-                w[1] = (int32_t)r0;
-                w[2] = (int32_t)((max(t0, A) - A) * kTileKeys);
-                w[3] = (int32_t)min((min(t1, Bt) - A) * kTileKeys, n);
-                if (t0 >= A && t0 < Bt) {
-                    // the CTA's first unit; CTAs before it with an empty range (T < G) start here too
-                    cta_off[c] = (int32_t)u;
-                    for (int64_t ce = c - 1; ce >= 0 && (T * ce) / Gl == t0; --ce) cta_off[ce] = (int32_t)u;
-                }
-            }
-        }
-        running += tot;
+        if (tid == 0) v_uf[total_groups] = (int32_t)tot;
+        running = tot;
     }
+    __syncthreads();
+    // one thread per unit: its group (the largest with first unit <= u; groups without units
+    // share their successor's index), its CTA, and its key range
+    for (int64_t u = tid; u < (int64_t)running; u += blockDim.x) {
+        const int64_t g = upper_index(v_uf, total_groups, u);
+        const int64_t A = v_gp[g], Bt = v_gp[g + 1];
+        int64_t b, r0;
+        const int64_t n = group_keys(g, &b, &r0);
+        const int64_t k = u - v_uf[g];
+        const int64_t c = dense ? cta_of(A) + k : cta_of(A + k);
+        const int64_t t0 = cta_start(c), t1 = cta_start(c + 1);
+        int4 w;
+        w.x = (int32_t)b;
+        w.y = (int32_t)r0;
+        w.z = (int32_t)((max(t0, A) - A) * kTileKeys);
+        w.w = (int32_t)min((min(t1, Bt) - A) * kTileKeys, n);
+        *reinterpret_cast<int4*>(units + u * kUnitWords) = w;
+        if (t0 >= A && t0 < Bt) {
+            // the CTA's first unit; CTAs before it with an empty range (T < G) start here too
+            cta_off[c] = (int32_t)u;
+            for (int64_t ce = c - 1; ce >= 0 && cta_start(ce) == t0; --ce) cta_off[ce] = (int32_t)u;
+        }
+    }
+    __syncthreads();
     if (tid == 0) cta_off[G] = (int32_t)running;
     __syncthreads();
     if (tid == 0) {

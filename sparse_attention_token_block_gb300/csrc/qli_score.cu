@@ -563,12 +563,14 @@ __global__ void __launch_bounds__(kThreads, kScoreCtasPerSm)
     const bool meta_ok = meta[kMhMagic] == kMetaMagic && meta[kMhLayoutHash] == a.p.hash;
     if (!meta_ok && blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrMetadata);
     if (meta_ok && blockIdx.x == 0 && tid == 0 && meta[kMhErr]) atomicOr(a.err, (uint32_t)meta[kMhErr]);
-    const int G = meta_ok ? meta[kMhCtas] : 0;
+    const int G = meta_ok ? min(meta[kMhCtas], kMaxCtas) : 0;
+    const int64_t nunits = meta_ok ? min((int64_t)meta[kMhUnits], a.p.meta.max_units) : 0;
 
     // this CTA's unit lists: CTA-lists blockIdx.x, blockIdx.x + gridDim.x, ... (normally one)
     for (int c = blockIdx.x; c < G; c += gridDim.x) {
-        const int64_t ubeg = meta[a.p.meta.cta_off + c];
-        const int64_t uend = meta[a.p.meta.cta_off + c + 1];
+        // offsets clamped to the units written, whatever the buffer holds
+        const int64_t ubeg = max((int64_t)0, min((int64_t)meta[a.p.meta.cta_off + c], nunits));
+        const int64_t uend = max(ubeg, min((int64_t)meta[a.p.meta.cta_off + c + 1], nunits));
         if (uend > ubeg) {
             if (warp < kEpiWarp0) converter<kFp8, kScaleF32>(a, tmem, ubeg, uend);
             else if (warp < kProducerWarp) epilogue<kScaleF32>(a, tmem, ubeg, uend);
