@@ -7,8 +7,8 @@ long-context decode: 32 sequences, one query token each, 64 int8 heads of dim 12
 uniform in [8192, 32768] in 64-key pages under a random block_table, sparse_count 2048, causal.
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the launching
-stream with an L2 flush (a 512 MB write) between steps, outside the events; barrier +
-synchronize around the timed region; the maximum over ranks.  A second pass of up to 50 steps
+stream with an L2 flush (a 512 MB write, then a read of it) between steps, outside the events;
+barrier + synchronize around the timed region; the maximum over ranks.  A second pass of up to 50 steps
 puts events between the three kernels as well, for the per-stage times and the scoring kernel's
 roofline.  SM clocks and throttle reasons are
 sampled with nvidia-smi over ~1.5 s of identical untimed load steps ending where the timed steps
@@ -271,7 +271,7 @@ def config_of(case, args, world):
                             int(case.seq_lens_k.min()), int(case.seq_lens_k.max()),
                             case.block_size, case.sparse_count, case.sparse_mode, case.cmp_ratio),
             "global_batch": case.batch * world, "parallelism": "independent sequences per rank",
-            "l2": "flushed between timed steps (%d MB write, outside the events)" % args.flush_mb}
+            "l2": "flushed between timed steps (%d MB write, then read back; outside the events)" % args.flush_mb}
 
 
 def main():
@@ -299,7 +299,14 @@ def main():
     ix = Q.Indexer(p, device=dev)
     d = W.to_device(case, dev)
     flush = torch.empty(args.flush_mb * (1 << 20) // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(v):
+        # write a buffer larger than L2 (evicts every input), then read it back so that the
+        # write-back of those dirty lines also happens before the next timed region
+        flush.fill_(v)
+        torch.sum(flush, dim=0, dtype=torch.int64, out=flush_sink)
 
     def step(evs=None):
         if evs:
@@ -317,7 +324,7 @@ def main():
             evs[3].record(stream)
 
     for _ in range(max(3, args.warmup)):
-        flush.fill_(1)
+        flush_l2(1)
         step()
     torch.cuda.synchronize()
     st, bits = ix.device_error()
@@ -332,7 +339,7 @@ def main():
     t_end = time.perf_counter() + (0 if args.no_clocks else 1.5)
     while time.perf_counter() < t_end:
         for _ in range(20):
-            flush.fill_(2)
+            flush_l2(2)
             step()
         torch.cuda.synchronize()
     if dist:
@@ -341,7 +348,7 @@ def main():
     # the timed steps: events only at step boundaries, so the three kernels may overlap their
     # launches (programmatic dependent launch) as they do in use
     for i in range(args.steps):
-        flush.fill_(i)
+        flush_l2(i)
         evs[i][0].record(stream)
         step()
         evs[i][3].record(stream)
@@ -355,7 +362,7 @@ def main():
     stage_steps = max(3, min(args.steps, 50))
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(stage_steps)]
     for i in range(stage_steps):
-        flush.fill_(i)
+        flush_l2(i)
         step(sev[i])
     torch.cuda.synchronize()
     meta_ms = [e[0].elapsed_time(e[1]) for e in sev]
@@ -387,7 +394,7 @@ def main():
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.fill_(i)
+            flush_l2(i)
             ev[i][0].record(stream)
             e2e_step()
             ev[i][1].record(stream)

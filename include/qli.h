@@ -128,7 +128,7 @@ qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const i
  * `workspace` is caller-owned device scratch of at least qli_workspace_size(p) bytes, 256-byte
  * aligned, zeroed once after allocation (qli_workspace_init); calls sharing a workspace must be
  * ordered on one stream.  sparse_values must be NULL (README: return_value unsupported).
- * query, key and k_scale must be 16-byte aligned.
+ * query, key, weights, q_scale, k_scale and metadata must be 16-byte aligned.
  */
 qli_status qli_score_topk(const qli_problem* p, const void* query, const void* key,
                           const void* weights, const void* q_scale, const void* k_scale,

@@ -247,7 +247,7 @@ qli_status check_call(const qli_problem* p, const int32_t* metadata, size_t meta
     *P = params_of(p);
     *W = ws_layout(*P);
     if (metadata_words < (size_t)P->meta.total_words || workspace_bytes < W->total) return QLI_ERR_WORKSPACE_TOO_SMALL;
-    if (!metadata || !workspace || !aligned(workspace, 256)) return QLI_ERR_INVALID_ARG;
+    if (!metadata || !aligned(metadata, 16) || !workspace || !aligned(workspace, 256)) return QLI_ERR_INVALID_ARG;
     *sms = device_sms(nullptr);
     if (*sms < 0) return QLI_ERR_CUDA;
     if (*sms == 0) return QLI_ERR_NO_DEVICE;

@@ -60,7 +60,9 @@ enum BatchEntry {
     kBeGroups = 5,      // query groups ceil(Sq_b / kGroupTokens) (0 if invalid)
     kBeGroupBase = 6,   // index of the batch's first group
 };
-constexpr int kUnitWords = 4;   // {batch, first row within batch, key_begin, key_end}
+// a unit: {batch, first row within batch, key_begin, key_end, first output row, Sq_b, Sk_b, Lc_b}
+// (the batch's fields travel with the unit so that a reader needs one 32-byte load)
+constexpr int kUnitWords = 8;
 
 struct MetaLayout {
     int64_t batch_off, cta_off, group_off, ufirst_off, unit_off, total_words;

@@ -10,8 +10,8 @@
 //     of its last row (the largest in the group under either mask);
 //   * the split: the concatenated tile sequence of all groups is cut into G equal ranges, one per
 //     CTA of the score kernel; each range becomes the list of (batch, first row, key_begin,
-//     key_end) units it overlaps, stored CTA by CTA with offsets (computed in parallel over
-//     groups).
+//     key_end, first output row, Sq_b, Sk_b, Lc_b) units it overlaps, stored CTA by CTA with
+//     offsets (one thread per unit).
 #include "qli_internal.cuh"
 #include "qli_ptx.cuh"
 
@@ -70,7 +70,7 @@ __device__ int64_t upper_index(const View& a, int64_t n, int64_t key)
 
 constexpr int kSmemBatch = 2048;     // batches whose fields are staged in shared memory
 constexpr int kSmemGroups = 16384;   // groups whose tile prefix is staged in shared memory
-constexpr int kMetaSmemBytes = (5 * kSmemBatch + 2 * (kSmemGroups + 1)) * 4;
+constexpr int kMetaSmemBytes = (6 * kSmemBatch + 2 * (kSmemGroups + 1)) * 4;
 
 __global__ void __launch_bounds__(kMetaThreads, 1)
     metadata_kernel(Params p, const int32_t* __restrict__ seq_lens_q,
@@ -93,8 +93,9 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     const View v_lc = sb ? View{msm + 2 * kSmemBatch, 1} : View{be + kBeLc, kBatchWords};
     const View v_gb = sb ? View{msm + 3 * kSmemBatch, 1} : View{be + kBeGroupBase, kBatchWords};
     const View v_ok = sb ? View{msm + 4 * kSmemBatch, 1} : View{be + kBeOk, kBatchWords};
-    const View v_gp = sg ? View{msm + 5 * kSmemBatch, 1} : View{meta + p.meta.group_off, 1};
-    const View v_uf = sg ? View{msm + 5 * kSmemBatch + kSmemGroups + 1, 1} : View{meta + p.meta.ufirst_off, 1};
+    const View v_fr = sb ? View{msm + 5 * kSmemBatch, 1} : View{be + kBeFirstRow, kBatchWords};
+    const View v_gp = sg ? View{msm + 6 * kSmemBatch, 1} : View{meta + p.meta.group_off, 1};
+    const View v_uf = sg ? View{msm + 6 * kSmemBatch + kSmemGroups + 1, 1} : View{meta + p.meta.ufirst_off, 1};
     int32_t* gpre_home = meta + p.meta.group_off;
     if (tid == 0) { s_err = 0; s_tnd_bad = 0; }
     // the lengths may come from the previous kernel, and the previous indexer call may still read
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
             v_sk[b] = (int32_t)(ok ? sk : 0);
             v_lc[b] = (int32_t)lc;
             v_ok[b] = ok ? 1 : 0;
+            v_fr[b] = (int32_t)first;
         }
     }
     __syncthreads();
@@ -250,12 +252,18 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
         const int64_t k = u - v_uf[g];
         const int64_t c = dense ? cta_of(A) + k : cta_of(A + k);
         const int64_t t0 = cta_start(c), t1 = cta_start(c + 1);
-        int4 w;
+        int4 w, v;
         w.x = (int32_t)b;
         w.y = (int32_t)r0;
         w.z = (int32_t)((max(t0, A) - A) * kTileKeys);
         w.w = (int32_t)min((min(t1, Bt) - A) * kTileKeys, n);
-        *reinterpret_cast<int4*>(units + u * kUnitWords) = w;
+        v.x = v_fr[b] + (int32_t)r0;
+        v.y = v_sq[b];
+        v.z = v_sk[b];
+        v.w = v_lc[b];
+        int4* dst = reinterpret_cast<int4*>(units + u * kUnitWords);
+        dst[0] = w;
+        dst[1] = v;
         if (t0 >= A && t0 < Bt) {
             // the CTA's first unit; CTAs before it with an empty range (T < G) start here too
             cta_off[c] = (int32_t)u;

@@ -9,9 +9,9 @@
 //
 //   producer warp    per unit: bulk-copies the group's query codes, weights and query scales;
 //                    per tile: TMA-loads the 128 key rows (128 B each, 128-byte swizzle) from the
-//                    pages the block_table names into a 6-stage ring; its 32 lanes copy the keys'
-//                    scales with cp.async into an 8-slot scale ring (own barriers: the epilogue
-//                    releases those slots);
+//                    pages the block_table names into a 4-stage ring (the lanes look the pages up
+//                    a batch of tiles ahead); its 32 lanes copy the keys' scales with cp.async
+//                    into a 10-slot scale ring (own barriers: the epilogue releases those slots);
 //   converter warps  (4) per unit: fold W * |sQ|, convert the query codes to fp16 (negating heads
 //                    with sQ < 0) into the MMA's B operand (K-major, 128-byte swizzle);
 //                    per tile: one thread per key reads its row, converts int8 / e4m3 to fp16
@@ -42,7 +42,7 @@ namespace qli {
 namespace {
 
 constexpr int kStages = 4;                       // key ring depth
-constexpr int kScaleSlots = 6;                   // scale ring depth (released by the epilogue)
+constexpr int kScaleSlots = 10;                  // scale ring depth (released by the epilogue)
 constexpr int kGroups = 1;                       // converter and epilogue groups; tile i -> i % groups
 constexpr int kNumA = 2;                         // A buffers in tensor memory
 constexpr int kNumD = 2;                         // D buffers in tensor memory
@@ -168,17 +168,17 @@ struct Unit {
 
 __device__ __forceinline__ Unit read_unit(const ScoreArgs& a, int64_t u)
 {
-    const int32_t* w = a.meta + a.p.meta.unit_off + u * kUnitWords;
+    const int4* w = reinterpret_cast<const int4*>(a.meta + a.p.meta.unit_off + u * kUnitWords);
+    const int4 w0 = w[0], w1 = w[1];
     Unit x;
-    x.b = w[0];
-    x.r0 = w[1];
-    x.kb = w[2];
-    x.ke = w[3];
-    const int32_t* e = a.meta + a.p.meta.batch_off + (int64_t)x.b * kBatchWords;
-    x.sq = e[kBeSq];
-    x.sk = e[kBeSk];
-    x.lc = e[kBeLc];
-    x.row0 = e[kBeFirstRow] + x.r0;
+    x.b = w0.x;
+    x.r0 = w0.y;
+    x.kb = w0.z;
+    x.ke = w0.w;
+    x.row0 = w1.x;
+    x.sq = w1.y;
+    x.sk = w1.z;
+    x.lc = w1.w;
     x.q_cnt = min(kGroupTokens, x.sq - x.r0);
     x.ntiles = (x.ke - x.kb + kTileKeys - 1) / kTileKeys;
     return x;
@@ -187,9 +187,14 @@ __device__ __forceinline__ Unit read_unit(const ScoreArgs& a, int64_t u)
 // ------------------------------------------------------------------------------------------------
 // Producer warp
 // ------------------------------------------------------------------------------------------------
-// The producer's 32 lanes also fetch the key scales (4 keys per lane) with per-thread cp.async
-// copies whose completion the scale slot's barrier tracks: TMA copies of a few hundred bytes would
-// double the copy operations per tile, and the TMA engine's throughput here is per operation.
+// The producer's 32 lanes resolve the block_table for a batch of tiles at a time: lane l owns chunk
+// (l mod cpt) of tile (l / cpt) of the batch, cpt = 128 / R chunks of R keys per tile, and holds
+// that chunk's first row in the key pool (page * block_size + slot).  The next batch (or the next
+// unit's first batch) is looked up while the current one is issued, so a tile costs a barrier
+// wait, a scale copy and one TMA box per chunk issued by the chunk's lane.  The lanes also fetch
+// the key scales (4 keys per lane) with per-thread cp.async copies whose completion the scale
+// slot's barrier tracks: TMA copies of a few hundred bytes would double the copy operations per
+// tile, and the TMA engine's throughput here is per operation.
 template <bool kScaleF32>
 __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, int64_t ubeg, int64_t uend)
 {
@@ -197,15 +202,33 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
     const int lane = threadIdx.x & 31;
     const Params& p = a.p;
     constexpr int esz = kScaleF32 ? 4 : 2;
-    const int R = p.box_rows;             // keys per TMA box; divides block_size and 128
+    const int lgR = __ffs(p.box_rows) - 1;          // R = keys per TMA box: a power of two >= 16
+    const int R = 1 << lgR;
+    const int lgc = 7 - lgR;                         // cpt = 128 / R chunks per tile
+    const int cpt = 1 << lgc;
+    const int tpb = 32 >> lgc;                       // tiles per batch
     const int bs = p.block_size;
     if (p.test_stall) return;     // test switch: nothing arrives, the consumers' waits run out
+    // this lane's chunk of tile t0 + lane / cpt of unit y: its first row in the pool, or -1 past
+    // the unit's keys (a page outside the pool is reported and read as page 0)
+    auto chunk_row = [&](const Unit& y, int t0) -> int32_t {
+        const int key = y.kb + ((t0 + (lane >> lgc)) << 7) + ((lane & (cpt - 1)) << lgR);
+        if (key >= y.ke) return -1;
+        const int lp = key / bs;
+        int32_t page = __ldg(a.block_table + (int64_t)y.b * p.max_blocks_per_seq + lp);
+        if (page < 0 || page >= p.num_blocks) {
+            atomicOr(a.err, kErrPage);
+            page = 0;
+        }
+        return page * bs + (key - lp * bs);
+    };
     uint32_t tile_i = 0;
+    Unit xn = read_unit(a, ubeg);
+    int32_t rows_next = chunk_row(xn, 0);
     for (int64_t u = ubeg; u < uend; ++u) {
         const int uu = (int)(u - ubeg);
-        const Unit x = read_unit(a, u);
-        const int qb = uu & 1;
-        (void)qb;
+        const Unit x = xn;
+        if (u + 1 < uend) xn = read_unit(a, u + 1);   // in flight while this unit runs
         // one raw query buffer: unit uu's codes land after the converters took unit uu - 1's
         if (!wait_bar(&S.bars[kBarQrempty], (uu & 1) ^ 1, S.abort, a.err)) return;
         if (lane == 0) {
@@ -217,65 +240,38 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
             ptx::bulk_load(S.base + kOffWraw, a.weights + (int64_t)x.row0 * kHeads * esz, vbytes, bar);
             ptx::bulk_load(S.base + kOffSQraw, a.q_scale + (int64_t)x.row0 * kHeads * esz, vbytes, bar);
         }
-        // logical page / slot of the current chunk, advanced without division; the block_table
-        // entries of 32 consecutive logical pages sit one per lane (cur), the next 32 in nxt
-        const int32_t* table = a.block_table + (int64_t)x.b * p.max_blocks_per_seq;
-        const int lp_end = (x.ke + bs - 1) / bs;
-        int lp = x.kb / bs;
-        int slot = x.kb - lp * bs;
-        int wbase = lp;
-        int32_t cur = (wbase + lane < lp_end) ? __ldg(table + wbase + lane) : 0;
-        int32_t nxt = (wbase + 32 + lane < lp_end) ? __ldg(table + wbase + 32 + lane) : 0;
-        int key = x.kb;
-        for (int t = 0; t < x.ntiles; ++t, ++tile_i) {
-            const int s = tile_i % kStages;
-            if (!wait_bar(&S.bars[kBarKempty + s], ((tile_i / kStages) & 1) ^ 1, S.abort, a.err)) return;
-            const int tile_end = min(x.kb + (t + 1) * kTileKeys, x.ke);
-            // scales of this tile: lane l copies those of keys key + 4l .. key + 4l + 3 (one page,
-            // since bs % 16 == 0) into scale slot ss
-            {
-                const int ss = tile_i % kScaleSlots;
-                if (!wait_bar(&S.bars[kBarSempty + ss], ((tile_i / kScaleSlots) & 1) ^ 1, S.abort, a.err)) return;
-                const int k4 = key + 4 * lane;
-                const int off = k4 / bs - wbase;              // < 64: a tile spans <= 8 pages
-                const int32_t pc = __shfl_sync(0xffffffffu, cur, off & 31);
-                const int32_t pn = __shfl_sync(0xffffffffu, nxt, off & 31);
-                int32_t page = off < 32 ? pc : pn;
-                if (page < 0 || page >= p.num_blocks) page = 0;   // reported with the key rows
-                if (k4 < tile_end) {
-                    const int64_t e = (int64_t)page * bs + (k4 % bs);
-                    ptx::cp_async<4 * esz>(S.base + kOffSring + ss * kSslotBytes + lane * 4 * esz,
-                                           a.k_scale + e * esz);
+        for (int t0 = 0; t0 < x.ntiles; t0 += tpb) {
+            const int32_t rows = rows_next;
+            // look up the next batch of this unit, else the next unit's first batch
+            if (t0 + tpb < x.ntiles) rows_next = chunk_row(x, t0 + tpb);
+            else if (u + 1 < uend) rows_next = chunk_row(xn, 0);
+            const int nt = min(tpb, x.ntiles - t0);
+            for (int tt = 0; tt < nt; ++tt, ++tile_i) {
+                const int t = t0 + tt;
+                const int s = tile_i % kStages;
+                if (!wait_bar(&S.bars[kBarKempty + s], ((tile_i / kStages) & 1) ^ 1, S.abort, a.err)) return;
+                const int first = x.kb + (t << 7);
+                // scales of this tile: lane l copies those of keys first + 4l .. first + 4l + 3 (one
+                // chunk, since R >= 16)
+                {
+                    const int ss = tile_i % kScaleSlots;
+                    if (!wait_bar(&S.bars[kBarSempty + ss], ((tile_i / kScaleSlots) & 1) ^ 1, S.abort, a.err)) return;
+                    const int k4 = 4 * lane;
+                    const int32_t crow = __shfl_sync(0xffffffffu, rows, (tt << lgc) + (k4 >> lgR));
+                    if (first + k4 < x.ke)
+                        ptx::cp_async<4 * esz>(S.base + kOffSring + ss * kSslotBytes + lane * 4 * esz,
+                                               a.k_scale + ((int64_t)crow + (k4 & (R - 1))) * esz);
+                    ptx::cp_async_arrive_noinc(&S.bars[kBarSfull + ss]);
                 }
-                ptx::cp_async_arrive_noinc(&S.bars[kBarSfull + ss]);
+                // key rows: one box per chunk, issued by the chunk's lane
+                const int nch = (min(first + kTileKeys, x.ke) - first + R - 1) >> lgR;
+                uint64_t* bar = &S.bars[kBarKfull + s];
+                const int c = lane - (tt << lgc);
+                if (c == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nch * R * kDim));
+                __syncwarp();
+                if (c >= 0 && c < nch)
+                    ptx::tma_load_2d(S.base + kOffKring + s * kKstageBytes + c * R * kDim, tmap, 0, rows, bar);
             }
-            const int nchunks = (tile_end - key + R - 1) / R;
-            uint64_t* bar = &S.bars[kBarKfull + s];
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nchunks * R * kDim));
-            for (int c = 0; c < nchunks; ++c) {
-                if (lp - wbase >= 32) {     // slide the page window by 32
-                    wbase += 32;
-                    cur = nxt;
-                    nxt = (wbase + 32 + lane < lp_end) ? __ldg(table + wbase + 32 + lane) : 0;
-                }
-                int32_t page = __shfl_sync(0xffffffffu, cur, lp - wbase);
-                if (lane == 0) {
-                    if (page < 0 || page >= p.num_blocks) {
-                        atomicOr(a.err, kErrPage);
-                        page = 0;
-                    }
-                    const int64_t prow = (int64_t)page * bs + slot;
-                    ptx::tma_load_2d(S.base + kOffKring + s * kKstageBytes + c * R * kDim, tmap, 0,
-                                     (int32_t)prow, bar);
-                }
-                key += R;
-                slot += R;
-                if (slot == bs) {
-                    slot = 0;
-                    ++lp;
-                }
-            }
-            __syncwarp();
         }
     }
 }
@@ -287,9 +283,11 @@ __device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, int64
 {
     const Shared S = shared_view();
     uint32_t tile_i = 0;
+    Unit xn = read_unit(a, ubeg);
     for (int64_t u = ubeg; u < uend; ++u) {
         const int uu = (int)(u - ubeg);
-        const Unit x = read_unit(a, u);
+        const Unit x = xn;
+        if (u + 1 < uend) xn = read_unit(a, u + 1);   // in flight while this unit runs
         const int qb = uu & 1;
         if (!wait_bar(&S.bars[kBarQfull + qb], (uu >> 1) & 1, S.abort, a.err)) return;
         const uint32_t n = kHeads * x.q_cnt;
@@ -327,9 +325,11 @@ __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_
     const int tid = gtid % kGroupThreads, lane = tid & 31, warp = tid >> 5;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     uint32_t tile_i = 0;
+    Unit xn = read_unit(a, ubeg);
     for (int64_t u = ubeg; u < uend; ++u) {
         const int uu = (int)(u - ubeg);
-        const Unit x = read_unit(a, u);
+        const Unit x = xn;
+        if (u + 1 < uend) xn = read_unit(a, u + 1);   // in flight while this unit runs
         const int qb = uu & 1;
         if (uu % kGroups == grp) {   // this group converts the unit's query group
             if (!wait_bar(&S.bars[kBarQrfull], uu & 1, S.abort, a.err)) return;
@@ -387,20 +387,19 @@ __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_
             const uint8_t* krow = S.base + kOffKring + s * kKstageBytes + tid * kDim;
             if (!wait_bar(&S.bars[kBarAempty + ab], ((tile_i / kNumA) & 1) ^ 1, S.abort, a.err)) return;
             ptx::tc_fence_after();
+            // the whole 128-byte row comes in first, so the stage is released before any conversion
+            uint4 kr[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) kr[c] = *reinterpret_cast<const uint4*>(krow + ((c ^ (tid & 7)) << 4));
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&S.bars[kBarKempty + s]);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                uint4 kr[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    kr[c] = *reinterpret_cast<const uint4*>(krow + (((half * 4 + c) ^ (tid & 7)) << 4));
-                if (half == 1) {
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&S.bars[kBarKempty + s]);
-                }
                 uint32_t h[32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint32_t wv[4] = {kr[c].x, kr[c].y, kr[c].z, kr[c].w};
+                    const uint4 v = kr[half * 4 + c];
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if (kFp8) ptx::e4m3x4_to_f16x4(wv[q], h[c * 8 + 2 * q], h[c * 8 + 2 * q + 1]);
@@ -432,9 +431,11 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, int64_t
     const int key_lane = tid;
     const Params& p = a.p;
     uint32_t tile_i = 0;
+    Unit xn = read_unit(a, ubeg);
     for (int64_t u = ubeg; u < uend; ++u) {
         const int uu = (int)(u - ubeg);
-        const Unit x = read_unit(a, u);
+        const Unit x = xn;
+        if (u + 1 < uend) xn = read_unit(a, u + 1);   // in flight while this unit runs
         const int qb = uu & 1;
         if (!wait_bar(&S.bars[kBarQfull + qb], (uu >> 1) & 1, S.abort, a.err)) return;
         const float* wq = reinterpret_cast<const float*>(S.base + kOffWq) + qb * kGroupTokens * kHeads;
@@ -460,7 +461,8 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, int64_t
                 score[tt] = 0.0f;
                 if (tt < x.q_cnt) {
                     const float4* w4 = reinterpret_cast<const float4*>(wq + tt * kHeads);
-                    float a0 = 0.0f, a1 = 0.0f;
+                    // heads h, h+1 in acc0 and h+2, h+3 in acc1 (packed pairs: four fma chains)
+                    uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t d[32];
@@ -470,23 +472,34 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, int64_t
 #pragma unroll
                             for (int h = 0; h < 32; h += 4) {
                                 const float4 w = w4[(half * 32 + h) >> 2];
-                                a0 = fmaf(w.x, fmaxf(__uint_as_float(d[h]), 0.0f), a0);
-                                a1 = fmaf(w.y, fmaxf(__uint_as_float(d[h + 1]), 0.0f), a1);
-                                a0 = fmaf(w.z, fmaxf(__uint_as_float(d[h + 2]), 0.0f), a0);
-                                a1 = fmaf(w.w, fmaxf(__uint_as_float(d[h + 3]), 0.0f), a1);
+                                acc0 = ptx::fma2(ptx::pack2(w.x, w.y),
+                                                 ptx::pack2(fmaxf(__uint_as_float(d[h]), 0.0f),
+                                                            fmaxf(__uint_as_float(d[h + 1]), 0.0f)),
+                                                 acc0);
+                                acc1 = ptx::fma2(ptx::pack2(w.z, w.w),
+                                                 ptx::pack2(fmaxf(__uint_as_float(d[h + 2]), 0.0f),
+                                                            fmaxf(__uint_as_float(d[h + 3]), 0.0f)),
+                                                 acc1);
                             }
                         } else {
 #pragma unroll
                             for (int h = 0; h < 32; h += 4) {
                                 const float4 w = w4[(half * 32 + h) >> 2];
-                                a0 = fmaf(w.x, fminf(__uint_as_float(d[h]), 0.0f), a0);
-                                a1 = fmaf(w.y, fminf(__uint_as_float(d[h + 1]), 0.0f), a1);
-                                a0 = fmaf(w.z, fminf(__uint_as_float(d[h + 2]), 0.0f), a0);
-                                a1 = fmaf(w.w, fminf(__uint_as_float(d[h + 3]), 0.0f), a1);
+                                acc0 = ptx::fma2(ptx::pack2(w.x, w.y),
+                                                 ptx::pack2(fminf(__uint_as_float(d[h]), 0.0f),
+                                                            fminf(__uint_as_float(d[h + 1]), 0.0f)),
+                                                 acc0);
+                                acc1 = ptx::fma2(ptx::pack2(w.z, w.w),
+                                                 ptx::pack2(fminf(__uint_as_float(d[h + 2]), 0.0f),
+                                                            fminf(__uint_as_float(d[h + 3]), 0.0f)),
+                                                 acc1);
                             }
                         }
                     }
-                    score[tt] = sk * (a0 + a1);
+                    float a0, a1, a2, a3;
+                    ptx::unpack2(acc0, a0, a1);
+                    ptx::unpack2(acc1, a2, a3);
+                    score[tt] = sk * ((a0 + a2) + (a1 + a3));
                 }
             }
             ptx::tc_fence_before();
@@ -559,18 +572,28 @@ __global__ void __launch_bounds__(kThreads, kScoreCtasPerSm)
     ptx::pdl_launch_dependents();
 
     // the metadata must have been written for this problem
+    // the header and this CTA's first list offsets are loaded together (the grid never exceeds
+    // kMaxCtas, so the offsets are inside the buffer whatever it holds)
     const int32_t* meta = a.meta;
-    const bool meta_ok = meta[kMhMagic] == kMetaMagic && meta[kMhLayoutHash] == a.p.hash;
+    const int4 h0 = *reinterpret_cast<const int4*>(meta);          // magic, G, units, tiles
+    const int4 h1 = *reinterpret_cast<const int4*>(meta + 4);      // err, batch, rows, groups
+    const int32_t h_hash = meta[kMhLayoutHash];
+    const int32_t off_first = meta[a.p.meta.cta_off + blockIdx.x];
+    const int32_t off_next = meta[a.p.meta.cta_off + blockIdx.x + 1];
+    static_assert(kMhMagic == 0 && kMhCtas == 1 && kMhUnits == 2 && kMhErr == 4, "header layout");
+    const bool meta_ok = h0.x == kMetaMagic && h_hash == a.p.hash;
     if (!meta_ok && blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrMetadata);
-    if (meta_ok && blockIdx.x == 0 && tid == 0 && meta[kMhErr]) atomicOr(a.err, (uint32_t)meta[kMhErr]);
-    const int G = meta_ok ? min(meta[kMhCtas], kMaxCtas) : 0;
-    const int64_t nunits = meta_ok ? min((int64_t)meta[kMhUnits], a.p.meta.max_units) : 0;
+    if (meta_ok && blockIdx.x == 0 && tid == 0 && h1.x) atomicOr(a.err, (uint32_t)h1.x);
+    const int G = meta_ok ? min(h0.y, kMaxCtas) : 0;
+    const int64_t nunits = meta_ok ? min((int64_t)h0.z, a.p.meta.max_units) : 0;
 
     // this CTA's unit lists: CTA-lists blockIdx.x, blockIdx.x + gridDim.x, ... (normally one)
     for (int c = blockIdx.x; c < G; c += gridDim.x) {
         // offsets clamped to the units written, whatever the buffer holds
-        const int64_t ubeg = max((int64_t)0, min((int64_t)meta[a.p.meta.cta_off + c], nunits));
-        const int64_t uend = max(ubeg, min((int64_t)meta[a.p.meta.cta_off + c + 1], nunits));
+        const int64_t o0 = c == (int)blockIdx.x ? off_first : meta[a.p.meta.cta_off + c];
+        const int64_t o1 = c == (int)blockIdx.x ? off_next : meta[a.p.meta.cta_off + c + 1];
+        const int64_t ubeg = max((int64_t)0, min(o0, nunits));
+        const int64_t uend = max(ubeg, min(o1, nunits));
         if (uend > ubeg) {
             if (warp < kEpiWarp0) converter<kFp8, kScaleF32>(a, tmem, ubeg, uend);
             else if (warp < kProducerWarp) epilogue<kScaleF32>(a, tmem, ubeg, uend);

@@ -4,20 +4,24 @@
 // One 1024-thread CTA per output row.  Scores are held as order-preserving uint32 codes; a key's
 // full sort key is (code << 32) | (0xFFFFFFFF - index): score descending, then index ascending.
 //
-// 1. Candidates.  n <= kCap: every visible key.  n <= 32768: the row is held in registers and a
-//    two-level 2048-bin histogram over its code range narrows the k-th largest code to a sub-bin;
-//    every key in that sub-bin or above is a candidate.  Longer rows: a threshold code is the rank-r largest
-//    of 2048 evenly spaced keys of the row (radix select over the samples), with
-//    r = 1.15 k S / n + 4 sqrt(k S / n) + 2, which leaves between k and kCap keys at or above it
-//    with overwhelming probability; one pass gathers them.  Outside [k, kCap], an exact radix
-//    select on the 64-bit sort keys finds the k-th key and exactly k keys are gathered.
-// 2. Order.  The candidates are distributed into 8192 buckets by code (bucket 0 = highest codes;
-//    the code range is scaled to the bucket count), and each bucket is insertion-sorted by its
-//    owner thread on the full sort key.  If any bucket holds more than kBigBucket keys (heavy ties),
-//    a block-wide bitonic sort on the 64-bit sort keys is used instead.
-// 3. The first min(k, n) indices are written, then -1 up to sparse_count.  Rows with no visible
-//    key, rows of an invalid batch and rows whose batch's block_table names a page outside the pool
-//    are all -1.
+// Rows of up to kCacheKeys keys are bulk-copied into shared memory and ordered by bins:
+//   1. the code range [lo, hi] of the row is cut into kBins equal bins (bin 0 holds the highest
+//      codes) and one pass counts the keys per bin;
+//   2. a scan finds the bin where the running count reaches min(k, n); every key in it or in a
+//      higher bin is a candidate, and the scan gives each bin its place in the candidate array;
+//   3. one pass scatters the candidates into their bins;
+//   4. each candidate's position is its bin's start plus the number of candidates of its bin with a
+//      larger sort key.
+// Longer rows first gather, in one pass over global memory, the keys at or above a threshold code:
+// the rank-r largest of 2048 evenly spaced keys of the row (radix select over the samples), with
+// r = 1.15 k S / n + 4 sqrt(k S / n) + 2, which leaves between k and kCap keys at or above it with
+// overwhelming probability; the same bins then order them.  Whenever the candidates would exceed
+// kCap (heavy ties) an exact radix select on the 64-bit sort keys finds the k-th key and exactly k
+// keys are gathered; when a bin holds more than kBigBucket candidates, a block-wide bitonic sort
+// orders them instead of step 4.
+// The first min(k, n) indices are written, then -1 up to sparse_count.  Rows with no visible key,
+// rows of an invalid batch and rows whose batch's block_table names a page outside the pool are all
+// -1.
 #include "qli_internal.cuh"
 #include "qli_ptx.cuh"
 
@@ -29,11 +33,13 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 4096;                    // candidates held in shared memory
 constexpr int kSamples = 2048;
-constexpr int kBuckets = 2048;
+constexpr int kBins = 8192;                   // ordering bins
+constexpr int kBinsPerThread = kBins / kThreads;
+constexpr int kSampleBins = 2048;             // bins of the sample histogram
 constexpr int kBigBucket = 256;
-constexpr int kOrderBuckets = 8192;           // ordering buckets (counters kept in the row cache)
 constexpr int kCacheKeys = 32768;             // score lines up to this length are cached in smem
-constexpr int kSmemBytes = kCacheKeys * 4 + 4 * kCap * 4 + 2 * kBuckets * 4 + 256 * 4 + 64 * 4 + 16;
+constexpr int kMiscWords = 128;
+constexpr int kSmemBytes = (kCacheKeys + kBins + 3 * kCap + 256 + kMiscWords) * 4 + 16;
 
 struct TopkArgs {
     Params p;
@@ -45,15 +51,13 @@ struct TopkArgs {
 };
 
 struct Smem {
-    uint32_t* key;    // [kCap] candidate codes (gather order)
+    uint32_t* cache;  // [kCacheKeys] one score line (uncached rows: scatter targets)
+    uint32_t* bins;   // [kBins] bin counts, then bin ends / starts; bitonic scratch
+    uint32_t* key;    // [kCap] candidate codes
     uint32_t* val;    // [kCap] candidate indices
-    uint32_t* okey;   // [kCap] ordered codes
-    uint32_t* oval;   // [kCap] ordered indices
-    uint32_t* cnt;    // [kBuckets]
-    uint32_t* off;    // [kBuckets]
-    uint32_t* hist;   // [256]
-    uint32_t* misc;   // [64]
-    uint32_t* cache;  // [kCacheKeys] one score line
+    uint32_t* outv;   // [kCap] ordered indices
+    uint32_t* hist;   // [256] radix-select digits
+    uint32_t* misc;   // [kMiscWords] reduction scratch
     uint64_t* bar;    // bulk-copy barrier
 };
 
@@ -88,25 +92,6 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* total, uint32_t* sh /*
     *total = sh[kWarps - 1];
     __syncthreads();
     return before;
-}
-
-__device__ uint32_t block_max(uint32_t v, uint32_t* sh)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (lane == 0) sh[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        uint32_t w = lane < kWarps ? sh[lane] : 0u;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, o));
-        if (lane == 0) sh[32] = w;
-    }
-    __syncthreads();
-    const uint32_t r = sh[32];
-    __syncthreads();
-    return r;
 }
 
 // Radix select over 64-bit sort keys produced by `get(i)` for i < n: the k-th largest key
@@ -179,8 +164,8 @@ __device__ uint64_t radix_select(const Smem& S, int64_t n, int k, Get get, int t
     return prefix;
 }
 
-// Gather (unordered) the keys j < n whose sort key is >= t64; returns how many (only the first
-// kCap are stored).
+// Gather (unordered) into key/val the keys j < n of `line` (shared or global memory) whose sort
+// key is >= t64; returns how many (only the first kCap are stored).
 __device__ int gather(const Smem& S, const uint32_t* line, int64_t n, uint64_t t64)
 {
     const int tid = threadIdx.x, lane = tid & 31;
@@ -192,7 +177,7 @@ __device__ int gather(const Smem& S, const uint32_t* line, int64_t n, uint64_t t
         uint32_t c = 0;
         bool take = false;
         if (j < n) {
-            c = __ldg(line + j);
+            c = line[j];
             take = sort_key(c, (uint32_t)j) >= t64;
         }
         const unsigned bal = __ballot_sync(0xffffffffu, take);
@@ -267,192 +252,340 @@ __device__ void bitonic_desc(uint64_t (&v)[E], uint64_t* xbuf)
     }
 }
 
-// Slow path: order key/val[0..c) with the bitonic network; the ordered indices end in val.
+// Order keys[0..c) / vals[0..c) descending by sort key with the bitonic network (c <= kThreads *
+// E); the ordered indices end in vals.  `scratch` holds kThreads * E 64-bit words.
 template <int E>
-__device__ void bitonic_order(const Smem& S, int c)
+__device__ void bitonic_order(uint32_t* keys, uint32_t* vals, int c, uint64_t* scratch)
 {
     uint64_t v[E];
     const int tid = threadIdx.x;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const int i = tid * E + e;
-        v[e] = i < c ? sort_key(S.key[i], S.val[i]) : 0ull;   // 0 sorts below every real key
+        v[e] = i < c ? sort_key(keys[i], vals[i]) : 0ull;   // 0 sorts below every real key
     }
     __syncthreads();
-    bitonic_desc<E>(v, reinterpret_cast<uint64_t*>(S.okey));   // okey/oval double as 64-bit scratch
+    bitonic_desc<E>(v, scratch);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const int i = tid * E + e;
-        if (i < c) S.val[i] = 0xFFFFFFFFu - (uint32_t)(v[e] & 0xFFFFFFFFu);
+        if (i < c) vals[i] = 0xFFFFFFFFu - (uint32_t)(v[e] & 0xFFFFFFFFu);
     }
     __syncthreads();
 }
 
-// Order the c candidates (key/val) descending by sort key; the ordered indices end in val.
-// lo = lower bound of codes.  The buckets' counters live in the row cache, idle by now.
-__device__ void order_candidates(const Smem& S, int c, uint32_t lo)
+__device__ void bitonic_any(uint32_t* keys, uint32_t* vals, int c, uint64_t* scratch)
 {
-    const int tid = threadIdx.x;
-    uint32_t* cnt = S.cache;                       // [kOrderBuckets]
-    uint32_t* off = S.cache + kOrderBuckets;       // [kOrderBuckets]
-    constexpr int per = kOrderBuckets / kThreads;
-    uint32_t hi_local = 0;
-    for (int i = tid; i < c; i += kThreads) hi_local = max(hi_local, S.key[i]);
-    const uint32_t hi = block_max(hi_local, S.misc);
-    const uint32_t range = hi - lo;
-    int shift = 0;
-    while (shift < 32 && (range >> shift) >= (uint32_t)kOrderBuckets) ++shift;
-    for (int b = tid; b < kOrderBuckets; b += kThreads) cnt[b] = 0;
-    __syncthreads();
-    for (int i = tid; i < c; i += kThreads) atomicAdd(&cnt[(hi - S.key[i]) >> shift], 1u);
-    __syncthreads();
-    // exclusive scan of the bucket counts, `per` consecutive buckets per thread
-    uint32_t mine[per], sum = 0;
-    bool big = false;
+    if (c <= kThreads) bitonic_order<1>(keys, vals, c, scratch);
+    else if (c <= 2 * kThreads) bitonic_order<2>(keys, vals, c, scratch);
+    else bitonic_order<4>(keys, vals, c, scratch);
+}
+
+// Calls f(i, code) for every i < c, reading src (16-byte aligned) four codes at a time
+template <class F>
+__device__ __forceinline__ void for_each_code(const uint32_t* src, int c, F f)
+{
+    const int c4 = c >> 2;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    for (int i = threadIdx.x; i < c4; i += kThreads) {
+        const uint4 v = s4[i];
+        f(4 * i, v.x);
+        f(4 * i + 1, v.y);
+        f(4 * i + 2, v.z);
+        f(4 * i + 3, v.w);
+    }
+    for (int i = 4 * c4 + (int)threadIdx.x; i < c; i += kThreads) f(i, src[i]);
+}
+
+// Largest of one value per thread and smallest of another, returned to every thread
+__device__ void block_max_min(uint32_t* mx, uint32_t* mn, uint32_t* sh /* >= 98 */)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t a = *mx, b = *mn;
 #pragma unroll
-    for (int q = 0; q < per; ++q) {
-        mine[q] = cnt[tid * per + q];
-        sum += mine[q];
-        big |= mine[q] > (uint32_t)kBigBucket;
+    for (int o = 16; o > 0; o >>= 1) {
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+        b = min(b, __shfl_xor_sync(0xffffffffu, b, o));
     }
-    uint32_t total;
-    uint32_t base = block_excl_scan(sum, &total, S.misc);
+    if (lane == 0) {
+        sh[warp] = a;
+        sh[64 + warp] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        a = sh[lane];
+        b = sh[64 + lane];
 #pragma unroll
-    for (int q = 0; q < per; ++q) {
-        off[tid * per + q] = base;
-        base += mine[q];
-    }
-    if (__syncthreads_or(big)) {
-        if (c <= kThreads) bitonic_order<1>(S, c);
-        else if (c <= 2 * kThreads) bitonic_order<2>(S, c);
-        else bitonic_order<4>(S, c);
-        return;
-    }
-    // scatter (filling each bucket from its end), then place every candidate at its bucket's start
-    // plus its rank among the bucket's keys (one thread per candidate)
-    for (int i = tid; i < c; i += kThreads) {
-        const uint32_t b = (hi - S.key[i]) >> shift;
-        const uint32_t pos = off[b] + atomicSub(&cnt[b], 1u) - 1u;
-        S.okey[pos] = S.key[i];
-        S.oval[pos] = S.val[i];
-    }
-    __syncthreads();
-    for (int i = tid; i < c; i += kThreads) {
-        const uint32_t kc = S.okey[i], kv = S.oval[i];
-        const uint64_t kk = sort_key(kc, kv);
-        const uint32_t b = (hi - kc) >> shift;
-        const uint32_t s0 = off[b];
-        const uint32_t e0 = (b + 1 < (uint32_t)kOrderBuckets) ? off[b + 1] : (uint32_t)c;
-        uint32_t r = 0;
-        for (uint32_t j = s0; j < e0; ++j) r += sort_key(S.okey[j], S.oval[j]) > kk ? 1u : 0u;
-        S.val[s0 + r] = kv;
-    }
-    __syncthreads();
-}
-
-// Find, from per-bin counts in S.cnt (bin 0 = highest codes), the bin where the running count
-// reaches `need`; returns it and stores the count of the bins before it in *above.
-__device__ uint32_t locate_bin(const Smem& S, uint32_t need, uint32_t* above)
-{
-    const int tid = threadIdx.x;
-    const uint32_t c0 = S.cnt[2 * tid], c1 = S.cnt[2 * tid + 1];
-    uint32_t total;
-    const uint32_t before = block_excl_scan(c0 + c1, &total, S.misc);
-    uint32_t* s_bin = S.misc + 56;
-    uint32_t* s_above = S.misc + 57;
-    if (before < need && before + c0 >= need) {
-        *s_bin = 2 * tid;
-        *s_above = before;
-    } else if (before + c0 < need && before + c0 + c1 >= need) {
-        *s_bin = 2 * tid + 1;
-        *s_above = before + c0;
-    }
-    __syncthreads();
-    const uint32_t b = *s_bin;
-    *above = *s_above;
-    __syncthreads();
-    return b;
-}
-
-// Rows of up to kCacheKeys keys, whose score line the caller bulk-copied into shared memory (one
-// memory latency).  A 2048-bin histogram over the line's code range finds the bin holding the k-th
-// largest code; a second 2048-bin histogram over that bin alone narrows it to a sub-bin.  Every
-// key above that sub-bin's lower edge becomes a candidate (written to key/val).  Returns the
-// candidate count, or -1 if it would exceed kCap; *lo receives a lower bound of their codes.
-__device__ int select_cached(const Smem& S, int64_t n, int k, uint32_t* lo)
-{
-    const int tid = threadIdx.x, lane = tid & 31;
-    const uint32_t* cache = S.cache;
-    uint32_t mn = 0xFFFFFFFFu, mx = 0;
-    for (int64_t j = tid; j < n; j += kThreads) {
-        const uint32_t c = cache[j];
-        mn = min(mn, c);
-        mx = max(mx, c);
-    }
-    mx = block_max(mx, S.misc);
-    mn = ~block_max(~mn, S.misc);
-    const uint32_t need = (uint32_t)((int64_t)k < n ? (int64_t)k : n);
-    // level 1: the whole range
-    int s1 = 0;
-    while (s1 < 32 && ((mx - mn) >> s1) >= (uint32_t)kBuckets) ++s1;
-    for (int b = tid; b < kBuckets; b += kThreads) S.cnt[b] = 0;
-    __syncthreads();
-    for (int64_t j = tid; j < n; j += kThreads) atomicAdd(&S.cnt[(mx - cache[j]) >> s1], 1u);
-    __syncthreads();
-    uint32_t above1;
-    const uint32_t b1 = locate_bin(S, need, &above1);
-    // level 2: inside bin b1 (offsets below mx in [b1 << s1, (b1 + 1) << s1))
-    const int s2 = s1 > 11 ? s1 - 11 : 0;
-    for (int b = tid; b < kBuckets; b += kThreads) S.cnt[b] = 0;
-    __syncthreads();
-    for (int64_t j = tid; j < n; j += kThreads) {
-        const uint32_t d = mx - cache[j];
-        if ((d >> s1) == b1) atomicAdd(&S.cnt[(d - (b1 << s1)) >> s2], 1u);
-    }
-    __syncthreads();
-    uint32_t above2;
-    const uint32_t b2 = locate_bin(S, need - above1, &above2);
-    (void)lane;
-    const uint64_t lim = (static_cast<uint64_t>(b1) << s1) + ((static_cast<uint64_t>(b2) + 1) << s2);
-    // every key with (mx - code) below the end of sub-bin b2 is a candidate: count per thread,
-    // scan, then write (thread t owns the keys t, t + kThreads, ...)
-    uint32_t mine = 0;
-    for (int64_t j = tid; j < n; j += kThreads) mine += (uint64_t)(mx - cache[j]) < lim ? 1u : 0u;
-    uint32_t total;
-    uint32_t pos = block_excl_scan(mine, &total, S.misc);
-    for (int64_t j = tid; j < n; j += kThreads) {
-        const uint32_t cj = cache[j];
-        if ((uint64_t)(mx - cj) < lim) {
-            if (pos < (uint32_t)kCap) {
-                S.key[pos] = cj;
-                S.val[pos] = (uint32_t)j;
-            }
-            ++pos;
+        for (int o = 16; o > 0; o >>= 1) {
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+            b = min(b, __shfl_xor_sync(0xffffffffu, b, o));
+        }
+        if (lane == 0) {
+            sh[96] = a;
+            sh[97] = b;
         }
     }
+    __syncthreads();
+    *mx = sh[96];
+    *mn = sh[97];
+    __syncthreads();
+}
+
+constexpr uint32_t kNoBin = 0xFFFFFFFFu;
+
+// Ordering of the candidates among c codes src[0..c) (shared memory, 16-byte aligned), source
+// index idx(i).  bin(code) is non-increasing in the code and either kNoBin (not a candidate) or
+// below kBins; bin 0 holds the highest codes.  Steps 1-4 above: the first min(need, #candidates)
+// positions of the order go to S.outv.  Candidates are scattered into tkey / tval (kCap each,
+// distinct from src); a bin of more than kBigBucket candidates sends them to the bitonic network
+// instead of step 4.  kBinTooMany: the bins up to the one reaching `need` hold more than kCap
+// keys, or fewer than `need` keys have a bin (nothing ordered).
+enum BinResult { kBinOrdered = 0, kBinTooMany = 1 };
+
+template <class Idx, class Bin>
+__device__ int bin_order(const Smem& S, const uint32_t* src, int c, Idx idx, int need, Bin bin,
+                         uint32_t* tkey, uint32_t* tval)
+{
+    const int tid = threadIdx.x;
+    uint32_t* bins = S.bins;
+    for (int b = tid; b < kBins; b += kThreads) bins[b] = 0;
+    __syncthreads();
+    // 1. counts per bin
+    for_each_code(src, c, [&](int, uint32_t x) {
+        const uint32_t b = bin(x);
+        if (b != kNoBin) atomicAdd(&bins[b], 1u);
+    });
+    __syncthreads();
+    // 2. thread t scans bins [8t, 8t + 8); the threshold bin is where the running count reaches need
+    uint32_t cnt[kBinsPerThread], sum = 0;
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) {
+        cnt[q] = bins[tid * kBinsPerThread + q];
+        sum += cnt[q];
+    }
+    uint32_t total;
+    const uint32_t before = block_excl_scan(sum, &total, S.misc);
+    uint32_t* s_thr = S.misc + 56;
+    uint32_t* s_cc = S.misc + 57;
+    if (before < (uint32_t)need && before + sum >= (uint32_t)need) {
+        uint32_t run = before;
+#pragma unroll
+        for (int q = 0; q < kBinsPerThread; ++q) {
+            if (run < (uint32_t)need && run + cnt[q] >= (uint32_t)need) {
+                *s_thr = tid * kBinsPerThread + q;
+                *s_cc = run + cnt[q];
+            }
+            run += cnt[q];
+        }
+    }
+    __syncthreads();
+    const uint32_t thr = *s_thr;
+    const int cc = (int)*s_cc;
+    if (total < (uint32_t)need || cc > kCap) {
+        __syncthreads();
+        return kBinTooMany;
+    }
+    // bin ends (inclusive prefix) for the scatter, which fills each bin from its end; a heavy bin
+    // among the candidates sends the order to the bitonic network
+    bool big = false;
+    {
+        uint32_t run = before;
+#pragma unroll
+        for (int q = 0; q < kBinsPerThread; ++q) {
+            const uint32_t b = tid * kBinsPerThread + q;
+            run += cnt[q];
+            bins[b] = run;
+            big |= b <= thr && cnt[q] > (uint32_t)kBigBucket;
+        }
+    }
+    big = __syncthreads_or(big);
+    // 3. scatter the candidates
+    for_each_code(src, c, [&](int i, uint32_t x) {
+        const uint32_t b = bin(x);
+        if (b <= thr) {                            // kNoBin never is
+            const uint32_t pos = atomicSub(&bins[b], 1u) - 1u;
+            tkey[pos] = x;
+            tval[pos] = idx(i);
+        }
+    });
+    __syncthreads();
+    if (big) {
+        bitonic_any(tkey, tval, cc, reinterpret_cast<uint64_t*>(S.bins));
+        for (int i = tid; i < need; i += kThreads) S.outv[i] = tval[i];
+        __syncthreads();
+        return kBinOrdered;
+    }
+    // 4. rank inside the bin (bins[b] is now the bin's start)
+    for (int i = tid; i < cc; i += kThreads) {
+        const uint32_t kc = tkey[i], kv = tval[i];
+        const uint64_t kk = sort_key(kc, kv);
+        const uint32_t b = bin(kc);
+        const uint32_t s0 = bins[b];
+        const uint32_t e0 = b < thr ? bins[b + 1] : (uint32_t)cc;
+        uint32_t r = 0;
+        for (uint32_t j = s0; j < e0; ++j) r += sort_key(tkey[j], tval[j]) > kk ? 1u : 0u;
+        S.outv[s0 + r] = kv;
+    }
+    __syncthreads();
+    return kBinOrdered;
+}
+
+// Bins over the whole code range [lo, hi] of src[0..c) (all keys are candidates)
+template <class Idx>
+__device__ int order_all(const Smem& S, const uint32_t* src, int c, Idx idx, int need, uint32_t* tkey,
+                         uint32_t* tval)
+{
+    uint32_t hi = 0, lo = 0xFFFFFFFFu;
+    for_each_code(src, c, [&](int, uint32_t x) {
+        hi = max(hi, x);
+        lo = min(lo, x);
+    });
+    block_max_min(&hi, &lo, S.misc);
+    int shift = 0;
+    while (shift < 32 && ((hi - lo) >> shift) >= (uint32_t)kBins) ++shift;
+    return bin_order(S, src, c, idx, need, [hi, shift](uint32_t x) { return (hi - x) >> shift; }, tkey,
+                     tval);
+}
+
+// Append the code and index of every key of src[0..c) (shared memory, 16-byte aligned) whose code
+// is at least L to S.key / S.val, one shared counter update per warp and four keys; returns how
+// many (only the first kCap are stored).
+__device__ int compact_at_least(const Smem& S, const uint32_t* src, int c, uint32_t L)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+    const unsigned below = (1u << lane) - 1u;
     uint32_t* s_cnt = S.misc + 48;
-    if (tid == 0) *s_cnt = total;
+    if (tid == 0) *s_cnt = 0;
     __syncthreads();
-    const int count = (int)*s_cnt;
-    *lo = lim > (uint64_t)(mx - mn) ? mn : (uint32_t)(mx - lim + 1);
+    const int c4 = c >> 2;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    for (int i0 = 0; i0 < c4; i0 += kThreads) {         // the same trip count in every lane
+        const int i = i0 + tid;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        const bool in = i < c4;
+        if (in) v = s4[i];
+        const bool f0 = in && v.x >= L, f1 = in && v.y >= L, f2 = in && v.z >= L, f3 = in && v.w >= L;
+        const unsigned b0 = __ballot_sync(0xffffffffu, f0), b1 = __ballot_sync(0xffffffffu, f1);
+        const unsigned b2 = __ballot_sync(0xffffffffu, f2), b3 = __ballot_sync(0xffffffffu, f3);
+        const uint32_t n0 = __popc(b0), n1 = __popc(b1), n2 = __popc(b2), n3 = __popc(b3);
+        const uint32_t nw = n0 + n1 + n2 + n3;
+        if (nw == 0) continue;
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(s_cnt, nw);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        auto put = [&](bool f, uint32_t pos, uint32_t code, int j) {
+            if (f && pos < (uint32_t)kCap) {
+                S.key[pos] = code;
+                S.val[pos] = (uint32_t)j;
+            }
+        };
+        put(f0, base + __popc(b0 & below), v.x, 4 * i);
+        put(f1, base + n0 + __popc(b1 & below), v.y, 4 * i + 1);
+        put(f2, base + n0 + n1 + __popc(b2 & below), v.z, 4 * i + 2);
+        put(f3, base + n0 + n1 + n2 + __popc(b3 & below), v.w, 4 * i + 3);
+    }
+    for (int i0 = 4 * c4; i0 < c; i0 += kThreads) {
+        const int i = i0 + tid;
+        const uint32_t x = i < c ? src[i] : 0u;
+        const bool f = i < c && x >= L;
+        const unsigned b = __ballot_sync(0xffffffffu, f);
+        if (b == 0) continue;
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(s_cnt, (uint32_t)__popc(b));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const uint32_t pos = base + __popc(b & below);
+        if (f && pos < (uint32_t)kCap) {
+            S.key[pos] = x;
+            S.val[pos] = (uint32_t)i;
+        }
+    }
     __syncthreads();
-    return count > kCap ? -1 : count;
+    const int m = (int)*s_cnt;
+    __syncthreads();
+    return m;
+}
+
+// Cached rows longer than kCap (the line in S.cache[0..c)): a lower bound L for the candidates'
+// codes from a sample of kThreads evenly spaced keys -- the code of the rank-r largest sample,
+// r = 1.15 l + 4 sqrt(l) + 2 with l = need * kThreads / c the samples expected above the need-th
+// key; the keys at or above L are compacted into S.key / S.val, then ordered by bins over
+// [L, largest sample] (codes above it share bin 0), scattered into the idle row cache.
+// kBinTooMany when fewer than `need` or more than kCap keys reach L (the caller falls back to
+// the exact selection).
+__device__ int order_sampled(const Smem& S, int c, int need)
+{
+    const int tid = threadIdx.x;
+    const uint32_t* src = S.cache;
+    const uint32_t x = src[((int64_t)tid * c) / kThreads];
+    uint32_t smx = x, smn = x;
+    block_max_min(&smx, &smn, S.misc);
+    // the sample's rank-r largest code, to the resolution of kSampleBins bins over its range
+    int s1 = 0;
+    while (s1 < 32 && ((smx - smn) >> s1) >= (uint32_t)kSampleBins) ++s1;
+    uint32_t* sb = S.bins;
+    for (int b = tid; b < kSampleBins; b += kThreads) sb[b] = 0;
+    __syncthreads();
+    atomicAdd(&sb[(smx - x) >> s1], 1u);
+    __syncthreads();
+    const float lam = (float)need * (float)kThreads / (float)c;   // single precision: FP64 is slow here
+    int r = (int)(1.15f * lam + 4.0f * sqrtf(lam) + 2.0f);
+    r = r < 1 ? 1 : (r > kThreads ? kThreads : r);
+    constexpr int per = kSampleBins / kThreads;
+    uint32_t cnt[per], sum = 0;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+        cnt[q] = sb[tid * per + q];
+        sum += cnt[q];
+    }
+    uint32_t total;
+    const uint32_t before = block_excl_scan(sum, &total, S.misc);
+    uint32_t* s_b = S.misc + 58;
+    if (before < (uint32_t)r && before + sum >= (uint32_t)r) {
+        uint32_t run = before;
+#pragma unroll
+        for (int q = 0; q < per; ++q) {
+            if (run < (uint32_t)r && run + cnt[q] >= (uint32_t)r) *s_b = tid * per + q;
+            run += cnt[q];
+        }
+    }
+    __syncthreads();
+    const uint32_t b1 = *s_b;
+    __syncthreads();
+    // L: the lowest code of bin b1
+    const uint64_t span = ((uint64_t)b1 + 1) << s1;
+    const uint32_t L = span > (uint64_t)(smx - smn) ? smn : (uint32_t)(smx - span + 1);
+    const int m = compact_at_least(S, src, c, L);
+    if (m < need || m > kCap) return kBinTooMany;
+    int shift = 0;
+    while (shift < 32 && ((smx - L) >> shift) >= (uint32_t)kBins) ++shift;
+    const uint32_t* vals = S.val;
+    return bin_order(
+        S, S.key, m, [vals](int i) { return vals[i]; }, need,
+        [L, smx, shift](uint32_t v) { return v < L ? kNoBin : (v >= smx ? 0u : (smx - v) >> shift); },
+        S.cache, S.cache + kCap);
+}
+
+// Exact fallback: the k-th largest sort key of the row (radix select), then exactly k keys at or
+// above it, ordered by the bitonic network; the ordered indices end in S.val.
+__device__ void exact_topk(const Smem& S, const uint32_t* line, int64_t n, int k)
+{
+    const uint64_t T = radix_select(S, n, k, [&](int64_t j) { return sort_key(line[j], (uint32_t)j); }, 56);
+    const int c = min(gather(S, line, n, T), kCap);
+    bitonic_any(S.key, S.val, c, reinterpret_cast<uint64_t*>(S.bins));
 }
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ TopkArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     Smem S;
-    S.key = reinterpret_cast<uint32_t*>(smem);
+    S.cache = reinterpret_cast<uint32_t*>(smem);
+    S.bins = S.cache + kCacheKeys;
+    S.key = S.bins + kBins;
     S.val = S.key + kCap;
-    S.okey = S.val + kCap;
-    S.oval = S.okey + kCap;
-    S.cnt = S.oval + kCap;
-    S.off = S.cnt + kBuckets;
-    S.hist = S.off + kBuckets;
+    S.outv = S.val + kCap;
+    S.hist = S.outv + kCap;
     S.misc = S.hist + 256;
-    S.cache = S.misc + 64;                                    // 16-byte aligned (offsets are)
-    S.bar = reinterpret_cast<uint64_t*>(S.cache + kCacheKeys);
+    S.bar = reinterpret_cast<uint64_t*>(S.misc + kMiscWords);
     if (threadIdx.x == 0) {
         ptx::mbar_init(S.bar, 1);
         ptx::fence_mbar_init();
@@ -474,7 +607,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
         int32_t* out = a.out + row * k;
         // ---- which batch / live row / how many visible keys
-        int64_t b = -1, r = 0, n = 0;
+        int64_t b = -1, r = 0, n = 0, lc = 0;
         if (meta_ok && p.batch > 0) {
             if (!p.layout_tnd) {
                 b = row / p.s1;
@@ -489,18 +622,15 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
                 r = row - be[b * kBatchWords + kBeFirstRow];
             }
             const int32_t* e = be + b * kBatchWords;
-            if (e[kBeOk] && r >= 0)
-                n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], e[kBeLc], r);
+            lc = e[kBeLc];
+            if (e[kBeOk] && r >= 0) n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], lc, r);
         }
         const uint32_t* line = a.scores + row * p.ld;
-        // rows cached in shared memory: start the line's bulk copy now, under the page check
-        const bool cached_path = n > kCap && n <= kCacheKeys;
-        // ---- every page this batch's rows can see must lie in the pool
-        __syncthreads();
+        const bool cached = n > 0 && n <= kCacheKeys;
+        __syncthreads();                           // the previous row is done with shared memory
         if (tid == 0) {
             s_bad = 0;
-            if (cached_path) {
-                // the previous row's generic reads of the cache came before (barrier above)
+            if (cached) {
                 ptx::fence_proxy_async_smem();
                 const uint32_t bytes = (uint32_t)(((n * 4) + 15) & ~(int64_t)15);
                 ptx::mbar_arrive_expect_tx(S.bar, bytes);
@@ -508,21 +638,20 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             }
         }
         __syncthreads();
-        if (n > 0) {
-            const int64_t pages = ceil_div64(be[b * kBatchWords + kBeLc], p.block_size);
-            const int32_t* table = a.block_table + b * p.max_blocks_per_seq;
-            bool bad = false;
-            for (int64_t i = tid; i < pages; i += kThreads) {
-                const int32_t pg = __ldg(table + i);
-                bad |= pg < 0 || pg >= p.num_blocks;
-            }
-            if (bad) s_bad = 1;
+        // ---- every page this batch's rows can see must lie in the pool: the first entry per
+        // thread is loaded now and checked after the selection, the rest (rows of > 1024 pages)
+        // at once
+        const int64_t pages = n > 0 ? ceil_div64(lc, p.block_size) : 0;
+        const int32_t* table = a.block_table + (b < 0 ? 0 : b) * p.max_blocks_per_seq;
+        const int32_t pg_first = tid < pages ? __ldg(table + tid) : 0;
+        bool bad = false;
+        for (int64_t i = tid + kThreads; i < pages; i += kThreads) {
+            const int32_t pg = __ldg(table + i);
+            bad |= pg < 0 || pg >= p.num_blocks;
         }
-        __syncthreads();
         bool copy_ok = true;
-        if (cached_path) {
-            // bounded wait for the line (also when the row turns out invalid: the copy must land
-            // before the cache is reused)
+        if (cached) {
+            // bounded wait for the line
             const uint64_t t0 = ptx::globaltimer();
             while (!ptx::mbar_try_wait(S.bar, bar_parity)) {
                 if (ptx::globaltimer() - t0 > 2000000000ull) {
@@ -534,60 +663,49 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             copy_ok = __syncthreads_and(copy_ok);
             if (!copy_ok && tid == 0) atomicOr(a.err, kErrTimeout);
         }
-        if (s_bad || !copy_ok) {
-            n = 0;
-            if (tid == 0 && s_bad) atomicOr(a.err, kErrPage);
-        }
-        if (n <= 0) {
-            for (int i = tid; i < k; i += kThreads) out[i] = -1;
-            continue;
-        }
-        const int64_t m = n < k ? n : k;
-        int count;
-        uint32_t lo = 0;
-        if (n <= kCap) {
-            uint32_t mn = 0xFFFFFFFFu;
-            for (int64_t j = tid; j < n; j += kThreads) {
-                const uint32_t c = __ldg(line + j);
-                S.key[j] = c;
-                S.val[j] = (uint32_t)j;
-                mn = min(mn, c);
-            }
-            lo = ~block_max(~mn, S.misc);
-            count = (int)n;
-        } else if (n <= kCacheKeys) {
-            count = select_cached(S, n, k, &lo);
-            if (count < 0) {
-                const uint64_t T = radix_select(
-                    S, n, k, [&](int64_t j) { return sort_key(__ldg(line + j), (uint32_t)j); }, 56);
-                count = min(gather(S, line, n, T), kCap);
-                lo = (uint32_t)(T >> 32);
-            }
-        } else {
-            // ---- threshold: the rank-r largest of evenly spaced samples
-            for (int i = tid; i < kSamples; i += kThreads) {
-                const int64_t j = ((int64_t)i * n) / kSamples;
-                S.key[i] = __ldg(line + j);
-            }
-            __syncthreads();
-            const double lam = (double)k * kSamples / (double)n;   // samples expected above the k-th
-            int rank = (int)(1.15 * lam + 4.0 * sqrt(lam) + 2.0);
-            rank = rank < 1 ? 1 : (rank > kSamples ? kSamples : rank);
-            const uint32_t* samp = S.key;
-            const uint64_t t = radix_select(
-                S, kSamples, rank, [&](int64_t i) { return static_cast<uint64_t>(samp[i]) << 32; }, 56);
-            lo = (uint32_t)(t >> 32);
-            count = gather(S, line, n, static_cast<uint64_t>(lo) << 32);
-            if (count < k || count > kCap) {
-                // ---- exact fallback: the k-th sort key of the row, then exactly k keys >= it
-                const uint64_t T = radix_select(
-                    S, n, k, [&](int64_t j) { return sort_key(__ldg(line + j), (uint32_t)j); }, 56);
-                count = min(gather(S, line, n, T), kCap);
-                lo = (uint32_t)(T >> 32);
+        const int need = (int)(n < k ? n : k);
+        const uint32_t* result = S.outv;           // ordered indices of this row
+        if (n > 0 && copy_ok) {
+            int st = kBinTooMany;
+            if (cached) {
+                st = n <= kCap ? order_all(S, S.cache, (int)n, [](int i) { return (uint32_t)i; }, need, S.key,
+                                           S.val)
+                               : order_sampled(S, (int)n, need);
+                if (st == kBinTooMany) {
+                    exact_topk(S, S.cache, n, k);
+                    result = S.val;
+                }
+            } else {
+                // ---- threshold: the rank-r largest of evenly spaced samples
+                for (int i = tid; i < kSamples; i += kThreads) {
+                    const int64_t j = ((int64_t)i * n) / kSamples;
+                    S.key[i] = __ldg(line + j);
+                }
+                __syncthreads();
+                const float lam = (float)k * (float)kSamples / (float)n;   // samples expected above the k-th
+                int rank = (int)(1.15f * lam + 4.0f * sqrtf(lam) + 2.0f);
+                rank = rank < 1 ? 1 : (rank > kSamples ? kSamples : rank);
+                const uint32_t* samp = S.key;
+                const uint64_t t = radix_select(
+                    S, kSamples, rank, [&](int64_t i) { return static_cast<uint64_t>(samp[i]) << 32; }, 56);
+                const int c = gather(S, line, n, t & 0xFFFFFFFF00000000ull);
+                if (c >= k && c <= kCap) {
+                    const uint32_t* vals = S.val;
+                    st = order_all(S, S.key, c, [vals](int i) { return vals[i]; }, need, S.cache, S.cache + kCap);
+                }
+                if (st == kBinTooMany) {
+                    exact_topk(S, line, n, k);
+                    result = S.val;
+                }
             }
         }
-        order_candidates(S, count, lo);
-        for (int i = tid; i < k; i += kThreads) out[i] = i < m ? (int32_t)S.val[i] : -1;
+        // ---- the page check, then the row
+        bad |= tid < pages && (pg_first < 0 || pg_first >= p.num_blocks);
+        if (bad) s_bad = 1;
+        __syncthreads();
+        const bool blank = n <= 0 || !copy_ok || s_bad;
+        if (tid == 0 && s_bad) atomicOr(a.err, kErrPage);
+        for (int i = tid; i < k; i += kThreads) out[i] = (!blank && i < need) ? (int32_t)result[i] : -1;
     }
 }
 

@@ -174,6 +174,20 @@ def test_bad_page_blanks_batch_and_reports(qli):
     assert np.array_equal(gpu_idx, ora_idx)
 
 
+def test_bad_page_in_long_rows_blanks_batch(qli):
+    """Long rows (split over several CTAs when few rows share the GPU): a bad page in the last
+    quarter of one batch's pages blanks that batch only."""
+    case = W.make_case("badpage_long", batch=3, s1=1, seq_lens_k=[9000, 9000, 7000], block_size=64,
+                       sparse_count=512, sparse_mode=3, seed=12)
+    case.block_table[1, 130] = -7
+    gpu_idx, _, st, bits = run_gpu(qli, case)
+    ora_idx, _, err = oracle.score_topk(case)
+    assert err & oracle.ERR_PAGE
+    assert st == 5 and bits & 2
+    assert (gpu_idx[1] == -1).all() and (gpu_idx[0] >= 0).all() and (gpu_idx[2] >= 0).all()
+    assert np.array_equal(gpu_idx, ora_idx)
+
+
 def test_bad_lengths_blank_batch_and_report(qli):
     case = W.make_case("badlen", batch=2, s1=2, q_lens=[2, 2], seq_lens_k=[300, 300],
                        block_size=64, sparse_count=16, seed=4)
