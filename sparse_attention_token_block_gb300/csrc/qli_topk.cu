@@ -29,8 +29,12 @@ namespace qli {
 
 namespace {
 
-constexpr int kThreads = 1024;
+#ifndef QLI_TOPK_THREADS
+#define QLI_TOPK_THREADS 1024
+#endif
+constexpr int kThreads = QLI_TOPK_THREADS;
 constexpr int kWarps = kThreads / 32;
+constexpr int kSampleKeys = 1024;             // keys sampled to bound the candidates' codes
 constexpr int kCap = 4096;                    // candidates held in shared memory
 constexpr int kSamples = 2048;
 constexpr int kBins = 8192;                   // ordering bins
@@ -38,7 +42,7 @@ constexpr int kBinsPerThread = kBins / kThreads;
 constexpr int kSampleBins = 2048;             // bins of the sample histogram
 constexpr int kBigBucket = 256;
 constexpr int kCacheKeys = 32768;             // score lines up to this length are cached in smem
-constexpr int kMiscWords = 128;
+constexpr int kMiscWords = 128;               // scratch: [0, 64) block reductions, [100, 111) single values
 constexpr int kSmemBytes = (kCacheKeys + kBins + 3 * kCap + 256 + kMiscWords) * 4 + 16;
 
 struct TopkArgs {
@@ -61,15 +65,36 @@ struct Smem {
     uint64_t* bar;    // bulk-copy barrier
 };
 
+extern __shared__ __align__(16) uint8_t topk_smem[];
+
+// The CTA's shared-memory carve-up, rebuilt from the dynamic shared memory symbol (cheaper than
+// passing it to non-inlined functions through local memory)
+__device__ __forceinline__ Smem smem_view()
+{
+    Smem S;
+    S.cache = reinterpret_cast<uint32_t*>(topk_smem);
+    S.bins = S.cache + kCacheKeys;
+    S.key = S.bins + kBins;
+    S.val = S.key + kCap;
+    S.outv = S.val + kCap;
+    S.hist = S.outv + kCap;
+    S.misc = S.hist + 256;
+    S.bar = reinterpret_cast<uint64_t*>(S.misc + kMiscWords);
+    return S;
+}
+
 __device__ __forceinline__ uint64_t sort_key(uint32_t code, uint32_t idx)
 {
     return (static_cast<uint64_t>(code) << 32) | (0xFFFFFFFFu - idx);
 }
 
-// Block-wide exclusive scan of one value per thread; also returns the total.
-__device__ uint32_t block_excl_scan(uint32_t v, uint32_t* total, uint32_t* sh /* >= kWarps */)
+// Block-wide exclusive scan of one value per thread; also returns the total.  One barrier: every
+// warp scans the 32 warp totals itself.  `sh` (kWarps words) must not be written again before a
+// later barrier.
+__device__ uint32_t block_excl_scan(uint32_t v, uint32_t* total, uint32_t* sh)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    static_assert(kWarps <= 32, "one warp total per lane");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -78,20 +103,15 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t* total, uint32_t* sh /*
     }
     if (lane == 31) sh[warp] = x;
     __syncthreads();
-    if (warp == 0) {
-        uint32_t w = lane < kWarps ? sh[lane] : 0;
+    const uint32_t wt = lane < kWarps ? sh[lane] : 0u;
+    uint32_t wi = wt;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        if (lane < kWarps) sh[lane] = w;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
     }
-    __syncthreads();
-    const uint32_t before = (warp > 0 ? sh[warp - 1] : 0) + x - v;
-    *total = sh[kWarps - 1];
-    __syncthreads();
-    return before;
+    *total = __shfl_sync(0xffffffffu, wi, 31);
+    return __shfl_sync(0xffffffffu, wi - wt, warp) + x - v;
 }
 
 // Radix select over 64-bit sort keys produced by `get(i)` for i < n: the k-th largest key
@@ -100,9 +120,9 @@ template <class Get>
 __device__ uint64_t radix_select(const Smem& S, int64_t n, int k, Get get, int top_shift)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t* s_digit = S.misc + 40;
-    uint32_t* s_rem = S.misc + 41;
-    uint32_t* s_done = S.misc + 42;
+    uint32_t* s_digit = S.misc + 100;
+    uint32_t* s_rem = S.misc + 101;
+    uint32_t* s_done = S.misc + 102;
     uint64_t prefix = 0, mask = 0;
     uint32_t rem = (uint32_t)k;
     for (int shift = top_shift; shift >= 0; shift -= 8) {
@@ -169,7 +189,7 @@ __device__ uint64_t radix_select(const Smem& S, int64_t n, int k, Get get, int t
 __device__ int gather(const Smem& S, const uint32_t* line, int64_t n, uint64_t t64)
 {
     const int tid = threadIdx.x, lane = tid & 31;
-    uint32_t* s_cnt = S.misc + 48;
+    uint32_t* s_cnt = S.misc + 104;
     if (tid == 0) *s_cnt = 0;
     __syncthreads();
     for (int64_t j0 = 0; j0 < n; j0 += kThreads) {
@@ -274,31 +294,21 @@ __device__ void bitonic_order(uint32_t* keys, uint32_t* vals, int c, uint64_t* s
     __syncthreads();
 }
 
-__device__ void bitonic_any(uint32_t* keys, uint32_t* vals, int c, uint64_t* scratch)
+// Rarely taken: heavy ties in one bin (or the exact fallback)
+__device__ __noinline__ void bitonic_any(uint32_t* keys, uint32_t* vals, int c, uint64_t* scratch)
 {
+    constexpr int kMaxE = kCap / kThreads;          // c <= kCap
+    static_assert(kMaxE * kThreads == kCap && kMaxE <= 16, "the network covers kCap keys");
     if (c <= kThreads) bitonic_order<1>(keys, vals, c, scratch);
     else if (c <= 2 * kThreads) bitonic_order<2>(keys, vals, c, scratch);
-    else bitonic_order<4>(keys, vals, c, scratch);
+    else if (c <= 4 * kThreads || kMaxE <= 4) bitonic_order<(kMaxE < 4 ? kMaxE : 4)>(keys, vals, c, scratch);
+    else if (c <= 8 * kThreads || kMaxE <= 8) bitonic_order<(kMaxE < 8 ? kMaxE : 8)>(keys, vals, c, scratch);
+    else bitonic_order<(kMaxE < 16 ? kMaxE : 16)>(keys, vals, c, scratch);
 }
 
-// Calls f(i, code) for every i < c, reading src (16-byte aligned) four codes at a time
-template <class F>
-__device__ __forceinline__ void for_each_code(const uint32_t* src, int c, F f)
-{
-    const int c4 = c >> 2;
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    for (int i = threadIdx.x; i < c4; i += kThreads) {
-        const uint4 v = s4[i];
-        f(4 * i, v.x);
-        f(4 * i + 1, v.y);
-        f(4 * i + 2, v.z);
-        f(4 * i + 3, v.w);
-    }
-    for (int i = 4 * c4 + (int)threadIdx.x; i < c; i += kThreads) f(i, src[i]);
-}
-
-// Largest of one value per thread and smallest of another, returned to every thread
-__device__ void block_max_min(uint32_t* mx, uint32_t* mn, uint32_t* sh /* >= 98 */)
+// Largest of one value per thread and smallest of another, returned to every thread.  One
+// barrier; `sh` (64 words) must not be written again before a later barrier.
+__device__ void block_max_min(uint32_t* mx, uint32_t* mn, uint32_t* sh)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t a = *mx, b = *mn;
@@ -309,64 +319,141 @@ __device__ void block_max_min(uint32_t* mx, uint32_t* mn, uint32_t* sh /* >= 98 
     }
     if (lane == 0) {
         sh[warp] = a;
-        sh[64 + warp] = b;
+        sh[32 + warp] = b;
     }
     __syncthreads();
-    if (warp == 0) {
-        a = sh[lane];
-        b = sh[64 + lane];
+    a = lane < kWarps ? sh[lane] : 0u;
+    b = lane < kWarps ? sh[32 + lane] : 0xFFFFFFFFu;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
-            b = min(b, __shfl_xor_sync(0xffffffffu, b, o));
+    for (int o = 16; o > 0; o >>= 1) {
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+        b = min(b, __shfl_xor_sync(0xffffffffu, b, o));
+    }
+    *mx = a;
+    *mn = b;
+}
+
+// The bins: codes in [L, top] fall in bin (top - code) >> shift (codes above top share bin 0);
+// bin 0 holds the highest codes.
+struct Binning {
+    uint32_t L, top;
+    int shift;
+    __device__ uint32_t operator()(uint32_t x) const { return x >= top ? 0u : (top - x) >> shift; }
+};
+
+__device__ Binning make_binning(uint32_t L, uint32_t top)
+{
+    Binning g;
+    g.L = L;
+    g.top = top;
+    g.shift = 0;
+    while (g.shift < 32 && ((top - L) >> g.shift) >= (uint32_t)kBins) ++g.shift;
+    return g;
+}
+
+// Steps 1-2 over src[0..c) (shared memory, 16-byte aligned, c <= kCacheKeys): each thread loads
+// its keys (4 * kVecPerThread of them, four at a time) into registers once; every key with code
+// >= g.L is appended to S.key / S.val (a count per thread, one scan, then each thread writes its
+// keys from its offset) and counted in its bin.  Returns how many keys reached g.L (only the first
+// kCap are stored or counted).
+constexpr int kVecPerThread = kCacheKeys / (4 * kThreads);
+__device__ __noinline__ int compact_and_count(const uint32_t* src, int c, Binning g)
+{
+    const Smem S = smem_view();
+    const int tid = threadIdx.x;
+    for (int b = tid; b < kBins; b += kThreads) S.bins[b] = 0;
+    const int c4 = c >> 2;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    const uint32_t L = g.L;
+    uint4 v[kVecPerThread];
+#pragma unroll
+    for (int q = 0; q < kVecPerThread; ++q) {
+        const int i = tid + q * kThreads;
+        v[q] = i < c4 ? s4[i] : make_uint4(0, 0, 0, 0);
+    }
+    // the c mod 4 keys past the last full vector: thread t < c - 4 c4 takes key 4 c4 + t
+    const int tail = c - 4 * c4;
+    const uint32_t xt = tid < tail ? src[4 * c4 + tid] : 0u;
+    uint32_t mine = (tid < tail && xt >= L) ? 1u : 0u;
+#pragma unroll
+    for (int q = 0; q < kVecPerThread; ++q) {
+        if (tid + q * kThreads < c4)
+            mine += (v[q].x >= L ? 1u : 0u) + (v[q].y >= L ? 1u : 0u) + (v[q].z >= L ? 1u : 0u) +
+                    (v[q].w >= L ? 1u : 0u);
+    }
+    uint32_t total;
+    uint32_t pos = block_excl_scan(mine, &total, S.misc);   // its barrier also orders the zeroing
+    auto put = [&](uint32_t x, int j) {
+        if (x >= L) {
+            if (pos < (uint32_t)kCap) {
+                S.key[pos] = x;
+                S.val[pos] = (uint32_t)j;
+                atomicAdd(&S.bins[g(x)], 1u);
+            }
+            ++pos;
         }
-        if (lane == 0) {
-            sh[96] = a;
-            sh[97] = b;
+    };
+#pragma unroll
+    for (int q = 0; q < kVecPerThread; ++q) {
+        const int i = tid + q * kThreads;
+        if (i < c4) {
+            put(v[q].x, 4 * i);
+            put(v[q].y, 4 * i + 1);
+            put(v[q].z, 4 * i + 2);
+            put(v[q].w, 4 * i + 3);
         }
     }
+    if (tid < tail) put(xt, 4 * c4 + tid);
     __syncthreads();
-    *mx = sh[96];
-    *mn = sh[97];
+    return (int)total;
+}
+
+// Bin counts of the m listed candidates lkey[0..m) (shared memory)
+__device__ __noinline__ void count_bins(const uint32_t* lkey, int m, Binning g)
+{
+    const Smem S = smem_view();
+    const int tid = threadIdx.x;
+    for (int b = tid; b < kBins; b += kThreads) S.bins[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < m; i += kThreads) atomicAdd(&S.bins[g(lkey[i])], 1u);
     __syncthreads();
 }
 
-constexpr uint32_t kNoBin = 0xFFFFFFFFu;
-
-// Ordering of the candidates among c codes src[0..c) (shared memory, 16-byte aligned), source
-// index idx(i).  bin(code) is non-increasing in the code and either kNoBin (not a candidate) or
-// below kBins; bin 0 holds the highest codes.  Steps 1-4 above: the first min(need, #candidates)
-// positions of the order go to S.outv.  Candidates are scattered into tkey / tval (kCap each,
-// distinct from src); a bin of more than kBigBucket candidates sends them to the bitonic network
-// instead of step 4.  kBinTooMany: the bins up to the one reaching `need` hold more than kCap
-// keys, or fewer than `need` keys have a bin (nothing ordered).
 enum BinResult { kBinOrdered = 0, kBinTooMany = 1 };
 
-template <class Idx, class Bin>
-__device__ int bin_order(const Smem& S, const uint32_t* src, int c, Idx idx, int need, Bin bin,
-                         uint32_t* tkey, uint32_t* tval)
+// Steps 3-4 over the m listed candidates lkey / lval (lval null: a candidate's index is its
+// position; bins counted): the scan finds the bin where
+// the running count reaches need; the candidates of that bin and above are scattered into
+// tkey / tval (kCap each) and each takes its bin's start plus its rank among the bin's keys; the
+// first min(need, m) indices of the order go to S.outv.  A bin of more than kBigBucket candidates
+// sends them to the bitonic network instead.  kBinTooMany: fewer than `need` candidates or more
+// than kCap up to the threshold bin (nothing ordered).
+__device__ __noinline__ int order_bins(const uint32_t* lkey, const uint32_t* lval, int m, int need, Binning g,
+                                       uint32_t* tkey, uint32_t* tval)
 {
+    const Smem S = smem_view();
     const int tid = threadIdx.x;
     uint32_t* bins = S.bins;
-    for (int b = tid; b < kBins; b += kThreads) bins[b] = 0;
-    __syncthreads();
-    // 1. counts per bin
-    for_each_code(src, c, [&](int, uint32_t x) {
-        const uint32_t b = bin(x);
-        if (b != kNoBin) atomicAdd(&bins[b], 1u);
-    });
-    __syncthreads();
-    // 2. thread t scans bins [8t, 8t + 8); the threshold bin is where the running count reaches need
+    // thread t scans bins [8t, 8t + 8)
+    static_assert(kBinsPerThread % 4 == 0, "16-byte loads");
     uint32_t cnt[kBinsPerThread], sum = 0;
+    {
+        const uint4* b4 = reinterpret_cast<const uint4*>(bins) + (kBinsPerThread / 4) * tid;
 #pragma unroll
-    for (int q = 0; q < kBinsPerThread; ++q) {
-        cnt[q] = bins[tid * kBinsPerThread + q];
-        sum += cnt[q];
+        for (int v = 0; v < kBinsPerThread / 4; ++v) {
+            const uint4 c = b4[v];
+            cnt[4 * v] = c.x;
+            cnt[4 * v + 1] = c.y;
+            cnt[4 * v + 2] = c.z;
+            cnt[4 * v + 3] = c.w;
+        }
     }
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) sum += cnt[q];
     uint32_t total;
     const uint32_t before = block_excl_scan(sum, &total, S.misc);
-    uint32_t* s_thr = S.misc + 56;
-    uint32_t* s_cc = S.misc + 57;
+    uint32_t* s_thr = S.misc + 108;
+    uint32_t* s_cc = S.misc + 109;
     if (before < (uint32_t)need && before + sum >= (uint32_t)need) {
         uint32_t run = before;
 #pragma unroll
@@ -381,33 +468,42 @@ __device__ int bin_order(const Smem& S, const uint32_t* src, int c, Idx idx, int
     __syncthreads();
     const uint32_t thr = *s_thr;
     const int cc = (int)*s_cc;
-    if (total < (uint32_t)need || cc > kCap) {
+    if (total < (uint32_t)need || m > kCap || cc > kCap) {
         __syncthreads();
         return kBinTooMany;
     }
-    // bin ends (inclusive prefix) for the scatter, which fills each bin from its end; a heavy bin
-    // among the candidates sends the order to the bitonic network
+    // bin ends (inclusive prefix) for the scatter, which fills each bin from its end
     bool big = false;
     {
-        uint32_t run = before;
+        uint32_t run = before, end[kBinsPerThread];
 #pragma unroll
         for (int q = 0; q < kBinsPerThread; ++q) {
             const uint32_t b = tid * kBinsPerThread + q;
             run += cnt[q];
-            bins[b] = run;
+            end[q] = run;
             big |= b <= thr && cnt[q] > (uint32_t)kBigBucket;
         }
+        uint4* b4 = reinterpret_cast<uint4*>(bins) + (kBinsPerThread / 4) * tid;
+#pragma unroll
+        for (int v = 0; v < kBinsPerThread / 4; ++v)
+            b4[v] = make_uint4(end[4 * v], end[4 * v + 1], end[4 * v + 2], end[4 * v + 3]);
     }
     big = __syncthreads_or(big);
-    // 3. scatter the candidates
-    for_each_code(src, c, [&](int i, uint32_t x) {
-        const uint32_t b = bin(x);
-        if (b <= thr) {                            // kNoBin never is
-            const uint32_t pos = atomicSub(&bins[b], 1u) - 1u;
-            tkey[pos] = x;
-            tval[pos] = idx(i);
+    // 3. scatter the candidates up to the threshold bin
+    constexpr int kPer = kCap / kThreads;           // m <= kCap: at most kPer per thread
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int i = tid + q * kThreads;
+        if (i < m) {
+            const uint32_t x = lkey[i];
+            const uint32_t b = g(x);
+            if (b <= thr) {
+                const uint32_t pos = atomicSub(&bins[b], 1u) - 1u;
+                tkey[pos] = x;
+                tval[pos] = lval ? lval[i] : (uint32_t)i;
+            }
         }
-    });
+    }
     __syncthreads();
     if (big) {
         bitonic_any(tkey, tval, cc, reinterpret_cast<uint64_t*>(S.bins));
@@ -416,108 +512,41 @@ __device__ int bin_order(const Smem& S, const uint32_t* src, int c, Idx idx, int
         return kBinOrdered;
     }
     // 4. rank inside the bin (bins[b] is now the bin's start)
-    for (int i = tid; i < cc; i += kThreads) {
-        const uint32_t kc = tkey[i], kv = tval[i];
-        const uint64_t kk = sort_key(kc, kv);
-        const uint32_t b = bin(kc);
-        const uint32_t s0 = bins[b];
-        const uint32_t e0 = b < thr ? bins[b + 1] : (uint32_t)cc;
-        uint32_t r = 0;
-        for (uint32_t j = s0; j < e0; ++j) r += sort_key(tkey[j], tval[j]) > kk ? 1u : 0u;
-        S.outv[s0 + r] = kv;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int i = tid + q * kThreads;
+        if (i < cc) {
+            const uint32_t kc = tkey[i], kv = tval[i];
+            const uint64_t kk = sort_key(kc, kv);
+            const uint32_t b = g(kc);
+            const uint32_t s0 = bins[b];
+            const uint32_t e0 = b < thr ? bins[b + 1] : (uint32_t)cc;
+            uint32_t r = 0;
+            for (uint32_t j = s0; j < e0; ++j) r += sort_key(tkey[j], tval[j]) > kk ? 1u : 0u;
+            S.outv[s0 + r] = kv;
+        }
     }
     __syncthreads();
     return kBinOrdered;
 }
 
-// Bins over the whole code range [lo, hi] of src[0..c) (all keys are candidates)
-template <class Idx>
-__device__ int order_all(const Smem& S, const uint32_t* src, int c, Idx idx, int need, uint32_t* tkey,
-                         uint32_t* tval)
-{
-    uint32_t hi = 0, lo = 0xFFFFFFFFu;
-    for_each_code(src, c, [&](int, uint32_t x) {
-        hi = max(hi, x);
-        lo = min(lo, x);
-    });
-    block_max_min(&hi, &lo, S.misc);
-    int shift = 0;
-    while (shift < 32 && ((hi - lo) >> shift) >= (uint32_t)kBins) ++shift;
-    return bin_order(S, src, c, idx, need, [hi, shift](uint32_t x) { return (hi - x) >> shift; }, tkey,
-                     tval);
-}
-
-// Append the code and index of every key of src[0..c) (shared memory, 16-byte aligned) whose code
-// is at least L to S.key / S.val, one shared counter update per warp and four keys; returns how
-// many (only the first kCap are stored).
-__device__ int compact_at_least(const Smem& S, const uint32_t* src, int c, uint32_t L)
-{
-    const int tid = threadIdx.x, lane = tid & 31;
-    const unsigned below = (1u << lane) - 1u;
-    uint32_t* s_cnt = S.misc + 48;
-    if (tid == 0) *s_cnt = 0;
-    __syncthreads();
-    const int c4 = c >> 2;
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    for (int i0 = 0; i0 < c4; i0 += kThreads) {         // the same trip count in every lane
-        const int i = i0 + tid;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        const bool in = i < c4;
-        if (in) v = s4[i];
-        const bool f0 = in && v.x >= L, f1 = in && v.y >= L, f2 = in && v.z >= L, f3 = in && v.w >= L;
-        const unsigned b0 = __ballot_sync(0xffffffffu, f0), b1 = __ballot_sync(0xffffffffu, f1);
-        const unsigned b2 = __ballot_sync(0xffffffffu, f2), b3 = __ballot_sync(0xffffffffu, f3);
-        const uint32_t n0 = __popc(b0), n1 = __popc(b1), n2 = __popc(b2), n3 = __popc(b3);
-        const uint32_t nw = n0 + n1 + n2 + n3;
-        if (nw == 0) continue;
-        uint32_t base = 0;
-        if (lane == 0) base = atomicAdd(s_cnt, nw);
-        base = __shfl_sync(0xffffffffu, base, 0);
-        auto put = [&](bool f, uint32_t pos, uint32_t code, int j) {
-            if (f && pos < (uint32_t)kCap) {
-                S.key[pos] = code;
-                S.val[pos] = (uint32_t)j;
-            }
-        };
-        put(f0, base + __popc(b0 & below), v.x, 4 * i);
-        put(f1, base + n0 + __popc(b1 & below), v.y, 4 * i + 1);
-        put(f2, base + n0 + n1 + __popc(b2 & below), v.z, 4 * i + 2);
-        put(f3, base + n0 + n1 + n2 + __popc(b3 & below), v.w, 4 * i + 3);
-    }
-    for (int i0 = 4 * c4; i0 < c; i0 += kThreads) {
-        const int i = i0 + tid;
-        const uint32_t x = i < c ? src[i] : 0u;
-        const bool f = i < c && x >= L;
-        const unsigned b = __ballot_sync(0xffffffffu, f);
-        if (b == 0) continue;
-        uint32_t base = 0;
-        if (lane == 0) base = atomicAdd(s_cnt, (uint32_t)__popc(b));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const uint32_t pos = base + __popc(b & below);
-        if (f && pos < (uint32_t)kCap) {
-            S.key[pos] = x;
-            S.val[pos] = (uint32_t)i;
-        }
-    }
-    __syncthreads();
-    const int m = (int)*s_cnt;
-    __syncthreads();
-    return m;
-}
-
 // Cached rows longer than kCap (the line in S.cache[0..c)): a lower bound L for the candidates'
-// codes from a sample of kThreads evenly spaced keys -- the code of the rank-r largest sample,
-// r = 1.15 l + 4 sqrt(l) + 2 with l = need * kThreads / c the samples expected above the need-th
-// key; the keys at or above L are compacted into S.key / S.val, then ordered by bins over
-// [L, largest sample] (codes above it share bin 0), scattered into the idle row cache.
-// kBinTooMany when fewer than `need` or more than kCap keys reach L (the caller falls back to
-// the exact selection).
-__device__ int order_sampled(const Smem& S, int c, int need)
+// codes from a sample of kSampleKeys evenly spaced keys -- the code of the rank-r largest sample,
+// r = 1.15 l + 4 sqrt(l) + 2 with l = need * kSampleKeys / c the samples expected above the
+// need-th key -- and the largest sample, the top of the bins.
+__device__ __noinline__ Binning sample_bound(int c, int need)
 {
+    const Smem S = smem_view();
     const int tid = threadIdx.x;
-    const uint32_t* src = S.cache;
-    const uint32_t x = src[((int64_t)tid * c) / kThreads];
-    uint32_t smx = x, smn = x;
+    constexpr int per = kSampleKeys / kThreads;     // samples per thread
+    uint32_t x[per];
+    uint32_t smx = 0, smn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+        x[q] = S.cache[((int64_t)(tid + q * kThreads) * c) / kSampleKeys];
+        smx = max(smx, x[q]);
+        smn = min(smn, x[q]);
+    }
     block_max_min(&smx, &smn, S.misc);
     // the sample's rank-r largest code, to the resolution of kSampleBins bins over its range
     int s1 = 0;
@@ -525,26 +554,30 @@ __device__ int order_sampled(const Smem& S, int c, int need)
     uint32_t* sb = S.bins;
     for (int b = tid; b < kSampleBins; b += kThreads) sb[b] = 0;
     __syncthreads();
-    atomicAdd(&sb[(smx - x) >> s1], 1u);
-    __syncthreads();
-    const float lam = (float)need * (float)kThreads / (float)c;   // single precision: FP64 is slow here
-    int r = (int)(1.15f * lam + 4.0f * sqrtf(lam) + 2.0f);
-    r = r < 1 ? 1 : (r > kThreads ? kThreads : r);
-    constexpr int per = kSampleBins / kThreads;
-    uint32_t cnt[per], sum = 0;
 #pragma unroll
-    for (int q = 0; q < per; ++q) {
-        cnt[q] = sb[tid * per + q];
-        sum += cnt[q];
+    for (int q = 0; q < per; ++q) atomicAdd(&sb[(smx - x[q]) >> s1], 1u);
+    __syncthreads();
+    const float lam = (float)need * (float)kSampleKeys / (float)c;   // single precision: FP64 is slow here
+    int r = (int)(1.15f * lam + 4.0f * sqrtf(lam) + 2.0f);
+    r = r < 1 ? 1 : (r > kSampleKeys ? kSampleKeys : r);
+    constexpr int bpt = kSampleBins / kThreads;     // sample bins per thread
+    static_assert(bpt % 2 == 0, "8-byte loads");
+    uint32_t cnt[bpt], sum = 0;
+#pragma unroll
+    for (int v = 0; v < bpt / 2; ++v) {
+        const uint2 cv = reinterpret_cast<const uint2*>(sb)[(bpt / 2) * tid + v];
+        cnt[2 * v] = cv.x;
+        cnt[2 * v + 1] = cv.y;
+        sum += cv.x + cv.y;
     }
     uint32_t total;
     const uint32_t before = block_excl_scan(sum, &total, S.misc);
-    uint32_t* s_b = S.misc + 58;
+    uint32_t* s_b = S.misc + 110;
     if (before < (uint32_t)r && before + sum >= (uint32_t)r) {
         uint32_t run = before;
 #pragma unroll
-        for (int q = 0; q < per; ++q) {
-            if (run < (uint32_t)r && run + cnt[q] >= (uint32_t)r) *s_b = tid * per + q;
+        for (int q = 0; q < bpt; ++q) {
+            if (run < (uint32_t)r && run + cnt[q] >= (uint32_t)r) *s_b = bpt * tid + q;
             run += cnt[q];
         }
     }
@@ -554,38 +587,43 @@ __device__ int order_sampled(const Smem& S, int c, int need)
     // L: the lowest code of bin b1
     const uint64_t span = ((uint64_t)b1 + 1) << s1;
     const uint32_t L = span > (uint64_t)(smx - smn) ? smn : (uint32_t)(smx - span + 1);
-    const int m = compact_at_least(S, src, c, L);
-    if (m < need || m > kCap) return kBinTooMany;
-    int shift = 0;
-    while (shift < 32 && ((smx - L) >> shift) >= (uint32_t)kBins) ++shift;
-    const uint32_t* vals = S.val;
-    return bin_order(
-        S, S.key, m, [vals](int i) { return vals[i]; }, need,
-        [L, smx, shift](uint32_t v) { return v < L ? kNoBin : (v >= smx ? 0u : (smx - v) >> shift); },
-        S.cache, S.cache + kCap);
+    return make_binning(L, smx);
 }
 
 // Exact fallback: the k-th largest sort key of the row (radix select), then exactly k keys at or
 // above it, ordered by the bitonic network; the ordered indices end in S.val.
-__device__ void exact_topk(const Smem& S, const uint32_t* line, int64_t n, int k)
+__device__ __noinline__ void exact_topk(const uint32_t* line, int64_t n, int k)
 {
+    const Smem S = smem_view();
     const uint64_t T = radix_select(S, n, k, [&](int64_t j) { return sort_key(line[j], (uint32_t)j); }, 56);
     const int c = min(gather(S, line, n, T), kCap);
     bitonic_any(S.key, S.val, c, reinterpret_cast<uint64_t*>(S.bins));
 }
 
+// Uncached rows (longer than kCacheKeys): the keys at or above the rank-r largest of kSamples
+// evenly spaced keys of the line, r = 1.15 k S / n + 4 sqrt(k S / n) + 2, gathered from global
+// memory into S.key / S.val; returns their count.
+__device__ __noinline__ int gather_sampled(const uint32_t* line, int64_t n, int k)
+{
+    const Smem S = smem_view();
+    const int tid = threadIdx.x;
+    for (int i = tid; i < kSamples; i += kThreads) {
+        const int64_t j = ((int64_t)i * n) / kSamples;
+        S.key[i] = __ldg(line + j);
+    }
+    __syncthreads();
+    const float lam = (float)k * (float)kSamples / (float)n;   // samples expected above the k-th
+    int rank = (int)(1.15f * lam + 4.0f * sqrtf(lam) + 2.0f);
+    rank = rank < 1 ? 1 : (rank > kSamples ? kSamples : rank);
+    const uint32_t* samp = S.key;
+    const uint64_t t = radix_select(
+        S, kSamples, rank, [&](int64_t i) { return static_cast<uint64_t>(samp[i]) << 32; }, 56);
+    return gather(S, line, n, t & 0xFFFFFFFF00000000ull);
+}
+
 __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ TopkArgs a)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
-    Smem S;
-    S.cache = reinterpret_cast<uint32_t*>(smem);
-    S.bins = S.cache + kCacheKeys;
-    S.key = S.bins + kBins;
-    S.val = S.key + kCap;
-    S.outv = S.val + kCap;
-    S.hist = S.outv + kCap;
-    S.misc = S.hist + 256;
-    S.bar = reinterpret_cast<uint64_t*>(S.misc + kMiscWords);
+    const Smem S = smem_view();
     if (threadIdx.x == 0) {
         ptx::mbar_init(S.bar, 1);
         ptx::fence_mbar_init();
@@ -668,33 +706,44 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         if (n > 0 && copy_ok) {
             int st = kBinTooMany;
             if (cached) {
-                st = n <= kCap ? order_all(S, S.cache, (int)n, [](int i) { return (uint32_t)i; }, need, S.key,
-                                           S.val)
-                               : order_sampled(S, (int)n, need);
+                // bins over the whole range (short rows: every key is a candidate) or from a sample
+                if (n <= kCap) {
+                    // every key is a candidate: bins over the row's whole code range, counted and
+                    // scattered straight from the row cache
+                    uint32_t hi = 0, lo = 0xFFFFFFFFu;
+                    for (int i = tid; i < (int)n; i += kThreads) {
+                        const uint32_t x = S.cache[i];
+                        hi = max(hi, x);
+                        lo = min(lo, x);
+                    }
+                    block_max_min(&hi, &lo, S.misc);
+                    const Binning g = make_binning(lo, hi);
+                    count_bins(S.cache, (int)n, g);
+                    st = order_bins(S.cache, nullptr, (int)n, need, g, S.key, S.val);
+                } else {
+                    const Binning g = sample_bound((int)n, need);
+                    const int m = compact_and_count(S.cache, (int)n, g);
+                    st = order_bins(S.key, S.val, m, need, g, S.cache, S.cache + kCap);
+                }
                 if (st == kBinTooMany) {
-                    exact_topk(S, S.cache, n, k);
+                    exact_topk(S.cache, n, k);
                     result = S.val;
                 }
             } else {
-                // ---- threshold: the rank-r largest of evenly spaced samples
-                for (int i = tid; i < kSamples; i += kThreads) {
-                    const int64_t j = ((int64_t)i * n) / kSamples;
-                    S.key[i] = __ldg(line + j);
-                }
-                __syncthreads();
-                const float lam = (float)k * (float)kSamples / (float)n;   // samples expected above the k-th
-                int rank = (int)(1.15f * lam + 4.0f * sqrtf(lam) + 2.0f);
-                rank = rank < 1 ? 1 : (rank > kSamples ? kSamples : rank);
-                const uint32_t* samp = S.key;
-                const uint64_t t = radix_select(
-                    S, kSamples, rank, [&](int64_t i) { return static_cast<uint64_t>(samp[i]) << 32; }, 56);
-                const int c = gather(S, line, n, t & 0xFFFFFFFF00000000ull);
+                const int c = gather_sampled(line, n, k);
                 if (c >= k && c <= kCap) {
-                    const uint32_t* vals = S.val;
-                    st = order_all(S, S.key, c, [vals](int i) { return vals[i]; }, need, S.cache, S.cache + kCap);
+                    uint32_t hi = 0, lo = 0xFFFFFFFFu;
+                    for (int i = tid; i < c; i += kThreads) {
+                        hi = max(hi, S.key[i]);
+                        lo = min(lo, S.key[i]);
+                    }
+                    block_max_min(&hi, &lo, S.misc);
+                    const Binning g = make_binning(lo, hi);
+                    count_bins(S.key, c, g);
+                    st = order_bins(S.key, S.val, c, need, g, S.cache, S.cache + kCap);
                 }
                 if (st == kBinTooMany) {
-                    exact_topk(S, line, n, k);
+                    exact_topk(line, n, k);
                     result = S.val;
                 }
             }
