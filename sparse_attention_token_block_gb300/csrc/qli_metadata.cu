@@ -22,32 +22,31 @@ namespace {
 constexpr int kMetaThreads = 1024;
 
 // Block-wide exclusive scan of one value per thread; returns the exclusive prefix and the total.
-__device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* total, uint32_t* sh /* [32] */)
+// One barrier: every warp scans the warp totals itself.  Calls alternate between the two halves
+// of `sh` ([64]) so that a call never overwrites totals another warp may still be reading.
+__device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* total, uint32_t* sh, int& parity)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = (int)(blockDim.x >> 5);
+    uint32_t* buf = sh + 32 * parity;
+    parity ^= 1;
     uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    if (lane == 31) sh[warp] = x;
+    if (lane == 31) buf[warp] = x;
     __syncthreads();
-    if (warp == 0) {
-        uint32_t w = lane < nwarps ? sh[lane] : 0u;
+    const uint32_t wt = lane < nwarps ? buf[lane] : 0u;
+    uint32_t wi = wt;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        sh[lane] = w;  // inclusive over warps
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
     }
-    __syncthreads();
-    const uint32_t warp_excl = warp > 0 ? sh[warp - 1] : 0u;
-    *total = sh[nwarps - 1];
-    __syncthreads();
-    return warp_excl + x - v;
+    *total = __shfl_sync(0xffffffffu, wi, 31);
+    return __shfl_sync(0xffffffffu, wi - wt, warp) + x - v;
 }
 
 // A strided int32 array in shared or global memory
@@ -77,7 +76,8 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
                     const int32_t* __restrict__ seq_lens_k, int32_t* __restrict__ meta, int G)
 {
     extern __shared__ int32_t msm[];
-    __shared__ uint32_t scan_sh[32];
+    __shared__ uint32_t scan_sh[64];
+    int scan_parity = 0;
     __shared__ uint32_t s_err;
     __shared__ int s_tnd_bad;
     const int tid = threadIdx.x;
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
             e[kBeGroups] = (int32_t)groups;
         }
         uint32_t tot;
-        const uint32_t ex = block_exclusive_scan(groups, &tot, scan_sh);
+        const uint32_t ex = block_exclusive_scan(groups, &tot, scan_sh, scan_parity);
         if (b < p.batch) {
             be[(int64_t)b * kBatchWords + kBeGroupBase] = (int32_t)(running + ex);
             if (sb) v_gb[b] = (int32_t)(running + ex);
@@ -163,30 +163,36 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     const int64_t total_groups = running;
     __syncthreads();
 
-    // each thread owns a contiguous run of groups, so each pass below needs one block scan
+    // each thread owns a contiguous run of groups, so each pass below needs one block scan; the
+    // batch of a run's first group comes from one binary search, later ones by advancing
     const int64_t per = (total_groups + blockDim.x - 1) / blockDim.x;
     const int64_t g_lo = min((int64_t)tid * per, total_groups);
     const int64_t g_hi = min(g_lo + per, total_groups);
-    auto group_keys = [&](int64_t g, int64_t* b_out, int64_t* r0_out) -> int64_t {
-        const int64_t b = upper_index(v_gb, p.batch, g);
+    // visible keys of group g of batch b (its last row's count, the largest in the group)
+    auto keys_of = [&](int64_t b, int64_t g) -> int64_t {
         const int64_t r0 = (g - v_gb[b]) * kGroupTokens;
         const int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)v_sq[b]) - 1;
-        *b_out = b;
-        *r0_out = r0;
         return visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl);
+    };
+    // first batch whose groups include g, moving forward from b (batches without groups share
+    // their successor's first group)
+    auto advance_batch = [&](int64_t b, int64_t g) -> int64_t {
+        while (b + 1 < p.batch && v_gb[b + 1] <= g) ++b;
+        return b;
     };
 
     // ---- tiles per group, then their exclusive prefix (gpre[g]; gpre[total_groups] = total)
     {
         uint32_t mine = 0;
+        int64_t b = g_lo < g_hi ? upper_index(v_gb, p.batch, g_lo) : 0;
         for (int64_t g = g_lo; g < g_hi; ++g) {
-            int64_t b, r0;
-            const uint32_t tiles = (uint32_t)((group_keys(g, &b, &r0) + kTileKeys - 1) / kTileKeys);
+            b = advance_batch(b, g);
+            const uint32_t tiles = (uint32_t)((keys_of(b, g) + kTileKeys - 1) / kTileKeys);
             v_gp[g] = (int32_t)tiles;                 // the count now, its prefix below
             mine += tiles;
         }
         uint32_t tot;
-        uint32_t pre = block_exclusive_scan(mine, &tot, scan_sh);
+        uint32_t pre = block_exclusive_scan(mine, &tot, scan_sh, scan_parity);
         for (int64_t g = g_lo; g < g_hi; ++g) {
             const uint32_t tiles = (uint32_t)v_gp[g];
             v_gp[g] = (int32_t)pre;
@@ -213,10 +219,14 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
                            : ((t + 1) * Gl + T - 1) / T - 1;
         return c < 0 ? 0 : (c >= Gl ? Gl - 1 : c);
     };
-    // floor(T c / G) without a 64-bit division per CTA: c * floor(T / G) + floor(c * (T mod G) / G)
+    // floor(T c / G) without a division per CTA: c * floor(T / G) + floor(c * (T mod G) / G), the
+    // last by a multiply with m = ceil(2^32 / G): for x = c (T mod G) < G^2 <= 2^20 the error of
+    // x m / 2^32 against x / G is below 2^-12 < 1 / G, so the floor is exact
     const uint32_t t_div = (uint32_t)(T / (Gl > 0 ? Gl : 1)), t_mod = (uint32_t)(T % (Gl > 0 ? Gl : 1));
+    const uint32_t inv_g = (uint32_t)((0xFFFFFFFFull + (uint64_t)G) / (uint64_t)(G > 0 ? G : 1));
+    static_assert(kMaxCtas <= 1024, "the reciprocal division needs G <= 1024");
     auto cta_start = [&](int64_t c) -> int64_t {
-        return (int64_t)c * t_div + (uint32_t)((uint32_t)c * t_mod / (uint32_t)G);
+        return (int64_t)c * t_div + __umulhi((uint32_t)c * t_mod, inv_g);
     };
     if (T == 0)
         for (int c = tid; c <= G; c += blockDim.x) cta_off[c] = 0;
@@ -233,7 +243,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
         uint32_t mine = 0;
         for (int64_t g = g_lo; g < g_hi && T > 0; ++g) mine += group_units(v_gp[g], v_gp[g + 1]);
         uint32_t tot;
-        uint32_t u = block_exclusive_scan(mine, &tot, scan_sh);
+        uint32_t u = block_exclusive_scan(mine, &tot, scan_sh, scan_parity);
         for (int64_t g = g_lo; g < g_hi; ++g) {
             v_uf[g] = (int32_t)u;
             if (T > 0) u += group_units(v_gp[g], v_gp[g + 1]);
@@ -242,32 +252,55 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
         running = tot;
     }
     __syncthreads();
-    // one thread per unit: its group (the largest with first unit <= u; groups without units
-    // share their successor's index), its CTA, and its key range
-    for (int64_t u = tid; u < (int64_t)running; u += blockDim.x) {
-        const int64_t g = upper_index(v_uf, total_groups, u);
-        const int64_t A = v_gp[g], Bt = v_gp[g + 1];
-        int64_t b, r0;
-        const int64_t n = group_keys(g, &b, &r0);
-        const int64_t k = u - v_uf[g];
-        const int64_t c = dense ? cta_of(A) + k : cta_of(A + k);
-        const int64_t t0 = cta_start(c), t1 = cta_start(c + 1);
-        int4 w, v;
-        w.x = (int32_t)b;
-        w.y = (int32_t)r0;
-        w.z = (int32_t)((max(t0, A) - A) * kTileKeys);
-        w.w = (int32_t)min((min(t1, Bt) - A) * kTileKeys, n);
-        v.x = v_fr[b] + (int32_t)r0;
-        v.y = v_sq[b];
-        v.z = v_sk[b];
-        v.w = v_lc[b];
-        int4* dst = reinterpret_cast<int4*>(units + u * kUnitWords);
-        dst[0] = w;
-        dst[1] = v;
-        if (t0 >= A && t0 < Bt) {
-            // the CTA's first unit; CTAs before it with an empty range (T < G) start here too
-            cta_off[c] = (int32_t)u;
-            for (int64_t ce = c - 1; ce >= 0 && cta_start(ce) == t0; --ce) cta_off[ce] = (int32_t)u;
+    // the records: thread t writes units [t U / n_t, (t + 1) U / n_t) in order; the group of its
+    // first unit (the largest with first unit <= u; groups without units share their successor's
+    // index) and that group's batch come from binary searches, later ones by advancing
+    {
+        const int64_t U = running;
+        const int64_t u_lo = U * tid / blockDim.x, u_hi = U * (tid + 1) / blockDim.x;
+        int64_t g = -1, b = 0, A = 0, Bt = 0, n = 0, r0 = 0, c = 0;
+        int64_t t1 = 0;
+        for (int64_t u = u_lo; u < u_hi; ++u) {
+            int64_t k;
+            if (g < 0 || u >= v_uf[g + 1]) {
+                // a new group: this thread's first, or the next one with units
+                if (g < 0) {
+                    g = upper_index(v_uf, total_groups, u);
+                    b = upper_index(v_gb, p.batch, g);
+                } else {
+                    do { ++g; } while (v_uf[g + 1] <= u);
+                }
+                b = advance_batch(b, g);
+                A = v_gp[g];
+                Bt = v_gp[g + 1];
+                r0 = (g - v_gb[b]) * kGroupTokens;
+                n = keys_of(b, g);
+                k = u - v_uf[g];
+                c = dense ? cta_of(A) + k : cta_of(A + k);
+                t1 = cta_start(c);
+            } else {
+                k = u - v_uf[g];
+                c = dense ? c + 1 : cta_of(A + k);
+            }
+            const int64_t t0 = dense ? t1 : cta_start(c);
+            t1 = cta_start(c + 1);
+            int4 w, v;
+            w.x = (int32_t)b;
+            w.y = (int32_t)r0;
+            w.z = (int32_t)((max(t0, A) - A) * kTileKeys);
+            w.w = (int32_t)min((min(t1, Bt) - A) * kTileKeys, n);
+            v.x = v_fr[b] + (int32_t)r0;
+            v.y = v_sq[b];
+            v.z = v_sk[b];
+            v.w = v_lc[b];
+            int4* dst = reinterpret_cast<int4*>(units + u * kUnitWords);
+            dst[0] = w;
+            dst[1] = v;
+            if (t0 >= A && t0 < Bt) {
+                // the CTA's first unit; CTAs before it with an empty range (T < G) start here too
+                cta_off[c] = (int32_t)u;
+                for (int64_t ce = c - 1; ce >= 0 && cta_start(ce) == t0; --ce) cta_off[ce] = (int32_t)u;
+            }
         }
     }
     __syncthreads();
