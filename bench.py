@@ -8,11 +8,13 @@ uniform in [8192, 32768] in 64-key pages under a random block_table, sparse_coun
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the launching
 stream with an L2 flush (a 512 MB write, then a read of it) between steps, outside the events;
-barrier + synchronize around the timed region; the maximum over ranks.  A second pass of up to 50 steps
-puts events between the three kernels as well, for the per-stage times and the scoring kernel's
-roofline.  SM clocks and throttle reasons are
-sampled with nvidia-smi over ~1.5 s of identical untimed load steps ending where the timed steps
-begin, and through the timed steps.  Printed: one JSON line.
+barrier + synchronize around the timed region; the maximum over ranks.  A timed step replays the
+library's execution plan (the three launches captured once as a CUDA graph, qli_plan_*), as a
+serving loop with fixed buffers runs them; ``--no-graph`` times plain stream launches instead, and
+the line also reports that time.  A further pass of up to 50 steps puts events between the three
+kernels, for the per-stage times and the scoring kernel's roofline.  SM clocks and throttle
+reasons are sampled with nvidia-smi over ~1.5 s of identical untimed load steps ending where the
+timed steps begin, and through the timed steps.  Printed: one JSON line.
 
 ``--impl reference`` times the CPU oracle instead (the reference arm): the plain C implementation
 run on the host cores on a bounded sample of the same workload.
@@ -52,6 +54,8 @@ def parse():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
     ap.add_argument("--flush-mb", type=int, default=512)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time stream launches instead of the captured execution plan")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the clock-sampling load window")
     return ap.parse_args()
@@ -329,6 +333,15 @@ def main():
     torch.cuda.synchronize()
     st, bits = ix.device_error()
     Q.check(st, "device error after warm-up (bits %d)" % bits)
+    # the timed step is the public execution plan (qli_plan_*): the same three launches captured
+    # once as a CUDA graph and replayed, as a serving loop with fixed buffers runs them
+    plan = None if args.no_graph else ix.plan(**d)
+    run_step = step if plan is None else plan.launch
+    if plan is not None:
+        for _ in range(max(3, args.warmup)):
+            flush_l2(1)
+            run_step()
+        torch.cuda.synchronize()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     # nvidia-smi samples every 100 ms: keep the GPU on the same load for ~1.5 s of untimed steps
@@ -340,7 +353,7 @@ def main():
     while time.perf_counter() < t_end:
         for _ in range(20):
             flush_l2(2)
-            step()
+            run_step()
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -350,12 +363,23 @@ def main():
     for i in range(args.steps):
         flush_l2(i)
         evs[i][0].record(stream)
-        step()
+        run_step()
         evs[i][3].record(stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clk = clocks.stop()
+    # the same steps launched one kernel at a time on the stream (no graph), for comparison
+    sstream = []
+    for i in range(max(3, min(args.steps, 50))):
+        flush_l2(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        sstream.append((a, b))
+    torch.cuda.synchronize()
+    stream_us = sum(a.elapsed_time(b) for a, b in sstream) / len(sstream) * 1e3
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
     # per-stage pass (stage times and the score kernel's roofline): events between the kernels
@@ -381,11 +405,17 @@ def main():
         h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
         d2h = out_h.numel() * 4
 
+        e2e_plan = None if args.no_graph else ix.plan(**dd)
+
         def e2e_step():
             for k, v in host.items():
                 if v is not None:
                     dd[k].copy_(v, non_blocking=True)
-            out = ix.run(**dd)
+            if e2e_plan is None:
+                out = ix.run(**dd)
+            else:
+                e2e_plan.launch()
+                out = ix.out
             out_h.copy_(out, non_blocking=True)
 
         for _ in range(2):
@@ -421,6 +451,8 @@ def main():
         "data": "synthetic", "config": config_of(case, args, world),
         "keys_scored_per_s": stats["pairs"] * args.steps * world / (total_ms * 1e-3),
         "us_per_call": 1e3 * total_ms / args.steps,
+        "launch": "stream launches" if args.no_graph else "execution plan (CUDA graph replay, qli_plan_launch)",
+        "us_per_call_stream_launches": stream_us,
         "stage_us": {"metadata": 1e3 * statistics.mean(meta_ms),
                      "score": 1e3 * score_avg, "topk": 1e3 * statistics.mean(topk_ms)},
         "roofline": {"kernel": "score_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,

@@ -27,6 +27,7 @@ INT64_MAX = (1 << 63) - 1
 EXPORTS = ("qli_problem_init", "qli_validate", "qli_metadata_words", "qli_workspace_size",
            "qli_metadata", "qli_score_topk", "qli_score", "qli_topk", "qli_score_topk_static",
            "qli_workspace_init", "qli_get_device_error",
+           "qli_plan_create", "qli_plan_launch", "qli_plan_destroy",
            "qli_status_string", "qli_version")
 
 
@@ -81,6 +82,13 @@ def _load():
     L.qli_status_string.restype = ctypes.c_char_p
     L.qli_version.argtypes = []
     L.qli_version.restype = ctypes.c_int
+    L.qli_plan_create.argtypes = [P, ctypes.c_int, vp, vp, vp, vp, vp, i32p, i32p, i32p, i32p, sz, vp,
+                                  sz, i32p, ctypes.POINTER(ctypes.c_void_p)]
+    L.qli_plan_create.restype = ctypes.c_int
+    L.qli_plan_launch.argtypes = [vp, vp]
+    L.qli_plan_launch.restype = ctypes.c_int
+    L.qli_plan_destroy.argtypes = [vp]
+    L.qli_plan_destroy.restype = None
     return L
 
 
@@ -173,6 +181,25 @@ def score_topk_static(p: Problem, query, key, weights, q_scale, k_scale, seq_len
         _ptr(sparse_indices), _ptr(device_error), _stream(stream))
 
 
+def plan_create(p: Problem, with_metadata, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k,
+                block_table, meta, workspace, sparse_indices):
+    """qli_plan_create: returns (status, plan handle or None)."""
+    h = ctypes.c_void_p(None)
+    st = _get_lib().qli_plan_create(
+        ctypes.byref(p), 1 if with_metadata else 0, _ptr(query), _ptr(key), _ptr(weights), _ptr(q_scale),
+        _ptr(k_scale), _ptr(seq_lens_q), _ptr(seq_lens_k), _ptr(block_table), _ptr(meta), meta.numel(),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(sparse_indices), ctypes.byref(h))
+    return st, (h.value if st == QLI_OK else None)
+
+
+def plan_launch(plan, stream=None) -> int:
+    return _get_lib().qli_plan_launch(plan, _stream(stream))
+
+
+def plan_destroy(plan) -> None:
+    _get_lib().qli_plan_destroy(plan)
+
+
 def workspace_init(workspace, stream=None) -> int:
     return _get_lib().qli_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream))
@@ -249,6 +276,17 @@ class Indexer:
                          block_table, self.meta, self.workspace, o), "score_topk")
         return o
 
+    def plan(self, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
+             with_metadata=True, out=None):
+        """A ``Plan`` replaying this call on these tensors (their addresses are captured)."""
+        o = self.out if out is None else out
+        st, h = plan_create(self.p, with_metadata, query, key, weights, q_scale, k_scale, seq_lens_q,
+                            seq_lens_k, block_table, self.meta, self.workspace, o)
+        check(st, "plan_create")
+        # the captured tensors stay referenced as long as the plan lives
+        return Plan(h, (query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
+                        self.meta, self.workspace, o))
+
     def device_error(self):
         return get_device_error(self.workspace)
 
@@ -263,3 +301,26 @@ class Indexer:
         neg = codes < 0x80000000
         bits = torch.where(neg, (~codes) & 0xFFFFFFFF, codes & 0x7FFFFFFF)
         return bits.to(torch.int32).view(torch.float32).reshape(self.rows, ld)
+
+
+class Plan:
+    """One indexer call captured as a CUDA graph (qli_plan_*); ``launch`` replays it on the current
+    stream.  Holds references to the captured tensors."""
+
+    def __init__(self, handle, keep):
+        self._h = handle
+        self._keep = keep
+
+    def launch(self, stream=None):
+        check(plan_launch(self._h, stream), "plan_launch")
+
+    def close(self):
+        if self._h is not None:
+            plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
