@@ -28,6 +28,9 @@ constexpr int kGroupTokens = 1;
 constexpr int kScoreCtasPerSm = 2;        // score CTAs resident per SM (the split is made for this)
 constexpr int kMaxCtas = 1024;            // bound on the split's CTA count (GB300 has 152 SMs)
 
+// Top-k: candidates held per row
+constexpr int kTopkCap = 4096;
+
 // Device error bits (sticky word at the start of the workspace)
 constexpr uint32_t kErrLength = 1u;       // a length beyond its bound / non-monotone prefix sums
 constexpr uint32_t kErrPage = 2u;         // a block_table entry outside [0, num_blocks)

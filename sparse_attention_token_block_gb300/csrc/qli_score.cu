@@ -571,9 +571,9 @@ __global__ void __launch_bounds__(kThreads, kScoreCtasPerSm)
     ptx::pdl_wait();
     ptx::pdl_launch_dependents();
 
-    // the metadata must have been written for this problem
-    // the header and this CTA's first list offsets are loaded together (the grid never exceeds
-    // kMaxCtas, so the offsets are inside the buffer whatever it holds)
+    // the metadata must have been written for this problem: the header and this CTA's first list
+    // offsets are loaded together (the grid never exceeds kMaxCtas, so the offsets are inside the
+    // buffer whatever it holds)
     const int32_t* meta = a.meta;
     const int4 h0 = *reinterpret_cast<const int4*>(meta);          // magic, G, units, tiles
     const int4 h1 = *reinterpret_cast<const int4*>(meta + 4);      // err, batch, rows, groups

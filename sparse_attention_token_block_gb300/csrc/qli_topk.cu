@@ -35,7 +35,7 @@ namespace {
 constexpr int kThreads = QLI_TOPK_THREADS;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSampleKeys = 1024;             // keys sampled to bound the candidates' codes
-constexpr int kCap = 4096;                    // candidates held in shared memory
+constexpr int kCap = kTopkCap;                // candidates held in shared memory
 constexpr int kSamples = 2048;
 constexpr int kBins = 8192;                   // ordering bins
 constexpr int kBinsPerThread = kBins / kThreads;
@@ -351,59 +351,54 @@ __device__ Binning make_binning(uint32_t L, uint32_t top)
     return g;
 }
 
-// Steps 1-2 over src[0..c) (shared memory, 16-byte aligned, c <= kCacheKeys): each thread loads
-// its keys (4 * kVecPerThread of them, four at a time) into registers once; every key with code
-// >= g.L is appended to S.key / S.val (a count per thread, one scan, then each thread writes its
-// keys from its offset) and counted in its bin.  Returns how many keys reached g.L (only the first
+// Steps 1-2 over src[0..c) (shared memory, 16-byte aligned, c <= kCacheKeys): each thread tests
+// its keys (4 * kVecPerThread of them, four at a time) against g.L and keeps one bit per key; a
+// scan of the per-thread counts gives each thread its offset, and each thread then visits only
+// its set bits, appending those keys to S.key / S.val and counting them in their bins (if
+// `count`).  Visiting set bits keeps the warp on the ~15 % of keys that pass instead of taking
+// the append path for every key position.  Returns how many keys reached g.L (only the first
 // kCap are stored or counted).
 constexpr int kVecPerThread = kCacheKeys / (4 * kThreads);
-__device__ __noinline__ int compact_and_count(const uint32_t* src, int c, Binning g)
+static_assert(kVecPerThread * 4 <= 32, "one pass bit per key in a 32-bit mask");
+__device__ __noinline__ int compact_and_count(const uint32_t* src, int c, Binning g, bool count)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
-    for (int b = tid; b < kBins; b += kThreads) S.bins[b] = 0;
+    if (count)
+        for (int b = tid; b < kBins; b += kThreads) S.bins[b] = 0;
     const int c4 = c >> 2;
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
     const uint32_t L = g.L;
-    uint4 v[kVecPerThread];
-#pragma unroll
-    for (int q = 0; q < kVecPerThread; ++q) {
-        const int i = tid + q * kThreads;
-        v[q] = i < c4 ? s4[i] : make_uint4(0, 0, 0, 0);
-    }
-    // the c mod 4 keys past the last full vector: thread t < c - 4 c4 takes key 4 c4 + t
-    const int tail = c - 4 * c4;
-    const uint32_t xt = tid < tail ? src[4 * c4 + tid] : 0u;
-    uint32_t mine = (tid < tail && xt >= L) ? 1u : 0u;
-#pragma unroll
-    for (int q = 0; q < kVecPerThread; ++q) {
-        if (tid + q * kThreads < c4)
-            mine += (v[q].x >= L ? 1u : 0u) + (v[q].y >= L ? 1u : 0u) + (v[q].z >= L ? 1u : 0u) +
-                    (v[q].w >= L ? 1u : 0u);
-    }
-    uint32_t total;
-    uint32_t pos = block_excl_scan(mine, &total, S.misc);   // its barrier also orders the zeroing
-    auto put = [&](uint32_t x, int j) {
-        if (x >= L) {
-            if (pos < (uint32_t)kCap) {
-                S.key[pos] = x;
-                S.val[pos] = (uint32_t)j;
-                atomicAdd(&S.bins[g(x)], 1u);
-            }
-            ++pos;
-        }
-    };
+    uint32_t mask = 0;                 // bit 4q + e: key e of this thread's vector q passes
 #pragma unroll
     for (int q = 0; q < kVecPerThread; ++q) {
         const int i = tid + q * kThreads;
         if (i < c4) {
-            put(v[q].x, 4 * i);
-            put(v[q].y, 4 * i + 1);
-            put(v[q].z, 4 * i + 2);
-            put(v[q].w, 4 * i + 3);
+            const uint4 v = s4[i];
+            mask |= ((v.x >= L ? 1u : 0u) | (v.y >= L ? 2u : 0u) | (v.z >= L ? 4u : 0u) | (v.w >= L ? 8u : 0u))
+                    << (4 * q);
         }
     }
-    if (tid < tail) put(xt, 4 * c4 + tid);
+    // the c mod 4 keys past the last full vector: thread t < c - 4 c4 takes key 4 c4 + t
+    const int tail = c - 4 * c4;
+    const bool tail_in = tid < tail && src[4 * c4 + tid] >= L;
+    uint32_t total;
+    uint32_t pos = block_excl_scan(__popc(mask) + (tail_in ? 1u : 0u), &total, S.misc);
+    auto put = [&](uint32_t x, int j) {
+        if (pos < (uint32_t)kCap) {
+            S.key[pos] = x;
+            S.val[pos] = (uint32_t)j;
+            if (count) atomicAdd(&S.bins[g(x)], 1u);
+        }
+        ++pos;
+    };
+    while (mask) {
+        const int bit = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int j = 4 * (tid + (bit >> 2) * kThreads) + (bit & 3);
+        put(src[j], j);
+    }
+    if (tail_in) put(src[4 * c4 + tid], 4 * c4 + tid);
     __syncthreads();
     return (int)total;
 }
@@ -530,11 +525,11 @@ __device__ __noinline__ int order_bins(const uint32_t* lkey, const uint32_t* lva
     return kBinOrdered;
 }
 
-// Cached rows longer than kCap (the line in S.cache[0..c)): a lower bound L for the candidates'
-// codes from a sample of kSampleKeys evenly spaced keys -- the code of the rank-r largest sample,
+// Rows longer than kCap (src: the line in the row cache or in global memory, c keys): a lower
+// bound L for the candidates' codes from a sample of kSampleKeys evenly spaced keys -- the code of the rank-r largest sample,
 // r = 1.15 l + 4 sqrt(l) + 2 with l = need * kSampleKeys / c the samples expected above the
 // need-th key -- and the largest sample, the top of the bins.
-__device__ __noinline__ Binning sample_bound(int c, int need)
+__device__ __noinline__ Binning sample_bound(const uint32_t* src, int c, int need)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
@@ -543,7 +538,7 @@ __device__ __noinline__ Binning sample_bound(int c, int need)
     uint32_t smx = 0, smn = 0xFFFFFFFFu;
 #pragma unroll
     for (int q = 0; q < per; ++q) {
-        x[q] = S.cache[((int64_t)(tid + q * kThreads) * c) / kSampleKeys];
+        x[q] = src[((int64_t)(tid + q * kThreads) * c) / kSampleKeys];
         smx = max(smx, x[q]);
         smn = min(smn, x[q]);
     }
@@ -621,6 +616,22 @@ __device__ __noinline__ int gather_sampled(const uint32_t* line, int64_t n, int 
     return gather(S, line, n, t & 0xFFFFFFFF00000000ull);
 }
 
+// Bounded wait for the row cache's bulk copy (false: it did not land within about 2 s)
+__device__ bool wait_copy(uint64_t* bar, uint32_t& parity)
+{
+    bool ok = true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer() - t0 > 2000000000ull) {
+            ok = false;
+            break;
+        }
+    }
+    parity ^= 1u;
+    return __syncthreads_and(ok);
+}
+
+// One CTA per row (the grid strides over rows).
 __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ TopkArgs a)
 {
     const Smem S = smem_view();
@@ -664,6 +675,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             if (e[kBeOk] && r >= 0) n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], lc, r);
         }
         const uint32_t* line = a.scores + row * p.ld;
+        const int need = (int)(n < k ? n : k);
+        const int64_t pages = n > 0 ? ceil_div64(lc, p.block_size) : 0;
+        const int32_t* table = a.block_table + (b < 0 ? 0 : b) * p.max_blocks_per_seq;
         const bool cached = n > 0 && n <= kCacheKeys;
         __syncthreads();                           // the previous row is done with shared memory
         if (tid == 0) {
@@ -679,8 +693,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         // ---- every page this batch's rows can see must lie in the pool: the first entry per
         // thread is loaded now and checked after the selection, the rest (rows of > 1024 pages)
         // at once
-        const int64_t pages = n > 0 ? ceil_div64(lc, p.block_size) : 0;
-        const int32_t* table = a.block_table + (b < 0 ? 0 : b) * p.max_blocks_per_seq;
         const int32_t pg_first = tid < pages ? __ldg(table + tid) : 0;
         bool bad = false;
         for (int64_t i = tid + kThreads; i < pages; i += kThreads) {
@@ -689,19 +701,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         }
         bool copy_ok = true;
         if (cached) {
-            // bounded wait for the line
-            const uint64_t t0 = ptx::globaltimer();
-            while (!ptx::mbar_try_wait(S.bar, bar_parity)) {
-                if (ptx::globaltimer() - t0 > 2000000000ull) {
-                    copy_ok = false;
-                    break;
-                }
-            }
-            bar_parity ^= 1u;
-            copy_ok = __syncthreads_and(copy_ok);
+            copy_ok = wait_copy(S.bar, bar_parity);   // bounded wait for the line
             if (!copy_ok && tid == 0) atomicOr(a.err, kErrTimeout);
         }
-        const int need = (int)(n < k ? n : k);
         const uint32_t* result = S.outv;           // ordered indices of this row
         if (n > 0 && copy_ok) {
             int st = kBinTooMany;
@@ -721,8 +723,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
                     count_bins(S.cache, (int)n, g);
                     st = order_bins(S.cache, nullptr, (int)n, need, g, S.key, S.val);
                 } else {
-                    const Binning g = sample_bound((int)n, need);
-                    const int m = compact_and_count(S.cache, (int)n, g);
+                    const Binning g = sample_bound(S.cache, (int)n, need);
+                    const int m = compact_and_count(S.cache, (int)n, g, true);
                     st = order_bins(S.key, S.val, m, need, g, S.cache, S.cache + kCap);
                 }
                 if (st == kBinTooMany) {
