@@ -107,10 +107,12 @@ Params params_of(const qli_problem* q)
     p.ld = ld > 0 ? ld : kTileKeys;
     p.meta = meta_layout(p.batch, max_groups_of(q));
     p.hash = problem_hash(p);
-    // failure-detection test switch (host-set, no device fault involved): the score kernel's
-    // producer issues no copies, so every consumer wait runs out and reports a timeout
+    // failure-detection test switches (host-set, no device fault involved): the score kernel's
+    // producer issues no copies (1), or its converters consume nothing (2) so the producer's key
+    // copies land and wait in the ring; either way the waits run out and report a timeout
     const char* stall = std::getenv("QLI_TEST_STALL_PRODUCER");
-    p.test_stall = (stall && stall[0] == '1') ? 1 : 0;
+    const char* stall_c = std::getenv("QLI_TEST_STALL_CONVERTER");
+    p.test_stall = (stall && stall[0] == '1') ? 1 : ((stall_c && stall_c[0] == '1') ? 2 : 0);
     return p;
 }
 

@@ -95,7 +95,7 @@ struct Params {
     int32_t rows;          // output rows
     int32_t meta_ctas;     // G
     int32_t hash;
-    int32_t test_stall;    // test switch: the score kernel's producer issues nothing (waits expire)
+    int32_t test_stall;    // test switch: 1 the score kernel's producer, 2 its converters do nothing
     int64_t ld;            // score line stride
     MetaLayout meta;
 };

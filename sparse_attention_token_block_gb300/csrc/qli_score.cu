@@ -87,7 +87,8 @@ enum {
     kBarAempty = kBarAfull + kNumA,
     kBarDfull = kBarAempty + kNumA,
     kBarDempty = kBarDfull + kNumD,
-    kNumBars = kBarDempty + kNumD
+    kBarDrain = kBarDempty + kNumD,      // the MMA thread's final commit (all its MMAs done)
+    kNumBars = kBarDrain + 1
 };
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;   // + slack to align the base to 1024
@@ -146,6 +147,19 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     }
 }
 
+// Wait, bounded (about 0.2 s) and regardless of the abort flag, for an asynchronous operation this
+// CTA issued (a copy into its shared memory, its MMAs) before the CTA releases what it targets.
+__device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err)
+{
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer() - t0 > 200000000ull) {
+            atomicOr(err, kErrTimeout);
+            return;
+        }
+    }
+}
+
 __device__ __forceinline__ float load_scale(const uint8_t* base, int i, bool f32)
 {
     if (f32) return reinterpret_cast<const float*>(base)[i];
@@ -196,7 +210,8 @@ __device__ __forceinline__ Unit read_unit(const ScoreArgs& a, int64_t u)
 // slot's barrier tracks: TMA copies of a few hundred bytes would double the copy operations per
 // tile, and the TMA engine's throughput here is per operation.
 template <bool kScaleF32>
-__device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, int64_t ubeg, int64_t uend)
+__device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs& a, int64_t ubeg, int64_t uend,
+                                        uint32_t& tile_i, int& q_unit)
 {
     const Shared S = shared_view();
     const int lane = threadIdx.x & 31;
@@ -208,7 +223,7 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
     const int cpt = 1 << lgc;
     const int tpb = 32 >> lgc;                       // tiles per batch
     const int bs = p.block_size;
-    if (p.test_stall) return;     // test switch: nothing arrives, the consumers' waits run out
+    if (p.test_stall == 1) return;   // test switch: nothing arrives, the consumers' waits run out
     // this lane's chunk of tile t0 + lane / cpt of unit y: its first row in the pool, or -1 past
     // the unit's keys (a page outside the pool is reported and read as page 0)
     auto chunk_row = [&](const Unit& y, int t0) -> int32_t {
@@ -222,7 +237,6 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
         }
         return page * bs + (key - lp * bs);
     };
-    uint32_t tile_i = 0;
     Unit xn = read_unit(a, ubeg);
     int32_t rows_next = chunk_row(xn, 0);
     for (int64_t u = ubeg; u < uend; ++u) {
@@ -240,6 +254,7 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
             ptx::bulk_load(S.base + kOffWraw, a.weights + (int64_t)x.row0 * kHeads * esz, vbytes, bar);
             ptx::bulk_load(S.base + kOffSQraw, a.q_scale + (int64_t)x.row0 * kHeads * esz, vbytes, bar);
         }
+        q_unit = uu;
         for (int t0 = 0; t0 < x.ntiles; t0 += tpb) {
             const int32_t rows = rows_next;
             // look up the next batch of this unit, else the next unit's first batch
@@ -276,10 +291,28 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
     }
 }
 
+template <bool kScaleF32>
+__device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, int64_t ubeg, int64_t uend)
+{
+    uint32_t tile_i = 0;        // tiles whose copies were issued
+    int q_unit = -1;            // last unit whose query copies were issued
+    produce<kScaleF32>(tmap, a, ubeg, uend, tile_i, q_unit);
+    // every copy this warp issued lands before the CTA moves on (normally all have been consumed
+    // and these waits return at once; after an abort some may still be in flight)
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    const Shared S = shared_view();
+    if ((threadIdx.x & 31) == 0) {
+        for (uint32_t t = tile_i > (uint32_t)kStages ? tile_i - kStages : 0u; t < tile_i; ++t)
+            drain_wait(&S.bars[kBarKfull + t % kStages], (t / kStages) & 1, a.err);
+        if (q_unit >= 0) drain_wait(&S.bars[kBarQrfull], (uint32_t)q_unit & 1, a.err);
+    }
+    __syncwarp();
+}
+
 // ------------------------------------------------------------------------------------------------
 // MMA thread
 // ------------------------------------------------------------------------------------------------
-__device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
+__device__ __forceinline__ void issue_mmas(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
 {
     const Shared S = shared_view();
     uint32_t tile_i = 0;
@@ -313,6 +346,15 @@ __device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, int64
     }
 }
 
+__device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
+{
+    issue_mmas(a, tmem, ubeg, uend);
+    // every MMA this thread issued has completed before tensor memory can be released
+    const Shared S = shared_view();
+    ptx::mma_commit(&S.bars[kBarDrain]);
+    drain_wait(&S.bars[kBarDrain], 0, a.err);
+}
+
 // ------------------------------------------------------------------------------------------------
 // Converter warps: query group -> B operand; key tiles -> A operand in tensor memory
 // ------------------------------------------------------------------------------------------------
@@ -320,6 +362,7 @@ template <bool kFp8, bool kScaleF32>
 __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
 {
     const Shared S = shared_view();
+    if (a.p.test_stall == 2) return;   // test switch: no tile is consumed; the copies wait in the ring
     const int gtid = threadIdx.x - kConvWarp0 * 32;
     const int grp = gtid / kGroupThreads;
     const int tid = gtid % kGroupThreads, lane = tid & 31, warp = tid >> 5;
@@ -542,6 +585,7 @@ __device__ void init_barriers(const Shared& S)
         ptx::mbar_init(&S.bars[kBarDfull + i], 1);
         ptx::mbar_init(&S.bars[kBarDempty + i], 4);
     }
+    ptx::mbar_init(&S.bars[kBarDrain], 1);
     ptx::fence_mbar_init();
 }
 

@@ -1,7 +1,7 @@
 """Failure detection on the GPU without a fault: every wait in the score kernel is bounded, so a
-producer that issues nothing (a host-set test switch) makes the consumers' waits run out; the
-kernel must report QLI_ERR_DEVICE_TIMEOUT through the workspace's error word and leave the CUDA
-context usable."""
+producer that issues nothing, or converters that consume nothing (host-set test switches), make
+the waits run out; the kernel must report QLI_ERR_DEVICE_TIMEOUT through the workspace's error word,
+let the copies already in flight land before its CTAs exit, and leave the CUDA context usable."""
 import os
 import subprocess
 import sys
@@ -56,8 +56,17 @@ def test_stalled_producer_reports_timeout(built):
     assert "AFTER 1024.0" in out.stdout
 
 
+def test_stalled_converter_reports_timeout_after_copies_land(built):
+    out = run_child({"QLI_TEST_STALL_CONVERTER": "1"})
+    assert out.returncode == 0, out.stderr[-2000:]
+    status = [l for l in out.stdout.splitlines() if l.startswith("STATUS")][0].split()
+    assert int(status[1]) == 6            # QLI_ERR_DEVICE_TIMEOUT
+    assert int(status[2]) & 4
+    assert "AFTER 1024.0" in out.stdout
+
+
 def test_normal_run_reports_no_error(built):
-    out = run_child({"QLI_TEST_STALL_PRODUCER": "0"})
+    out = run_child({"QLI_TEST_STALL_PRODUCER": "0", "QLI_TEST_STALL_CONVERTER": "0"})
     assert out.returncode == 0, out.stderr[-2000:]
     status = [l for l in out.stdout.splitlines() if l.startswith("STATUS")][0].split()
     assert int(status[1]) == 0 and int(status[2]) == 0
