@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
     QLI_OK = 0,
     QLI_ERR_INVALID_ARG = 1,          /* argument wrong on its face; nothing enqueued */
-    QLI_ERR_UNSUPPORTED = 2,          /* valid per the README but not implemented (return_value) */
+    QLI_ERR_UNSUPPORTED = 2,          /* valid per the README but not implemented */
     QLI_ERR_WORKSPACE_TOO_SMALL = 3,  /* metadata or workspace buffer below the required size */
     QLI_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
     QLI_ERR_DEVICE_BAD_INPUT = 5,     /* (qli_get_device_error) device data was invalid */
@@ -86,7 +86,7 @@ typedef struct {
     int32_t cmp_ratio;          /* key compression multiple: 1, 2, 4, ..., 128 */
     int32_t query_quant_mode;   /* must be 0 (per-token-head) */
     int32_t key_quant_mode;     /* must be 0 (per-token-head) */
-    int32_t return_value;       /* must be 0: sparse_values output not supported */
+    int32_t return_value;       /* 1: also write sparse_values (the scores of the indices); 0: not */
     int64_t pre_tokens;         /* reserved by the README: must be INT64_MAX */
     int64_t next_tokens;        /* reserved by the README: must be INT64_MAX */
     int32_t max_seqlen_q;       /* host-known bound on per-batch query tokens (>= every one) */
@@ -127,7 +127,10 @@ qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const i
  * sparse_indices.  `metadata` must come from qli_metadata with the same `p` and lengths.
  * `workspace` is caller-owned device scratch of at least qli_workspace_size(p) bytes, 256-byte
  * aligned, zeroed once after allocation (qli_workspace_init); calls sharing a workspace must be
- * ordered on one stream.  sparse_values must be NULL (README: return_value unsupported).
+ * ordered on one stream.  sparse_values (README return_value, which the README lists as not yet
+ * supported there): with p->return_value = 1, float32 [rows, sparse_count], device, caller-owned,
+ * receives the score of each index written (as the kernel computed it, fp32) and -infinity where
+ * the index is -1; with return_value = 0 it must be NULL.  A mismatch is QLI_ERR_INVALID_ARG.
  * query, key, weights, q_scale, k_scale and metadata must be 16-byte aligned.
  */
 qli_status qli_score_topk(const qli_problem* p, const void* query, const void* key,
@@ -144,7 +147,7 @@ qli_status qli_score_topk(const qli_problem* p, const void* query, const void* k
  *   qli_score: README steps 1-2 and the weighted head sum -- every visible key's score, kept in the
  *              workspace (one line per query row);
  *   qli_topk:  README step 3 -- the top-sparse_count indices of each row's score line, padded
- *              with -1, into sparse_indices.
+ *              with -1, into sparse_indices (and their scores into sparse_values).
  */
 qli_status qli_score(const qli_problem* p, const void* query, const void* key, const void* weights,
                      const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
@@ -152,7 +155,7 @@ qli_status qli_score(const qli_problem* p, const void* query, const void* key, c
                      size_t metadata_words, void* workspace, size_t workspace_bytes, void* stream);
 qli_status qli_topk(const qli_problem* p, const int32_t* block_table, const int32_t* metadata,
                     size_t metadata_words, void* workspace, size_t workspace_bytes,
-                    int32_t* sparse_indices, void* stream);
+                    int32_t* sparse_indices, float* sparse_values, void* stream);
 
 /*
  * qli_score_topk without a caller-provided workspace.  The README has no counterpart: this entry
@@ -162,7 +165,7 @@ qli_status qli_topk(const qli_problem* p, const int32_t* block_table, const int3
  * the device.  The scratch lives in one 16 MiB array inside the library, reserved on every GPU
  * that loads the library until the process exits; a problem whose qli_workspace_size exceeds
  * 16 MiB is rejected with QLI_ERR_WORKSPACE_TOO_SMALL.  Inputs, metadata and sparse_indices are
- * as for qli_score_topk; `device_error` (optional device pointer to one uint32) receives this
+ * as for qli_score_topk (return_value must be 0: no sparse_values here); `device_error` (optional device pointer to one uint32) receives this
  * call's device error word (bits as for qli_get_device_error).  The first call on a device looks
  * up the array's address with that device current; make it before any stream capture.  All
  * calls share the array: calls that overlap on the GPU race, so order them on one stream.  No
@@ -195,7 +198,7 @@ qli_status qli_plan_create(const qli_problem* p, int with_metadata, const void* 
                            const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                            const int32_t* block_table, int32_t* metadata, size_t metadata_words,
                            void* workspace, size_t workspace_bytes, int32_t* sparse_indices,
-                           qli_plan** plan);
+                           float* sparse_values, qli_plan** plan);
 /* Enqueue one replay of the plan on `stream` (any stream of the plan's device). */
 qli_status qli_plan_launch(const qli_plan* plan, void* stream);
 /* Release a plan (NULL is ignored).  Launches already enqueued still run. */

@@ -69,7 +69,7 @@ def _load():
     L.qli_score_topk.restype = ctypes.c_int
     L.qli_score.argtypes = [P, vp, vp, vp, vp, vp, i32p, i32p, i32p, i32p, sz, vp, sz, vp]
     L.qli_score.restype = ctypes.c_int
-    L.qli_topk.argtypes = [P, i32p, i32p, sz, vp, sz, i32p, vp]
+    L.qli_topk.argtypes = [P, i32p, i32p, sz, vp, sz, i32p, vp, vp]
     L.qli_topk.restype = ctypes.c_int
     L.qli_score_topk_static.argtypes = [P, vp, vp, vp, vp, vp, i32p, i32p, i32p, i32p, sz, i32p,
                                         vp, vp]
@@ -83,7 +83,7 @@ def _load():
     L.qli_version.argtypes = []
     L.qli_version.restype = ctypes.c_int
     L.qli_plan_create.argtypes = [P, ctypes.c_int, vp, vp, vp, vp, vp, i32p, i32p, i32p, i32p, sz, vp,
-                                  sz, i32p, ctypes.POINTER(ctypes.c_void_p)]
+                                  sz, i32p, vp, ctypes.POINTER(ctypes.c_void_p)]
     L.qli_plan_create.restype = ctypes.c_int
     L.qli_plan_launch.argtypes = [vp, vp]
     L.qli_plan_launch.restype = ctypes.c_int
@@ -166,10 +166,10 @@ def score(p: Problem, query, key, weights, q_scale, k_scale, seq_lens_q, seq_len
                                 workspace.numel() * workspace.element_size(), _stream(stream))
 
 
-def topk(p: Problem, block_table, meta, workspace, sparse_indices, stream=None) -> int:
+def topk(p: Problem, block_table, meta, workspace, sparse_indices, sparse_values=None, stream=None) -> int:
     return _get_lib().qli_topk(ctypes.byref(p), _ptr(block_table), _ptr(meta), meta.numel(),
                                _ptr(workspace), workspace.numel() * workspace.element_size(),
-                               _ptr(sparse_indices), _stream(stream))
+                               _ptr(sparse_indices), _ptr(sparse_values), _stream(stream))
 
 
 def score_topk_static(p: Problem, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k,
@@ -182,13 +182,14 @@ def score_topk_static(p: Problem, query, key, weights, q_scale, k_scale, seq_len
 
 
 def plan_create(p: Problem, with_metadata, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k,
-                block_table, meta, workspace, sparse_indices):
+                block_table, meta, workspace, sparse_indices, sparse_values=None):
     """qli_plan_create: returns (status, plan handle or None)."""
     h = ctypes.c_void_p(None)
     st = _get_lib().qli_plan_create(
         ctypes.byref(p), 1 if with_metadata else 0, _ptr(query), _ptr(key), _ptr(weights), _ptr(q_scale),
         _ptr(k_scale), _ptr(seq_lens_q), _ptr(seq_lens_k), _ptr(block_table), _ptr(meta), meta.numel(),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(sparse_indices), ctypes.byref(h))
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(sparse_indices),
+        _ptr(sparse_values), ctypes.byref(h))
     return st, (h.value if st == QLI_OK else None)
 
 
@@ -227,7 +228,7 @@ def check(st: int, what: str = "qli"):
 # ------------------------------------------------------------------------------------ convenience
 def make_problem(*, batch, layout_q=BSND, max_q_tokens=0, total_q_tokens=0, qk_dtype=INT8,
                  scale_dtype=F16, num_blocks, block_size, max_blocks_per_seq, sparse_count,
-                 sparse_mode, cmp_ratio, max_seqlen_q, max_seqlen_k) -> Problem:
+                 sparse_mode, cmp_ratio, max_seqlen_q, max_seqlen_k, return_value=0) -> Problem:
     p = problem_init()
     p.batch = batch
     p.layout_q = layout_q
@@ -243,6 +244,7 @@ def make_problem(*, batch, layout_q=BSND, max_q_tokens=0, total_q_tokens=0, qk_d
     p.cmp_ratio = cmp_ratio
     p.max_seqlen_q = max_seqlen_q
     p.max_seqlen_k = max_seqlen_k
+    p.return_value = return_value
     return p
 
 
@@ -266,6 +268,9 @@ class Indexer:
         rows = p.batch * p.max_q_tokens if p.layout_q == BSND else p.total_q_tokens
         self.rows = rows
         self.out = torch.empty((rows, p.sparse_count), dtype=torch.int32, device=device)
+        # the indices' scores (README return_value), when the problem asks for them
+        self.values = (torch.empty((rows, p.sparse_count), dtype=torch.float32, device=device)
+                       if p.return_value else None)
 
     def run(self, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
             refresh_metadata=True, out=None):
@@ -273,7 +278,7 @@ class Indexer:
             check(metadata(self.p, seq_lens_q, seq_lens_k, self.meta), "metadata")
         o = self.out if out is None else out
         check(score_topk(self.p, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k,
-                         block_table, self.meta, self.workspace, o), "score_topk")
+                         block_table, self.meta, self.workspace, o, self.values), "score_topk")
         return o
 
     def plan(self, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
@@ -281,11 +286,11 @@ class Indexer:
         """A ``Plan`` replaying this call on these tensors (their addresses are captured)."""
         o = self.out if out is None else out
         st, h = plan_create(self.p, with_metadata, query, key, weights, q_scale, k_scale, seq_lens_q,
-                            seq_lens_k, block_table, self.meta, self.workspace, o)
+                            seq_lens_k, block_table, self.meta, self.workspace, o, self.values)
         check(st, "plan_create")
         # the captured tensors stay referenced as long as the plan lives
         return Plan(h, (query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
-                        self.meta, self.workspace, o))
+                        self.meta, self.workspace, o, self.values))
 
     def device_error(self):
         return get_device_error(self.workspace)

@@ -68,7 +68,7 @@ qli_status check(const qli_problem* p, const char** why)
     const int64_t rows = p->layout_q == QLI_BSND ? (int64_t)p->batch * p->max_q_tokens : p->total_q_tokens;
     QLI_REJECT(rows >= INT32_MAX, "too many query rows", QLI_ERR_INVALID_ARG);
     QLI_REJECT(rows * ceil_div64(max_lc, kTileKeys) >= INT32_MAX, "problem too large for one call", QLI_ERR_UNSUPPORTED);
-    QLI_REJECT(p->return_value != 0, "return_value (sparse_values) is not supported", QLI_ERR_UNSUPPORTED);
+    QLI_REJECT(p->return_value != 0 && p->return_value != 1, "return_value must be 0 or 1", QLI_ERR_INVALID_ARG);
 #undef QLI_REJECT
     if (why) *why = "ok";
     return QLI_OK;
@@ -286,19 +286,21 @@ qli_status qli_score(const qli_problem* p, const void* query, const void* key, c
 
 qli_status qli_topk(const qli_problem* p, const int32_t* block_table, const int32_t* metadata,
                     size_t metadata_words, void* workspace, size_t workspace_bytes, int32_t* sparse_indices,
-                    void* stream)
+                    float* sparse_values, void* stream)
 {
     Params P;
     WsLayout W;
     int sms = 0;
     qli_status s = check_call(p, metadata, metadata_words, workspace, workspace_bytes, &P, &W, &sms);
     if (s != QLI_OK) return s;
+    if ((p->return_value != 0) != (sparse_values != nullptr)) return QLI_ERR_INVALID_ARG;
     if (P.rows == 0) return QLI_OK;
     if (!sparse_indices) return QLI_ERR_INVALID_ARG;
     if (P.batch > 0 && !block_table) return QLI_ERR_INVALID_ARG;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaError_t e = launch_topk(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),
-                                reinterpret_cast<uint32_t*>(ws), sparse_indices, static_cast<cudaStream_t>(stream));
+                                reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values,
+                                static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
 
@@ -310,17 +312,19 @@ qli_status qli_score_topk(const qli_problem* p, const void* query, const void* k
 {
     qli_status s = check(p, nullptr);
     if (s != QLI_OK) return s;
-    if (sparse_values) return QLI_ERR_UNSUPPORTED;
+    // validate everything the top-k stage checks before enqueueing the score stage
+    if ((p->return_value != 0) != (sparse_values != nullptr)) return QLI_ERR_INVALID_ARG;
     {
         const Params P = params_of(p);
         if (P.rows > 0 && !sparse_indices &&
             metadata_words >= (size_t)P.meta.total_words && workspace_bytes >= ws_layout(P).total)
-            return QLI_ERR_INVALID_ARG;   // validate everything before enqueueing the first stage
+            return QLI_ERR_INVALID_ARG;
     }
     s = qli_score(p, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table, metadata,
                   metadata_words, workspace, workspace_bytes, stream);
     if (s != QLI_OK) return s;
-    return qli_topk(p, block_table, metadata, metadata_words, workspace, workspace_bytes, sparse_indices, stream);
+    return qli_topk(p, block_table, metadata, metadata_words, workspace, workspace_bytes, sparse_indices,
+                    sparse_values, stream);
 }
 
 qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream)

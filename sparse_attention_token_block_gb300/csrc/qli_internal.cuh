@@ -170,7 +170,7 @@ cudaError_t launch_score(const Params& p, const void* tmap_key, const void* quer
                          const int32_t* block_table, const int32_t* meta, uint32_t* scores,
                          uint32_t* err_word, int grid, cudaStream_t st);
 cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
-                        const uint32_t* scores, uint32_t* err_word, int32_t* out,
+                        const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
                         cudaStream_t st);
 
 }  // namespace qli

@@ -18,7 +18,8 @@ extern "C" qli_status qli_plan_create(const qli_problem* p, int with_metadata, c
                                       const void* k_scale, const int32_t* seq_lens_q,
                                       const int32_t* seq_lens_k, const int32_t* block_table,
                                       int32_t* metadata, size_t metadata_words, void* workspace,
-                                      size_t workspace_bytes, int32_t* sparse_indices, qli_plan** plan)
+                                      size_t workspace_bytes, int32_t* sparse_indices, float* sparse_values,
+                                      qli_plan** plan)
 {
     if (!plan) return QLI_ERR_INVALID_ARG;
     *plan = nullptr;
@@ -33,7 +34,7 @@ extern "C" qli_status qli_plan_create(const qli_problem* p, int with_metadata, c
     if (with_metadata) s = qli_metadata(p, seq_lens_q, seq_lens_k, metadata, metadata_words, cs);
     if (s == QLI_OK)
         s = qli_score_topk(p, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
-                           metadata, metadata_words, workspace, workspace_bytes, sparse_indices, nullptr, cs);
+                           metadata, metadata_words, workspace, workspace_bytes, sparse_indices, sparse_values, cs);
     cudaGraph_t graph = nullptr;
     const cudaError_t end = cudaStreamEndCapture(cs, &graph);   // always ends the capture
     cudaStreamDestroy(cs);

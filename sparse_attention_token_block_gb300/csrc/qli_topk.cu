@@ -52,6 +52,7 @@ struct TopkArgs {
     const uint32_t* scores;
     uint32_t* err;
     int32_t* out;
+    float* values;     // optional: the score of each index written, -inf beside -1
 };
 
 struct Smem {
@@ -757,16 +758,29 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         const bool blank = n <= 0 || !copy_ok || s_bad;
         if (tid == 0 && s_bad) atomicOr(a.err, kErrPage);
         for (int i = tid; i < k; i += kThreads) out[i] = (!blank && i < need) ? (int32_t)result[i] : -1;
+        if (a.values) {
+            // the written indices' scores, decoded from the row's score line (in L2)
+            float* val = a.values + row * k;
+            for (int i = tid; i < k; i += kThreads) {
+                float v = -__int_as_float(0x7F800000);
+                if (!blank && i < need) {
+                    const uint32_t c = __ldg(line + result[i]);
+                    v = __uint_as_float((c & 0x80000000u) ? (c & 0x7FFFFFFFu) : ~c);
+                }
+                val[i] = v;
+            }
+        }
     }
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
-                        const uint32_t* scores, uint32_t* err_word, int32_t* out, cudaStream_t st)
+                        const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
+                        cudaStream_t st)
 {
     if (p.rows == 0) return cudaSuccess;
-    TopkArgs a{p, block_table, meta, scores, err_word, out};
+    TopkArgs a{p, block_table, meta, scores, err_word, out, values};
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.rows < (1 << 30) ? p.rows : (1 << 30);

@@ -226,3 +226,35 @@ def test_topk_few_distinct_scores(qli):
     ora_idx, _, _ = oracle.score_topk(case)
     assert st == 0
     assert np.array_equal(gpu_idx, ora_idx)     # exact ties resolve by index on both sides
+
+
+# ---------------------------------------------------------------------------- sparse_values
+
+@pytest.mark.parametrize("name", ["page_decode", "fp8_compressed_decode", "long_decode"])
+def test_sparse_values_are_the_indices_scores(qli, name):
+    """return_value = 1: sparse_values holds each written index's score -- bit-equal to the kernel's
+    own score line, within the row tolerance of the oracle's score -- and -inf beside -1."""
+    import torch
+    case = W.WORKLOADS[name]()
+    p = qli.make_problem(**W.problem_kwargs(case), return_value=1)
+    ix = qli.Indexer(p)
+    d = W.to_device(case)
+    idx = ix.run(**d).cpu().numpy()
+    vals = ix.values.cpu().numpy()
+    lines = ix.score_lines().cpu().numpy()
+    torch.cuda.synchronize()
+    assert ix.device_error()[0] == 0
+    plain = qli.Indexer(qli.make_problem(**W.problem_kwargs(case)))
+    assert np.array_equal(plain.run(**d).cpu().numpy(), idx)     # the indices do not change
+    rows = range(idx.shape[0]) if idx.shape[0] <= 64 else range(0, idx.shape[0], 7)
+    ora_idx, ora_scores, err = oracle.score_topk(case, with_scores=True, rows=list(rows))
+    assert err == 0
+    for r in rows:
+        live = idx[r] >= 0
+        assert np.isneginf(vals[r][~live]).all()
+        assert np.array_equal(vals[r][live], lines[r][idx[r][live]])
+        if not live.any():
+            continue
+        tau = 1e-5 * float(np.nanmax(ora_scores[r]))             # the row tolerance
+        ref = ora_scores[r][idx[r][live]].astype(np.float64)
+        assert np.all(np.abs(vals[r][live].astype(np.float64) - ref) <= tau), r

@@ -52,7 +52,7 @@ def test_validate_accepts_readme_example(Q):
     ("sparse_mode", 1, 1), ("cmp_ratio", 3, 1), ("cmp_ratio", 256, 1), ("query_quant_mode", 1, 1),
     ("key_quant_mode", 1, 1), ("pre_tokens", 5, 1), ("next_tokens", 0, 1), ("qk_dtype", 2, 1),
     ("scale_dtype", 7, 1), ("layout_q", 2, 1), ("max_blocks_per_seq", 3, 1),
-    ("return_value", 1, 2), ("num_blocks", 0, 1), ("batch", -1, 1),
+    ("return_value", 2, 1), ("num_blocks", 0, 1), ("batch", -1, 1),
 ])
 def test_validate_rejects(Q, field, value, status):
     p = _ok_problem(Q)
@@ -73,7 +73,12 @@ def test_invalid_calls_enqueue_nothing(Q):
     assert Q.lib.qli_metadata(ctypes.byref(p), None, None, 16, 10, None) == 3       # too small
     assert Q.lib.qli_score_topk(ctypes.byref(p), *([None] * 9), 0, None, 0, None, None,
                                 None) == 3
+    # sparse_values must be given exactly when return_value = 1
     assert Q.lib.qli_score_topk(ctypes.byref(p), *([None] * 9), 1 << 20, None, 1 << 30, None,
-                                1024, None) == 2                                       # values
+                                1024, None) == 1
+    p.return_value = 1
+    assert Q.lib.qli_score_topk(ctypes.byref(p), *([None] * 9), 1 << 20, None, 1 << 30, None,
+                                None, None) == 1
+    assert Q.lib.qli_topk(ctypes.byref(p), None, None, 1 << 20, None, 1 << 30, None, None, None) == 1
     assert Q.status_string(6) == "device wait timed out"
     assert Q.version() >= 100
