@@ -31,7 +31,7 @@ class Problem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "s1", "total_q", "layout_tnd", "qk_fp8", "scale_f32", "num_heads", "head_dim",
         "num_blocks", "block_size", "max_blocks_per_seq", "sparse_count", "sparse_mode",
-        "cmp_ratio", "complete_blocks_only", "reserved")]
+        "cmp_ratio", "complete_blocks_only", "key_stride")]
 
 
 def build(force: bool = False) -> str:
@@ -79,7 +79,8 @@ def problem_of(case, complete_blocks_only: bool = False) -> Problem:
                    num_blocks=case.num_blocks, block_size=case.block_size,
                    max_blocks_per_seq=case.max_blocks_per_seq, sparse_count=case.sparse_count,
                    sparse_mode=case.sparse_mode, cmp_ratio=case.cmp_ratio,
-                   complete_blocks_only=1 if complete_blocks_only else 0, reserved=0)
+                   complete_blocks_only=1 if complete_blocks_only else 0,
+                   key_stride=getattr(case, "key_stride", 0))
 
 
 def _ptr(a):

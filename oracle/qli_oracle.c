@@ -54,7 +54,8 @@ typedef struct {
     int32_t sparse_mode;        /* 0 or 3 */
     int32_t cmp_ratio;          /* key compression multiple */
     int32_t complete_blocks_only;
-    int32_t reserved;
+    int32_t key_stride;         /* elements between consecutive pages of the key pool (the README's
+                                   `stride` of key's first axis); 0 = block_size * head_dim */
 } qlio_problem;
 
 enum { QLIO_ERR_LENGTH = 1, QLIO_ERR_PAGE = 2 };
@@ -223,7 +224,8 @@ static double dot_qk(const job* J, int64_t row, int h, int64_t page, int64_t slo
 {
     const qlio_problem* p = J->p;
     int64_t qoff = (row * p->num_heads + h) * (int64_t)p->head_dim;
-    int64_t koff = (page * p->block_size + slot) * (int64_t)p->head_dim; /* one key head */
+    const int64_t page_stride = p->key_stride ? (int64_t)p->key_stride : (int64_t)p->block_size * p->head_dim;
+    int64_t koff = page * page_stride + slot * (int64_t)p->head_dim; /* one key head */
     if (!p->qk_fp8) {
         const int8_t* q = (const int8_t*)J->query + qoff;
         const int8_t* k = (const int8_t*)J->key + koff;

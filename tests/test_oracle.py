@@ -236,6 +236,20 @@ def test_page_permutation_leaves_output_unchanged():
     assert np.array_equal(idx0, idx1)
 
 
+@pytest.mark.parametrize("pad", [16, 4096])
+def test_key_stride_only_moves_the_pages(pad):
+    """README parameter table, `stride` of key's first axis: a pool whose pages sit `pad` junk
+    elements apart gives exactly the contiguous pool's scores and indices (reading the junk, or a
+    page at the contiguous offset, would change them)."""
+    case = _small(5)
+    idx0, s0, _ = oracle.score_topk(case, with_scores=True)
+    strided = W.with_key_stride(case, pad, seed=pad)
+    assert strided.key_stride == case.block_size * 128 + pad
+    idx1, s1, _ = oracle.score_topk(strided, with_scores=True)
+    assert np.array_equal(idx0, idx1)
+    assert np.array_equal(s0, s1, equal_nan=True)
+
+
 def test_duplicate_keys_tie_in_index_order():
     case = _small(4, batch=1, s1=1, seq_lens_k=[64], sparse_count=64, sparse_mode=0)
     case.key[:] = case.key[0, 0]          # every key identical

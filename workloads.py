@@ -63,6 +63,7 @@ class Case:
     seq_lens_q: Optional[np.ndarray]  # int32 [B] (TND: prefix sums) or None
     seq_lens_k: np.ndarray        # int32 [B], original (uncompressed) key tokens
     block_table: np.ndarray       # int32 [B, max_blocks_per_seq]
+    key_stride: int = 0           # elements between key pages (0: contiguous, block_size * 128)
 
     @property
     def rows(self) -> int:
@@ -252,6 +253,18 @@ WORKLOADS = {
 # Marshalling for the CUDA library (torch device tensors and the problem attributes)
 # ----------------------------------------------------------------------------------------------
 
+def with_key_stride(case: Case, pad: int, seed: int = 0) -> Case:
+    """The same case with its key pool laid out with ``pad`` junk elements after every page, so the
+    stride of the pool's first axis is block_size * 128 + pad (the indexer's ``stride`` attribute).
+    ``key`` becomes the strided buffer, [num_blocks, block_size * 128 + pad]."""
+    nb, page = case.num_blocks, case.block_size * HEAD_DIM
+    stride = page + pad
+    rng = np.random.default_rng(seed)
+    buf = rng.integers(0, 256, size=(nb, stride)).astype(np.uint8).view(case.key.dtype)
+    buf[:, :page] = case.key.reshape(nb, page)
+    return dataclasses.replace(case, key=buf, key_stride=stride)
+
+
 def problem_kwargs(case: Case) -> dict:
     """Attributes of ``case`` as keyword arguments of the binding's ``make_problem``."""
     return dict(batch=case.batch, layout_q=0 if case.layout_q == "BSND" else 1,
@@ -261,7 +274,7 @@ def problem_kwargs(case: Case) -> dict:
                 block_size=case.block_size, max_blocks_per_seq=case.max_blocks_per_seq,
                 sparse_count=case.sparse_count, sparse_mode=case.sparse_mode,
                 cmp_ratio=case.cmp_ratio, max_seqlen_q=case.max_seqlen_q,
-                max_seqlen_k=case.max_seqlen_k)
+                max_seqlen_k=case.max_seqlen_k, key_stride=case.key_stride)
 
 
 def to_device(case: Case, device="cuda") -> dict:
