@@ -91,6 +91,11 @@ typedef struct {
     int64_t next_tokens;        /* reserved by the README: must be INT64_MAX */
     int32_t max_seqlen_q;       /* host-known bound on per-batch query tokens (>= every one) */
     int32_t max_seqlen_k;       /* host-known bound on seq_lens_k (>= every entry) */
+    int32_t key_stride;         /* README `stride`: elements between consecutive pages of the key
+                                   pool, >= block_size * 128 and a multiple of 16; 0 = contiguous */
+    int32_t mask_complete_blocks; /* sparse_mode 3 with cmp_ratio > 1: 0 = a compressed key is
+                                   visible once its block has started, n = ceil((p + 1) / cmp);
+                                   1 = only complete blocks, n = floor((p + 1) / cmp) */
 } qli_problem;
 
 /* Fill `p` with the README's defaults (BSND, int8, fp16, mode 0, cmp 1, k 2048, reserved fields

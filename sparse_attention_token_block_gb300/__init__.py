@@ -44,7 +44,8 @@ class Problem(ctypes.Structure):
         "qk_dtype", "scale_dtype", "layout_q", "num_blocks", "block_size", "max_blocks_per_seq",
         "sparse_count", "sparse_mode", "cmp_ratio", "query_quant_mode", "key_quant_mode",
         "return_value")] + [("pre_tokens", ctypes.c_int64), ("next_tokens", ctypes.c_int64),
-                            ("max_seqlen_q", ctypes.c_int32), ("max_seqlen_k", ctypes.c_int32)]
+                            ("max_seqlen_q", ctypes.c_int32), ("max_seqlen_k", ctypes.c_int32),
+                            ("key_stride", ctypes.c_int32), ("mask_complete_blocks", ctypes.c_int32)]
 
 
 def _load():
@@ -228,7 +229,8 @@ def check(st: int, what: str = "qli"):
 # ------------------------------------------------------------------------------------ convenience
 def make_problem(*, batch, layout_q=BSND, max_q_tokens=0, total_q_tokens=0, qk_dtype=INT8,
                  scale_dtype=F16, num_blocks, block_size, max_blocks_per_seq, sparse_count,
-                 sparse_mode, cmp_ratio, max_seqlen_q, max_seqlen_k, return_value=0) -> Problem:
+                 sparse_mode, cmp_ratio, max_seqlen_q, max_seqlen_k, return_value=0, key_stride=0,
+                 mask_complete_blocks=0) -> Problem:
     p = problem_init()
     p.batch = batch
     p.layout_q = layout_q
@@ -245,6 +247,8 @@ def make_problem(*, batch, layout_q=BSND, max_q_tokens=0, total_q_tokens=0, qk_d
     p.max_seqlen_q = max_seqlen_q
     p.max_seqlen_k = max_seqlen_k
     p.return_value = return_value
+    p.key_stride = key_stride
+    p.mask_complete_blocks = mask_complete_blocks
     return p
 
 

@@ -69,6 +69,10 @@ qli_status check(const qli_problem* p, const char** why)
     QLI_REJECT(rows >= INT32_MAX, "too many query rows", QLI_ERR_INVALID_ARG);
     QLI_REJECT(rows * ceil_div64(max_lc, kTileKeys) >= INT32_MAX, "problem too large for one call", QLI_ERR_UNSUPPORTED);
     QLI_REJECT(p->return_value != 0 && p->return_value != 1, "return_value must be 0 or 1", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->mask_complete_blocks != 0 && p->mask_complete_blocks != 1, "mask_complete_blocks must be 0 or 1",
+               QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->key_stride != 0 && ((int64_t)p->key_stride < (int64_t)p->block_size * 128 || p->key_stride % 16 != 0),
+               "key_stride must be 0 or a multiple of 16 of at least block_size * 128", QLI_ERR_INVALID_ARG);
 #undef QLI_REJECT
     if (why) *why = "ok";
     return QLI_OK;
@@ -110,6 +114,8 @@ Params params_of(const qli_problem* q)
     // failure-detection test switches (host-set, no device fault involved): the score kernel's
     // producer issues no copies (1), or its converters consume nothing (2) so the producer's key
     // copies land and wait in the ring; either way the waits run out and report a timeout
+    p.complete_blocks = q->mask_complete_blocks;
+    p.key_stride = q->key_stride ? q->key_stride : q->block_size * kDim;
     const char* stall = std::getenv("QLI_TEST_STALL_PRODUCER");
     const char* stall_c = std::getenv("QLI_TEST_STALL_CONVERTER");
     p.test_stall = (stall && stall[0] == '1') ? 1 : ((stall_c && stall_c[0] == '1') ? 2 : 0);
@@ -163,17 +169,18 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Key pool viewed as a 2-D byte matrix [num_blocks * block_size rows, 128 B]; the box is
-// box_rows x 128 B with the 128-byte swizzle the score kernel reads back.
+// Key pool viewed as a 3-D byte tensor [num_blocks pages][block_size keys][128 B] with the page
+// stride of the problem (README `stride`); the box is 128 B x box_rows keys x 1 page with the
+// 128-byte swizzle the score kernel reads back.
 bool encode_key_map(CUtensorMap* tm, const void* key, const Params& p)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)p.num_blocks * (cuuint64_t)p.block_size};
-    cuuint64_t strides[1] = {(cuuint64_t)kDim};
-    cuuint32_t box[2] = {(cuuint32_t)kDim, (cuuint32_t)p.box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(key), dims, strides, box, estr,
+    cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)p.block_size, (cuuint64_t)p.num_blocks};
+    cuuint64_t strides[2] = {(cuuint64_t)kDim, (cuuint64_t)p.key_stride};
+    cuuint32_t box[3] = {(cuuint32_t)kDim, (cuuint32_t)p.box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(key), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;

@@ -96,6 +96,8 @@ struct Params {
     int32_t meta_ctas;     // G
     int32_t hash;
     int32_t test_stall;    // test switch: 1 the score kernel's producer, 2 its converters do nothing
+    int32_t complete_blocks;   // mode 3 visibility: 0 ceil((p + 1) / cmp), 1 floor((p + 1) / cmp)
+    int32_t key_stride;        // elements between key pages
     int64_t ld;            // score line stride
     MetaLayout meta;
 };
@@ -118,15 +120,16 @@ __host__ __device__ inline int64_t compressed_keys(int64_t sk, int cmp)
 }
 
 // Visible compressed keys of live row r (0 <= r < sq); mode 3 counts the compressed blocks that
-// have started at or before the row's right-aligned original position: ceil((pos + 1) / cmp).
+// have started at or before the row's right-aligned original position, ceil((pos + 1) / cmp), or
+// with `complete` only those that have ended, floor((pos + 1) / cmp).
 __host__ __device__ inline int64_t visible_keys(int mode, int cmp, int64_t sq, int64_t sk, int64_t lc,
-                                                int64_t r)
+                                                int64_t r, int complete)
 {
     if (r < 0 || r >= sq) return 0;
     if (mode == 0) return lc;
     const int64_t pos = sk - sq + r;
     if (pos < 0) return 0;
-    const int64_t n = (pos + cmp) >> log2_pow2(cmp);
+    const int64_t n = (pos + (complete ? 1 : cmp)) >> log2_pow2(cmp);
     return n < lc ? n : lc;
 }
 
@@ -135,8 +138,9 @@ __host__ __device__ inline int32_t problem_hash(const Params& p)
 {
     uint32_t h = 2166136261u;
     const int32_t f[] = {p.batch, p.s1, p.total_q, p.layout_tnd, p.sparse_mode, p.cmp_ratio,
-                         p.max_seqlen_q, p.max_seqlen_k, p.block_size, p.max_blocks_per_seq};
-    for (int i = 0; i < 10; ++i) { h ^= (uint32_t)f[i]; h *= 16777619u; }
+                         p.max_seqlen_q, p.max_seqlen_k, p.block_size, p.max_blocks_per_seq,
+                         p.complete_blocks};
+    for (int i = 0; i < 11; ++i) { h ^= (uint32_t)f[i]; h *= 16777619u; }
     return (int32_t)(h & 0x7fffffff);
 }
 

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     auto keys_of = [&](int64_t b, int64_t g) -> int64_t {
         const int64_t r0 = (g - v_gb[b]) * kGroupTokens;
         const int64_t rl = min((int64_t)(r0 + kGroupTokens), (int64_t)v_sq[b]) - 1;
-        return visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl);
+        return visible_keys(p.sparse_mode, p.cmp_ratio, v_sq[b], v_sk[b], v_lc[b], rl, p.complete_blocks);
     };
     // first batch whose groups include g, moving forward from b (batches without groups share
     // their successor's first group)

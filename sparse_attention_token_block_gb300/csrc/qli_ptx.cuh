@@ -115,6 +115,17 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
 
 // ------------------------------------------------------------------------------------ TMA
 // 2-D tiled tensor load into shared memory, completion counted on `bar` (transaction bytes)
+// 3-D tiled load (x innermost); x * element size must be a multiple of 16 bytes
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t x, int32_t y,
                                             uint64_t* bar)
 {

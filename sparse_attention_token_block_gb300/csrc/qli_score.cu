@@ -224,21 +224,22 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs
     const int tpb = 32 >> lgc;                       // tiles per batch
     const int bs = p.block_size;
     if (p.test_stall == 1) return;   // test switch: nothing arrives, the consumers' waits run out
-    // this lane's chunk of tile t0 + lane / cpt of unit y: its first row in the pool, or -1 past
-    // the unit's keys (a page outside the pool is reported and read as page 0)
-    auto chunk_row = [&](const Unit& y, int t0) -> int32_t {
+    // this lane's chunk of tile t0 + lane / cpt of unit y: its first key's page (x) and its row in
+    // the scale pool, page * bs + slot (y); y = -1 past the unit's keys (a page outside the pool is
+    // reported and read as page 0)
+    auto chunk_row = [&](const Unit& y, int t0) -> int2 {
         const int key = y.kb + ((t0 + (lane >> lgc)) << 7) + ((lane & (cpt - 1)) << lgR);
-        if (key >= y.ke) return -1;
+        if (key >= y.ke) return make_int2(0, -1);
         const int lp = key / bs;
         int32_t page = __ldg(a.block_table + (int64_t)y.b * p.max_blocks_per_seq + lp);
         if (page < 0 || page >= p.num_blocks) {
             atomicOr(a.err, kErrPage);
             page = 0;
         }
-        return page * bs + (key - lp * bs);
+        return make_int2(page, page * bs + (key - lp * bs));
     };
     Unit xn = read_unit(a, ubeg);
-    int32_t rows_next = chunk_row(xn, 0);
+    int2 rows_next = chunk_row(xn, 0);
     for (int64_t u = ubeg; u < uend; ++u) {
         const int uu = (int)(u - ubeg);
         const Unit x = xn;
@@ -256,7 +257,7 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs
         }
         q_unit = uu;
         for (int t0 = 0; t0 < x.ntiles; t0 += tpb) {
-            const int32_t rows = rows_next;
+            const int32_t pages = rows_next.x, rows = rows_next.y;
             // look up the next batch of this unit, else the next unit's first batch
             if (t0 + tpb < x.ntiles) rows_next = chunk_row(x, t0 + tpb);
             else if (u + 1 < uend) rows_next = chunk_row(xn, 0);
@@ -284,8 +285,9 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs
                 const int c = lane - (tt << lgc);
                 if (c == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nch * R * kDim));
                 __syncwarp();
-                if (c >= 0 && c < nch)
-                    ptx::tma_load_2d(S.base + kOffKring + s * kKstageBytes + c * R * kDim, tmap, 0, rows, bar);
+                if (c >= 0 && c < nch)      // the key pool is [pages, bs, 128] with a page stride
+                    ptx::tma_load_3d(S.base + kOffKring + s * kKstageBytes + c * R * kDim, tmap, 0,
+                                     rows - pages * bs, pages, bar);
             }
         }
     }
@@ -487,7 +489,7 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, int64_t
         for (int tt = 0; tt < kGroupTokens; ++tt)
             nvis[tt] = tt < x.q_cnt
                            ? (int32_t)min((int64_t)x.ke, visible_keys(p.sparse_mode, p.cmp_ratio, x.sq, x.sk,
-                                                                      x.lc, x.r0 + tt))
+                                                                      x.lc, x.r0 + tt, p.complete_blocks))
                            : 0;
         for (int t = 0; t < x.ntiles; ++t, ++tile_i) {
             if ((int)(tile_i % kGroups) != grp) continue;

@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             }
             const int32_t* e = be + b * kBatchWords;
             lc = e[kBeLc];
-            if (e[kBeOk] && r >= 0) n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], lc, r);
+            if (e[kBeOk] && r >= 0) n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], lc, r, p.complete_blocks);
         }
         const uint32_t* line = a.scores + row * p.ld;
         const int need = (int)(n < k ? n : k);

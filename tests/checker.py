@@ -93,8 +93,9 @@ def check_scores(gpu_scores, ora_scores, visible, rows=None):
     return worst
 
 
-def visible_counts(case, oracle_mod):
+def visible_counts(case, oracle_mod, complete_blocks_only=False):
     """Visible-key count of every output row (from the oracle's mask function)."""
+    cb = complete_blocks_only
     rows = case.rows
     out = np.zeros(rows, dtype=np.int64)
     if case.layout_q == "BSND":
@@ -102,13 +103,14 @@ def visible_counts(case, oracle_mod):
             sq = case.s1 if case.seq_lens_q is None else int(case.seq_lens_q[b])
             sk = int(case.seq_lens_k[b])
             for r in range(case.s1):
-                out[b * case.s1 + r] = oracle_mod.visible(case, sq, sk, r) if 0 <= sq <= case.s1 else 0
+                out[b * case.s1 + r] = (oracle_mod.visible(case, sq, sk, r, complete_blocks_only=cb)
+                                        if 0 <= sq <= case.s1 else 0)
     else:
         lo = 0
         for b in range(case.batch):
             hi = int(case.seq_lens_q[b])
             sk = int(case.seq_lens_k[b])
             for r in range(hi - lo):
-                out[lo + r] = oracle_mod.visible(case, hi - lo, sk, r)
+                out[lo + r] = oracle_mod.visible(case, hi - lo, sk, r, complete_blocks_only=cb)
             lo = hi
     return out

@@ -258,3 +258,45 @@ def test_sparse_values_are_the_indices_scores(qli, name):
         tau = 1e-5 * float(np.nanmax(ora_scores[r]))             # the row tolerance
         ref = ora_scores[r][idx[r][live]].astype(np.float64)
         assert np.all(np.abs(vals[r][live].astype(np.float64) - ref) <= tau), r
+
+
+# ---------------------------------------------------------------------------- stride and mask rows
+
+@pytest.mark.parametrize("kw,pad", [
+    (dict(batch=3, s1=2, seq_lens_k=[700, 90, 1500], block_size=64, sparse_count=128, sparse_mode=3), 48),
+    (dict(batch=2, s1=1, seq_lens_k=[5000, 333], block_size=16, sparse_count=512, sparse_mode=0), 4096),
+    (dict(batch=2, s1=2, seq_lens_k=[9000, 4100], block_size=128, sparse_count=2048, sparse_mode=3,
+          qk_dtype=W.FP8, scale_dtype=W.F32, cmp_ratio=4), 256),
+])
+def test_strided_key_pool_matches_oracle(qli, kw, pad):
+    """README `stride` of key's first axis: pages `pad` junk elements apart, read by the 3-D
+    tensor map with that page stride."""
+    case = W.with_key_stride(W.make_case("strided", seed=31, **kw), pad, seed=7)
+    assert case.key_stride == case.block_size * 128 + pad
+    assert_parity(qli, case)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(batch=3, s1=3, seq_lens_k=[4099, 1025, 37], block_size=64, sparse_count=256, sparse_mode=3,
+         cmp_ratio=4),
+    dict(layout_q="TND", q_lens=[5, 300, 64], seq_lens_k=[5, 300, 640], block_size=32, sparse_count=64,
+         sparse_mode=3, cmp_ratio=8),
+])
+def test_complete_blocks_mask_matches_oracle(qli, kw):
+    """The other reading of the causal rule under compression (only complete compressed blocks are
+    visible: n = floor((p + 1) / cmp)) as a runtime flag, against the oracle's same switch."""
+    import torch
+    case = W.make_case("complete", seed=41, **kw)
+    p = qli.make_problem(**W.problem_kwargs(case), mask_complete_blocks=1)
+    ix = qli.Indexer(p)
+    gpu_idx = ix.run(**W.to_device(case)).cpu().numpy()
+    torch.cuda.synchronize()
+    assert ix.device_error()[0] == 0
+    ora_idx, ora_scores, err = oracle.score_topk(case, with_scores=True, complete_blocks_only=True)
+    assert err == 0
+    counts = visible_counts(case, oracle, complete_blocks_only=True)
+    exact, checked, fails = check(gpu_idx, ora_idx, ora_scores, counts, case.sparse_count)
+    assert not fails, fails[:5]
+    # the flag changes the result for these shapes (some rows lose their partial block)
+    ceil_idx, _, _ = oracle.score_topk(case)
+    assert not np.array_equal(ceil_idx, ora_idx)
