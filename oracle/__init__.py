@@ -66,6 +66,10 @@ def lib():
             L.qlio_score_topk.restype = ctypes.c_int
             L.qlio_score_topk.argtypes = [ctypes.POINTER(Problem), vp, vp, vp, vp, vp, vp, vp, vp,
                                           vp, vp, ctypes.c_int64, vp, ctypes.c_int]
+            L.qlio_quantize_vectors.restype = None
+            L.qlio_quantize_vectors.argtypes = [ctypes.c_int, ctypes.c_int, vp, ctypes.c_int64, vp, vp]
+            L.qlio_quantize_keys.restype = ctypes.c_int
+            L.qlio_quantize_keys.argtypes = [ctypes.POINTER(Problem), vp, ctypes.c_int64, vp, vp, vp, vp, vp]
             _lib = L
     return _lib
 
@@ -135,3 +139,28 @@ def score_topk(case, with_scores: bool = False, nthreads: int | None = None,
     err = L.qlio_score_topk(ctypes.byref(p), *[_ptr(a) for a in arrs], _ptr(slq), _ptr(slk),
                             _ptr(bt), _ptr(out), _ptr(scores), ld, _ptr(mask), int(nthreads))
     return out, scores, int(err)
+
+
+# ------------------------------------------------------------------------------------ quantizer
+
+def quantize(x_bf16: np.ndarray, fp8: bool, scale_f32: bool):
+    """Per-(token, head) quantization of ``x_bf16`` (uint16 bfloat16 bits, [..., 128]): returns
+    ``(codes [..., 128] (int8, or uint8 e4m3 codes), scales [...] (float16 or float32))``."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    n = x.size // 128
+    codes = np.empty(x.shape, dtype=np.uint8 if fp8 else np.int8)
+    scales = np.empty(x.shape[:-1], dtype=np.float32 if scale_f32 else np.float16)
+    lib().qlio_quantize_vectors(1 if fp8 else 0, 1 if scale_f32 else 0, _ptr(x), n, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def quantize_keys(case, key_bf16: np.ndarray, token_batch, token_pos):
+    """The paged key-cache write of ``key_bf16`` ([tokens, 128] bfloat16 bits) into ``case.key``
+    and ``case.k_scale`` (in place) at the (batch, compressed position) of each token; returns the
+    error mask."""
+    p = problem_of(case)
+    kb = np.ascontiguousarray(key_bf16, dtype=np.uint16)
+    tb = np.ascontiguousarray(token_batch, dtype=np.int32)
+    tp = np.ascontiguousarray(token_pos, dtype=np.int32)
+    return lib().qlio_quantize_keys(ctypes.byref(p), _ptr(kb), len(tb), _ptr(tb), _ptr(tp),
+                                    _ptr(case.block_table), _ptr(case.key), _ptr(case.k_scale))

@@ -407,3 +407,132 @@ int qlio_score_topk(const qlio_problem* p, const void* query, const void* key, c
     free(J.batch_sq);
     return err;
 }
+
+/* ---------------------------------------------------------------------------------------------
+ * Upstream quantizer (README: query and key are quantized per token and head -- quant mode 0 --
+ * "store 8-bit, compute 8-bit"; the dequant scales are the ScaleQ / ScaleK of the formula).  The
+ * README names the mode only; the reading used: symmetric absmax per 128-element (token, head)
+ * vector,
+ *     amax  = max_d |x_d|                      (x: bfloat16 widened exactly to fp32)
+ *     s     = amax / Qmax   (fp32 division)    Qmax = 127 (int8) or 448 (e4m3, its largest finite)
+ *     s     = the scale's storage value: fp16 rounds to nearest (ties to even), saturating at 65504
+ *     code  = int8:  rint(x_d / s) clamped to [-127, 127]   (fp32 division; ties to even)
+ *             e4m3:  the nearest e4m3 value to x_d / s (ties to the even code), saturating at 448
+ *     s = 0 (an all-zero vector): every code is 0.
+ * Nearest-value searches below run over the formats' own code tables, so no conversion of the C
+ * library or the hardware is involved.
+ * ------------------------------------------------------------------------------------------- */
+
+/* binary16 code nearest to v in [0, 65504] (ties: the even code) */
+static uint16_t nearest_half_code(double v)
+{
+    uint16_t lo = 0, hi = 0x7BFF; /* largest finite */
+    if (v >= (double)qlio_half_to_float(hi)) return hi;
+    while (hi - lo > 1) { /* invariant: value(lo) <= v < value(hi) */
+        uint16_t mid = (uint16_t)((lo + hi) / 2);
+        if ((double)qlio_half_to_float(mid) <= v) lo = mid; else hi = mid;
+    }
+    double dl = v - (double)qlio_half_to_float(lo), dh = (double)qlio_half_to_float(hi) - v;
+    if (dl < dh) return lo;
+    if (dh < dl) return hi;
+    return (lo & 1) ? hi : lo;
+}
+
+/* e4m3 code (sign bit clear) nearest to v in [0, 448] (ties: the even code) */
+static uint8_t nearest_e4m3_code(double v)
+{
+    uint8_t lo = 0, hi = 0x7E; /* 0x7E = 448, the largest finite */
+    if (v >= qlio_e4m3_value(hi)) return hi;
+    while (hi - lo > 1) {
+        uint8_t mid = (uint8_t)((lo + hi) / 2);
+        if (qlio_e4m3_value(mid) <= v) lo = mid; else hi = mid;
+    }
+    double dl = v - qlio_e4m3_value(lo), dh = qlio_e4m3_value(hi) - v;
+    if (dl < dh) return lo;
+    if (dh < dl) return hi;
+    return (lo & 1) ? hi : lo;
+}
+
+static float bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof(f));
+    return f;
+}
+
+/* one 128-element vector: codes (int8 or e4m3) and its scale as stored (fp16 or fp32) */
+static void quantize_vector(int qk_fp8, int scale_f32, const uint16_t* x_bf16, void* codes, void* scale_out)
+{
+    float x[128];
+    float amax = 0.0f;
+    for (int d = 0; d < 128; ++d) {
+        x[d] = bf16_to_float(x_bf16[d]);
+        amax = fmaxf(amax, fabsf(x[d]));
+    }
+    const float qmax = qk_fp8 ? 448.0f : 127.0f;
+    float s = amax / qmax;
+    uint16_t s_half = 0;
+    if (!scale_f32) {
+        s_half = nearest_half_code(s < 65504.0f ? (double)s : 65504.0);
+        s = qlio_half_to_float(s_half);
+    }
+    if (scale_f32) memcpy(scale_out, &s, sizeof(float));
+    else memcpy(scale_out, &s_half, sizeof(uint16_t));
+    for (int d = 0; d < 128; ++d) {
+        if (s == 0.0f) {
+            ((uint8_t*)codes)[d] = 0;
+            continue;
+        }
+        const float y = x[d] / s;
+        if (!qk_fp8) {
+            float r = rintf(y);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            ((int8_t*)codes)[d] = (int8_t)r;
+        } else {
+            const double a = fabs((double)y);
+            ((uint8_t*)codes)[d] = (uint8_t)((signbit(y) ? 0x80 : 0) | nearest_e4m3_code(a > 448.0 ? 448.0 : a));
+        }
+    }
+}
+
+/* Quantize n_vec vectors of 128 bfloat16 (a query [rows, 64, 128] is rows * 64 vectors) into
+ * codes [n_vec, 128] and scales [n_vec]. */
+void qlio_quantize_vectors(int qk_fp8, int scale_f32, const uint16_t* x_bf16, int64_t n_vec, void* codes,
+                           void* scales)
+{
+    const size_t ssz = scale_f32 ? 4 : 2;
+    for (int64_t v = 0; v < n_vec; ++v)
+        quantize_vector(qk_fp8, scale_f32, x_bf16 + v * 128, (uint8_t*)codes + v * 128,
+                        (uint8_t*)scales + v * ssz);
+}
+
+/* The paged key-cache write: token t's key (one head, 128 bfloat16) goes to compressed position
+ * token_pos[t] of batch token_batch[t], i.e. page block_table[b][pos / bs], slot pos % bs, of the
+ * pool (pages p->key_stride elements apart, 0 = contiguous) and of k_scale [num_blocks, bs].  A
+ * batch or position out of range skips the token (QLIO_ERR_LENGTH), a page outside the pool too
+ * (QLIO_ERR_PAGE).  Returns the error mask. */
+int qlio_quantize_keys(const qlio_problem* p, const uint16_t* key_bf16, int64_t tokens, const int32_t* token_batch,
+                       const int32_t* token_pos, const int32_t* block_table, void* key_pool, void* k_scale)
+{
+    int err = 0;
+    const int64_t bs = p->block_size;
+    const int64_t stride = p->key_stride ? (int64_t)p->key_stride : bs * 128;
+    const size_t ssz = p->scale_f32 ? 4 : 2;
+    for (int64_t t = 0; t < tokens; ++t) {
+        const int64_t b = token_batch[t], pos = token_pos[t];
+        if (b < 0 || b >= p->batch || pos < 0 || pos >= (int64_t)p->max_blocks_per_seq * bs) {
+            err |= QLIO_ERR_LENGTH;
+            continue;
+        }
+        const int64_t page = block_table[b * p->max_blocks_per_seq + pos / bs], slot = pos % bs;
+        if (page < 0 || page >= p->num_blocks) {
+            err |= QLIO_ERR_PAGE;
+            continue;
+        }
+        quantize_vector(p->qk_fp8, p->scale_f32, key_bf16 + t * 128, (uint8_t*)key_pool + page * stride + slot * 128,
+                        (uint8_t*)k_scale + (page * bs + slot) * ssz);
+    }
+    return err;
+}
