@@ -209,6 +209,46 @@ qli_status qli_plan_launch(const qli_plan* plan, void* stream);
 /* Release a plan (NULL is ignored).  Launches already enqueued still run. */
 void qli_plan_destroy(qli_plan* plan);
 
+/*
+ * Upstream quantizer (README parameter table: query_quant_mode / key_quant_mode 0, the
+ * per-token-head mode; the README names the mode but gives no formula, so this is the plain
+ * symmetric absmax reading).  Each vector of 128 bfloat16 values x (one token of one head) becomes
+ *
+ *     amax = max_d |x_d|,   s = amax / Qmax   (Qmax = 127 for int8, 448 for float8_e4m3fn)
+ *
+ * computed in fp32 and then rounded to the scale dtype (fp16: to nearest, ties to even, values
+ * above 65504 saturate to 65504), and codes  c_d = x_d / s  (fp32 division by the stored s)
+ * rounded to nearest with ties to even: int8 saturates to [-127, 127], e4m3 to +-448.  A vector
+ * whose stored s is 0 gets zero codes.  So x_d ~= s * c_d, which is how the indexer reads them.
+ * Non-finite inputs are outside the definition.
+ *
+ * qli_quantize: `x` bfloat16 [n_vec][128] (8-byte aligned) -> `codes` [n_vec][128] of qk_dtype
+ * (4-byte aligned) and `scales` [n_vec] of scale_dtype (aligned to its element).  For the query of
+ * the indexer, n_vec = rows * 64 and the outputs are exactly its query / q_scale arguments.  All
+ * device pointers, caller-owned; one kernel on `stream`.  n_vec = 0 enqueues nothing.
+ * QLI_ERR_INVALID_ARG for a bad dtype, a negative count, a NULL or misaligned pointer.
+ */
+qli_status qli_quantize(int32_t qk_dtype, int32_t scale_dtype, const void* x, int64_t n_vec, void* codes,
+                        void* scales, void* stream);
+
+/*
+ * The paged key-cache write of new keys (README layout: key is the PA_BSND pool addressed by
+ * block_table, k_scale is [num_blocks, block_size, 1]).  Token t's key `key_bf16[t]` (128
+ * bfloat16, 8-byte aligned rows) is quantized as in qli_quantize (qk_dtype and scale_dtype of `p`)
+ * and written to compressed position `token_pos[t]` of batch `token_batch[t]`: page
+ * block_table[b][pos / block_size], slot pos % block_size, of `key` (pages p->key_stride bytes apart,
+ * 0 = contiguous; 16-byte aligned) and of `k_scale`.  Nothing else of the pool changes.  Positions
+ * must be distinct (two tokens writing one slot leave either).  Lengths are not consulted: the
+ * caller raises seq_lens_k afterwards.  A batch outside [0, batch) or a position outside
+ * [0, max_blocks_per_seq * block_size) skips the token and sets error bit 1 (length), a page
+ * outside the pool skips it and sets bit 2 (page), in `workspace`'s device error word when
+ * `workspace` is given (NULL: not reported); qli_get_device_error reads it.  One kernel on
+ * `stream`; tokens = 0 enqueues nothing.
+ */
+qli_status qli_quantize_keys(const qli_problem* p, const void* key_bf16, int64_t tokens, const int32_t* token_batch,
+                             const int32_t* token_pos, const int32_t* block_table, void* key, void* k_scale,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* Zero the workspace's device error word (enqueued on `stream`).  Call once after allocating a
  * workspace, before its first qli_score_topk. */
 qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

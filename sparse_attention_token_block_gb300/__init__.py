@@ -28,6 +28,7 @@ EXPORTS = ("qli_problem_init", "qli_validate", "qli_metadata_words", "qli_worksp
            "qli_metadata", "qli_score_topk", "qli_score", "qli_topk", "qli_score_topk_static",
            "qli_workspace_init", "qli_get_device_error",
            "qli_plan_create", "qli_plan_launch", "qli_plan_destroy",
+           "qli_quantize", "qli_quantize_keys",
            "qli_status_string", "qli_version")
 
 
@@ -90,6 +91,10 @@ def _load():
     L.qli_plan_launch.restype = ctypes.c_int
     L.qli_plan_destroy.argtypes = [vp]
     L.qli_plan_destroy.restype = None
+    L.qli_quantize.argtypes = [ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int64, vp, vp, vp]
+    L.qli_quantize.restype = ctypes.c_int
+    L.qli_quantize_keys.argtypes = [P, vp, ctypes.c_int64, i32p, i32p, i32p, vp, vp, vp, sz, vp]
+    L.qli_quantize_keys.restype = ctypes.c_int
     return L
 
 
@@ -200,6 +205,23 @@ def plan_launch(plan, stream=None) -> int:
 
 def plan_destroy(plan) -> None:
     _get_lib().qli_plan_destroy(plan)
+
+
+def quantize(qk_dtype, scale_dtype, x, codes, scales, stream=None) -> int:
+    """qli_quantize: ``x`` bfloat16 [..., 128] -> ``codes`` (int8 / uint8 e4m3 bytes, same shape)
+    and ``scales`` ([...], float16 or float32)."""
+    return _get_lib().qli_quantize(qk_dtype, scale_dtype, _ptr(x), x.numel() // 128, _ptr(codes),
+                                   _ptr(scales), _stream(stream))
+
+
+def quantize_keys(p: Problem, key_bf16, token_batch, token_pos, block_table, key, k_scale,
+                  workspace=None, stream=None) -> int:
+    """qli_quantize_keys: write ``key_bf16`` ([tokens, 128] bfloat16) into the paged pool ``key``
+    and ``k_scale`` at each token's (batch, compressed position)."""
+    return _get_lib().qli_quantize_keys(
+        ctypes.byref(p), _ptr(key_bf16), token_batch.numel(), _ptr(token_batch), _ptr(token_pos),
+        _ptr(block_table), _ptr(key), _ptr(k_scale), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
 
 
 def workspace_init(workspace, stream=None) -> int:

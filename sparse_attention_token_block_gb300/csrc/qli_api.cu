@@ -334,6 +334,45 @@ qli_status qli_score_topk(const qli_problem* p, const void* query, const void* k
                     sparse_values, stream);
 }
 
+qli_status qli_quantize(int32_t qk_dtype, int32_t scale_dtype, const void* x, int64_t n_vec, void* codes,
+                        void* scales, void* stream)
+{
+    if (qk_dtype != QLI_INT8 && qk_dtype != QLI_FP8_E4M3) return QLI_ERR_INVALID_ARG;
+    if (scale_dtype != QLI_F16 && scale_dtype != QLI_F32) return QLI_ERR_INVALID_ARG;
+    if (n_vec < 0 || n_vec > (INT64_C(1) << 40)) return QLI_ERR_INVALID_ARG;
+    if (n_vec == 0) return QLI_OK;
+    if (!x || !codes || !scales || !aligned(x, 8) || !aligned(codes, 4) ||
+        !aligned(scales, scale_dtype == QLI_F32 ? 4 : 2))
+        return QLI_ERR_INVALID_ARG;
+    int sms = device_sms(nullptr);
+    if (sms < 0) return QLI_ERR_CUDA;
+    if (sms == 0) return QLI_ERR_NO_DEVICE;
+    cudaError_t e = launch_quantize_vectors(x, n_vec, codes, scales, qk_dtype == QLI_FP8_E4M3,
+                                            scale_dtype == QLI_F32, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
+qli_status qli_quantize_keys(const qli_problem* p, const void* key_bf16, int64_t tokens, const int32_t* token_batch,
+                             const int32_t* token_pos, const int32_t* block_table, void* key, void* k_scale,
+                             void* workspace, size_t workspace_bytes, void* stream)
+{
+    qli_status s = check(p, nullptr);
+    if (s != QLI_OK) return s;
+    if (tokens < 0 || tokens > (INT64_C(1) << 40)) return QLI_ERR_INVALID_ARG;
+    if (workspace && (workspace_bytes < kWsHeaderBytes || !aligned(workspace, 256))) return QLI_ERR_INVALID_ARG;
+    if (tokens == 0) return QLI_OK;
+    if (!key_bf16 || !token_batch || !token_pos || !block_table || !key || !k_scale) return QLI_ERR_INVALID_ARG;
+    if (!aligned(key_bf16, 8) || !aligned(key, 16) || !aligned(k_scale, p->scale_dtype == QLI_F32 ? 4 : 2))
+        return QLI_ERR_INVALID_ARG;
+    int sms = device_sms(nullptr);
+    if (sms < 0) return QLI_ERR_CUDA;
+    if (sms == 0) return QLI_ERR_NO_DEVICE;
+    const Params P = params_of(p);
+    cudaError_t e = launch_quantize_keys(P, key_bf16, tokens, token_batch, token_pos, block_table, key, k_scale,
+                                         static_cast<uint32_t*>(workspace), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
 qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream)
 {
     if (!workspace || workspace_bytes < kWsHeaderBytes || !aligned(workspace, 256)) return QLI_ERR_INVALID_ARG;

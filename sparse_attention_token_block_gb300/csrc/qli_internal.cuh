@@ -176,5 +176,10 @@ cudaError_t launch_score(const Params& p, const void* tmap_key, const void* quer
 cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
                         const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
                         cudaStream_t st);
+cudaError_t launch_quantize_vectors(const void* x_bf16, int64_t nvec, void* codes, void* scales, bool fp8,
+                                    bool scale_f32, cudaStream_t st);
+cudaError_t launch_quantize_keys(const Params& p, const void* k_bf16, int64_t tokens, const int32_t* tok_batch,
+                                 const int32_t* tok_pos, const int32_t* block_table, void* pool, void* k_scale,
+                                 uint32_t* err, cudaStream_t st);
 
 }  // namespace qli

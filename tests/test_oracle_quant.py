@@ -108,3 +108,33 @@ def test_key_cache_write_lands_on_its_page_and_slot():
     err = oracle.quantize_keys(case, kb[:2], np.array([0, 2], np.int32), np.array([1, 0], np.int32))
     assert err == (oracle.ERR_PAGE | oracle.ERR_LENGTH)
     assert np.array_equal(case.key, k0)
+
+
+def test_degenerate_vectors_of_the_generator():
+    """The generator's special vectors: exact halfway quotients round to even (numpy's rint for
+    int8, torch's float8_e4m3fn cast for e4m3), a zero vector, a scale in the float subnormal range
+    (which float16 storage rounds to 0, zeroing the codes), and a scale beyond float16's range
+    (saturated at 65504, codes then clamp)."""
+    torch = pytest.importorskip("torch")
+    b = W.bf16_vectors((5, 128), seed=7)
+    x = _f32(b)
+    c16, s16 = oracle.quantize(b, False, False)
+    c32, s32 = oracle.quantize(b, False, True)
+    # halfway cases: amax 127 gives s = 1 exactly, so codes are x rounded half to even
+    assert s16[3] == 1.0 and s32[3] == 1.0
+    assert np.array_equal(c16[3], np.rint(x[3]).astype(np.int8))
+    assert np.any(np.abs(x[3] - np.trunc(x[3])) == 0.5)
+    e8, se = oracle.quantize(b, True, True)
+    assert se[4] == 1.0
+    assert np.array_equal(e8[4], torch.from_numpy(x[4].copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    # zero vector
+    assert s16[0] == 0 and s32[0] == 0 and not c16[0].any() and not e8[0].any()
+    # subnormal scale: kept in float32, rounds to 0 in float16
+    assert 0 < s32[1] < np.finfo(np.float32).tiny
+    assert s16[1] == 0 and not c16[1].any()
+    assert np.abs(c32[1]).max() == 127
+    # beyond float16: the stored scale saturates and the codes clamp
+    assert s16[2] == np.float16(65504)
+    assert np.array_equal(c16[2], np.clip(np.rint(x[2] / np.float32(65504)), -127, 127).astype(np.int8))
+    e16, _ = oracle.quantize(b, True, False)
+    assert np.all((e16[2] & 0x7F).max() == 0x7E)

@@ -250,6 +250,48 @@ WORKLOADS = {
 
 
 # ----------------------------------------------------------------------------------------------
+# Unquantized activations (inputs of the upstream per-token-head quantizer)
+# ----------------------------------------------------------------------------------------------
+
+def bf16_vectors(shape, seed: int, special: bool = True) -> np.ndarray:
+    """Seeded bfloat16 bit patterns (uint16) of ``shape`` (last axis 128): normal draws, each
+    vector scaled by a log-uniform magnitude in [1e-3, 1e3] (activations whose range differs from
+    token to token and head to head).  Values are truncated to bfloat16, so they are exact.
+
+    With ``special`` the first vectors (as many as fit) are degenerate ones: all zero; magnitudes
+    near 1e-38 (scales in the float subnormal range); magnitudes near 1e10 (scales beyond the
+    float16 range); integers with one element 127 and the rest at k + 1/2 (every quotient an exact
+    halfway case for int8 codes); and one element 448 with the rest at midpoints of the e4m3 grid
+    (halfway cases for e4m3 codes)."""
+    rng = np.random.default_rng(seed)
+    shape = tuple(shape)
+    assert shape[-1] == HEAD_DIM
+    n = int(np.prod(shape[:-1]))
+    mag = np.exp(rng.uniform(math.log(1e-3), math.log(1e3), size=(n, 1)))
+    x = (rng.normal(0.0, 1.0, size=(n, HEAD_DIM)) * mag).astype(np.float32)
+    if special:
+        extra = []
+        extra.append(np.zeros(HEAD_DIM, np.float32))
+        extra.append((rng.normal(0.0, 1.0, HEAD_DIM) * 1e-38).astype(np.float32))
+        extra.append((rng.normal(0.0, 1.0, HEAD_DIM) * 1e10).astype(np.float32))
+        halves = rng.integers(-127, 127, size=HEAD_DIM) + 0.5
+        halves[rng.integers(0, HEAD_DIM)] = 127.0 * (1 if rng.integers(0, 2) else -1)
+        extra.append(halves.astype(np.float32))
+        # e4m3 grid below 448: exponents 2^-6 .. 2^8 with 3 mantissa bits; midpoints between neighbours
+        grid = np.array(sorted({m / 8.0 * 2.0 ** e for e in range(-6, 9) for m in range(8, 16)} |
+                               {m / 8.0 * 2.0 ** -6 for m in range(0, 8)}))
+        grid = grid[grid <= 448.0]
+        mids = (grid[:-1] + grid[1:]) / 2.0
+        pick = mids[rng.integers(0, len(mids), size=HEAD_DIM)] * rng.choice([-1.0, 1.0], size=HEAD_DIM)
+        pick[rng.integers(0, HEAD_DIM)] = 448.0
+        extra.append(pick.astype(np.float32))
+        m = min(len(extra), n)
+        x[:m] = np.stack(extra[:m])
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    return bits.reshape(shape)
+
+
+# ----------------------------------------------------------------------------------------------
 # Marshalling for the CUDA library (torch device tensors and the problem attributes)
 # ----------------------------------------------------------------------------------------------
 
