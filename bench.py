@@ -58,6 +58,8 @@ def parse():
                     help="time stream launches instead of the captured execution plan")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the clock-sampling load window")
+    ap.add_argument("--op", default="indexer", choices=["indexer", "quantize"],
+                    help="indexer: the indexer step (default); quantize: the upstream quantizer")
     return ap.parse_args()
 
 
@@ -278,6 +280,120 @@ def config_of(case, args, world):
             "l2": "flushed between timed steps (%d MB write, then read back; outside the events)" % args.flush_mb}
 
 
+def quantize_bytes(nvec, tokens, esz):
+    """Algorithmic bytes of one quantizer step: every query vector read as bfloat16 (256 B) and
+    written as codes (128 B) plus its scale; every key the same plus its (batch, position) pair
+    and the block_table entry it reads."""
+    return nvec * (256 + 128 + esz) + tokens * (256 + 128 + esz + 8 + 4)
+
+
+def run_quantize(args, rank, world, local):
+    """The upstream quantizer on the TND prefill workload (4 sequences of 1024..8192 tokens,
+    T = 15360): one step quantizes the query (T x 64 vectors, qli_quantize) and writes every
+    token's key into the paged cache (T keys, qli_quantize_keys)."""
+    import torch
+    import sparse_attention_token_block_gb300 as Q
+    from sparse_attention_token_block_gb300 import build as B
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    case = W.varlen_prefill(seed=5 + 1000 * rank)
+    p = Q.make_problem(**W.problem_kwargs(case))
+    esz = 2 if case.scale_dtype == W.F16 else 4
+    q_bits = W.bf16_vectors(case.query.shape, seed=31 + rank)
+    k_bits = W.bf16_vectors((int(case.seq_lens_k.sum()), 128), seed=32 + rank, special=False)
+    tok_b = np.repeat(np.arange(case.batch, dtype=np.int32), case.seq_lens_k)
+    tok_p = np.concatenate([np.arange(n, dtype=np.int32) for n in case.seq_lens_k])
+    d = W.to_device(case, dev)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    xq, xk = bf(q_bits), bf(k_bits)
+    tb, tp = torch.from_numpy(tok_b).to(dev), torch.from_numpy(tok_p).to(dev)
+    ws = torch.zeros(64, dtype=torch.int32, device=dev)
+    Q.check(Q.workspace_init(ws), "workspace_init")
+    flush = torch.empty(args.flush_mb * (1 << 20) // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        Q.check(Q.quantize(p.qk_dtype, p.scale_dtype, xq, d["query"], d["q_scale"]), "quantize")
+        if ev:
+            ev[1].record(stream)
+        Q.check(Q.quantize_keys(p, xk, tb, tp, d["block_table"], d["key"], d["k_scale"], ws), "quantize_keys")
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        torch.amax(flush, dim=0, out=sink)
+        step()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    if not args.no_clocks:
+        clocks.start()
+    t_end = time.perf_counter() + (0 if args.no_clocks else 1.5)
+    while time.perf_counter() < t_end:
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i)
+        torch.amax(flush, dim=0, out=sink)
+        step(evs[i])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    st, bits = Q.get_device_error(ws)
+    Q.check(st, "device error (bits %d)" % bits)
+    nvec, tokens = q_bits.size // 128, len(tok_b)
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    k_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = max_over_ranks(sum(q_ms) + sum(k_ms), None, dev)
+    nbytes = quantize_bytes(nvec, tokens, esz)
+    value = nbytes * args.steps * world / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    q_avg = statistics.mean(q_ms)
+    achieved = quantize_bytes(nvec, 0, esz) / (q_avg * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        take = 32768
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 5.0:
+            oracle.quantize(q_bits.reshape(-1, 128)[:take], case.qk_dtype == W.FP8, esz == 4)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": quantize_bytes(take, 0, esz) * reps / dt / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": "%d query vectors, %d passes" % (take, reps)}
+    line = {
+        "metric": "quantizer GB/s (algorithmic bytes: bfloat16 in, codes and scales out)", "value": value,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 -> " + ("int8" if case.qk_dtype == W.INT8 else "fp8_e4m3"), "data": "synthetic",
+        "config": {"workload": "query quantization and key-cache write of a TND prefill: T=%d tokens "
+                               "(%s), 64 heads of 128, %s scales, key pages of %d" % (
+                                   tokens, "+".join(str(int(x)) for x in case.seq_lens_k), case.scale_dtype,
+                                   case.block_size),
+                   "l2": "flushed between timed steps (%d MB write, then read back; outside the events)"
+                         % args.flush_mb},
+        "stage_us": {"quantize_query": 1e3 * q_avg, "quantize_keys": 1e3 * statistics.mean(k_ms)},
+        "roofline": {"kernel": "quantize_vectors_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": quantize_bytes(nvec, 0, esz), "traffic": None},
+        "clocks": clk,
+        "gpu_launches": 2 * args.steps,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -285,6 +401,9 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.op == "quantize":
+        run_quantize(args, rank, world, local)
         return
     import torch
     import sparse_attention_token_block_gb300 as Q

@@ -222,10 +222,11 @@ void qli_plan_destroy(qli_plan* plan);
  * whose stored s is 0 gets zero codes.  So x_d ~= s * c_d, which is how the indexer reads them.
  * Non-finite inputs are outside the definition.
  *
- * qli_quantize: `x` bfloat16 [n_vec][128] (8-byte aligned) -> `codes` [n_vec][128] of qk_dtype
- * (4-byte aligned) and `scales` [n_vec] of scale_dtype (aligned to its element).  For the query of
+ * qli_quantize: `x` bfloat16 [n_vec][128] (16-byte aligned) -> `codes` [n_vec][128] of qk_dtype
+ * (8-byte aligned) and `scales` [n_vec] of scale_dtype (aligned to its element).  For the query of
  * the indexer, n_vec = rows * 64 and the outputs are exactly its query / q_scale arguments.  All
- * device pointers, caller-owned; one kernel on `stream`.  n_vec = 0 enqueues nothing.
+ * device pointers, caller-owned; one kernel on `stream`.  n_vec = 0 enqueues nothing; n_vec is
+ * at most 2^36.
  * QLI_ERR_INVALID_ARG for a bad dtype, a negative count, a NULL or misaligned pointer.
  */
 qli_status qli_quantize(int32_t qk_dtype, int32_t scale_dtype, const void* x, int64_t n_vec, void* codes,
@@ -234,7 +235,7 @@ qli_status qli_quantize(int32_t qk_dtype, int32_t scale_dtype, const void* x, in
 /*
  * The paged key-cache write of new keys (README layout: key is the PA_BSND pool addressed by
  * block_table, k_scale is [num_blocks, block_size, 1]).  Token t's key `key_bf16[t]` (128
- * bfloat16, 8-byte aligned rows) is quantized as in qli_quantize (qk_dtype and scale_dtype of `p`)
+ * bfloat16, 16-byte aligned rows) is quantized as in qli_quantize (qk_dtype and scale_dtype of `p`)
  * and written to compressed position `token_pos[t]` of batch `token_batch[t]`: page
  * block_table[b][pos / block_size], slot pos % block_size, of `key` (pages p->key_stride bytes apart,
  * 0 = contiguous; 16-byte aligned) and of `k_scale`.  Nothing else of the pool changes.  Positions

@@ -339,9 +339,9 @@ qli_status qli_quantize(int32_t qk_dtype, int32_t scale_dtype, const void* x, in
 {
     if (qk_dtype != QLI_INT8 && qk_dtype != QLI_FP8_E4M3) return QLI_ERR_INVALID_ARG;
     if (scale_dtype != QLI_F16 && scale_dtype != QLI_F32) return QLI_ERR_INVALID_ARG;
-    if (n_vec < 0 || n_vec > (INT64_C(1) << 40)) return QLI_ERR_INVALID_ARG;
+    if (n_vec < 0 || n_vec > (INT64_C(1) << 36)) return QLI_ERR_INVALID_ARG;   // grid.x < 2^31
     if (n_vec == 0) return QLI_OK;
-    if (!x || !codes || !scales || !aligned(x, 8) || !aligned(codes, 4) ||
+    if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 8) ||
         !aligned(scales, scale_dtype == QLI_F32 ? 4 : 2))
         return QLI_ERR_INVALID_ARG;
     int sms = device_sms(nullptr);
@@ -358,11 +358,11 @@ qli_status qli_quantize_keys(const qli_problem* p, const void* key_bf16, int64_t
 {
     qli_status s = check(p, nullptr);
     if (s != QLI_OK) return s;
-    if (tokens < 0 || tokens > (INT64_C(1) << 40)) return QLI_ERR_INVALID_ARG;
+    if (tokens < 0 || tokens > (INT64_C(1) << 36)) return QLI_ERR_INVALID_ARG;
     if (workspace && (workspace_bytes < kWsHeaderBytes || !aligned(workspace, 256))) return QLI_ERR_INVALID_ARG;
     if (tokens == 0) return QLI_OK;
     if (!key_bf16 || !token_batch || !token_pos || !block_table || !key || !k_scale) return QLI_ERR_INVALID_ARG;
-    if (!aligned(key_bf16, 8) || !aligned(key, 16) || !aligned(k_scale, p->scale_dtype == QLI_F32 ? 4 : 2))
+    if (!aligned(key_bf16, 16) || !aligned(key, 16) || !aligned(k_scale, p->scale_dtype == QLI_F32 ? 4 : 2))
         return QLI_ERR_INVALID_ARG;
     int sms = device_sms(nullptr);
     if (sms < 0) return QLI_ERR_CUDA;

@@ -60,6 +60,16 @@ def test_quantize_full_query_of_a_decode_step(qli):
         assert np.array_equal(scales, ref_scales)
 
 
+def test_quantize_at_the_prefill_size(qli):
+    """The quantizer benchmark's query: a TND prefill of T = 15360 tokens x 64 heads (983040
+    vectors, 252 MB of bfloat16), every code and scale compared."""
+    bits = W.bf16_vectors((15360, 64, 128), seed=31)
+    codes, scales = _gpu_quantize(qli, bits, False, False)
+    ref_codes, ref_scales = oracle.quantize(bits, False, False)
+    assert np.array_equal(codes, ref_codes.view(np.uint8))
+    assert np.array_equal(scales, ref_scales)
+
+
 def test_quantize_rejects_bad_arguments(qli):
     import torch
     x = _bf16_dev(W.bf16_vectors((2, 128), seed=1))
@@ -74,6 +84,8 @@ def test_quantize_rejects_bad_arguments(qli):
         "QLI_ERR_INVALID_ARG"
     assert bad[lib.qli_quantize(qli.INT8, qli.F16, x.data_ptr() + 2, 1, codes.data_ptr(), scales.data_ptr(), st)] == \
         "QLI_ERR_INVALID_ARG"
+    assert bad[lib.qli_quantize(qli.INT8, qli.F16, x.data_ptr() + 8, 1, codes.data_ptr(), scales.data_ptr(), st)] == \
+        "QLI_ERR_INVALID_ARG"                          # rows are read 16 bytes at a time
     assert lib.qli_quantize(qli.INT8, qli.F16, None, 0, None, None, st) == qli.QLI_OK
 
 
