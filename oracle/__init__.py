@@ -70,6 +70,9 @@ def lib():
             L.qlio_quantize_vectors.argtypes = [ctypes.c_int, ctypes.c_int, vp, ctypes.c_int64, vp, vp]
             L.qlio_quantize_keys.restype = ctypes.c_int
             L.qlio_quantize_keys.argtypes = [ctypes.POINTER(Problem), vp, ctypes.c_int64, vp, vp, vp, vp, vp]
+            L.qlio_gather_kv.restype = ctypes.c_int
+            L.qlio_gather_kv.argtypes = [ctypes.POINTER(Problem), vp, vp, vp, vp, vp, ctypes.c_int64,
+                                         ctypes.c_int64, vp, vp]
             _lib = L
     return _lib
 
@@ -164,3 +167,25 @@ def quantize_keys(case, key_bf16: np.ndarray, token_batch, token_pos):
     tp = np.ascontiguousarray(token_pos, dtype=np.int32)
     return lib().qlio_quantize_keys(ctypes.byref(p), _ptr(kb), len(tb), _ptr(tb), _ptr(tp),
                                     _ptr(case.block_table), _ptr(case.key), _ptr(case.k_scale))
+
+
+# ------------------------------------------------------------------------------ downstream gather
+
+def gather_kv(case, sparse_indices, kv, entry_bytes: int, kv_stride: int = 0, use_seq_lens_k: bool = True):
+    """The sparse-attention gather: for every row and selected index, the KV entry at that
+    compressed position of the row's batch through ``case.block_table``.  ``kv`` is the pool as
+    bytes ([num_blocks, page bytes]); returns ``(out uint8 [rows, k, entry_bytes], counts int32
+    [rows], error_mask)``."""
+    p = problem_of(case)
+    rows = int(lib().qlio_rows(ctypes.byref(p)))
+    k = case.sparse_count
+    idx = np.ascontiguousarray(sparse_indices, dtype=np.int32).reshape(rows, k)
+    pool = np.ascontiguousarray(kv).view(np.uint8)
+    out = np.empty((rows, k, entry_bytes), dtype=np.uint8)
+    counts = np.empty(max(rows, 1), dtype=np.int32)[:rows]
+    slq = None if case.seq_lens_q is None else np.ascontiguousarray(case.seq_lens_q, np.int32)
+    slk = np.ascontiguousarray(case.seq_lens_k, np.int32) if use_seq_lens_k else None
+    bt = np.ascontiguousarray(case.block_table, np.int32)
+    err = lib().qlio_gather_kv(ctypes.byref(p), _ptr(slq), _ptr(slk), _ptr(bt), _ptr(idx), _ptr(pool),
+                               int(entry_bytes), int(kv_stride), _ptr(out), _ptr(counts))
+    return out, counts, int(err)

@@ -536,3 +536,76 @@ int qlio_quantize_keys(const qlio_problem* p, const uint16_t* key_bf16, int64_t 
     }
     return err;
 }
+
+/* ---------------------------------------------------------------------------------------------
+ * Downstream sparse-attention gather (README: sparse_indices are the token indices that take part
+ * in the sparse attention, the output "as the input of Attention"; block_table is the PageAttention
+ * KV storage block map).  Reading used: the attention reads, for every output row and every
+ * selected compressed position j of the row's batch b, the KV entry stored at that position through
+ * the same block map:
+ *     out[r][i] = kv[ block_table[b][j / block_size] ][ j % block_size ]     (entry_bytes bytes)
+ * where j = sparse_indices[r][i]; j = -1 (padding) gives an all-zero entry.  The KV pool holds
+ * num_blocks pages of block_size entries, pages kv_stride bytes apart (0 = contiguous).
+ * Row r belongs to batch r / S1 (BSND) or to the b with seq_lens_q[b-1] <= r < seq_lens_q[b]
+ * (TND prefix sums, seq_lens_q[-1] = 0, within T).  An index other than -1 that is negative, not
+ * below the block_table's capacity max_blocks_per_seq * block_size, not below the batch's
+ * Lc = ceil(seq_lens_k[b] / cmp_ratio) (when seq_lens_k is given), or in a row with no batch, gives
+ * a zero entry and QLIO_ERR_LENGTH; a page outside the pool gives a zero entry and QLIO_ERR_PAGE.
+ * counts[r] (optional) = the entries of row r copied from the pool.  Returns the error mask.
+ * ------------------------------------------------------------------------------------------- */
+
+/* batch of global row r, or -1 */
+static int64_t gather_row_batch(const qlio_problem* p, const int32_t* seq_lens_q, int64_t r)
+{
+    if (!p->layout_tnd)
+        return p->s1 > 0 ? r / p->s1 : -1;
+    for (int b = 0; b < p->batch; ++b) {
+        int64_t lo = b > 0 ? seq_lens_q[b - 1] : 0, hi = seq_lens_q[b];
+        if (r < hi)
+            return (lo <= r && hi <= p->total_q) ? b : -1;
+    }
+    return -1;
+}
+
+int qlio_gather_kv(const qlio_problem* p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                   const int32_t* block_table, const int32_t* sparse_indices, const void* kv, int64_t entry_bytes,
+                   int64_t kv_stride, void* out, int32_t* counts)
+{
+    int err = 0;
+    const int64_t rows = qlio_rows(p), k = p->sparse_count, bs = p->block_size;
+    const int64_t stride = kv_stride ? kv_stride : bs * entry_bytes;
+    for (int64_t r = 0; r < rows; ++r) {
+        const int64_t b = gather_row_batch(p, seq_lens_q, r);
+        int64_t limit = -1;
+        if (b >= 0) {
+            limit = (int64_t)p->max_blocks_per_seq * bs;
+            if (seq_lens_k) {
+                const int64_t lc = seq_lens_k[b] < 0 ? -1 : compressed_len(p, seq_lens_k[b]);
+                if (lc < limit)
+                    limit = lc;
+            }
+        }
+        int32_t copied = 0;
+        for (int64_t i = 0; i < k; ++i) {
+            const int64_t j = sparse_indices[r * k + i];
+            uint8_t* dst = (uint8_t*)out + (r * k + i) * entry_bytes;
+            memset(dst, 0, (size_t)entry_bytes);
+            if (j == -1)
+                continue;
+            if (j < 0 || j >= limit) {
+                err |= QLIO_ERR_LENGTH;
+                continue;
+            }
+            const int64_t page = block_table[b * p->max_blocks_per_seq + j / bs];
+            if (page < 0 || page >= p->num_blocks) {
+                err |= QLIO_ERR_PAGE;
+                continue;
+            }
+            memcpy(dst, (const uint8_t*)kv + page * stride + (j % bs) * entry_bytes, (size_t)entry_bytes);
+            ++copied;
+        }
+        if (counts)
+            counts[r] = copied;
+    }
+    return err;
+}

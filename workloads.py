@@ -292,6 +292,19 @@ def bf16_vectors(shape, seed: int, special: bool = True) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------------------------
+# The attention's KV cache (input of the downstream gather)
+# ----------------------------------------------------------------------------------------------
+
+def kv_pool(case: Case, entry_bytes: int, pad: int = 0, seed: int = 0) -> np.ndarray:
+    """Random bytes standing for the attention's paged KV cache of ``case``: the same pages as the
+    key pool (``case.num_blocks`` pages of ``case.block_size`` entries, addressed by the same
+    block_table), ``entry_bytes`` per entry, ``pad`` junk bytes after every page.  Returns uint8
+    [num_blocks, block_size * entry_bytes + pad]."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, 256, size=(case.num_blocks, case.block_size * entry_bytes + pad), dtype=np.uint8)
+
+
+# ----------------------------------------------------------------------------------------------
 # Marshalling for the CUDA library (torch device tensors and the problem attributes)
 # ----------------------------------------------------------------------------------------------
 
