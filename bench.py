@@ -58,8 +58,10 @@ def parse():
                     help="time stream launches instead of the captured execution plan")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the clock-sampling load window")
-    ap.add_argument("--op", default="indexer", choices=["indexer", "quantize"],
-                    help="indexer: the indexer step (default); quantize: the upstream quantizer")
+    ap.add_argument("--op", default="indexer", choices=["indexer", "quantize", "gather"],
+                    help="indexer: the indexer step (default); quantize: the upstream quantizer; "
+                         "gather: the downstream sparse-attention gather")
+    ap.add_argument("--entry-bytes", type=int, default=512, help="KV entry size of --op gather")
     return ap.parse_args()
 
 
@@ -394,6 +396,100 @@ def run_quantize(args, rank, world, local):
         print(json.dumps(line))
 
 
+def run_gather(args, rank, world, local):
+    """The downstream sparse-attention gather on the long-context decode: the indexer's output
+    (32 rows x 2048 indices, computed once) selects KV entries of ``--entry-bytes`` bytes from a
+    paged KV cache that shares the key pool's block_table; one step is one qli_gather_kv."""
+    import torch
+    import sparse_attention_token_block_gb300 as Q
+    from sparse_attention_token_block_gb300 import build as B
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    case = make_workload(args.workload, args.batch, rank)
+    p = Q.make_problem(**W.problem_kwargs(case))
+    ix = Q.Indexer(p, device=dev)
+    d = W.to_device(case, dev)
+    idx = ix.run(**d).clone()
+    E = args.entry_bytes
+    pool = torch.from_numpy(W.kv_pool(case, E, 0, seed=17 + rank)).to(dev)
+    out = torch.empty((case.rows, case.sparse_count, E), dtype=torch.uint8, device=dev)
+    counts = torch.empty(case.rows, dtype=torch.int32, device=dev)
+    flush = torch.empty(args.flush_mb * (1 << 20) // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        Q.check(Q.gather_kv(p, d["seq_lens_q"], d["seq_lens_k"], d["block_table"], idx, pool, E, out, counts,
+                            0, ix.workspace), "gather_kv")
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        torch.amax(flush, dim=0, out=sink)
+        step()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    if not args.no_clocks:
+        clocks.start()
+    t_end = time.perf_counter() + (0 if args.no_clocks else 1.5)
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i)
+        torch.amax(flush, dim=0, out=sink)
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    st, bits = ix.device_error()
+    Q.check(st, "device error (bits %d)" % bits)
+    valid = int((idx >= 0).sum().item())
+    entries = case.rows * case.sparse_count
+    nbytes = valid * E + entries * E + entries * 4 + case.rows * 4
+    ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(ms)
+    avg = statistics.mean(ms)
+    value = nbytes * args.steps * world / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        h_idx, h_pool = idx.cpu().numpy(), pool.cpu().numpy()
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 5.0:
+            oracle.gather_kv(case, h_idx, h_pool, E)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "the whole gather, %d passes" % reps}
+    line = {
+        "metric": "sparse-attention gather GB/s (algorithmic bytes: selected entries read, all entries written)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bytes", "data": "synthetic",
+        "config": {"workload": "gather after the %s indexer: %d rows x %d indices (%d valid), %d-byte KV entries "
+                               "through a %d-entry-page block_table" % (case.name, case.rows, case.sparse_count,
+                                                                       valid, E, case.block_size),
+                   "l2": "flushed between timed steps (%d MB write, then read back; outside the events)"
+                         % args.flush_mb},
+        "us_per_call": 1e3 * avg,
+        "roofline": {"kernel": "gather_kernel", "bound": "hbm", "achieved": nbytes / (avg * 1e-3) / 1e9,
+                     "peak": peak, "unit": "GB/s", "frac": nbytes / (avg * 1e-3) / 1e9 / peak,
+                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+        "clocks": clk,
+        "gpu_launches": args.steps,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -404,6 +500,9 @@ def main():
         return
     if args.op == "quantize":
         run_quantize(args, rank, world, local)
+        return
+    if args.op == "gather":
+        run_gather(args, rank, world, local)
         return
     import torch
     import sparse_attention_token_block_gb300 as Q

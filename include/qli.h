@@ -250,6 +250,36 @@ qli_status qli_quantize_keys(const qli_problem* p, const void* key_bf16, int64_t
                              const int32_t* token_pos, const int32_t* block_table, void* key, void* k_scale,
                              void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Downstream sparse-attention gather (README function section: the selected indices are the token
+ * indices that take part in the sparse attention, the output is the attention's input; parameter
+ * table: block_table is the PageAttention KV block map).  Reading: the attention reads, for each
+ * output row r (batch b = r / max_q_tokens for BSND; for TND the b with seq_lens_q[b-1] <= r <
+ * seq_lens_q[b]) and each i < sparse_count, the KV entry at compressed position
+ * j = sparse_indices[r][i] of its batch through the same block map:
+ *
+ *     out[r][i][0 .. entry_bytes) = kv page block_table[b][j / block_size], entry j % block_size
+ *
+ * `kv` is the attention's paged KV cache: num_blocks pages of block_size entries of `entry_bytes`
+ * bytes (a multiple of 16, at most 65536), pages `kv_stride` bytes apart (0 = contiguous
+ * block_size * entry_bytes; else a multiple of 16 of at least that), 16-byte aligned; its content
+ * is opaque bytes.  `out` [rows, sparse_count, entry_bytes] (16-byte aligned).  j = -1 (padding)
+ * gives an all-zero entry.  An index that is otherwise negative, not below the block_table's
+ * capacity max_blocks_per_seq * block_size, not below the batch's ceil(seq_lens_k[b] / cmp_ratio)
+ * (when seq_lens_k is given; NULL skips that bound), or in a row that belongs to no batch, gives a
+ * zero entry and error bit 1; a page outside the pool gives a zero entry and bit 2 (in
+ * `workspace`'s device error word when `workspace` is given).  `counts` (optional, int32 [rows])
+ * receives the number of entries of each row copied from the pool.  seq_lens_q: TND prefix sums
+ * (required for TND, unused for BSND); prefix sums that are not non-decreasing are invalid input
+ * (then rows may be zero-filled; nothing is read or written outside the buffers).  One kernel on
+ * `stream`; it may begin while the previous kernel on the stream finishes and waits for it before
+ * reading the indices.
+ */
+qli_status qli_gather_kv(const qli_problem* p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                         const int32_t* block_table, const int32_t* sparse_indices, const void* kv,
+                         int64_t entry_bytes, int64_t kv_stride, void* out, int32_t* counts, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* Zero the workspace's device error word (enqueued on `stream`).  Call once after allocating a
  * workspace, before its first qli_score_topk. */
 qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

@@ -28,7 +28,7 @@ EXPORTS = ("qli_problem_init", "qli_validate", "qli_metadata_words", "qli_worksp
            "qli_metadata", "qli_score_topk", "qli_score", "qli_topk", "qli_score_topk_static",
            "qli_workspace_init", "qli_get_device_error",
            "qli_plan_create", "qli_plan_launch", "qli_plan_destroy",
-           "qli_quantize", "qli_quantize_keys",
+           "qli_quantize", "qli_quantize_keys", "qli_gather_kv",
            "qli_status_string", "qli_version")
 
 
@@ -95,6 +95,9 @@ def _load():
     L.qli_quantize.restype = ctypes.c_int
     L.qli_quantize_keys.argtypes = [P, vp, ctypes.c_int64, i32p, i32p, i32p, vp, vp, vp, sz, vp]
     L.qli_quantize_keys.restype = ctypes.c_int
+    L.qli_gather_kv.argtypes = [P, i32p, i32p, i32p, i32p, vp, ctypes.c_int64, ctypes.c_int64, vp, i32p, vp, sz,
+                                vp]
+    L.qli_gather_kv.restype = ctypes.c_int
     return L
 
 
@@ -221,6 +224,16 @@ def quantize_keys(p: Problem, key_bf16, token_batch, token_pos, block_table, key
     return _get_lib().qli_quantize_keys(
         ctypes.byref(p), _ptr(key_bf16), token_batch.numel(), _ptr(token_batch), _ptr(token_pos),
         _ptr(block_table), _ptr(key), _ptr(k_scale), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def gather_kv(p: Problem, seq_lens_q, seq_lens_k, block_table, sparse_indices, kv, entry_bytes, out,
+              counts=None, kv_stride=0, workspace=None, stream=None) -> int:
+    """qli_gather_kv: ``out`` [rows, sparse_count, entry_bytes] (uint8) receives the KV entries the
+    indices select through the block_table; ``counts`` (optional int32 [rows]) the entries copied."""
+    return _get_lib().qli_gather_kv(
+        ctypes.byref(p), _ptr(seq_lens_q), _ptr(seq_lens_k), _ptr(block_table), _ptr(sparse_indices), _ptr(kv),
+        int(entry_bytes), int(kv_stride), _ptr(out), _ptr(counts), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
 
 

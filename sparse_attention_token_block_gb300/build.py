@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqli.so")
-SOURCES = ["qli_api.cu", "qli_metadata.cu", "qli_score.cu", "qli_topk.cu", "qli_noalloc.cu", "qli_plan.cu", "qli_quant.cu"]
+SOURCES = ["qli_api.cu", "qli_metadata.cu", "qli_score.cu", "qli_topk.cu", "qli_noalloc.cu", "qli_plan.cu", "qli_quant.cu", "qli_gather.cu"]
 HEADERS = ["qli_internal.cuh", "qli_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

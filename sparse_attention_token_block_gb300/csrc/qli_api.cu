@@ -373,6 +373,32 @@ qli_status qli_quantize_keys(const qli_problem* p, const void* key_bf16, int64_t
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
 
+qli_status qli_gather_kv(const qli_problem* p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                         const int32_t* block_table, const int32_t* sparse_indices, const void* kv,
+                         int64_t entry_bytes, int64_t kv_stride, void* out, int32_t* counts, void* workspace,
+                         size_t workspace_bytes, void* stream)
+{
+    qli_status s = check(p, nullptr);
+    if (s != QLI_OK) return s;
+    if (entry_bytes < 16 || entry_bytes > 65536 || entry_bytes % 16 != 0) return QLI_ERR_INVALID_ARG;
+    const int64_t page_bytes = (int64_t)p->block_size * entry_bytes;
+    if (kv_stride != 0 && (kv_stride < page_bytes || kv_stride % 16 != 0)) return QLI_ERR_INVALID_ARG;
+    if (workspace && (workspace_bytes < kWsHeaderBytes || !aligned(workspace, 256))) return QLI_ERR_INVALID_ARG;
+    const Params P = params_of(p);
+    if (P.rows == 0) return QLI_OK;
+    if (!sparse_indices || !out || !aligned(out, 16) || (counts && !aligned(counts, 4))) return QLI_ERR_INVALID_ARG;
+    if (P.batch > 0 && (!block_table || !kv || !aligned(kv, 16))) return QLI_ERR_INVALID_ARG;
+    if (P.layout_tnd && P.batch > 0 && !seq_lens_q) return QLI_ERR_INVALID_ARG;
+    if ((int64_t)P.rows * p->sparse_count * (entry_bytes / 16) >= (INT64_C(1) << 40)) return QLI_ERR_UNSUPPORTED;
+    int sms = device_sms(nullptr);
+    if (sms < 0) return QLI_ERR_CUDA;
+    if (sms == 0) return QLI_ERR_NO_DEVICE;
+    cudaError_t e = launch_gather(P, seq_lens_q, seq_lens_k, block_table, sparse_indices, kv, entry_bytes,
+                                  kv_stride ? kv_stride : page_bytes, out, counts, static_cast<uint32_t*>(workspace),
+                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
 qli_status qli_workspace_init(void* workspace, size_t workspace_bytes, void* stream)
 {
     if (!workspace || workspace_bytes < kWsHeaderBytes || !aligned(workspace, 256)) return QLI_ERR_INVALID_ARG;

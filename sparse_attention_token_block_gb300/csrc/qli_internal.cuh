@@ -181,5 +181,8 @@ cudaError_t launch_quantize_vectors(const void* x_bf16, int64_t nvec, void* code
 cudaError_t launch_quantize_keys(const Params& p, const void* k_bf16, int64_t tokens, const int32_t* tok_batch,
                                  const int32_t* tok_pos, const int32_t* block_table, void* pool, void* k_scale,
                                  uint32_t* err, cudaStream_t st);
+cudaError_t launch_gather(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                          const int32_t* block_table, const int32_t* idx, const void* kv, int64_t entry_bytes,
+                          int64_t kv_stride, void* out, int32_t* counts, uint32_t* err, cudaStream_t st);
 
 }  // namespace qli

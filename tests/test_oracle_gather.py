@@ -45,24 +45,7 @@ def test_hand_worked_example():
     assert out[0, 3].tolist() == list(range(0, 16))        # j = 2: page 0, slot 0
 
 
-def _random_indices(case, rng, frac_pad=0.2):
-    rows, k = case.rows, case.sparse_count
-    lc = -(-case.seq_lens_k.astype(np.int64) // case.cmp_ratio)
-    if case.layout_q == "BSND":
-        b = np.arange(rows) // case.s1
-    else:
-        b = np.searchsorted(case.seq_lens_q, np.arange(rows), side="right")
-    idx = np.empty((rows, k), np.int32)
-    for r in range(rows):
-        n = int(min(k, lc[b[r]]))
-        m = int(n * (1 - frac_pad * rng.random()))
-        idx[r, :m] = rng.choice(int(lc[b[r]]), size=m, replace=False)
-        idx[r, m:] = -1
-    return idx
-
-
 def test_matches_numpy_indexing_bsnd_and_tnd():
-    rng = np.random.default_rng(1)
     cases = [W.make_case("gb", batch=3, s1=2, seq_lens_k=[700, 90, 1500], block_size=64, sparse_count=128, seed=2),
              W.make_case("gt", layout_q="TND", q_lens=[3, 0, 5], seq_lens_k=[300, 50, 999], block_size=32,
                          sparse_count=64, seed=3)]
@@ -70,7 +53,7 @@ def test_matches_numpy_indexing_bsnd_and_tnd():
         for entry_bytes, pad in ((16, 0), (48, 32), (1152, 0)):
             pool = W.kv_pool(case, entry_bytes, pad, seed=4)
             stride = case.block_size * entry_bytes + pad
-            idx = _random_indices(case, rng)
+            idx = W.random_indices(case, seed=entry_bytes + pad)
             out, counts, err = oracle.gather_kv(case, idx, pool, entry_bytes, stride if pad else 0)
             ref, ref_counts = _numpy_gather(case, idx, pool, entry_bytes, stride)
             assert err == 0

@@ -304,6 +304,27 @@ def kv_pool(case: Case, entry_bytes: int, pad: int = 0, seed: int = 0) -> np.nda
     return rng.integers(0, 256, size=(case.num_blocks, case.block_size * entry_bytes + pad), dtype=np.uint8)
 
 
+def random_indices(case: Case, seed: int, frac_pad: float = 0.2) -> np.ndarray:
+    """Seeded stand-ins for an indexer's output: per row, distinct compressed positions of the
+    row's batch in random order (up to sparse_count of them, a random share of up to ``frac_pad``
+    left out), then -1 padding.  int32 [rows, sparse_count]."""
+    rng = np.random.default_rng(seed)
+    rows, k = case.rows, case.sparse_count
+    lc = -(-case.seq_lens_k.astype(np.int64) // case.cmp_ratio)
+    if case.layout_q == "BSND":
+        b = np.arange(rows) // max(case.s1, 1)
+    else:
+        b = np.searchsorted(case.seq_lens_q, np.arange(rows), side="right")
+    idx = np.full((rows, k), -1, np.int32)
+    for r in range(rows):
+        if b[r] >= case.batch:
+            continue
+        n = int(min(k, lc[b[r]]))
+        m = int(n * (1 - frac_pad * rng.random()))
+        idx[r, :m] = rng.choice(int(lc[b[r]]), size=m, replace=False)
+    return idx
+
+
 # ----------------------------------------------------------------------------------------------
 # Marshalling for the CUDA library (torch device tensors and the problem attributes)
 # ----------------------------------------------------------------------------------------------
