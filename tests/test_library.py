@@ -82,3 +82,47 @@ def test_invalid_calls_enqueue_nothing(Q):
     assert Q.lib.qli_topk(ctypes.byref(p), None, None, 1 << 20, None, 1 << 30, None, None, None) == 1
     assert Q.status_string(6) == "device wait timed out"
     assert Q.version() >= 100
+
+
+def test_quantizer_and_gather_reject_bad_arguments(Q):
+    # qli_quantize / qli_quantize_keys / qli_gather_kv check their arguments before any CUDA call;
+    # the pointers below are aligned dummies that the rejected calls never dereference
+    A = 1 << 20                                        # a 16-byte aligned stand-in address
+    L = Q.lib
+    assert L.qli_quantize(2, Q.F16, A, 1, A, A, None) == 1                 # qk dtype
+    assert L.qli_quantize(Q.INT8, 5, A, 1, A, A, None) == 1                # scale dtype
+    assert L.qli_quantize(Q.INT8, Q.F16, A, -1, A, A, None) == 1           # count
+    assert L.qli_quantize(Q.INT8, Q.F16, A, 1 << 37, A, A, None) == 1      # grid limit
+    assert L.qli_quantize(Q.INT8, Q.F16, None, 1, A, A, None) == 1
+    assert L.qli_quantize(Q.INT8, Q.F16, A + 8, 1, A, A, None) == 1        # 16-byte rows
+    assert L.qli_quantize(Q.INT8, Q.F16, A, 1, A + 4, A, None) == 1        # 8-byte codes
+    assert L.qli_quantize(Q.INT8, Q.F32, A, 1, A, A + 2, None) == 1        # fp32 scales
+    assert L.qli_quantize(Q.INT8, Q.F16, None, 0, None, None, None) == 0   # nothing to do
+    p = _ok_problem(Q)
+    assert L.qli_quantize_keys(ctypes.byref(p), A, -1, A, A, A, A, A, None, 0, None) == 1
+    assert L.qli_quantize_keys(ctypes.byref(p), A, 1, A, A, A, A, A, A + 16, 256, None) == 1  # workspace alignment
+    assert L.qli_quantize_keys(ctypes.byref(p), A, 1, A, A, A, A, A, A, 64, None) == 1       # workspace size
+    assert L.qli_quantize_keys(ctypes.byref(p), A, 1, None, A, A, A, A, None, 0, None) == 1
+    assert L.qli_quantize_keys(ctypes.byref(p), A + 8, 1, A, A, A, A, A, None, 0, None) == 1
+    assert L.qli_quantize_keys(ctypes.byref(p), A, 1, A, A, A, A + 8, A, None, 0, None) == 1  # key pool
+    assert L.qli_quantize_keys(ctypes.byref(p), None, 0, None, None, None, None, None, None, 0, None) == 0
+    bad = _ok_problem(Q)
+    bad.head_dim = 64
+    assert L.qli_quantize_keys(ctypes.byref(bad), A, 1, A, A, A, A, A, None, 0, None) == 1
+    g = lambda *args: L.qli_gather_kv(ctypes.byref(p), *args)
+    assert g(None, A, A, A, A, 24, 0, A, None, None, 0, None) == 1         # entry not a multiple of 16
+    assert g(None, A, A, A, A, 0, 0, A, None, None, 0, None) == 1
+    assert g(None, A, A, A, A, 65552, 0, A, None, None, 0, None) == 1      # above 64 KiB
+    page = p.block_size * 64
+    assert g(None, A, A, A, A, 64, page - 16, A, None, None, 0, None) == 1  # stride below a page
+    assert g(None, A, A, A, A, 64, page + 8, A, None, None, 0, None) == 1   # stride not 16-aligned
+    assert g(None, A, A, None, A, 64, 0, A, None, None, 0, None) == 1       # indices
+    assert g(None, A, None, A, A, 64, 0, A, None, None, 0, None) == 1       # block_table
+    assert g(None, A, A, A, A + 8, 64, 0, A, None, None, 0, None) == 1      # pool alignment
+    assert g(None, A, A, A, A, 64, 0, A + 8, None, None, 0, None) == 1      # output alignment
+    assert g(None, A, A, A, A, 64, 0, A, A + 2, None, 0, None) == 1         # counts alignment
+    assert g(None, A, A, A, A, 64, 0, A, None, A, 16, None) == 1            # workspace size
+    t = _ok_problem(Q)
+    t.layout_q = Q.TND
+    t.total_q_tokens = 8
+    assert L.qli_gather_kv(ctypes.byref(t), None, A, A, A, A, 64, 0, A, None, None, 0, None) == 1  # TND prefix sums
