@@ -42,6 +42,10 @@ METRIC = "indexer GOPS (algorithmic: 16384 ops per visible query-key pair)"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "score_kernel_long_decode.md")
 SCORE_SOURCES = ["qli_score.cu", "qli_ptx.cuh", "qli_internal.cuh"]
+QUANT_PROFILE = os.path.join(ROOT, "profiles", "quantize_kernel_prefill.md")
+QUANT_SOURCES = ["qli_quant.cu", "qli_ptx.cuh", "qli_internal.cuh"]
+GATHER_PROFILE = os.path.join(ROOT, "profiles", "gather_kernel_long_decode.md")
+GATHER_SOURCES = ["qli_gather.cu", "qli_ptx.cuh", "qli_internal.cuh"]
 
 
 def parse():
@@ -136,15 +140,15 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic():
-    """Per-launch DRAM bytes of the scoring kernel from the committed ncu summary, if that summary
-    was taken on the current kernel source (else None)."""
+def recorded_traffic(profile=PROFILE_TRAFFIC, sources=SCORE_SOURCES):
+    """Per-launch DRAM bytes of a kernel from its committed ncu summary, if that summary was taken
+    on the current kernel source (else None)."""
     try:
-        text = open(PROFILE_TRAFFIC).read()
+        text = open(profile).read()
     except OSError:
         return None, None
     h = hashlib.sha256()
-    for s in SCORE_SOURCES:
+    for s in sources:
         with open(os.path.join(ROOT, "sparse_attention_token_block_gb300", "csrc", s), "rb") as f:
             h.update(f.read())
     sha = h.hexdigest()[:16]
@@ -387,7 +391,8 @@ def run_quantize(args, rank, world, local):
         "stage_us": {"quantize_query": 1e3 * q_avg, "quantize_keys": 1e3 * statistics.mean(k_ms)},
         "roofline": {"kernel": "quantize_vectors_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
-                     "algorithmic_bytes_per_launch": quantize_bytes(nvec, 0, esz), "traffic": None},
+                     "algorithmic_bytes_per_launch": quantize_bytes(nvec, 0, esz),
+                     "traffic": recorded_traffic(QUANT_PROFILE, QUANT_SOURCES)[0]},
         "clocks": clk,
         "gpu_launches": 2 * args.steps,
         "cpu_baseline": cpu,
@@ -481,7 +486,10 @@ def run_gather(args, rank, world, local):
         "us_per_call": 1e3 * avg,
         "roofline": {"kernel": "gather_kernel", "bound": "hbm", "achieved": nbytes / (avg * 1e-3) / 1e9,
                      "peak": peak, "unit": "GB/s", "frac": nbytes / (avg * 1e-3) / 1e9 / peak,
-                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": nbytes,
+                     # the committed capture is of the default line (long decode, 512-byte entries)
+                     "traffic": (recorded_traffic(GATHER_PROFILE, GATHER_SOURCES)[0]
+                                 if (E, args.workload, args.batch) == (512, "long_decode", 0) else None)},
         "clocks": clk,
         "gpu_launches": args.steps,
         "cpu_baseline": cpu,
