@@ -165,7 +165,9 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
 
     // each thread owns a contiguous run of groups, so each pass below needs one block scan; the
     // batch of a run's first group comes from one binary search, later ones by advancing
-    const int64_t per = (total_groups + blockDim.x - 1) / blockDim.x;
+    // the block is 256 or 1024 threads: divisions by its size are shifts
+    const int lg_threads = __ffs((int)blockDim.x) - 1;
+    const int64_t per = (total_groups + blockDim.x - 1) >> lg_threads;
     const int64_t g_lo = min((int64_t)tid * per, total_groups);
     const int64_t g_hi = min(g_lo + per, total_groups);
     // visible keys of group g of batch b (its last row's count, the largest in the group)
@@ -222,8 +224,11 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     // floor(T c / G) without a division per CTA: c * floor(T / G) + floor(c * (T mod G) / G), the
     // last by a multiply with m = ceil(2^32 / G): for x = c (T mod G) < G^2 <= 2^20 the error of
     // x m / 2^32 against x / G is below 2^-12 < 1 / G, so the floor is exact
-    const uint32_t t_div = (uint32_t)(T / (Gl > 0 ? Gl : 1)), t_mod = (uint32_t)(T % (Gl > 0 ? Gl : 1));
-    const uint32_t inv_g = (uint32_t)((0xFFFFFFFFull + (uint64_t)G) / (uint64_t)(G > 0 ? G : 1));
+    // T < 2^31 (the host bounds rows x tiles) and 1 <= G <= 1024, so 32-bit divisions suffice, and
+    // ceil(2^32 / G) = floor((2^32 - 1) / G) + 1 (0 for G = 1, where t_mod is 0)
+    const uint32_t G32 = (uint32_t)(G > 0 ? G : 1);
+    const uint32_t t_div = (uint32_t)T / G32, t_mod = (uint32_t)T % G32;
+    const uint32_t inv_g = 0xFFFFFFFFu / G32 + 1u;
     static_assert(kMaxCtas <= 1024, "the reciprocal division needs G <= 1024");
     auto cta_start = [&](int64_t c) -> int64_t {
         return (int64_t)c * t_div + __umulhi((uint32_t)c * t_mod, inv_g);
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     // index) and that group's batch come from binary searches, later ones by advancing
     {
         const int64_t U = running;
-        const int64_t u_lo = U * tid / blockDim.x, u_hi = U * (tid + 1) / blockDim.x;
+        const int64_t u_lo = (U * tid) >> lg_threads, u_hi = (U * (tid + 1)) >> lg_threads;
         int64_t g = -1, b = 0, A = 0, Bt = 0, n = 0, r0 = 0, c = 0;
         int64_t t1 = 0;
         for (int64_t u = u_lo; u < u_hi; ++u) {
@@ -329,7 +334,7 @@ cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const in
                                          kMetaSmemBytes);
     if (e != cudaSuccess) return e;
     // few groups: fewer warps make each block-wide step cheaper; many groups: more lanes per pass
-    const int threads = p.meta.max_groups <= 4096 && p.batch <= 4096 ? 256 : kMetaThreads;
+    const int threads = p.meta.max_groups <= 4096 && p.batch <= 4096 ? 256 : kMetaThreads;   // powers of two
     return launch_pdl(metadata_kernel, dim3(1), dim3(threads), kMetaSmemBytes, st, p, seq_lens_q,
                       seq_lens_k, meta, G);
 }
