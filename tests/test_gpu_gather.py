@@ -156,3 +156,32 @@ def test_after_the_indexer_at_full_size(qli, name):
     assert err == 0
     assert np.array_equal(counts.cpu().numpy(), ref_counts)
     assert np.array_equal(out.cpu().numpy(), ref)
+
+
+def test_after_a_plan_replay(qli):
+    """The gather enqueued straight after an execution-plan replay (a CUDA graph whose last kernel
+    is the top-k) reads that replay's indices."""
+    import torch
+    case = W.WORKLOADS["fp8_compressed_decode"]()
+    p = qli.make_problem(**W.problem_kwargs(case))
+    ix = qli.Indexer(p)
+    d = W.to_device(case)
+    plan = ix.plan(**d)
+    entry = 256
+    pool = _dev(W.kv_pool(case, entry, 0, seed=12))
+    out = torch.empty((case.rows, case.sparse_count, entry), dtype=torch.uint8, device="cuda")
+    counts = torch.empty(case.rows, dtype=torch.int32, device="cuda")
+    ix.out.fill_(-1)                              # stale indices: the gather must see the replay's
+    torch.cuda.synchronize()
+    plan.launch()
+    qli.check(qli.gather_kv(p, d["seq_lens_q"], d["seq_lens_k"], d["block_table"], ix.out, pool, entry, out,
+                            counts, 0, ix.workspace), "gather_kv")
+    torch.cuda.synchronize()
+    assert ix.device_error()[0] == qli.QLI_OK
+    gpu_idx = ix.out.cpu().numpy()
+    assert (gpu_idx[:, 0] >= 0).all()
+    ref, ref_counts, err = oracle.gather_kv(case, gpu_idx, pool.cpu().numpy(), entry)
+    assert err == 0
+    assert np.array_equal(counts.cpu().numpy(), ref_counts)
+    assert np.array_equal(out.cpu().numpy(), ref)
+    plan.close()

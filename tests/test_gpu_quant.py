@@ -60,14 +60,15 @@ def test_quantize_full_query_of_a_decode_step(qli):
         assert np.array_equal(scales, ref_scales)
 
 
-def test_quantize_at_the_prefill_size(qli):
+@pytest.mark.parametrize("fp8,scale_f32", [(False, False), (True, True)])
+def test_quantize_at_the_prefill_size(qli, fp8, scale_f32):
     """The quantizer benchmark's query: a TND prefill of T = 15360 tokens x 64 heads (983040
     vectors, 252 MB of bfloat16), every code and scale compared."""
     bits = W.bf16_vectors((15360, 64, 128), seed=31)
-    codes, scales = _gpu_quantize(qli, bits, False, False)
-    ref_codes, ref_scales = oracle.quantize(bits, False, False)
+    codes, scales = _gpu_quantize(qli, bits, fp8, scale_f32)
+    ref_codes, ref_scales = oracle.quantize(bits, fp8, scale_f32)
     assert np.array_equal(codes, ref_codes.view(np.uint8))
-    assert np.array_equal(scales, ref_scales)
+    assert np.array_equal(scales.view(np.uint8), ref_scales.view(np.uint8))
 
 
 def test_quantize_rejects_bad_arguments(qli):
