@@ -181,7 +181,7 @@ def gather_kv(case, sparse_indices, kv, entry_bytes: int, kv_stride: int = 0, us
     k = case.sparse_count
     idx = np.ascontiguousarray(sparse_indices, dtype=np.int32).reshape(rows, k)
     pool = np.ascontiguousarray(kv).view(np.uint8)
-    out = np.empty((rows, k, entry_bytes), dtype=np.uint8)
+    out = np.full((rows, k, entry_bytes), 0xA5, dtype=np.uint8)   # every byte is written
     counts = np.empty(max(rows, 1), dtype=np.int32)[:rows]
     slq = None if case.seq_lens_q is None else np.ascontiguousarray(case.seq_lens_q, np.int32)
     slk = np.ascontiguousarray(case.seq_lens_k, np.int32) if use_seq_lens_k else None

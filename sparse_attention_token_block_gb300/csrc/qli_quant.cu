@@ -132,6 +132,13 @@ __device__ __forceinline__ QuantOut quantize_group(const uint4& a, const uint4& 
         qa = __fdiv_rn(amax, s);
     }
     if (fp8) {
+        // the quotient of x and s > 0 has x's sign; the remainder corrections can turn a -0 quotient
+        // (x = -0, or an underflow) into +0, and e4m3 keeps the sign of zero, so copy x's sign back
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint64_t sign = ((uint64_t)(w[i] & 0x80000000u) << 32) | ((w[i] << 16) & 0x80000000u);
+            y[i] = (y[i] & 0x7FFFFFFF7FFFFFFFull) | sign;
+        }
         q.lo = make_uint2(e4m3x2(y[0]) | (e4m3x2(y[1]) << 16), e4m3x2(y[2]) | (e4m3x2(y[3]) << 16));
         q.hi = make_uint2(e4m3x2(y[4]) | (e4m3x2(y[5]) << 16), e4m3x2(y[6]) | (e4m3x2(y[7]) << 16));
         return q;

@@ -1,6 +1,7 @@
 """The pins must catch plausible mistakes: each case plants one mistake in a copy of the oracle's
-C source, builds it, and runs the pin suite (tests/test_oracle.py) against it in a subprocess;
-the suite has to fail."""
+C source, builds it, and runs the pin suite of that part (tests/test_oracle.py for the indexer,
+test_oracle_quant.py for the quantizer, test_oracle_gather.py for the gather) against it in a
+subprocess; the suite has to fail."""
 import os
 import shutil
 import subprocess
@@ -28,8 +29,42 @@ MUTANTS = [
 ]
 
 
+E4M3_TIES = ("    double dl = v - qlio_e4m3_value(lo), dh = qlio_e4m3_value(hi) - v;\n"
+             "    if (dl < dh) return lo;\n    if (dh < dl) return hi;\n    return (lo & 1) ? hi : lo;")
+
+# (name, anchor, replacement, pin file)
+MUTANTS_MORE = [
+    ("quant_qmax_128", "const float qmax = qk_fp8 ? 448.0f : 127.0f;", "const float qmax = qk_fp8 ? 448.0f : 128.0f;",
+     "test_oracle_quant.py"),
+    ("quant_truncate", "float r = rintf(y);", "float r = truncf(y);", "test_oracle_quant.py"),
+    ("quant_round_half_away", "float r = rintf(y);", "float r = roundf(y);", "test_oracle_quant.py"),
+    ("quant_signed_max", "amax = fmaxf(amax, fabsf(x[d]));", "amax = fmaxf(amax, x[d]);", "test_oracle_quant.py"),
+    ("quant_e4m3_ties_up", E4M3_TIES, E4M3_TIES.replace("return (lo & 1) ? hi : lo;", "return hi;"),
+     "test_oracle_quant.py"),
+    ("quant_e4m3_sign", "(signbit(y) ? 0x80 : 0)", "(y < 0.0f ? 0x80 : 0)", "test_oracle_quant.py"),
+    ("quant_key_slot", "slot = pos % bs;", "slot = (pos + 1) % bs;", "test_oracle_quant.py"),
+    ("quant_key_stride", "(uint8_t*)key_pool + page * stride + slot * 128",
+     "(uint8_t*)key_pool + page * bs * 128 + slot * 128", "test_oracle_quant.py"),
+    ("gather_slot", "page * stride + (j % bs) * entry_bytes", "page * stride + ((j + 1) % bs) * entry_bytes",
+     "test_oracle_gather.py"),
+    ("gather_no_zero_fill", "memset(dst, 0, (size_t)entry_bytes);", "(void)dst;", "test_oracle_gather.py"),
+    ("gather_limit_inclusive", "if (j < 0 || j >= limit) {", "if (j < 0 || j > limit) {", "test_oracle_gather.py"),
+    ("gather_row_batch", "        if (r < hi)\n", "        if (r <= hi)\n", "test_oracle_gather.py"),
+    ("gather_counts_all", "counts[r] = copied;", "counts[r] = (int32_t)k;", "test_oracle_gather.py"),
+]
+
+
+@pytest.mark.parametrize("name,old,new,pins", MUTANTS_MORE, ids=[m[0] for m in MUTANTS_MORE])
+def test_quantizer_and_gather_pins_catch_planted_mistake(name, old, new, pins, tmp_path):
+    _run_mutant(name, old, new, pins, tmp_path)
+
+
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_pins_catch_planted_mistake(name, old, new, tmp_path):
+    _run_mutant(name, old, new, "test_oracle.py", tmp_path)
+
+
+def _run_mutant(name, old, new, pins, tmp_path):
     src = open(SRC).read()
     assert old in src, "mutation anchor missing: " + name
     mutant_c = tmp_path / ("mutant_%s.c" % name)
@@ -39,6 +74,6 @@ def test_pins_catch_planted_mistake(name, old, new, tmp_path):
                            "-pthread", "-o", str(lib), str(mutant_c), "-lm"])
     env = dict(os.environ, QLI_ORACLE_LIB=str(lib))
     out = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                          os.path.join(ROOT, "tests", "test_oracle.py")],
+                          os.path.join(ROOT, "tests", pins)],
                          env=env, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert out.returncode != 0, "planted mistake %s was not caught:\n%s" % (name, out.stdout[-1500:])

@@ -138,3 +138,22 @@ def test_degenerate_vectors_of_the_generator():
     assert np.array_equal(c16[2], np.clip(np.rint(x[2] / np.float32(65504)), -127, 127).astype(np.int8))
     e16, _ = oracle.quantize(b, True, False)
     assert np.all((e16[2] & 0x7F).max() == 0x7E)
+
+
+def test_signed_zeros_keep_their_sign_in_e4m3():
+    """x = -0 (and a negative quotient that underflows to zero) divides to -0, whose nearest e4m3
+    value is -0 (code 0x80): torch's float8_e4m3fn cast of x / s says the same; int8 has one zero."""
+    torch = pytest.importorskip("torch")
+    b = W.bf16_vectors((6, 128), seed=7)              # vector 5: signed zeros beside ~1e30 values
+    x = _f32(b[5])
+    assert np.any(np.signbit(x) & (x == 0)) and np.any(~np.signbit(x) & (x == 0))
+    for scale_f32 in (True, False):
+        codes, scales = oracle.quantize(b[5:6], True, scale_f32)
+        y = (x / scales[0].astype(np.float32)).astype(np.float32)
+        ref = torch.from_numpy(y.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        inside = np.abs(y) <= 448.0               # torch's cast does not saturate: NaN beyond 448
+        assert np.array_equal(codes[0][inside], ref[inside])
+        assert np.all(codes[0][~inside] == (0x7E | (np.signbit(y[~inside]) << 7)))
+        assert np.all(codes[0][np.signbit(x) & (x == 0)] == 0x80)
+    c8, _ = oracle.quantize(b[5:6], False, False)
+    assert np.all(c8[0][x == 0] == 0)

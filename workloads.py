@@ -261,8 +261,9 @@ def bf16_vectors(shape, seed: int, special: bool = True) -> np.ndarray:
     With ``special`` the first vectors (as many as fit) are degenerate ones: all zero; magnitudes
     near 1e-38 (scales in the float subnormal range); magnitudes near 1e10 (scales beyond the
     float16 range); integers with one element 127 and the rest at k + 1/2 (every quotient an exact
-    halfway case for int8 codes); and one element 448 with the rest at midpoints of the e4m3 grid
-    (halfway cases for e4m3 codes)."""
+    halfway case for int8 codes); one element 448 with the rest at midpoints of the e4m3 grid
+    (halfway cases for e4m3 codes); and magnitudes near 1e30 mixed with signed zeros and -1e-40
+    (zero and underflowing quotients, whose sign the e4m3 code keeps)."""
     rng = np.random.default_rng(seed)
     shape = tuple(shape)
     assert shape[-1] == HEAD_DIM
@@ -285,6 +286,12 @@ def bf16_vectors(shape, seed: int, special: bool = True) -> np.ndarray:
         pick = mids[rng.integers(0, len(mids), size=HEAD_DIM)] * rng.choice([-1.0, 1.0], size=HEAD_DIM)
         pick[rng.integers(0, HEAD_DIM)] = 448.0
         extra.append(pick.astype(np.float32))
+        # signed zeros, and tiny negative elements beside a huge maximum (their quotients underflow)
+        sz = (rng.normal(0.0, 1.0, HEAD_DIM) * 1e30).astype(np.float32)
+        sz[::4] = -0.0
+        sz[1::8] = 0.0
+        sz[2::16] = -1e-40
+        extra.append(sz)
         m = min(len(extra), n)
         x[:m] = np.stack(extra[:m])
     bits = (x.view(np.uint32) >> 16).astype(np.uint16)
