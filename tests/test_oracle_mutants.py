@@ -26,6 +26,9 @@ MUTANTS = [
     ("e4m3_bias", "v = ldexp(8.0 + m, e - 10);", "v = ldexp(8.0 + m, e - 9);"),
     ("sort_ascending", "if (x->score > y->score) return -1;", "if (x->score > y->score) return 1;"),
     ("tnd_rows", "int32_t lo = b > 0 ? seq_lens_q[b - 1] : 0;", "int32_t lo = b > 1 ? seq_lens_q[b - 2] : 0;"),
+    ("key_stride_ignored", "int64_t koff = page * page_stride + slot",
+     "int64_t koff = page * (int64_t)p->block_size * p->head_dim + slot"),
+    ("complete_blocks_ceil", "        n = (pos + 1) / p->cmp_ratio;\n", "        n = (pos + 1 + p->cmp_ratio - 1) / p->cmp_ratio;\n"),
 ]
 
 
