@@ -126,3 +126,20 @@ def test_quantizer_and_gather_reject_bad_arguments(Q):
     t.layout_q = Q.TND
     t.total_q_tokens = 8
     assert L.qli_gather_kv(ctypes.byref(t), None, A, A, A, A, 64, 0, A, None, None, 0, None) == 1  # TND prefix sums
+
+
+def test_problem_struct_layout_matches_the_header(Q, tmp_path):
+    """The binding's ctypes mirror of qli_problem has the header's size and field offsets (a C
+    program built against include/qli.h prints them)."""
+    import subprocess
+    fields = [f[0] for f in Q.Problem._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stddef.h>\n#include <stdio.h>\n#include \"qli.h\"\nint main(void) {\n"
+                   "  printf(\"%zu\\n\", sizeof(qli_problem));\n"
+                   + "".join("  printf(\"%%zu\\n\", offsetof(qli_problem, %s));\n" % f for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)])
+    got = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert got[0] == ctypes.sizeof(Q.Problem)
+    assert got[1:] == [getattr(Q.Problem, f).offset for f in fields]
