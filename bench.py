@@ -633,6 +633,26 @@ def main():
         torch.cuda.synchronize()
         reuse_us = sum(a.elapsed_time(b) for a, b in rev) / len(rev) * 1e3
         plan_nm.close()
+    # the same step also writing sparse_values (the README's return_value): a second indexer whose
+    # problem asks for the values, replayed as a plan like the timed step
+    values_us = None
+    if plan is not None:
+        pv = Q.make_problem(**W.problem_kwargs(case), return_value=1)
+        ixv = Q.Indexer(pv, device=dev)
+        planv = ixv.plan(**d)
+        vev = []
+        for i in range(max(3, min(args.steps, 50)) + 3):
+            flush_l2(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            planv.launch()
+            b.record(stream)
+            vev.append((a, b))
+        torch.cuda.synchronize()
+        Q.check(ixv.device_error()[0], "device error with sparse_values")
+        vev = vev[3:]
+        values_us = sum(a.elapsed_time(b) for a, b in vev) / len(vev) * 1e3
+        planv.close()
     # hot L2: the same plan replayed back to back without the flush (inputs partly L2-resident)
     hot_us = None
     if plan is not None:
@@ -731,6 +751,7 @@ def main():
         "us_per_call_stream_launches": stream_us,
         "us_per_call_metadata_reused": reuse_us,
         "us_per_call_hot_l2": hot_us,
+        "us_per_call_with_sparse_values": values_us,
         "stage_us": {"metadata": 1e3 * statistics.mean(meta_ms),
                      "score": 1e3 * score_avg, "topk": 1e3 * statistics.mean(topk_ms)},
         "roofline": roofline,
