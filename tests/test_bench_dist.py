@@ -52,3 +52,21 @@ def test_whole_job_value_counts_every_rank():
 
 def test_single_process_max_is_identity():
     assert bench.max_over_ranks(3.5, None, "cpu") == 3.5
+
+
+def test_metric_counts_exactly_the_oracles_visible_pairs():
+    """The benchmark's algorithmic work (16384 ops per visible query-key pair) counts the pairs the
+    oracle's mask makes visible, over the benchmarked workloads and shapes that exercise the mask
+    (BSND with short rows, TND with an empty sequence, compression, both sparse modes)."""
+    import oracle
+    import workloads as W
+    from checker import visible_counts
+    cases = [W.long_decode(batch=4), W.fp8_compressed_decode(batch=3),
+             W.make_case("m0", batch=3, s1=4, q_lens=[4, 2, 0], seq_lens_k=[300, 3, 64], block_size=16,
+                         sparse_count=8, sparse_mode=3, cmp_ratio=4, seed=1),
+             W.make_case("m1", layout_q="TND", q_lens=[5, 0, 9], seq_lens_k=[40, 7, 9], block_size=16,
+                         sparse_count=8, sparse_mode=3, cmp_ratio=2, seed=2),
+             W.make_case("m2", batch=2, s1=3, seq_lens_k=[50, 2], block_size=16, sparse_count=8,
+                         sparse_mode=0, cmp_ratio=8, seed=3)]
+    for case in cases:
+        assert bench.visible_pairs(case) == int(visible_counts(case, oracle).sum()), case.name
