@@ -237,8 +237,9 @@ qli_status qli_quantize(int32_t qk_dtype, int32_t scale_dtype, const void* x, in
  * block_table, k_scale is [num_blocks, block_size, 1]).  Token t's key `key_bf16[t]` (128
  * bfloat16, 16-byte aligned rows) is quantized as in qli_quantize (qk_dtype and scale_dtype of `p`)
  * and written to compressed position `token_pos[t]` of batch `token_batch[t]`: page
- * block_table[b][pos / block_size], slot pos % block_size, of `key` (pages p->key_stride bytes apart,
- * 0 = contiguous; 16-byte aligned) and of `k_scale`.  Nothing else of the pool changes.  Positions
+ * block_table[b][pos / block_size], slot pos % block_size, of `key` (pages p->key_stride elements
+ * apart as in qli_score_topk -- bytes, since a code is one byte -- 0 = contiguous; 16-byte
+ * aligned) and of `k_scale`.  Nothing else of the pool changes.  Positions
  * must be distinct (two tokens writing one slot leave either).  Lengths are not consulted: the
  * caller raises seq_lens_k afterwards.  A batch outside [0, batch) or a position outside
  * [0, max_blocks_per_seq * block_size) skips the token and sets error bit 1 (length), a page

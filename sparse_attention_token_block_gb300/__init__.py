@@ -13,6 +13,10 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqli.so")
+# the testing build (include/qli_testing.h): the same library plus a failure-detection switch;
+# only the failure-detection tests select it, with use_testing_library() before the first call
+TESTING_LIB_PATH = os.path.join(_HERE, "libqli_testing.so")
+_lib_path = LIB_PATH
 
 QLI_OK = 0
 STATUS_NAMES = {0: "QLI_OK", 1: "QLI_ERR_INVALID_ARG", 2: "QLI_ERR_UNSUPPORTED",
@@ -50,10 +54,13 @@ class Problem(ctypes.Structure):
 
 
 def _load():
-    if not os.path.exists(LIB_PATH):
-        raise ImportError("libqli.so is not built (run __graft_entry__.build() or "
-                          "python sparse_attention_token_block_gb300/build.py)")
-    L = ctypes.CDLL(LIB_PATH)
+    if not os.path.exists(_lib_path):
+        raise ImportError("%s is not built (run __graft_entry__.build() or "
+                          "python sparse_attention_token_block_gb300/build.py)" % os.path.basename(_lib_path))
+    L = ctypes.CDLL(_lib_path)
+    if _lib_path == TESTING_LIB_PATH:
+        L.qli_testing_set_stall.argtypes = [ctypes.c_int]
+        L.qli_testing_set_stall.restype = None
     vp, sz, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
     P = ctypes.POINTER(Problem)
     L.qli_problem_init.argtypes = [P]
@@ -102,6 +109,15 @@ def _load():
 
 
 _lib_handle = None
+
+
+def use_testing_library():
+    """Load the testing build (libqli_testing.so) instead of the product library.  Must be called
+    before the first call into the library in this process."""
+    global _lib_path
+    if _lib_handle is not None and _lib_path != TESTING_LIB_PATH:
+        raise RuntimeError("the product library is already loaded in this process")
+    _lib_path = TESTING_LIB_PATH
 
 
 def _get_lib():

@@ -16,8 +16,12 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqli.so")
+# the testing build: the same objects except the host API, compiled with QLI_TESTING (it adds the
+# failure-detection test switch of include/qli_testing.h); the product library has no switch
+TEST_LIB = os.path.join(HERE, "libqli_testing.so")
 SOURCES = ["qli_api.cu", "qli_metadata.cu", "qli_score.cu", "qli_topk.cu", "qli_noalloc.cu", "qli_plan.cu", "qli_quant.cu", "qli_gather.cu"]
 HEADERS = ["qli_internal.cuh", "qli_ptx.cuh"]
+TEST_SOURCE = "qli_api.cu"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -45,6 +49,7 @@ def _newer(target, deps):
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     os.makedirs(OBJ, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "qli.h")]
+    hdrs.append(os.path.join(ROOT, "include", "qli_testing.h"))
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
@@ -52,6 +57,10 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
         if ptxas_info or _newer(o, [s] + hdrs):
             extra = ["-Xptxas", "-v"] if ptxas_info else []
             jobs.append((src, [nvcc(), "-c", s, "-o", o] + _flags(extra)))
+    s = os.path.join(CSRC, TEST_SOURCE)
+    o_test = os.path.join(OBJ, TEST_SOURCE.replace(".cu", "_testing.o"))
+    if _newer(o_test, [s] + hdrs):
+        jobs.append((TEST_SOURCE + " (testing)", [nvcc(), "-c", s, "-o", o_test] + _flags(["-DQLI_TESTING"])))
 
     def run(job):
         name, cmd = job
@@ -66,15 +75,17 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
                 if r.returncode != 0:
                     raise RuntimeError("nvcc failed on %s" % name)
     objs = [os.path.join(OBJ, s.replace(".cu", ".o")) for s in SOURCES]
-    if _newer(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
-        cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + [
-            "-cudart", "shared", "-Xlinker", "-rpath=" + cuda_lib_dir()]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            sys.stderr.write(r.stdout + r.stderr)
-            raise RuntimeError("link of libqli.so failed")
-        os.replace(tmp, LIB)
+    test_objs = [o_test if s == TEST_SOURCE else o for s, o in zip(SOURCES, objs)]
+    for lib, parts in ((LIB, objs), (TEST_LIB, test_objs)):
+        if _newer(lib, parts):
+            tmp = lib + ".tmp%d" % os.getpid()
+            cmd = [nvcc(), "-shared", "-o", tmp] + parts + ARCH + [
+                "-cudart", "shared", "-Xlinker", "-rpath=" + cuda_lib_dir()]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                sys.stderr.write(r.stdout + r.stderr)
+                raise RuntimeError("link of %s failed" % os.path.basename(lib))
+            os.replace(tmp, lib)
     return LIB
 
 

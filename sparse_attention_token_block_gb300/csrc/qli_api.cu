@@ -3,8 +3,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -17,17 +17,18 @@ MetaLayout meta_layout(int64_t batch, int64_t max_groups)
     MetaLayout m;
     m.batch_off = kMhWords;
     m.cta_off = m.batch_off + batch * kBatchWords;
-    m.group_off = m.cta_off + kMaxCtas + 1;
-    m.ufirst_off = m.group_off + max_groups + 1;                    // first unit of each group
-    m.unit_off = (m.ufirst_off + max_groups + 1 + 3) & ~int64_t(3);  // 16-byte aligned units
+    m.group_off = (m.cta_off + kCtaWords * (int64_t)kMaxCtas + 3) & ~int64_t(3);   // 16-byte aligned records
     m.max_groups = max_groups;
-    m.max_units = max_groups + kMaxCtas;
-    m.total_words = m.unit_off + m.max_units * kUnitWords;
+    m.total_words = m.group_off + max_groups * kGroupWords;
     if (m.total_words < 1024) m.total_words = 1024;
     return m;
 }
 
 namespace {
+
+#ifdef QLI_TESTING
+std::atomic<int> g_test_stall{0};
+#endif
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
@@ -78,10 +79,18 @@ qli_status check(const qli_problem* p, const char** why)
     return QLI_OK;
 }
 
+// Query tokens scored together by one MMA (N = 64 per token)
+int group_tokens_of(const qli_problem* p)
+{
+    (void)p;
+    return 1;
+}
+
 int64_t max_groups_of(const qli_problem* p)
 {
-    if (p->layout_q == QLI_BSND) return (int64_t)p->batch * ceil_div64(p->max_q_tokens, kGroupTokens);
-    return ceil_div64(p->total_q_tokens, kGroupTokens) + p->batch;
+    const int gt = group_tokens_of(p);
+    if (p->layout_q == QLI_BSND) return (int64_t)p->batch * ceil_div64(p->max_q_tokens, gt);
+    return ceil_div64(p->total_q_tokens, gt) + p->batch;
 }
 
 Params params_of(const qli_problem* q)
@@ -109,16 +118,20 @@ Params params_of(const qli_problem* q)
     const int64_t max_lc = compressed_keys(q->max_seqlen_k, q->cmp_ratio);
     int64_t ld = ceil_div64(max_lc, kTileKeys) * kTileKeys;
     p.ld = ld > 0 ? ld : kTileKeys;
+    p.group_tokens = group_tokens_of(q);
     p.meta = meta_layout(p.batch, max_groups_of(q));
     p.hash = problem_hash(p);
-    // failure-detection test switches (host-set, no device fault involved): the score kernel's
-    // producer issues no copies (1), or its converters consume nothing (2) so the producer's key
-    // copies land and wait in the ring; either way the waits run out and report a timeout
     p.complete_blocks = q->mask_complete_blocks;
     p.key_stride = q->key_stride ? q->key_stride : q->block_size * kDim;
-    const char* stall = std::getenv("QLI_TEST_STALL_PRODUCER");
-    const char* stall_c = std::getenv("QLI_TEST_STALL_CONVERTER");
-    p.test_stall = (stall && stall[0] == '1') ? 1 : ((stall_c && stall_c[0] == '1') ? 2 : 0);
+#ifdef QLI_TESTING
+    // failure-detection test switch of the testing build only (no device fault involved): the
+    // score kernel's producer issues no copies (1), or its converters consume nothing (2) so the
+    // producer's key copies land and wait in the ring; either way the waits run out and report a
+    // timeout
+    p.test_stall = g_test_stall.load();
+#else
+    p.test_stall = 0;
+#endif
     return p;
 }
 
@@ -240,7 +253,7 @@ qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const i
     int sms = device_sms(nullptr);
     if (sms < 0) return QLI_ERR_CUDA;
     if (sms == 0) return QLI_ERR_NO_DEVICE;
-    cudaError_t e = launch_metadata(P, seq_lens_q, seq_lens_k, metadata, sms * kScoreCtasPerSm,
+    cudaError_t e = launch_metadata(P, seq_lens_q, seq_lens_k, metadata, score_ctas(sms),
                                     static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
@@ -265,11 +278,18 @@ qli_status check_call(const qli_problem* p, const int32_t* metadata, size_t meta
 
 }  // namespace
 
-qli_status qli_score(const qli_problem* p, const void* query, const void* key, const void* weights,
-                     const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
-                     const int32_t* seq_lens_k, const int32_t* block_table, const int32_t* metadata,
-                     size_t metadata_words, void* workspace, size_t workspace_bytes, void* stream)
+}  // extern "C"
+
+namespace {
+
+// The score stage; *launched tells whether a kernel was enqueued
+qli_status score_impl(const qli_problem* p, const void* query, const void* key, const void* weights,
+                      const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
+                      const int32_t* seq_lens_k, const int32_t* block_table, const int32_t* metadata,
+                      size_t metadata_words, void* workspace, size_t workspace_bytes, void* stream,
+                      bool* launched)
 {
+    *launched = false;
     Params P;
     WsLayout W;
     int sms = 0;
@@ -284,16 +304,18 @@ qli_status qli_score(const qli_problem* p, const void* query, const void* key, c
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     CUtensorMap tm;
     if (!encode_key_map(&tm, key, P)) return QLI_ERR_CUDA;
-    const int grid = sms * kScoreCtasPerSm < kMaxCtas ? sms * kScoreCtasPerSm : kMaxCtas;
-    cudaError_t e = launch_score(P, &tm, query, key, weights, q_scale, k_scale, block_table, metadata,
-                                 reinterpret_cast<uint32_t*>(ws + W.scores_off), reinterpret_cast<uint32_t*>(ws),
-                                 grid, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+    cudaError_t e = launch_score(P, &tm, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k,
+                                 block_table, metadata, reinterpret_cast<uint32_t*>(ws + W.scores_off),
+                                 reinterpret_cast<uint32_t*>(ws), score_ctas(sms), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return QLI_ERR_CUDA;
+    *launched = true;
+    return QLI_OK;
 }
 
-qli_status qli_topk(const qli_problem* p, const int32_t* block_table, const int32_t* metadata,
-                    size_t metadata_words, void* workspace, size_t workspace_bytes, int32_t* sparse_indices,
-                    float* sparse_values, void* stream)
+// The top-k stage; after_score: the launch directly follows this library's score kernel
+qli_status topk_impl(const qli_problem* p, const int32_t* block_table, const int32_t* metadata,
+                     size_t metadata_words, void* workspace, size_t workspace_bytes, int32_t* sparse_indices,
+                     float* sparse_values, void* stream, bool after_score)
 {
     Params P;
     WsLayout W;
@@ -306,9 +328,31 @@ qli_status qli_topk(const qli_problem* p, const int32_t* block_table, const int3
     if (P.batch > 0 && !block_table) return QLI_ERR_INVALID_ARG;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaError_t e = launch_topk(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),
-                                reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values,
+                                reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values, after_score,
                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+qli_status qli_score(const qli_problem* p, const void* query, const void* key, const void* weights,
+                     const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
+                     const int32_t* seq_lens_k, const int32_t* block_table, const int32_t* metadata,
+                     size_t metadata_words, void* workspace, size_t workspace_bytes, void* stream)
+{
+    bool launched = false;
+    return score_impl(p, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table, metadata,
+                      metadata_words, workspace, workspace_bytes, stream, &launched);
+}
+
+qli_status qli_topk(const qli_problem* p, const int32_t* block_table, const int32_t* metadata,
+                    size_t metadata_words, void* workspace, size_t workspace_bytes, int32_t* sparse_indices,
+                    float* sparse_values, void* stream)
+{
+    return topk_impl(p, block_table, metadata, metadata_words, workspace, workspace_bytes, sparse_indices,
+                     sparse_values, stream, false);
 }
 
 qli_status qli_score_topk(const qli_problem* p, const void* query, const void* key, const void* weights,
@@ -327,11 +371,14 @@ qli_status qli_score_topk(const qli_problem* p, const void* query, const void* k
             metadata_words >= (size_t)P.meta.total_words && workspace_bytes >= ws_layout(P).total)
             return QLI_ERR_INVALID_ARG;
     }
-    s = qli_score(p, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table, metadata,
-                  metadata_words, workspace, workspace_bytes, stream);
+    bool launched = false;
+    s = score_impl(p, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table, metadata,
+                   metadata_words, workspace, workspace_bytes, stream, &launched);
     if (s != QLI_OK) return s;
-    return qli_topk(p, block_table, metadata, metadata_words, workspace, workspace_bytes, sparse_indices,
-                    sparse_values, stream);
+    // the top-k directly follows the score kernel, which let it start only after its own wait on
+    // the metadata kernel returned: it may read the metadata before its own wait
+    return topk_impl(p, block_table, metadata, metadata_words, workspace, workspace_bytes, sparse_indices,
+                     sparse_values, stream, launched);
 }
 
 qli_status qli_quantize(int32_t qk_dtype, int32_t scale_dtype, const void* x, int64_t n_vec, void* codes,
@@ -437,5 +484,9 @@ const char* qli_status_string(qli_status s)
 }
 
 int qli_version(void) { return 100; }
+
+#ifdef QLI_TESTING
+void qli_testing_set_stall(int mode) { g_test_stall.store(mode == 1 || mode == 2 ? mode : 0); }
+#endif
 
 }  // extern "C"

@@ -28,6 +28,14 @@ constexpr int kGroupTokens = 1;
 constexpr int kScoreCtasPerSm = 2;        // score CTAs resident per SM (the split is made for this)
 constexpr int kMaxCtas = 1024;            // bound on the split's CTA count (GB300 has 152 SMs)
 
+// Score CTAs of the split on a device with `sms` SMs: two per SM, less two so that a concurrently
+// resident metadata CTA never delays one (at most kMaxCtas)
+inline int score_ctas(int sms)
+{
+    const int g = 2 * sms - 2;
+    return g < 1 ? 1 : (g > kMaxCtas ? kMaxCtas : g);
+}
+
 // Top-k: candidates held per row
 constexpr int kTopkCap = 4096;
 
@@ -40,16 +48,16 @@ constexpr uint32_t kErrMetadata = 8u;     // metadata buffer not written for thi
 // ------------------------------------------------------------------------------------------------
 // Metadata buffer (int32 words), written by qli_metadata, read by qli_score_topk
 // ------------------------------------------------------------------------------------------------
-constexpr int32_t kMetaMagic = 0x514C4931;  // "QLI1"
+constexpr int32_t kMetaMagic = 0x514C4932;  // "QLI2"
 enum MetaHeader {
     kMhMagic = 0,
-    kMhCtas = 1,        // G: CTAs the split was made for
-    kMhUnits = 2,       // units written
-    kMhTiles = 3,       // total key tiles over all groups
+    kMhCtas = 1,        // G: score CTAs the split was made for
+    kMhLive = 2,        // live query groups (groups with at least one visible key), records written
+    kMhTiles = 3,       // T: key tiles over all live groups
     kMhErr = 4,         // error bits found while reading the lengths
     kMhBatch = 5,
     kMhRows = 6,        // output rows (B * S1 or T)
-    kMhGroups = 7,      // live query groups
+    kMhGroups = 7,      // query groups, live or not
     kMhLayoutHash = 8,  // hash of the problem fields the split depends on
     kMhWords = 16
 };
@@ -60,16 +68,31 @@ enum BatchEntry {
     kBeLc = 2,          // compressed keys Lc_b
     kBeFirstRow = 3,    // first output row of the batch
     kBeOk = 4,          // 1 when the lengths are valid
-    kBeGroups = 5,      // query groups ceil(Sq_b / kGroupTokens) (0 if invalid)
+    kBeGroups = 5,      // query groups ceil(Sq_b / group_tokens) (0 if invalid)
     kBeGroupBase = 6,   // index of the batch's first group
 };
-// a unit: {batch, first row within batch, key_begin, key_end, first output row, Sq_b, Sk_b, Lc_b}
-// (the batch's fields travel with the unit so that a reader needs one 32-byte load)
-constexpr int kUnitWords = 8;
+// A live query group (group_tokens consecutive live rows of one batch whose last row sees at least
+// one key), in batch and row order; its key tiles are tiles [first tile, first tile + tiles) of the
+// concatenated tile sequence that the split cuts into G equal ranges, one per score CTA.  The
+// batch's fields travel with the group so that a reader needs one 32-byte load.
+constexpr int kGroupWords = 8;
+enum GroupRecord {
+    kGrBatch = 0,
+    kGrRow = 1,         // first row of the group within its batch
+    kGrOutRow = 2,      // first output row of the group
+    kGrSq = 3,          // Sq_b
+    kGrSk = 4,          // Sk_b
+    kGrLc = 5,          // Lc_b
+    kGrTile = 6,        // first tile of the group in the concatenated sequence
+    kGrTiles = 7,       // tiles of the group: ceil(visible keys of its last row / kTileKeys)
+};
+// Per score CTA c (two words): the live groups [first, end) that its tile range
+// [T c / G, T (c + 1) / G) overlaps (first = end when the range is empty).
+constexpr int kCtaWords = 2;
 
 struct MetaLayout {
-    int64_t batch_off, cta_off, group_off, ufirst_off, unit_off, total_words;
-    int64_t max_groups, max_units;
+    int64_t batch_off, cta_off, group_off, total_words;
+    int64_t max_groups;
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -98,6 +121,7 @@ struct Params {
     int32_t test_stall;    // test switch: 1 the score kernel's producer, 2 its converters do nothing
     int32_t complete_blocks;   // mode 3 visibility: 0 ceil((p + 1) / cmp), 1 floor((p + 1) / cmp)
     int32_t key_stride;        // elements between key pages
+    int32_t group_tokens;      // query tokens per group (1 .. kGroupTokens)
     int64_t ld;            // score line stride
     MetaLayout meta;
 };
@@ -133,18 +157,69 @@ __host__ __device__ inline int64_t visible_keys(int mode, int cmp, int64_t sq, i
     return n < lc ? n : lc;
 }
 
+// Extents of batch b read from the device lengths (the metadata's definition, shared by every
+// kernel that derives it): live query rows sq, key tokens sk (0 when invalid), compressed keys lc,
+// first output row, validity, and whether b's TND prefix sums are themselves invalid (which
+// invalidates every batch).  A batch is invalid when a length is negative or beyond its bound
+// (BSND seq_lens_q above S1, TND prefix sums not non-decreasing or beyond T, seq_lens_k above
+// max_seqlen_k, more compressed keys than the block_table row holds).
+struct BatchExtent {
+    int32_t sq, sk, lc, first;
+    bool ok, tnd_bad;
+};
+
+__device__ __forceinline__ BatchExtent batch_extent(const Params& p, const int32_t* seq_lens_q,
+                                                    const int32_t* seq_lens_k, int b)
+{
+    BatchExtent e{0, 0, 0, 0, true, false};
+    int64_t sq = 0, first = 0;
+    if (!p.layout_tnd) {
+        first = (int64_t)b * p.s1;
+        const int64_t v = seq_lens_q ? seq_lens_q[b] : p.s1;
+        e.ok = v >= 0 && v <= p.s1;
+        sq = e.ok ? v : 0;
+    } else {
+        const int64_t lo = b > 0 ? seq_lens_q[b - 1] : 0, hi = seq_lens_q[b];
+        e.ok = lo >= 0 && hi >= lo && hi <= p.total_q;
+        e.tnd_bad = !e.ok;
+        first = lo < 0 ? 0 : lo;
+        sq = e.ok ? hi - lo : 0;
+    }
+    const int64_t sk = seq_lens_k[b];
+    e.ok = e.ok && sk >= 0 && sk <= p.max_seqlen_k;
+    const int64_t lc = e.ok ? compressed_keys(sk, p.cmp_ratio) : 0;
+    e.ok = e.ok && lc <= (int64_t)p.max_blocks_per_seq * p.block_size;
+    e.sq = (int32_t)sq;
+    e.sk = (int32_t)(e.ok ? sk : 0);
+    e.lc = (int32_t)lc;
+    e.first = (int32_t)first;
+    return e;
+}
+
+// Key tiles of the query group of batch rows [r0, min(r0 + gt, sq)): ceil(n / kTileKeys), n the
+// visible keys of its last row (the largest in the group under either mask)
+__host__ __device__ inline int64_t group_tiles(const Params& p, int64_t sq, int64_t sk, int64_t lc, int64_t r0)
+{
+    const int64_t rl = (r0 + p.group_tokens < sq ? r0 + p.group_tokens : sq) - 1;
+    const int64_t n = visible_keys(p.sparse_mode, p.cmp_ratio, sq, sk, lc, rl, p.complete_blocks);
+    return (n + kTileKeys - 1) / kTileKeys;
+}
+
 // Problem fields the metadata depends on, folded into one word to catch mismatched buffers
 __host__ __device__ inline int32_t problem_hash(const Params& p)
 {
     uint32_t h = 2166136261u;
     const int32_t f[] = {p.batch, p.s1, p.total_q, p.layout_tnd, p.sparse_mode, p.cmp_ratio,
                          p.max_seqlen_q, p.max_seqlen_k, p.block_size, p.max_blocks_per_seq,
-                         p.complete_blocks};
-    for (int i = 0; i < 11; ++i) { h ^= (uint32_t)f[i]; h *= 16777619u; }
+                         p.complete_blocks, p.group_tokens};
+    for (int i = 0; i < 12; ++i) { h ^= (uint32_t)f[i]; h *= 16777619u; }
     return (int32_t)(h & 0x7fffffff);
 }
 
 MetaLayout meta_layout(int64_t batch, int64_t max_groups);
+
+// First tile of score CTA c's range: floor(T c / G) (T < 2^31, G <= kMaxCtas, so the product fits)
+__host__ __device__ inline int64_t split_start(int64_t T, int64_t G, int64_t c) { return (T * c) / G; }
 
 // Launch `kernel` with programmatic stream serialization: it may begin launching while the
 // previous kernel in the stream finishes; every kernel of this library calls griddepcontrol.wait
@@ -171,11 +246,12 @@ cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const in
                             int32_t* meta, int num_ctas, cudaStream_t st);
 cudaError_t launch_score(const Params& p, const void* tmap_key, const void* query, const void* key,
                          const void* weights, const void* q_scale, const void* k_scale,
+                         const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                          const int32_t* block_table, const int32_t* meta, uint32_t* scores,
                          uint32_t* err_word, int grid, cudaStream_t st);
 cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
                         const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
-                        cudaStream_t st);
+                        bool after_score, cudaStream_t st);
 cudaError_t launch_quantize_vectors(const void* x_bf16, int64_t nvec, void* codes, void* scales, bool fp8,
                                     bool scale_f32, cudaStream_t st);
 cudaError_t launch_quantize_keys(const Params& p, const void* k_bf16, int64_t tokens, const int32_t* tok_batch,

@@ -91,10 +91,12 @@ enum {
     kNumBars = kBarDrain + 1
 };
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
+static_assert(kOffKring % 1024 == 0 && kOffQbuf % 1024 == 0, "shared-memory alignment");
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;   // + slack to align the base to 1024
 static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM must fit in shared memory");
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 
 struct ScoreArgs {
     Params p;
@@ -104,6 +106,8 @@ struct ScoreArgs {
     const uint8_t* k_scale;
     const int32_t* block_table;
     const int32_t* meta;
+    const int32_t* seq_lens_q;
+    const int32_t* seq_lens_k;
     uint32_t* scores;
     uint32_t* err;
 };
@@ -180,20 +184,32 @@ struct Unit {
     int32_t ntiles;
 };
 
-__device__ __forceinline__ Unit read_unit(const ScoreArgs& a, int64_t u)
+// This CTA's tile range [t0, t1) and the live group records [g0, g1) it overlaps, in `recs` (the
+// metadata buffer's group records)
+struct Span {
+    int64_t g0, g1, t0, t1;
+    const int32_t* recs;
+};
+
+// The unit of live group g within the span: the group's tiles that fall in [t0, t1)
+__device__ __forceinline__ Unit read_unit(const ScoreArgs& a, int64_t g, const Span& s)
 {
-    const int4* w = reinterpret_cast<const int4*>(a.meta + a.p.meta.unit_off + u * kUnitWords);
+    const int4* w = reinterpret_cast<const int4*>(s.recs + g * kGroupWords);
     const int4 w0 = w[0], w1 = w[1];
     Unit x;
     x.b = w0.x;
     x.r0 = w0.y;
-    x.kb = w0.z;
-    x.ke = w0.w;
-    x.row0 = w1.x;
-    x.sq = w1.y;
-    x.sk = w1.z;
-    x.lc = w1.w;
-    x.q_cnt = min(kGroupTokens, x.sq - x.r0);
+    x.row0 = w0.z;
+    x.sq = w0.w;
+    x.sk = w1.x;
+    x.lc = w1.y;
+    const int64_t tb = w1.z, tn = w1.w;
+    x.q_cnt = min(a.p.group_tokens, x.sq - x.r0);
+    const int64_t n = visible_keys(a.p.sparse_mode, a.p.cmp_ratio, x.sq, x.sk, x.lc, x.r0 + x.q_cnt - 1,
+                                   a.p.complete_blocks);
+    const int64_t lo = max(s.t0, tb) - tb, hi = max(lo, min(s.t1, tb + tn) - tb);
+    x.kb = (int32_t)(lo * kTileKeys);
+    x.ke = (int32_t)max((int64_t)x.kb, min(hi * kTileKeys, n));
     x.ntiles = (x.ke - x.kb + kTileKeys - 1) / kTileKeys;
     return x;
 }
@@ -210,7 +226,7 @@ __device__ __forceinline__ Unit read_unit(const ScoreArgs& a, int64_t u)
 // slot's barrier tracks: TMA copies of a few hundred bytes would double the copy operations per
 // tile, and the TMA engine's throughput here is per operation.
 template <bool kScaleF32>
-__device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs& a, int64_t ubeg, int64_t uend,
+__device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs& a, const Span& sp,
                                         uint32_t& tile_i, int& q_unit)
 {
     const Shared S = shared_view();
@@ -238,12 +254,12 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs
         }
         return make_int2(page, page * bs + (key - lp * bs));
     };
-    Unit xn = read_unit(a, ubeg);
+    Unit xn = read_unit(a, sp.g0, sp);
     int2 rows_next = chunk_row(xn, 0);
-    for (int64_t u = ubeg; u < uend; ++u) {
-        const int uu = (int)(u - ubeg);
+    for (int64_t u = sp.g0; u < sp.g1; ++u) {
+        const int uu = (int)(u - sp.g0);
         const Unit x = xn;
-        if (u + 1 < uend) xn = read_unit(a, u + 1);   // in flight while this unit runs
+        if (u + 1 < sp.g1) xn = read_unit(a, u + 1, sp);   // in flight while this unit runs
         // one raw query buffer: unit uu's codes land after the converters took unit uu - 1's
         if (!wait_bar(&S.bars[kBarQrempty], (uu & 1) ^ 1, S.abort, a.err)) return;
         if (lane == 0) {
@@ -260,7 +276,7 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs
             const int32_t pages = rows_next.x, rows = rows_next.y;
             // look up the next batch of this unit, else the next unit's first batch
             if (t0 + tpb < x.ntiles) rows_next = chunk_row(x, t0 + tpb);
-            else if (u + 1 < uend) rows_next = chunk_row(xn, 0);
+            else if (u + 1 < sp.g1) rows_next = chunk_row(xn, 0);
             const int nt = min(tpb, x.ntiles - t0);
             for (int tt = 0; tt < nt; ++tt, ++tile_i) {
                 const int t = t0 + tt;
@@ -294,11 +310,11 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs
 }
 
 template <bool kScaleF32>
-__device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, int64_t ubeg, int64_t uend)
+__device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, Span sp)
 {
     uint32_t tile_i = 0;        // tiles whose copies were issued
     int q_unit = -1;            // last unit whose query copies were issued
-    produce<kScaleF32>(tmap, a, ubeg, uend, tile_i, q_unit);
+    produce<kScaleF32>(tmap, a, sp, tile_i, q_unit);
     // every copy this warp issued lands before the CTA moves on (normally all have been consumed
     // and these waits return at once; after an abort some may still be in flight)
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -314,15 +330,15 @@ __device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& 
 // ------------------------------------------------------------------------------------------------
 // MMA thread
 // ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ void issue_mmas(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
+__device__ __forceinline__ void issue_mmas(const ScoreArgs& a, uint32_t tmem, const Span& sp)
 {
     const Shared S = shared_view();
     uint32_t tile_i = 0;
-    Unit xn = read_unit(a, ubeg);
-    for (int64_t u = ubeg; u < uend; ++u) {
-        const int uu = (int)(u - ubeg);
+    Unit xn = read_unit(a, sp.g0, sp);
+    for (int64_t u = sp.g0; u < sp.g1; ++u) {
+        const int uu = (int)(u - sp.g0);
         const Unit x = xn;
-        if (u + 1 < uend) xn = read_unit(a, u + 1);   // in flight while this unit runs
+        if (u + 1 < sp.g1) xn = read_unit(a, u + 1, sp);   // in flight while this unit runs
         const int qb = uu & 1;
         if (!wait_bar(&S.bars[kBarQfull + qb], (uu >> 1) & 1, S.abort, a.err)) return;
         const uint32_t n = kHeads * x.q_cnt;
@@ -348,9 +364,9 @@ __device__ __forceinline__ void issue_mmas(const ScoreArgs& a, uint32_t tmem, in
     }
 }
 
-__device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
+__device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, Span sp)
 {
-    issue_mmas(a, tmem, ubeg, uend);
+    issue_mmas(a, tmem, sp);
     // every MMA this thread issued has completed before tensor memory can be released
     const Shared S = shared_view();
     ptx::mma_commit(&S.bars[kBarDrain]);
@@ -361,7 +377,7 @@ __device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, int64
 // Converter warps: query group -> B operand; key tiles -> A operand in tensor memory
 // ------------------------------------------------------------------------------------------------
 template <bool kFp8, bool kScaleF32>
-__device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
+__device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, Span sp)
 {
     const Shared S = shared_view();
     if (a.p.test_stall == 2) return;   // test switch: no tile is consumed; the copies wait in the ring
@@ -370,11 +386,11 @@ __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_
     const int tid = gtid % kGroupThreads, lane = tid & 31, warp = tid >> 5;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     uint32_t tile_i = 0;
-    Unit xn = read_unit(a, ubeg);
-    for (int64_t u = ubeg; u < uend; ++u) {
-        const int uu = (int)(u - ubeg);
+    Unit xn = read_unit(a, sp.g0, sp);
+    for (int64_t u = sp.g0; u < sp.g1; ++u) {
+        const int uu = (int)(u - sp.g0);
         const Unit x = xn;
-        if (u + 1 < uend) xn = read_unit(a, u + 1);   // in flight while this unit runs
+        if (u + 1 < sp.g1) xn = read_unit(a, u + 1, sp);   // in flight while this unit runs
         const int qb = uu & 1;
         if (uu % kGroups == grp) {   // this group converts the unit's query group
             if (!wait_bar(&S.bars[kBarQrfull], uu & 1, S.abort, a.err)) return;
@@ -465,7 +481,7 @@ __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, int64_
 // Epilogue warps
 // ------------------------------------------------------------------------------------------------
 template <bool kScaleF32>
-__device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, int64_t ubeg, int64_t uend)
+__device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp)
 {
     const Shared S = shared_view();
     const int gtid = threadIdx.x - kEpiWarp0 * 32;
@@ -476,11 +492,11 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, int64_t
     const int key_lane = tid;
     const Params& p = a.p;
     uint32_t tile_i = 0;
-    Unit xn = read_unit(a, ubeg);
-    for (int64_t u = ubeg; u < uend; ++u) {
-        const int uu = (int)(u - ubeg);
+    Unit xn = read_unit(a, sp.g0, sp);
+    for (int64_t u = sp.g0; u < sp.g1; ++u) {
+        const int uu = (int)(u - sp.g0);
         const Unit x = xn;
-        if (u + 1 < uend) xn = read_unit(a, u + 1);   // in flight while this unit runs
+        if (u + 1 < sp.g1) xn = read_unit(a, u + 1, sp);   // in flight while this unit runs
         const int qb = uu & 1;
         if (!wait_bar(&S.bars[kBarQfull + qb], (uu >> 1) & 1, S.abort, a.err)) return;
         const float* wq = reinterpret_cast<const float*>(S.base + kOffWq) + qb * kGroupTokens * kHeads;
@@ -612,52 +628,65 @@ __global__ void __launch_bounds__(kThreads, kScoreCtasPerSm)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *S.tmem_slot;
-    // the metadata comes from the previous kernel and the previous top-k may still read the score
-    // lines this kernel overwrites
-    ptx::pdl_wait();
-    ptx::pdl_launch_dependents();
-
-    // the metadata must have been written for this problem: the header and this CTA's first list
-    // offsets are loaded together (the grid never exceeds kMaxCtas, so the offsets are inside the
-    // buffer whatever it holds)
-    const int32_t* meta = a.meta;
-    const int4 h0 = *reinterpret_cast<const int4*>(meta);          // magic, G, units, tiles
-    const int4 h1 = *reinterpret_cast<const int4*>(meta + 4);      // err, batch, rows, groups
-    const int32_t h_hash = meta[kMhLayoutHash];
-    const int32_t off_first = meta[a.p.meta.cta_off + blockIdx.x];
-    const int32_t off_next = meta[a.p.meta.cta_off + blockIdx.x + 1];
-    static_assert(kMhMagic == 0 && kMhCtas == 1 && kMhUnits == 2 && kMhErr == 4, "header layout");
-    const bool meta_ok = h0.x == kMetaMagic && h_hash == a.p.hash;
-    if (!meta_ok && blockIdx.x == 0 && tid == 0) atomicOr(a.err, kErrMetadata);
-    if (meta_ok && blockIdx.x == 0 && tid == 0 && h1.x) atomicOr(a.err, (uint32_t)h1.x);
-    const int G = meta_ok ? min(h0.y, kMaxCtas) : 0;
-    const int64_t nunits = meta_ok ? min((int64_t)h0.z, a.p.meta.max_units) : 0;
-
-    // this CTA's unit lists: CTA-lists blockIdx.x, blockIdx.x + gridDim.x, ... (normally one)
-    for (int c = blockIdx.x; c < G; c += gridDim.x) {
-        // offsets clamped to the units written, whatever the buffer holds
-        const int64_t o0 = c == (int)blockIdx.x ? off_first : meta[a.p.meta.cta_off + c];
-        const int64_t o1 = c == (int)blockIdx.x ? off_next : meta[a.p.meta.cta_off + c + 1];
-        const int64_t ubeg = max((int64_t)0, min(o0, nunits));
-        const int64_t uend = max(ubeg, min(o1, nunits));
-        if (uend > ubeg) {
-            if (warp < kEpiWarp0) converter<kFp8, kScaleF32>(a, tmem, ubeg, uend);
-            else if (warp < kProducerWarp) epilogue<kScaleF32>(a, tmem, ubeg, uend);
-            else if (warp == kProducerWarp) producer<kScaleF32>(&tmap, a, ubeg, uend);
-            else if (tid == kMmaWarp * 32) mma_issuer(a, tmem, ubeg, uend);
+    // the header fields every launch reports: the metadata kernel's error bits, or a mismatch
+    auto report_metadata = [&](const int4& h0, const int4& h1, int32_t hash) {
+        if (blockIdx.x != 0 || tid != 0) return;
+        const bool ok = h0.x == kMetaMagic && hash == a.p.hash;
+        if (!ok) atomicOr(a.err, kErrMetadata);
+        else if (h1.x) atomicOr(a.err, (uint32_t)h1.x);
+    };
+    static_assert(kMhMagic == 0 && kMhCtas == 1 && kMhLive == 2 && kMhTiles == 3 && kMhErr == 4, "header layout");
+    auto run_span = [&](const Span& sp) {
+        if (sp.g1 > sp.g0 && sp.t1 > sp.t0) {
+            if (warp < kEpiWarp0) converter<kFp8, kScaleF32>(a, tmem, sp);
+            else if (warp < kProducerWarp) epilogue<kScaleF32>(a, tmem, sp);
+            else if (warp == kProducerWarp) producer<kScaleF32>(&tmap, a, sp);
+            else if (tid == kMmaWarp * 32) mma_issuer(a, tmem, sp);
         }
         ptx::tc_fence_before();
         __syncthreads();
         ptx::tc_fence_after();
-        if (*S.abort) break;
-        if (c + (int)gridDim.x < G) {
-            // another list follows: restart every barrier's phase
-            if (tid == 0) {
-                for (int i = 0; i < kNumBars; ++i)
-                    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(ptx::smem_addr(&S.bars[i])) : "memory");
-                init_barriers(S);
+    };
+
+    // the metadata comes from the previous kernel and the previous top-k may still read the
+    // score lines this kernel overwrites
+    ptx::pdl_wait();
+    ptx::pdl_launch_dependents();
+    {
+        // the metadata must have been written for this problem: the header and this CTA's group
+        // range are loaded together (the grid never exceeds kMaxCtas, so the range is inside the
+        // buffer whatever it holds)
+        const int32_t* meta = a.meta;
+        const int4 h0 = *reinterpret_cast<const int4*>(meta);          // magic, G, live groups, tiles
+        const int4 h1 = *reinterpret_cast<const int4*>(meta + 4);      // err, batch, rows, groups
+        const int32_t h_hash = meta[kMhLayoutHash];
+        const int2 mine = reinterpret_cast<const int2*>(meta + a.p.meta.cta_off)[blockIdx.x];
+        report_metadata(h0, h1, h_hash);
+        const bool meta_ok = h0.x == kMetaMagic && h_hash == a.p.hash;
+        const int G = meta_ok ? max(0, min(h0.y, kMaxCtas)) : 0;
+        const int64_t live = meta_ok ? max((int64_t)0, min((int64_t)h0.z, a.p.meta.max_groups)) : 0;
+        const int64_t T = meta_ok ? max(0, h0.w) : 0;
+        // this CTA's tile ranges: CTA-ranges blockIdx.x, blockIdx.x + gridDim.x, ... (normally one)
+        for (int c = blockIdx.x; c < G; c += gridDim.x) {
+            // group range clamped to the records written, whatever the buffer holds
+            const int2 gr = c == (int)blockIdx.x ? mine : reinterpret_cast<const int2*>(meta + a.p.meta.cta_off)[c];
+            Span sp;
+            sp.t0 = split_start(T, G, c);
+            sp.t1 = split_start(T, G, c + 1);
+            sp.g0 = max((int64_t)0, min((int64_t)gr.x, live));
+            sp.g1 = max(sp.g0, min((int64_t)gr.y, live));
+            sp.recs = meta + a.p.meta.group_off;
+            run_span(sp);
+            if (*S.abort) break;
+            if (c + (int)gridDim.x < G) {
+                // another range follows: restart every barrier's phase
+                if (tid == 0) {
+                    for (int i = 0; i < kNumBars; ++i)
+                        asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(ptx::smem_addr(&S.bars[i])) : "memory");
+                    init_barriers(S);
+                }
+                __syncthreads();
             }
-            __syncthreads();
         }
     }
     ptx::tc_fence_before();
@@ -679,12 +708,15 @@ cudaError_t launch_variant(const CUtensorMap* tmap, const ScoreArgs& a, int grid
 
 cudaError_t launch_score(const Params& p, const void* tmap_key, const void* query, const void* key,
                          const void* weights, const void* q_scale, const void* k_scale,
+                         const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                          const int32_t* block_table, const int32_t* meta, uint32_t* scores,
                          uint32_t* err_word, int grid, cudaStream_t st)
 {
     (void)key;
     ScoreArgs a;
     a.p = p;
+    a.seq_lens_q = seq_lens_q;
+    a.seq_lens_k = seq_lens_k;
     a.query = static_cast<const uint8_t*>(query);
     a.weights = static_cast<const uint8_t*>(weights);
     a.q_scale = static_cast<const uint8_t*>(q_scale);

@@ -53,7 +53,43 @@ struct TopkArgs {
     uint32_t* err;
     int32_t* out;
     float* values;     // optional: the score of each index written, -inf beside -1
+    // 1 when this launch directly follows the library's score kernel in the stream: that kernel
+    // lets its dependents start only after its own griddepcontrol.wait returned, i.e. after the
+    // metadata kernel before it had completed, so the metadata and the (unchanged) block_table can
+    // be read before this kernel's own wait; 0 for a standalone top-k launch
+    int32_t early;
 };
+
+// Where output row `row` lives: its batch b, row r within the batch, visible keys n and the
+// batch's compressed length lc (n = 0 for rows of no batch or an invalid one).  Loads bypass L1.
+struct RowInfo {
+    int64_t b, r, n, lc;
+};
+
+__device__ RowInfo row_info(const TopkArgs& a, bool meta_ok, int64_t row)
+{
+    const Params& p = a.p;
+    const int32_t* be = a.meta + p.meta.batch_off;
+    RowInfo ri{-1, 0, 0, 0};
+    if (!meta_ok || p.batch <= 0) return ri;
+    if (!p.layout_tnd) {
+        ri.b = row / p.s1;
+        ri.r = row % p.s1;
+    } else {
+        int64_t lo = 0, hi = p.batch - 1;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if (__ldcg(be + mid * kBatchWords + kBeFirstRow) <= row) lo = mid; else hi = mid - 1;
+        }
+        ri.b = lo;
+    }
+    const int4 e0 = __ldcg(reinterpret_cast<const int4*>(be + ri.b * kBatchWords));       // sq, sk, lc, first
+    const int ok = __ldcg(be + ri.b * kBatchWords + kBeOk);
+    if (p.layout_tnd) ri.r = row - e0.w;
+    ri.lc = e0.z;
+    if (ok && ri.r >= 0) ri.n = visible_keys(p.sparse_mode, p.cmp_ratio, e0.x, e0.y, ri.lc, ri.r, p.complete_blocks);
+    return ri;
+}
 
 struct Smem {
     uint32_t* cache;  // [kCacheKeys] one score line (uncached rows: scatter targets)
@@ -647,38 +683,47 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     const Params& p = a.p;
     const int tid = threadIdx.x;
     const int k = p.sparse_count;
-    // the score lines and metadata come from earlier kernels; the next call may overwrite them
-    // only after this grid completes (it waits too)
+    bool meta_ok = false;
+    RowInfo ri{};
+    int64_t pages = 0;
+    int32_t pg_first = 0;
+    bool bad = false;
+    // the row's place and its pages: every page the batch's rows can see must lie in the pool; the
+    // first entry per thread is loaded now and checked after the selection, the rest (rows of more
+    // than kThreads pages) at once
+    auto prepare = [&](int64_t row) {
+        ri = row_info(a, meta_ok, row);
+        pages = ri.n > 0 ? ceil_div64(ri.lc, p.block_size) : 0;
+        const int32_t* table = a.block_table + (ri.b < 0 ? 0 : ri.b) * p.max_blocks_per_seq;
+        pg_first = tid < pages ? __ldcg(table + tid) : 0;
+        bad = false;
+        for (int64_t i = tid + kThreads; i < pages; i += kThreads) {
+            const int32_t pg = __ldcg(table + i);
+            bad |= pg < 0 || pg >= p.num_blocks;
+        }
+    };
+    auto read_header = [&]() {
+        meta_ok = __ldcg(a.meta + kMhMagic) == kMetaMagic && __ldcg(a.meta + kMhLayoutHash) == p.hash;
+    };
+    if (a.early) {
+        read_header();
+        if (blockIdx.x < p.rows) prepare(blockIdx.x);
+    }
+    // the score lines (and, for a standalone launch, the metadata) come from earlier kernels; the
+    // next call may overwrite them only after this grid completes (it waits too)
     ptx::pdl_wait();
     ptx::pdl_launch_dependents();
-    const bool meta_ok = a.meta[kMhMagic] == kMetaMagic && a.meta[kMhLayoutHash] == p.hash;
-    const int32_t* be = a.meta + p.meta.batch_off;
+    if (!a.early) {
+        read_header();
+        if (blockIdx.x < p.rows) prepare(blockIdx.x);
+    }
 
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
         int32_t* out = a.out + row * k;
-        // ---- which batch / live row / how many visible keys
-        int64_t b = -1, r = 0, n = 0, lc = 0;
-        if (meta_ok && p.batch > 0) {
-            if (!p.layout_tnd) {
-                b = row / p.s1;
-                r = row % p.s1;
-            } else {
-                int64_t lo = 0, hi = p.batch - 1;
-                while (lo < hi) {
-                    const int64_t mid = (lo + hi + 1) >> 1;
-                    if (be[mid * kBatchWords + kBeFirstRow] <= row) lo = mid; else hi = mid - 1;
-                }
-                b = lo;
-                r = row - be[b * kBatchWords + kBeFirstRow];
-            }
-            const int32_t* e = be + b * kBatchWords;
-            lc = e[kBeLc];
-            if (e[kBeOk] && r >= 0) n = visible_keys(p.sparse_mode, p.cmp_ratio, e[kBeSq], e[kBeSk], lc, r, p.complete_blocks);
-        }
+        if (row != blockIdx.x) prepare(row);
+        const int64_t n = ri.n;
         const uint32_t* line = a.scores + row * p.ld;
         const int need = (int)(n < k ? n : k);
-        const int64_t pages = n > 0 ? ceil_div64(lc, p.block_size) : 0;
-        const int32_t* table = a.block_table + (b < 0 ? 0 : b) * p.max_blocks_per_seq;
         const bool cached = n > 0 && n <= kCacheKeys;
         __syncthreads();                           // the previous row is done with shared memory
         if (tid == 0) {
@@ -691,15 +736,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
             }
         }
         __syncthreads();
-        // ---- every page this batch's rows can see must lie in the pool: the first entry per
-        // thread is loaded now and checked after the selection, the rest (rows of > 1024 pages)
-        // at once
-        const int32_t pg_first = tid < pages ? __ldg(table + tid) : 0;
-        bool bad = false;
-        for (int64_t i = tid + kThreads; i < pages; i += kThreads) {
-            const int32_t pg = __ldg(table + i);
-            bad |= pg < 0 || pg >= p.num_blocks;
-        }
         bool copy_ok = true;
         if (cached) {
             copy_ok = wait_copy(S.bar, bar_parity);   // bounded wait for the line
@@ -777,10 +813,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
 
 cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
                         const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
-                        cudaStream_t st)
+                        bool after_score, cudaStream_t st)
 {
     if (p.rows == 0) return cudaSuccess;
-    TopkArgs a{p, block_table, meta, scores, err_word, out, values};
+    TopkArgs a{p, block_table, meta, scores, err_word, out, values, after_score ? 1 : 0};
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.rows < (1 << 30) ? p.rows : (1 << 30);

@@ -1,7 +1,8 @@
 """Failure detection on the GPU without a fault: every wait in the score kernel is bounded, so a
-producer that issues nothing, or converters that consume nothing (host-set test switches), make
-the waits run out; the kernel must report QLI_ERR_DEVICE_TIMEOUT through the workspace's error word,
-let the copies already in flight land before its CTAs exit, and leave the CUDA context usable."""
+producer that issues nothing, or converters that consume nothing (the stall switch of the testing
+build of the library, include/qli_testing.h), make the waits run out; the kernel must report
+QLI_ERR_DEVICE_TIMEOUT through the workspace's error word, let the copies already in flight land
+before its CTAs exit, and leave the CUDA context usable.  The product library has no such switch."""
 import os
 import subprocess
 import sys
@@ -19,6 +20,8 @@ import torch
 import numpy as np
 import workloads as W
 import sparse_attention_token_block_gb300 as Q
+Q.use_testing_library()
+Q.lib.qli_testing_set_stall(%d)
 case = W.make_case("stall", batch=2, s1=1, seq_lens_k=[700, 300], block_size=64, sparse_count=16, seed=1)
 p = Q.make_problem(**W.problem_kwargs(case))
 ix = Q.Indexer(p)
@@ -30,10 +33,8 @@ print("AFTER", x)
 """
 
 
-def run_child(env_extra):
-    env = dict(os.environ)
-    env.update(env_extra)
-    out = subprocess.run([sys.executable, "-c", CHILD % ROOT], env=env, capture_output=True,
+def run_child(stall):
+    out = subprocess.run([sys.executable, "-c", CHILD % (ROOT, stall)], capture_output=True,
                          text=True, timeout=120)
     return out
 
@@ -48,7 +49,7 @@ def built():
 
 
 def test_stalled_producer_reports_timeout(built):
-    out = run_child({"QLI_TEST_STALL_PRODUCER": "1"})
+    out = run_child(1)
     assert out.returncode == 0, out.stderr[-2000:]
     status = [l for l in out.stdout.splitlines() if l.startswith("STATUS")][0].split()
     assert int(status[1]) == 6            # QLI_ERR_DEVICE_TIMEOUT
@@ -57,7 +58,7 @@ def test_stalled_producer_reports_timeout(built):
 
 
 def test_stalled_converter_reports_timeout_after_copies_land(built):
-    out = run_child({"QLI_TEST_STALL_CONVERTER": "1"})
+    out = run_child(2)
     assert out.returncode == 0, out.stderr[-2000:]
     status = [l for l in out.stdout.splitlines() if l.startswith("STATUS")][0].split()
     assert int(status[1]) == 6            # QLI_ERR_DEVICE_TIMEOUT
@@ -66,7 +67,7 @@ def test_stalled_converter_reports_timeout_after_copies_land(built):
 
 
 def test_normal_run_reports_no_error(built):
-    out = run_child({"QLI_TEST_STALL_PRODUCER": "0", "QLI_TEST_STALL_CONVERTER": "0"})
+    out = run_child(0)
     assert out.returncode == 0, out.stderr[-2000:]
     status = [l for l in out.stdout.splitlines() if l.startswith("STATUS")][0].split()
     assert int(status[1]) == 0 and int(status[2]) == 0

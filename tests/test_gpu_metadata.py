@@ -1,0 +1,141 @@
+"""The work split written by qli_metadata, word by word against a host re-derivation of its
+definition (needs a GB300).
+
+Definition (the metadata call: the cores used and each core's start point): query groups of
+group_tokens consecutive live rows per batch; a group's tiles are ceil(n / 128), n the visible keys
+of its last row; live groups (at least one tile) are listed in batch and row order with their first
+tile in the concatenated tile sequence of T tiles; score CTA c of G owns tiles [T c / G,
+T (c + 1) / G) and the live groups that range overlaps."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAGIC = 0x514C4932
+
+
+@pytest.fixture(scope="module")
+def qli():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_attention_token_block_gb300 import build as B
+    B.build()
+    import sparse_attention_token_block_gb300 as Q
+    return Q
+
+
+def derive(case, G, gt=1):
+    """Header fields, batch entries, live group records and CTA ranges of the definition."""
+    B = case.batch
+    batches, records = [], []
+    tnd = case.layout_q == "TND"
+    lc_cap = case.max_blocks_per_seq * case.block_size
+    bad_tnd = False
+    err = 0
+    raw = []
+    for b in range(B):
+        if not tnd:
+            first = b * case.s1
+            v = case.s1 if case.seq_lens_q is None else int(case.seq_lens_q[b])
+            ok = 0 <= v <= case.s1
+            sq = v if ok else 0
+        else:
+            lo = int(case.seq_lens_q[b - 1]) if b > 0 else 0
+            hi = int(case.seq_lens_q[b])
+            ok = lo >= 0 and hi >= lo and hi <= case.total_q
+            bad_tnd |= not ok
+            first = max(lo, 0)
+            sq = hi - lo if ok else 0
+        sk = int(case.seq_lens_k[b])
+        ok = ok and 0 <= sk <= case.max_seqlen_k
+        lc = -(-sk // case.cmp_ratio) if ok else 0
+        ok = ok and lc <= lc_cap
+        if not ok:
+            err |= 1
+        raw.append([sq, sk if ok else 0, lc, first, ok])
+    gbase = 0
+    T = 0
+    for b, (sq, sk, lc, first, ok) in enumerate(raw):
+        okb = ok and not bad_tnd
+        groups = -(-sq // gt) if okb else 0
+        batches.append([sq, sk, lc, first, int(okb), groups, gbase])
+        for g in range(groups):
+            r0 = g * gt
+            rl = min(r0 + gt, sq) - 1
+            n = oracle.visible(case, sq, sk, rl)
+            tiles = -(-n // 128)
+            if tiles:
+                records.append([b, r0, first + r0, sq, sk, lc, T, tiles])
+                T += tiles
+        gbase += groups
+    ctas = []
+    starts = [rec[6] for rec in records]
+    for c in range(G):
+        t0, t1 = T * c // G, T * (c + 1) // G
+        if t1 <= t0:
+            ctas.append((0, 0))
+            continue
+        first = max(i for i, s in enumerate(starts) if s <= t0)
+        end = next((i for i, s in enumerate(starts) if s >= t1), len(starts))
+        ctas.append((first, end))
+    return dict(live=len(records), T=T, err=err, groups=gbase, batches=batches, records=records, ctas=ctas)
+
+
+CASES = [
+    ("tiny_decode", lambda: W.tiny_decode()),
+    ("long_decode", lambda: W.long_decode()),
+    ("fp8_compressed_decode", lambda: W.fp8_compressed_decode()),
+    ("varlen_prefill", lambda: W.varlen_prefill()),
+    ("tnd_empty_and_short", lambda: W.make_case("m1", layout_q="TND", q_lens=[5, 0, 9, 1, 30],
+                                                seq_lens_k=[3, 40, 600, 0, 30], block_size=32,
+                                                sparse_count=64, sparse_mode=3, seed=1)),
+    ("bsnd_qlens", lambda: W.make_case("m2", batch=4, s1=4, q_lens=[4, 0, 1, 3],
+                                       seq_lens_k=[600, 600, 129, 2], block_size=64,
+                                       sparse_count=200, sparse_mode=3, seed=2)),
+    ("bad_length", lambda: W.make_case("m3", batch=3, s1=2, q_lens=[2, 3, 1],
+                                       seq_lens_k=[300, 300, 5000], block_size=64,
+                                       sparse_count=16, seed=3)),
+]
+
+
+@pytest.mark.parametrize("name,make", CASES, ids=[c[0] for c in CASES])
+def test_metadata_matches_definition(qli, name, make):
+    import torch
+    case = make()
+    if name == "bad_length":
+        case.seq_lens_q = np.array([2, 3, 1], np.int32)      # 3 > S1: batch 1 invalid
+    p = qli.make_problem(**W.problem_kwargs(case))
+    meta = torch.full((qli.metadata_words(p),), -7, dtype=torch.int32, device="cuda")
+    d = W.to_device(case)
+    qli.check(qli.metadata(p, d["seq_lens_q"], d["seq_lens_k"], meta), "metadata")
+    m = meta.cpu().numpy()
+    G = int(m[1])
+    assert m[0] == MAGIC and 1 <= G <= 1024
+    ref = derive(case, G)
+    assert int(m[2]) == ref["live"] and int(m[3]) == ref["T"]
+    assert int(m[4]) == ref["err"] and int(m[5]) == case.batch and int(m[6]) == case.rows
+    assert int(m[7]) == ref["groups"]
+    B = case.batch
+    be = m[16:16 + 8 * B].reshape(B, 8)[:, :7]
+    assert np.array_equal(be, np.array(ref["batches"], dtype=np.int64).reshape(B, 7))
+    cta_off = 16 + 8 * B
+    ctas = m[cta_off:cta_off + 2 * G].reshape(G, 2)
+    assert [tuple(map(int, x)) for x in ctas] == ref["ctas"]
+    rec_off = (cta_off + 2 * 1024 + 3) & ~3
+    recs = m[rec_off:rec_off + 8 * ref["live"]].reshape(-1, 8)
+    assert np.array_equal(recs, np.array(ref["records"], dtype=np.int64).reshape(-1, 8))
+    # every live group's tiles are covered exactly once by the CTAs' (group, tile range) units
+    cover = np.zeros(ref["T"], np.int64)
+    for c in range(G):
+        t0, t1 = ref["T"] * c // G, ref["T"] * (c + 1) // G
+        f, e = ctas[c]
+        for g in range(f, e):
+            tb, tn = recs[g][6], recs[g][7]
+            lo, hi = max(t0, tb), min(t1, tb + tn)
+            assert hi > lo
+            cover[lo:hi] += 1
+    assert (cover == 1).all()

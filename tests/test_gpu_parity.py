@@ -300,3 +300,61 @@ def test_complete_blocks_mask_matches_oracle(qli, kw):
     # the flag changes the result for these shapes (some rows lose their partial block)
     ceil_idx, _, _ = oracle.score_topk(case)
     assert not np.array_equal(ceil_idx, ora_idx)
+
+
+# ---------------------------------------------------------------------------- rows beyond the row cache
+
+# The top-k keeps a row of up to 32768 scores in shared memory; longer rows take the path that
+# samples and gathers from global memory.  These cases reach it with uncompressed keys.
+LONG_ROWS = [
+    ("long_m3", dict(batch=3, s1=1, seq_lens_k=[40000, 70000, 131072], block_size=128,
+                     sparse_count=2048, sparse_mode=3)),
+    ("long_m0_s2", dict(batch=2, s1=2, seq_lens_k=[33000, 65536], block_size=64,
+                        sparse_count=2048, sparse_mode=0)),
+    ("long_fp8_k777", dict(batch=2, s1=1, qk_dtype=W.FP8, scale_dtype=W.F32,
+                           seq_lens_k=[50001, 32769], block_size=256, sparse_count=777,
+                           sparse_mode=3)),
+]
+
+
+@pytest.mark.parametrize("name,kw", LONG_ROWS, ids=[s[0] for s in LONG_ROWS])
+def test_rows_beyond_row_cache(qli, name, kw):
+    case = W.make_case(name, seed=zlib.crc32(name.encode()) % 1000, **kw)
+    assert case.max_seqlen_k > 32768
+    assert_parity(qli, case)
+
+
+def test_tnd_sequence_beyond_row_cache(qli):
+    case = W.make_case("tnd_long", layout_q="TND", q_lens=[3, 2, 1], seq_lens_k=[40000, 5000, 36000],
+                       block_size=128, sparse_count=2048, sparse_mode=3, seed=61)
+    assert_parity(qli, case)
+
+
+def test_all_equal_row_beyond_row_cache(qli):
+    """Every key identical in rows of 40000 and 33000 keys: the sampled bound keeps every key, far
+    more than the candidate buffer holds, so the exact selection must return the lowest indices."""
+    case = W.make_case("ties_long", batch=2, s1=1, seq_lens_k=[40000, 33000], block_size=128,
+                       sparse_count=2048, sparse_mode=0, seed=62)
+    case.key[:] = case.key[0, 0]
+    case.k_scale[:] = case.k_scale[0, 0]
+    gpu_idx, _, st, _ = run_gpu(qli, case)
+    assert st == 0
+    for r in range(2):
+        assert gpu_idx[r].tolist() == list(range(2048))
+    ora_idx, _, _ = oracle.score_topk(case)
+    assert np.array_equal(gpu_idx, ora_idx)
+
+
+def test_few_distinct_scores_beyond_row_cache(qli):
+    """Keys drawn from 5 distinct rows in a 60000-key row: long runs of exact ties at the cut."""
+    case = W.make_case("few_long", batch=1, s1=1, seq_lens_k=[60000], block_size=128,
+                       sparse_count=2048, sparse_mode=3, seed=63)
+    rng = np.random.default_rng(63)
+    pick = rng.integers(0, 5, size=case.key.shape[:2])
+    protos = case.key[0, :5, 0].copy()
+    case.key[:, :, 0] = protos[pick]
+    case.k_scale[:] = np.float16(1.0)
+    gpu_idx, _, st, _ = run_gpu(qli, case)
+    ora_idx, _, _ = oracle.score_topk(case)
+    assert st == 0
+    assert np.array_equal(gpu_idx, ora_idx)

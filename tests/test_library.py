@@ -17,8 +17,8 @@ def Q():
     return Q
 
 
-def declared_symbols():
-    text = open(os.path.join(ROOT, "include", "qli.h")).read()
+def declared_symbols(header="qli.h"):
+    text = open(os.path.join(ROOT, "include", header)).read()
     return sorted(set(re.findall(r"\b(qli_[a-z_]+)\s*\(", text)))
 
 
@@ -27,6 +27,15 @@ def test_exports_every_declared_symbol(Q):
     assert set(names) == set(Q.EXPORTS)
     for n in names:
         assert hasattr(Q.lib, n), n
+    # the product library carries no test switch
+    for n in declared_symbols("qli_testing.h"):
+        assert not hasattr(Q.lib, n), n
+
+
+def test_testing_build_exports_product_and_testing_symbols(Q):
+    L = ctypes.CDLL(Q.TESTING_LIB_PATH)
+    for n in declared_symbols() + declared_symbols("qli_testing.h"):
+        assert hasattr(L, n), n
 
 
 def _ok_problem(Q, **kw):

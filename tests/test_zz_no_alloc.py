@@ -10,8 +10,9 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import workloads as W
-from checker import REL_TOL  # noqa: F401  (same tolerance rule as the parity tests)
+from checker import check, visible_counts
 
 pytestmark = pytest.mark.gpu
 
@@ -64,6 +65,12 @@ def test_static_scratch_matches_workspace_path_twice(Q):
             # same kernels on the same inputs: identical, which is within any tolerance
             assert np.array_equal(got, ref)
             assert int(err.item()) == 0
+        # and the oracle's indices under the parity tests' tie-aware rule (row tolerance 1e-5 of
+        # the row's largest score)
+        ora_idx, ora_scores, ora_err = oracle.score_topk(case, with_scores=True)
+        assert ora_err == 0
+        _, checked, fails = check(got, ora_idx, ora_scores, visible_counts(case, oracle), case.sparse_count)
+        assert checked == case.rows and not fails, fails[:3]
 
 
 def test_static_scratch_rejects_oversized_problems(Q):
