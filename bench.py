@@ -67,6 +67,8 @@ def parse():
                     help="indexer: the indexer step (default); quantize: the upstream quantizer; "
                          "gather: the downstream sparse-attention gather")
     ap.add_argument("--entry-bytes", type=int, default=512, help="KV entry size of --op gather")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload timings of the other configurations")
     return ap.parse_args()
 
 
@@ -262,7 +264,15 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     nthreads = os.cpu_count() or 1
-    take = max(1, min(case.batch, 2)) if case.layout_q == "BSND" else None
+    # each step scores whole sequences of the workload, as many as keep every host core busy (the
+    # oracle runs its rows on all of them) while K + W steps stay within a few minutes
+    take = None
+    if case.layout_q == "BSND":
+        t0 = time.perf_counter()
+        oracle.score_topk(subcase(case, list(range(min(case.batch, nthreads)))), nthreads=nthreads)
+        per_seq = max(time.perf_counter() - t0, 1e-3) / min(case.batch, nthreads)
+        budget = 120.0 / max(1, args.steps + args.warmup)          # seconds of oracle work per step
+        take = int(max(min(case.batch, nthreads), min(case.batch, budget / per_seq)))
     sub = subcase(case, list(range(take))) if take else case
     pairs = visible_pairs(sub)
     for _ in range(args.warmup):
@@ -294,7 +304,8 @@ def config_of(case, args, world):
                             int(case.seq_lens_k.min()), int(case.seq_lens_k.max()),
                             case.block_size, case.sparse_count, case.sparse_mode, case.cmp_ratio),
             "global_batch": case.batch * world, "parallelism": "independent sequences per rank",
-            "l2": "flushed between timed steps (%d MB write, then read back; outside the events)" % args.flush_mb}
+            "l2": "flushed between timed steps (%d MB write, then read back; outside the events)" % (
+                args.flush_mb if args is not None else 512)}
 
 
 def quantize_bytes(nvec, tokens, esz):
@@ -507,6 +518,76 @@ def run_gather(args, rank, world, local):
     }
     if rank == 0:
         print(json.dumps(line))
+
+
+def score_roofline(stats, score_us, traffic=None):
+    """Roofline of the scoring kernel for one workload: its algorithmic bytes per launch over the
+    event-timed duration against the measured copy peak -- or, above the ridge point of the two
+    measured peaks (algorithmic ops per byte), its algorithmic ops against the dense bf16 peak."""
+    peak, peak_kind = peaks()
+    tpeak, tpeak_kind = tensor_peak()
+    ops_launch = stats["pairs"] * OPS_PER_PAIR
+    if ops_launch / max(stats["score_bytes"], 1) > tpeak * 1e12 / (peak * 1e9):
+        t_achieved = ops_launch / (score_us * 1e-6) / 1e12
+        return {"kernel": "score_kernel", "bound": "tensor", "achieved": t_achieved, "peak": tpeak,
+                "unit": "TFLOP/s", "frac": t_achieved / tpeak, "peak_source": tpeak_kind,
+                "algorithmic_ops_per_launch": ops_launch, "traffic": traffic}
+    achieved = stats["score_bytes"] / (score_us * 1e-6) / 1e9
+    return {"kernel": "score_kernel", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": peak_kind,
+            "algorithmic_bytes_per_launch": stats["score_bytes"], "traffic": traffic}
+
+
+def time_workload(Q, case, dev, flush_l2, steps, warmup):
+    """One workload's indexer call timed like the headline step (the execution plan replayed, L2
+    flushed between calls, events on the launching stream), plus a pass with events between the
+    three kernels for the per-stage times.  Returns the workload's summary for the JSON line."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    stats = workload_stats(case)
+    p = Q.make_problem(**W.problem_kwargs(case))
+    ix = Q.Indexer(p, device=dev)
+    d = W.to_device(case, dev)
+    plan = ix.plan(**d)
+    for _ in range(max(3, warmup)):
+        flush_l2(1)
+        plan.launch()
+    torch.cuda.synchronize()
+    Q.check(ix.device_error()[0], "device error (%s)" % case.name)
+    pairs_ev = []
+    for i in range(steps):
+        flush_l2(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        plan.launch()
+        b.record(stream)
+        pairs_ev.append((a, b))
+    sev = []
+    for i in range(steps):
+        flush_l2(i)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        Q.check(Q.metadata(p, d["seq_lens_q"], d["seq_lens_k"], ix.meta), "metadata")
+        e[1].record(stream)
+        Q.check(Q.score(p, d["query"], d["key"], d["weights"], d["q_scale"], d["k_scale"], d["seq_lens_q"],
+                        d["seq_lens_k"], d["block_table"], ix.meta, ix.workspace), "score")
+        e[2].record(stream)
+        Q.check(Q.topk(p, d["block_table"], ix.meta, ix.workspace, ix.out), "topk")
+        e[3].record(stream)
+        sev.append(e)
+    torch.cuda.synchronize()
+    Q.check(ix.device_error()[0], "device error (%s)" % case.name)
+    plan.close()
+    us = statistics.mean(a.elapsed_time(b) for a, b in pairs_ev) * 1e3
+    stage = {"metadata": 1e3 * statistics.mean(e[0].elapsed_time(e[1]) for e in sev),
+             "score": 1e3 * statistics.mean(e[1].elapsed_time(e[2]) for e in sev),
+             "topk": 1e3 * statistics.mean(e[2].elapsed_time(e[3]) for e in sev)}
+    peak, _ = peaks()
+    return {"config": config_of(case, None, 1)["workload"], "steps": steps,
+            "us_per_call": us, "gops": stats["pairs"] * OPS_PER_PAIR / (us * 1e-6) / 1e9,
+            "keys_scored_per_s": stats["pairs"] / (us * 1e-6), "stage_us": stage,
+            "call_hbm_frac": stats["total_bytes"] / (us * 1e-6) / 1e9 / peak,
+            "roofline": score_roofline(stats, stage["score"])}
 
 
 def main():
@@ -723,20 +804,18 @@ def main():
         return
     peak, peak_kind = peaks()
     score_avg = sum(score_ms) / len(score_ms)
-    achieved = stats["score_bytes"] / (score_avg * 1e-3) / 1e9
     # the committed score-kernel capture is of the long decode at its default size
     traffic = recorded_traffic()[0] if (args.workload, args.batch) == ("long_decode", 0) else None
-    roofline = {"kernel": "score_kernel", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": stats["score_bytes"], "traffic": traffic}
-    # above the ridge point (ops per byte of the peaks) the scoring is bound by the tensor cores
-    tpeak, tpeak_kind = tensor_peak()
-    ops_launch = stats["pairs"] * OPS_PER_PAIR
-    if ops_launch / max(stats["score_bytes"], 1) > tpeak * 1e12 / (peak * 1e9):
-        t_achieved = ops_launch / (score_avg * 1e-3) / 1e12
-        roofline = {"kernel": "score_kernel", "bound": "tensor", "achieved": t_achieved, "peak": tpeak,
-                    "unit": "TFLOP/s", "frac": t_achieved / tpeak, "peak_source": tpeak_kind,
-                    "algorithmic_ops_per_launch": ops_launch, "traffic": traffic}
+    roofline = score_roofline(stats, score_avg * 1e3, traffic)
+    # the other configurations, each timed the same way (fewer steps), for their own figures
+    others = None
+    if not args.no_workloads:
+        others = {}
+        for name in W.WORKLOADS:
+            if name == args.workload:
+                continue
+            others[name] = time_workload(Q, make_workload(name, 0, rank), dev, flush_l2,
+                                         max(3, min(args.steps, 30)), args.warmup)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case)
@@ -754,7 +833,10 @@ def main():
         "us_per_call_with_sparse_values": values_us,
         "stage_us": {"metadata": 1e3 * statistics.mean(meta_ms),
                      "score": 1e3 * score_avg, "topk": 1e3 * statistics.mean(topk_ms)},
+        # the whole call's algorithmic bytes (scoring inputs, indices, lengths) over us_per_call
+        "call_hbm_frac": stats["total_bytes"] / (total_ms / args.steps * 1e-3) / 1e9 / peak,
         "roofline": roofline,
+        "workloads": others,
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,
