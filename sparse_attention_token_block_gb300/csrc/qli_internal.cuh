@@ -218,8 +218,24 @@ __host__ __device__ inline int32_t problem_hash(const Params& p)
 
 MetaLayout meta_layout(int64_t batch, int64_t max_groups);
 
-// First tile of score CTA c's range: floor(T c / G) (T < 2^31, G <= kMaxCtas, so the product fits)
-__host__ __device__ inline int64_t split_start(int64_t T, int64_t G, int64_t c) { return (T * c) / G; }
+// The split of the T tiles over G score CTAs.  Two CTAs share each SM and the one that arrived first
+// (CTAs 0 .. (G + 2) / 2 - 1 for G = 2 x SMs - 2) streams its tiles about 9 % faster than the other
+// (measured: 0.91 against 1.00 us per 128-key tile on the long decode), so ranges are in
+// proportion 12 : 11 and both finish together.  W(c) is the weight of CTAs 0 .. c - 1; CTA c owns
+// tiles [T W(c) / W(G), T W(c + 1) / W(G)).  (T < 2^31 and W(G) < 2^14, so the product fits.)
+constexpr int64_t kSplitFirst = 12, kSplitSecond = 11;
+
+__host__ __device__ inline int64_t split_weight(int64_t G, int64_t c)
+{
+    const int64_t h = (G + 2) / 2;
+    return c <= h ? c * kSplitFirst : h * kSplitFirst + (c - h) * kSplitSecond;
+}
+
+// First tile of score CTA c's range
+__host__ __device__ inline int64_t split_start(int64_t T, int64_t G, int64_t c)
+{
+    return (T * split_weight(G, c)) / split_weight(G, G);
+}
 
 // Launch `kernel` with programmatic stream serialization: it may begin launching while the
 // previous kernel in the stream finishes; every kernel of this library calls griddepcontrol.wait

@@ -4,8 +4,9 @@ definition (needs a GB300).
 Definition (the metadata call: the cores used and each core's start point): query groups of
 group_tokens consecutive live rows per batch; a group's tiles are ceil(n / 128), n the visible keys
 of its last row; live groups (at least one tile) are listed in batch and row order with their first
-tile in the concatenated tile sequence of T tiles; score CTA c of G owns tiles [T c / G,
-T (c + 1) / G) and the live groups that range overlaps."""
+tile in the concatenated tile sequence of T tiles; score CTA c of G owns tiles
+[T W(c) / W(G), T W(c + 1) / W(G)) and the live groups that range overlaps, where W(c) weighs the
+first (G + 2) / 2 CTAs 12 and the others 11 (the first CTA on each SM streams faster)."""
 import numpy as np
 import pytest
 
@@ -15,6 +16,14 @@ import workloads as W
 pytestmark = pytest.mark.gpu
 
 MAGIC = 0x514C4932
+
+
+def split_start(T, G, c):
+    h = (G + 2) // 2
+
+    def w(x):
+        return x * 12 if x <= h else h * 12 + (x - h) * 11
+    return T * w(c) // w(G)
 
 
 @pytest.fixture(scope="module")
@@ -75,7 +84,7 @@ def derive(case, G, gt=1):
     ctas = []
     starts = [rec[6] for rec in records]
     for c in range(G):
-        t0, t1 = T * c // G, T * (c + 1) // G
+        t0, t1 = split_start(T, G, c), split_start(T, G, c + 1)
         if t1 <= t0:
             ctas.append((0, 0))
             continue
@@ -131,7 +140,7 @@ def test_metadata_matches_definition(qli, name, make):
     # every live group's tiles are covered exactly once by the CTAs' (group, tile range) units
     cover = np.zeros(ref["T"], np.int64)
     for c in range(G):
-        t0, t1 = ref["T"] * c // G, ref["T"] * (c + 1) // G
+        t0, t1 = split_start(ref["T"], G, c), split_start(ref["T"], G, c + 1)
         f, e = ctas[c]
         for g in range(f, e):
             tb, tn = recs[g][6], recs[g][7]
