@@ -42,7 +42,7 @@ METRIC = "indexer GOPS (algorithmic: 16384 ops per visible query-key pair)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "score_kernel_long_decode.md")
-SCORE_SOURCES = ["qli_score.cu", "qli_ptx.cuh", "qli_internal.cuh"]
+SCORE_SOURCES = ["qli_score.cuh", "qli_ptx.cuh", "qli_internal.cuh"]
 QUANT_PROFILE = os.path.join(ROOT, "profiles", "quantize_kernel_prefill.md")
 QUANT_SOURCES = ["qli_quant.cu", "qli_ptx.cuh", "qli_internal.cuh"]
 GATHER_PROFILE = os.path.join(ROOT, "profiles", "gather_kernel_long_decode.md")

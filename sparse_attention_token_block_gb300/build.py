@@ -19,8 +19,8 @@ LIB = os.path.join(HERE, "libqli.so")
 # the testing build: the same objects except the host API, compiled with QLI_TESTING (it adds the
 # failure-detection test switch of include/qli_testing.h); the product library has no switch
 TEST_LIB = os.path.join(HERE, "libqli_testing.so")
-SOURCES = ["qli_api.cu", "qli_metadata.cu", "qli_score.cu", "qli_topk.cu", "qli_noalloc.cu", "qli_plan.cu", "qli_quant.cu", "qli_gather.cu"]
-HEADERS = ["qli_internal.cuh", "qli_ptx.cuh"]
+SOURCES = ["qli_api.cu", "qli_metadata.cu", "qli_score.cu", "qli_score_multi.cu", "qli_topk.cu", "qli_noalloc.cu", "qli_plan.cu", "qli_quant.cu", "qli_gather.cu"]
+HEADERS = ["qli_internal.cuh", "qli_ptx.cuh", "qli_score.cuh"]
 TEST_SOURCE = "qli_api.cu"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -79,11 +79,12 @@ qli_status check(const qli_problem* p, const char** why)
     return QLI_OK;
 }
 
-// Query tokens scored together by one MMA (N = 64 per token)
+// Query tokens scored together by one MMA (N = 64 per token): one for one query token per
+// sequence, else up to kMultiTokens
 int group_tokens_of(const qli_problem* p)
 {
-    (void)p;
-    return 1;
+    if (p->layout_q == QLI_BSND) return p->max_q_tokens <= 1 ? 1 : (p->max_q_tokens < kMultiTokens ? p->max_q_tokens : kMultiTokens);
+    return kMultiTokens;
 }
 
 int64_t max_groups_of(const qli_problem* p)
@@ -253,8 +254,8 @@ qli_status qli_metadata(const qli_problem* p, const int32_t* seq_lens_q, const i
     int sms = device_sms(nullptr);
     if (sms < 0) return QLI_ERR_CUDA;
     if (sms == 0) return QLI_ERR_NO_DEVICE;
-    cudaError_t e = launch_metadata(P, seq_lens_q, seq_lens_k, metadata, score_ctas(sms),
-                                    static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_metadata(P, seq_lens_q, seq_lens_k, metadata, score_ctas(sms, P.group_tokens),
+                                    score_first_ctas(sms, P.group_tokens), static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
 
@@ -304,9 +305,10 @@ qli_status score_impl(const qli_problem* p, const void* query, const void* key, 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     CUtensorMap tm;
     if (!encode_key_map(&tm, key, P)) return QLI_ERR_CUDA;
-    cudaError_t e = launch_score(P, &tm, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k,
-                                 block_table, metadata, reinterpret_cast<uint32_t*>(ws + W.scores_off),
-                                 reinterpret_cast<uint32_t*>(ws), score_ctas(sms), static_cast<cudaStream_t>(stream));
+    auto launch = P.group_tokens == 1 ? launch_score : launch_score_multi;
+    cudaError_t e = launch(P, &tm, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
+                           metadata, reinterpret_cast<uint32_t*>(ws + W.scores_off), reinterpret_cast<uint32_t*>(ws),
+                           score_ctas(sms, P.group_tokens), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return QLI_ERR_CUDA;
     *launched = true;
     return QLI_OK;

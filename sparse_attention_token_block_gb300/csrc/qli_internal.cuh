@@ -20,20 +20,29 @@ constexpr int kDim = 128;
 constexpr int kMaxSparse = 2048;
 
 // Score kernel tiling: a tile is 128 consecutive compressed keys of one batch (one TMEM lane per
-// key); a query group is up to kGroupTokens consecutive query tokens of one batch scored together
-// (MMA N = 64 * tokens).  Two score CTAs share each SM: separate CTAs keep more key copies in flight
-// than one CTA with twice the resources.
+// key); a query group is up to group_tokens consecutive query tokens of one batch scored together
+// (MMA N = 64 * tokens).  One query token per sequence (decode): groups of one token, two score CTAs
+// per SM (separate CTAs keep more key copies in flight than one CTA with twice the resources).
+// Several tokens per sequence: groups of up to kMultiTokens tokens, one CTA per SM with all of the
+// SM's tensor memory, each converted key tile serving every token of the group.
 constexpr int kTileKeys = 128;
-constexpr int kGroupTokens = 1;
-constexpr int kScoreCtasPerSm = 2;        // score CTAs resident per SM (the split is made for this)
+constexpr int kMultiTokens = 3;
 constexpr int kMaxCtas = 1024;            // bound on the split's CTA count (GB300 has 152 SMs)
 
-// Score CTAs of the split on a device with `sms` SMs: two per SM, less two so that a concurrently
-// resident metadata CTA never delays one (at most kMaxCtas)
-inline int score_ctas(int sms)
+// Score CTAs of the split on a device with `sms` SMs for groups of `gt` tokens: two per SM less two
+// for single-token groups (so that a concurrently resident metadata CTA never delays one), one per
+// SM otherwise (at most kMaxCtas)
+inline int score_ctas(int sms, int gt)
 {
-    const int g = 2 * sms - 2;
+    const int g = gt == 1 ? 2 * sms - 2 : sms;
     return g < 1 ? 1 : (g > kMaxCtas ? kMaxCtas : g);
+}
+
+// The CTAs of such a split that are the first to arrive on their SM
+inline int score_first_ctas(int sms, int gt)
+{
+    const int g = score_ctas(sms, gt);
+    return gt == 1 ? (sms < g ? sms : g) : g;
 }
 
 // Top-k: candidates held per row
@@ -59,6 +68,7 @@ enum MetaHeader {
     kMhRows = 6,        // output rows (B * S1 or T)
     kMhGroups = 7,      // query groups, live or not
     kMhLayoutHash = 8,  // hash of the problem fields the split depends on
+    kMhFirst = 9,       // G1: the first G1 CTAs are the first to arrive on their SM (see split_start)
     kMhWords = 16
 };
 constexpr int kBatchWords = 8;
@@ -121,7 +131,7 @@ struct Params {
     int32_t test_stall;    // test switch: 1 the score kernel's producer, 2 its converters do nothing
     int32_t complete_blocks;   // mode 3 visibility: 0 ceil((p + 1) / cmp), 1 floor((p + 1) / cmp)
     int32_t key_stride;        // elements between key pages
-    int32_t group_tokens;      // query tokens per group (1 .. kGroupTokens)
+    int32_t group_tokens;      // query tokens per group (1, or up to kMultiTokens)
     int64_t ld;            // score line stride
     MetaLayout meta;
 };
@@ -218,23 +228,23 @@ __host__ __device__ inline int32_t problem_hash(const Params& p)
 
 MetaLayout meta_layout(int64_t batch, int64_t max_groups);
 
-// The split of the T tiles over G score CTAs.  Two CTAs share each SM and the one that arrived first
-// (CTAs 0 .. (G + 2) / 2 - 1 for G = 2 x SMs - 2) streams its tiles about 9 % faster than the other
-// (measured: 0.91 against 1.00 us per 128-key tile on the long decode), so ranges are in
-// proportion 12 : 11 and both finish together.  W(c) is the weight of CTAs 0 .. c - 1; CTA c owns
-// tiles [T W(c) / W(G), T W(c + 1) / W(G)).  (T < 2^31 and W(G) < 2^14, so the product fits.)
+// The split of the T tiles over G score CTAs.  When two CTAs share each SM, the one that arrived
+// first (CTAs 0 .. G1 - 1) streams its tiles about 9 % faster than the other (measured: 0.91 against
+// 1.00 us per 128-key tile on the long decode), so their ranges are in proportion 12 : 11 and
+// both finish together; with G1 = G every range weighs the same.  W(c) is the weight of CTAs
+// 0 .. c - 1; CTA c owns tiles [T W(c) / W(G), T W(c + 1) / W(G)).  (T < 2^31 and W(G) < 2^14, so
+// the product fits.)
 constexpr int64_t kSplitFirst = 12, kSplitSecond = 11;
 
-__host__ __device__ inline int64_t split_weight(int64_t G, int64_t c)
+__host__ __device__ inline int64_t split_weight(int64_t G1, int64_t c)
 {
-    const int64_t h = (G + 2) / 2;
-    return c <= h ? c * kSplitFirst : h * kSplitFirst + (c - h) * kSplitSecond;
+    return c <= G1 ? c * kSplitFirst : G1 * kSplitFirst + (c - G1) * kSplitSecond;
 }
 
 // First tile of score CTA c's range
-__host__ __device__ inline int64_t split_start(int64_t T, int64_t G, int64_t c)
+__host__ __device__ inline int64_t split_start(int64_t T, int64_t G, int64_t G1, int64_t c)
 {
-    return (T * split_weight(G, c)) / split_weight(G, G);
+    return (T * split_weight(G1, c)) / split_weight(G1, G);
 }
 
 // Launch `kernel` with programmatic stream serialization: it may begin launching while the
@@ -259,12 +269,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Launchers (defined in the kernel translation units)
 cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
-                            int32_t* meta, int num_ctas, cudaStream_t st);
+                            int32_t* meta, int num_ctas, int first_ctas, cudaStream_t st);
 cudaError_t launch_score(const Params& p, const void* tmap_key, const void* query, const void* key,
                          const void* weights, const void* q_scale, const void* k_scale,
                          const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                          const int32_t* block_table, const int32_t* meta, uint32_t* scores,
                          uint32_t* err_word, int grid, cudaStream_t st);
+cudaError_t launch_score_multi(const Params& p, const void* tmap_key, const void* query, const void* key,
+                               const void* weights, const void* q_scale, const void* k_scale,
+                               const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                               const int32_t* block_table, const int32_t* meta, uint32_t* scores,
+                               uint32_t* err_word, int grid, cudaStream_t st);
 cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
                         const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
                         bool after_score, cudaStream_t st);

@@ -88,7 +88,7 @@ __device__ int64_t first_at_least(const View& a, int64_t n, int64_t key)
 
 __global__ void __launch_bounds__(kMetaThreads, 1)
     metadata_kernel(Params p, const int32_t* __restrict__ seq_lens_q,
-                    const int32_t* __restrict__ seq_lens_k, int32_t* __restrict__ meta, int G)
+                    const int32_t* __restrict__ seq_lens_k, int32_t* __restrict__ meta, int G, int G1)
 {
     extern __shared__ int32_t msm[];
     __shared__ uint64_t scan_sh[2 * kMetaWarps];
@@ -209,10 +209,10 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     if (!sl) __threadfence_block();
     __syncthreads();
 
-    // ---- the split: CTA c owns tiles [T c / G, T (c + 1) / G); its live groups are those from
+    // ---- the split: CTA c owns tiles [split_start(c), split_start(c + 1)); its live groups are those from
     // the one holding its first tile up to (excluding) the first that starts at or after its end
     for (int c = tid; c < G; c += kMetaThreads) {
-        const int64_t t0 = split_start(T, G, c), t1 = split_start(T, G, c + 1);
+        const int64_t t0 = split_start(T, G, G1, c), t1 = split_start(T, G, G1, c + 1);
         int32_t first = 0, end = 0;
         if (t1 > t0) {
             first = (int32_t)last_at_most(v_tb, live, t0);
@@ -224,16 +224,17 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
         int4* h = reinterpret_cast<int4*>(meta);
         h[0] = make_int4(kMetaMagic, G, (int32_t)live, (int32_t)T);
         h[1] = make_int4((int32_t)s_err, p.batch, p.rows, (int32_t)total_groups);
-        h[2] = make_int4(p.hash, 0, 0, 0);
+        h[2] = make_int4(p.hash, G1, 0, 0);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
-                            int32_t* meta, int num_ctas, cudaStream_t st)
+                            int32_t* meta, int num_ctas, int first_ctas, cudaStream_t st)
 {
     int G = num_ctas < kMaxCtas ? num_ctas : kMaxCtas;
+    const int G1 = first_ctas < 1 ? 1 : (first_ctas > G ? G : first_ctas);
     cudaError_t e = cudaFuncSetAttribute(metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kMetaSmemMax);
     if (e != cudaSuccess) return e;
@@ -242,7 +243,7 @@ cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const in
     const int64_t ng = p.meta.max_groups < kSmemLive ? p.meta.max_groups : kSmemLive;
     const size_t smem = (size_t)(6 * nb + ng) * 4 + 16;
     return launch_pdl(metadata_kernel, dim3(1), dim3(kMetaThreads), smem, st, p, seq_lens_q,
-                      seq_lens_k, meta, G);
+                      seq_lens_k, meta, G, G1);
 }
 
 }  // namespace qli

@@ -6,7 +6,8 @@ group_tokens consecutive live rows per batch; a group's tiles are ceil(n / 128),
 of its last row; live groups (at least one tile) are listed in batch and row order with their first
 tile in the concatenated tile sequence of T tiles; score CTA c of G owns tiles
 [T W(c) / W(G), T W(c + 1) / W(G)) and the live groups that range overlaps, where W(c) weighs the
-first (G + 2) / 2 CTAs 12 and the others 11 (the first CTA on each SM streams faster)."""
+first G1 CTAs (the first to arrive on their SM) 12 and the others 11.  Groups hold one token when a
+sequence has one query token, else up to three."""
 import numpy as np
 import pytest
 
@@ -18,12 +19,17 @@ pytestmark = pytest.mark.gpu
 MAGIC = 0x514C4932
 
 
-def split_start(T, G, c):
-    h = (G + 2) // 2
-
+def split_start(T, G, G1, c):
     def w(x):
-        return x * 12 if x <= h else h * 12 + (x - h) * 11
+        return x * 12 if x <= G1 else G1 * 12 + (x - G1) * 11
     return T * w(c) // w(G)
+
+
+def group_tokens(case):
+    """Query tokens per group: one for one query token per sequence, else up to three."""
+    if case.layout_q == "BSND":
+        return 1 if case.s1 <= 1 else min(case.s1, 3)
+    return 3
 
 
 @pytest.fixture(scope="module")
@@ -37,7 +43,7 @@ def qli():
     return Q
 
 
-def derive(case, G, gt=1):
+def derive(case, G, G1, gt):
     """Header fields, batch entries, live group records and CTA ranges of the definition."""
     B = case.batch
     batches, records = [], []
@@ -84,7 +90,7 @@ def derive(case, G, gt=1):
     ctas = []
     starts = [rec[6] for rec in records]
     for c in range(G):
-        t0, t1 = split_start(T, G, c), split_start(T, G, c + 1)
+        t0, t1 = split_start(T, G, G1, c), split_start(T, G, G1, c + 1)
         if t1 <= t0:
             ctas.append((0, 0))
             continue
@@ -122,9 +128,9 @@ def test_metadata_matches_definition(qli, name, make):
     d = W.to_device(case)
     qli.check(qli.metadata(p, d["seq_lens_q"], d["seq_lens_k"], meta), "metadata")
     m = meta.cpu().numpy()
-    G = int(m[1])
-    assert m[0] == MAGIC and 1 <= G <= 1024
-    ref = derive(case, G)
+    G, G1 = int(m[1]), int(m[9])
+    assert m[0] == MAGIC and 1 <= G <= 1024 and 1 <= G1 <= G
+    ref = derive(case, G, G1, group_tokens(case))
     assert int(m[2]) == ref["live"] and int(m[3]) == ref["T"]
     assert int(m[4]) == ref["err"] and int(m[5]) == case.batch and int(m[6]) == case.rows
     assert int(m[7]) == ref["groups"]
@@ -140,7 +146,7 @@ def test_metadata_matches_definition(qli, name, make):
     # every live group's tiles are covered exactly once by the CTAs' (group, tile range) units
     cover = np.zeros(ref["T"], np.int64)
     for c in range(G):
-        t0, t1 = split_start(ref["T"], G, c), split_start(ref["T"], G, c + 1)
+        t0, t1 = split_start(ref["T"], G, G1, c), split_start(ref["T"], G, G1, c + 1)
         f, e = ctas[c]
         for g in range(f, e):
             tb, tn = recs[g][6], recs[g][7]
