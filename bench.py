@@ -63,9 +63,10 @@ def parse():
                     help="time stream launches instead of the captured execution plan")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the clock-sampling load window")
-    ap.add_argument("--op", default="indexer", choices=["indexer", "quantize", "gather"],
+    ap.add_argument("--op", default="indexer", choices=["indexer", "quantize", "gather", "mma"],
                     help="indexer: the indexer step (default); quantize: the upstream quantizer; "
-                         "gather: the downstream sparse-attention gather")
+                         "gather: the downstream sparse-attention gather; mma: the rate of the score "
+                         "kernel's tensor-core instruction form (libqli_peak.so)")
     ap.add_argument("--entry-bytes", type=int, default=512, help="KV entry size of --op gather")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload timings of the other configurations")
@@ -590,6 +591,51 @@ def time_workload(Q, case, dev, flush_l2, steps, warmup):
             "roofline": score_roofline(stats, stage["score"])}
 
 
+def run_mma(args, rank, world, local):
+    """Rate of tcgen05.mma kind::f16 (M 128, K 16, fp32 accumulator in tensor memory) with A from
+    tensor memory -- the score kernel's form -- or from shared memory, N 64 .. 256: one CTA per SM
+    issuing MMAs back to back.  Prints one JSON line per (A source, N)."""
+    import ctypes
+    import torch
+    from sparse_attention_token_block_gb300 import build as B
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    L = ctypes.CDLL(B.PEAK_LIB)
+    L.qli_peak_mma_f16.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p] * 4
+    L.qli_peak_mma_f16.restype = ctypes.c_int
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
+    ns = torch.zeros(sms, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    tpeak, tkind = tensor_peak()
+    iters = 8192
+    out = []
+    for a_tmem in (1, 0):
+        for n in (64, 128, 192, 256):
+            best = None
+            for _ in range(max(3, args.warmup)):
+                assert L.qli_peak_mma_f16(a_tmem, n, iters, sms, cyc.data_ptr(), ns.data_ptr(), err.data_ptr(),
+                                          stream) == 0
+                torch.cuda.synchronize()
+                assert int(err.item()) == 0, "a bounded wait gave up"
+                c = cyc.cpu().numpy().astype(np.float64)
+                t = ns.cpu().numpy().astype(np.float64)
+                flop = 2.0 * 128 * n * 16 * iters
+                tf = sms * flop / (t.max() * 1e-9) / 1e12
+                if best is None or tf > best["tflops"]:
+                    best = {"a_operand": "tensor memory" if a_tmem else "shared memory", "n": n,
+                            "tflops": tf, "frac_of_bf16_peak": tf / tpeak,
+                            "flop_per_sm_cycle": float(np.median(flop / c)),
+                            "sm_mhz_implied": float(np.median(c / t * 1e3))}
+            out.append(best)
+    if rank == 0:
+        print(json.dumps({"metric": "tcgen05.mma kind::f16 rate, M 128 K 16, one CTA per SM", "unit": "TFLOP/s",
+                          "bf16_peak": tpeak, "bf16_peak_source": tkind, "sms": sms, "iters_per_cta": iters,
+                          "results": out}))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -603,6 +649,9 @@ def main():
         return
     if args.op == "gather":
         run_gather(args, rank, world, local)
+        return
+    if args.op == "mma":
+        run_mma(args, rank, world, local)
         return
     import torch
     import sparse_attention_token_block_gb300 as Q

@@ -19,9 +19,12 @@ LIB = os.path.join(HERE, "libqli.so")
 # the testing build: the same objects except the host API, compiled with QLI_TESTING (it adds the
 # failure-detection test switch of include/qli_testing.h); the product library has no switch
 TEST_LIB = os.path.join(HERE, "libqli_testing.so")
+PEAK_LIB = os.path.join(HERE, "libqli_peak.so")
 SOURCES = ["qli_api.cu", "qli_metadata.cu", "qli_score.cu", "qli_score_multi.cu", "qli_topk.cu", "qli_noalloc.cu", "qli_plan.cu", "qli_quant.cu", "qli_gather.cu"]
 HEADERS = ["qli_internal.cuh", "qli_ptx.cuh", "qli_score.cuh"]
 TEST_SOURCE = "qli_api.cu"
+# the tensor-core rate micro-benchmark (include/qli_peak.h), a library of its own
+PEAK_SOURCE = "qli_peak.cu"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -57,6 +60,10 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
         if ptxas_info or _newer(o, [s] + hdrs):
             extra = ["-Xptxas", "-v"] if ptxas_info else []
             jobs.append((src, [nvcc(), "-c", s, "-o", o] + _flags(extra)))
+    s = os.path.join(CSRC, PEAK_SOURCE)
+    o_peak = os.path.join(OBJ, "qli_peak.o")
+    if ptxas_info or _newer(o_peak, [s] + hdrs + [os.path.join(ROOT, "include", "qli_peak.h")]):
+        jobs.append((PEAK_SOURCE, [nvcc(), "-c", s, "-o", o_peak] + _flags(["-Xptxas", "-v"] if ptxas_info else [])))
     s = os.path.join(CSRC, TEST_SOURCE)
     o_test = os.path.join(OBJ, TEST_SOURCE.replace(".cu", "_testing.o"))
     if _newer(o_test, [s] + hdrs):
@@ -76,7 +83,8 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
                     raise RuntimeError("nvcc failed on %s" % name)
     objs = [os.path.join(OBJ, s.replace(".cu", ".o")) for s in SOURCES]
     test_objs = [o_test if s == TEST_SOURCE else o for s, o in zip(SOURCES, objs)]
-    for lib, parts in ((LIB, objs), (TEST_LIB, test_objs)):
+    peak_objs = [os.path.join(OBJ, "qli_peak.o")]
+    for lib, parts in ((LIB, objs), (TEST_LIB, test_objs), (PEAK_LIB, peak_objs)):
         if _newer(lib, parts):
             tmp = lib + ".tmp%d" % os.getpid()
             cmd = [nvcc(), "-shared", "-o", tmp] + parts + ARCH + [

@@ -1,0 +1,111 @@
+// qli_peak.cu -- rate of the score kernel's tensor-core contraction form (see include/qli_peak.h):
+// tcgen05.mma kind::f16, M = 128, K = 16, N columns, A from tensor memory or shared memory, fp32
+// accumulator in tensor memory.  One thread per CTA issues the MMAs back to back into one
+// accumulator, so the measured interval is the tensor pipe's own throughput for that shape.
+#include <cuda_runtime.h>
+
+#include "qli_peak.h"
+#include "qli_ptx.cuh"
+
+namespace {
+
+using namespace qli;
+
+constexpr int kThreads = 128;
+constexpr int kMaxN = 256;
+constexpr int kAbytes = 128 * 256;                 // A: 128 rows x 128 fp16, two 64-dim blocks
+constexpr int kBbytes = kMaxN * 256;               // B: N rows x 128 fp16, two 64-dim blocks
+// more than half of an SM's shared memory, so that exactly one CTA (holding all 512 tensor-memory
+// columns) runs per SM
+constexpr int kSmem = 120 * 1024;
+static_assert(kAbytes + kBbytes + 64 + 1024 <= kSmem, "shared-memory carve-up");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mma_rate_kernel(int a_tmem, int n, int iters, unsigned long long* cycles, unsigned long long* nanos,
+                    unsigned int* err)
+{
+    extern __shared__ uint8_t peak_smem[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(peak_smem) + 1023) & ~uintptr_t(1023));
+    uint8_t* a_s = base;
+    uint8_t* b_s = base + kAbytes;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(b_s + kBbytes);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    // operands: fp16 1.0 everywhere (the values do not change the rate)
+    uint32_t* w = reinterpret_cast<uint32_t*>(base);
+    for (int i = tid; i < (kAbytes + n * 256) / 4; i += kThreads) w[i] = 0x3C003C00u;
+    if (tid == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(slot, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *slot;
+    if (a_tmem) {
+        // A in columns [0, 64): each warp writes its 32 lanes
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0x3C003C00u;
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        QLI_TMEM_ST_X32(tmem + lane_base, r);
+        QLI_TMEM_ST_X32(tmem + lane_base + 32, r);
+        ptx::tmem_wait_st();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (tid == 0) {
+        const uint32_t idesc = ptx::idesc_f16_f32(128, (uint32_t)n);
+        const uint32_t d = tmem + 64;                       // D in columns [64, 64 + n)
+        const uint32_t a0 = ptx::smem_addr(a_s), b0 = ptx::smem_addr(b_s);
+        const unsigned long long c0 = clock64();
+        const unsigned long long g0 = ptx::globaltimer();
+        for (int i = 0; i < iters; ++i) {
+            const int kk = i & 7;                           // the 8 K steps of a 128-dim row
+            const uint64_t bd = ptx::sdesc_kmajor_sw128(b0 + (kk >> 2) * (n * 128) + (kk & 3) * 32);
+            if (a_tmem) {
+                ptx::mma_f16_ts(d, tmem + kk * 8, bd, idesc, i > 0 ? 1u : 0u);
+            } else {
+                const uint64_t ad = ptx::sdesc_kmajor_sw128(a0 + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
+                ptx::mma_f16_ss(d, ad, bd, idesc, i > 0 ? 1u : 0u);
+            }
+        }
+        ptx::mma_commit(bar);
+        // bounded wait for every MMA to complete (about 1 s); on expiry record the error and wait
+        // once more, bounded, before the tensor memory is released
+        bool ok = false;
+        for (long long spin = 0; spin < (1ll << 26) && !ok; ++spin) ok = ptx::mbar_try_wait(bar, 0);
+        const unsigned long long c1 = clock64();
+        const unsigned long long g1 = ptx::globaltimer();
+        if (!ok) {
+            atomicOr(err, 1u);
+            for (long long spin = 0; spin < (1ll << 26) && !ok; ++spin) ok = ptx::mbar_try_wait(bar, 0);
+        }
+        cycles[blockIdx.x] = c1 - c0;
+        nanos[blockIdx.x] = g1 - g0;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 0) ptx::tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+extern "C" int qli_peak_mma_f16(int a_from_tmem, int n, int iters, int ctas, unsigned long long* cycles,
+                                unsigned long long* nanos, unsigned int* err, void* stream)
+{
+    if (n < 16 || n > kMaxN || n % 16 != 0 || iters < 1 || ctas < 1 || !cycles || !nanos || !err)
+        return (int)cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return (int)e;
+    mma_rate_kernel<<<ctas, kThreads, kSmem, static_cast<cudaStream_t>(stream)>>>(a_from_tmem ? 1 : 0, n, iters,
+                                                                                  cycles, nanos, err);
+    return (int)cudaGetLastError();
+}

@@ -9,7 +9,7 @@
 //
 // A persistent CTA walks the units the metadata assigned to it.  A unit is a query group (up to
 // QLI_SCORE_GT tokens of one batch, 64 heads each) and a range of its compressed keys, cut into tiles
-// of 128 keys.  Ten warps, four roles, connected by mbarriers:
+// of 128 keys.  Ten warps (fourteen with two epilogue groups), four roles, connected by mbarriers:
 //
 //   producer warp    per unit: bulk-copies the group's query codes, weights and query scales;
 //                    per tile: TMA-loads the 128 key rows (128 B each, 128-byte swizzle) from the
@@ -24,7 +24,8 @@
 //   MMA thread       D[128 keys x 64*tokens] = K_tile[128 x 128] . Q_group^T, tcgen05 kind::f16,
 //                    A from tensor memory, B from shared memory, fp32 accumulation (int8 products
 //                    and sums are integers below 2^21: exact), two D buffers;
-//   epilogue warps   (4) one thread per key reads its row of D and forms, per token,
+//   epilogue warps   (4 per group; tile i goes to group i mod groups) one thread per key reads
+//                    its row of D and forms, per token,
 //                    score = sK * sum_h (W[h]*|sQ[h]|) * relu_or_min(dot'_h), where dot' uses the
 //                    negated query head when sQ[h] < 0 -- algebraically the README's
 //                    sum_h W[h] * ReLU(sQ[h] * sK * dot_h) -- and writes it as an order-preserving
@@ -51,13 +52,17 @@ constexpr int kGT = QLI_SCORE_GT;                 // most query tokens per group
 constexpr int kCtasPerSm = kGT == 1 ? 2 : 1;      // resident score CTAs per SM
 constexpr int kStages = kGT == 1 ? 4 : 5;         // key ring depth
 constexpr int kScaleSlots = 10;                  // scale ring depth (released by the epilogue)
-constexpr int kGroups = 1;                       // converter and epilogue groups; tile i -> i % groups
+constexpr int kGroups = 1;                       // converter groups; tile i -> i % groups
+// epilogue groups: tile i -> group i % kEpiGroups, which always drains D buffer i % kNumD.  Groups
+// of several tokens give each tile kGT times the epilogue work, so that build has two groups.
+constexpr int kEpiGroups = kGT == 1 ? 1 : 2;
 constexpr int kNumA = 2;                         // A buffers in tensor memory
 constexpr int kNumD = 2;                         // D buffers in tensor memory
+static_assert(kNumD % kEpiGroups == 0, "an epilogue group owns its D buffers");
 constexpr int kGroupThreads = 128;               // 4 warps, one key (TMEM lane) per thread
 constexpr int kConvWarp0 = 0;                    // converter group g: warps 4g .. 4g+3
 constexpr int kEpiWarp0 = 4 * kGroups;           // epilogue group g: warps kEpiWarp0 + 4g ..
-constexpr int kProducerWarp = 8 * kGroups;
+constexpr int kProducerWarp = kEpiWarp0 + 4 * kEpiGroups;
 constexpr int kMmaWarp = kProducerWarp + 1;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kDcols = kHeads * kGT;        // one D buffer (fp32 per lane)
@@ -516,7 +521,7 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp
                                                                       x.lc, x.r0 + tt, p.complete_blocks))
                            : 0;
         for (int t = 0; t < x.ntiles; ++t, ++tile_i) {
-            if ((int)(tile_i % kGroups) != grp) continue;
+            if ((int)(tile_i % kEpiGroups) != grp) continue;
             const uint32_t db = tile_i % kNumD;
             const int ss = tile_i % kScaleSlots;
             if (!wait_bar(&S.bars[kBarDfull + db], (tile_i / kNumD) & 1, S.abort, a.err)) return;
@@ -532,15 +537,12 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp
                     const float4* w4 = reinterpret_cast<const float4*>(wq + tt * kHeads);
                     // heads h, h+1 in acc0 and h+2, h+3 in acc1 (packed pairs: four fma chains)
                     uint64_t acc0 = 0, acc1 = 0;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t d[32];
-                        QLI_TMEM_LD_X32(tmem + lane_base + kDcol0 + db * kDcols + tt * 64 + half * 32, d);
-                        ptx::tmem_wait_ld();
+                    // the weighted ReLU (min for a negative sK) sum of heads [h0, h0 + len)
+                    auto accumulate = [&](const uint32_t* d, int h0, int len) {
                         if (sk >= 0.0f) {
 #pragma unroll
-                            for (int h = 0; h < 32; h += 4) {
-                                const float4 w = w4[(half * 32 + h) >> 2];
+                            for (int h = 0; h < len; h += 4) {
+                                const float4 w = w4[(h0 + h) >> 2];
                                 acc0 = ptx::fma2(ptx::pack2(w.x, w.y),
                                                  ptx::pack2(fmaxf(__uint_as_float(d[h]), 0.0f),
                                                             fmaxf(__uint_as_float(d[h + 1]), 0.0f)),
@@ -552,8 +554,8 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp
                             }
                         } else {
 #pragma unroll
-                            for (int h = 0; h < 32; h += 4) {
-                                const float4 w = w4[(half * 32 + h) >> 2];
+                            for (int h = 0; h < len; h += 4) {
+                                const float4 w = w4[(h0 + h) >> 2];
                                 acc0 = ptx::fma2(ptx::pack2(w.x, w.y),
                                                  ptx::pack2(fminf(__uint_as_float(d[h]), 0.0f),
                                                             fminf(__uint_as_float(d[h + 1]), 0.0f)),
@@ -564,6 +566,23 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp
                                                  acc1);
                             }
                         }
+                    };
+                    const uint32_t dcol = tmem + lane_base + kDcol0 + db * kDcols + tt * 64;
+                    if constexpr (kGT == 1) {
+                        // two loads of 32 heads: the one-token build has registers for 32 at a time
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t d[32];
+                            QLI_TMEM_LD_X32(dcol + half * 32, d);
+                            ptx::tmem_wait_ld();
+                            accumulate(d, half * 32, 32);
+                        }
+                    } else {
+                        // the token's 64 head dots in one load, one wait
+                        uint32_t d[64];
+                        QLI_TMEM_LD_X64(dcol, d);
+                        ptx::tmem_wait_ld();
+                        accumulate(d, 0, 64);
                     }
                     float a0, a1, a2, a3;
                     ptx::unpack2(acc0, a0, a1);
@@ -601,7 +620,7 @@ __device__ void init_barriers(const Shared& S)
         ptx::mbar_init(&S.bars[kBarQrfull + i], 1);
         ptx::mbar_init(&S.bars[kBarQrempty + i], 4);
         ptx::mbar_init(&S.bars[kBarQfull + i], 4);
-        ptx::mbar_init(&S.bars[kBarQempty + i], 4 * kGroups);
+        ptx::mbar_init(&S.bars[kBarQempty + i], 4 * kEpiGroups);   // every epilogue warp, per unit
     }
     for (int i = 0; i < kNumA; ++i) {
         ptx::mbar_init(&S.bars[kBarAfull + i], 4);

@@ -32,6 +32,15 @@ def test_exports_every_declared_symbol(Q):
         assert not hasattr(Q.lib, n), n
 
 
+def test_measurement_library_exports_its_symbol(Q):
+    from sparse_attention_token_block_gb300 import build as B
+    L = ctypes.CDLL(B.PEAK_LIB)
+    for n in declared_symbols("qli_peak.h"):
+        assert hasattr(L, n), n
+    for n in declared_symbols("qli_peak.h"):
+        assert not hasattr(Q.lib, n), n
+
+
 def test_testing_build_exports_product_and_testing_symbols(Q):
     L = ctypes.CDLL(Q.TESTING_LIB_PATH)
     for n in declared_symbols() + declared_symbols("qli_testing.h"):
