@@ -329,9 +329,12 @@ qli_status topk_impl(const qli_problem* p, const int32_t* block_table, const int
     if (!sparse_indices) return QLI_ERR_INVALID_ARG;
     if (P.batch > 0 && !block_table) return QLI_ERR_INVALID_ARG;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    cudaError_t e = launch_topk(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),
-                                reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values, after_score,
-                                static_cast<cudaStream_t>(stream));
+    // more rows than SMs, each of at most kTopkSmallRows keys (ld bounds every row's visible keys):
+    // the two-per-SM form for throughput; few rows: the 1024-thread form for latency
+    auto launch = (P.ld <= kTopkSmallRows && P.rows > sms) ? launch_topk_small : launch_topk;
+    cudaError_t e = launch(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),
+                           reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values, after_score,
+                           static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
 
