@@ -69,6 +69,7 @@ enum MetaHeader {
     kMhGroups = 7,      // query groups, live or not
     kMhLayoutHash = 8,  // hash of the problem fields the split depends on
     kMhFirst = 9,       // G1: the first G1 CTAs are the first to arrive on their SM (see split_start)
+    kMhUnitCost = 10,   // kUnitCost: virtual tiles charged to each live group in the split
     kMhWords = 16
 };
 constexpr int kBatchWords = 8;
@@ -82,9 +83,11 @@ enum BatchEntry {
     kBeGroupBase = 6,   // index of the batch's first group
 };
 // A live query group (group_tokens consecutive live rows of one batch whose last row sees at least
-// one key), in batch and row order; its key tiles are tiles [first tile, first tile + tiles) of the
-// concatenated tile sequence that the split cuts into G equal ranges, one per score CTA.  The
-// batch's fields travel with the group so that a reader needs one 32-byte load.
+// one key), in batch and row order.  The split cuts a sequence in which every live group occupies
+// kUnitCost virtual tiles (the cost of loading and converting its query, which a CTA pays per group
+// it touches) followed by its key tiles; the record holds the position of its first key tile in
+// that sequence.  The batch's fields travel with the group so that a reader needs one 32-byte load.
+constexpr int kUnitCost = 2;
 constexpr int kGroupWords = 8;
 enum GroupRecord {
     kGrBatch = 0,
@@ -93,11 +96,11 @@ enum GroupRecord {
     kGrSq = 3,          // Sq_b
     kGrSk = 4,          // Sk_b
     kGrLc = 5,          // Lc_b
-    kGrTile = 6,        // first tile of the group in the concatenated sequence
+    kGrTile = 6,        // position of the group's first key tile in the split's sequence
     kGrTiles = 7,       // tiles of the group: ceil(visible keys of its last row / kTileKeys)
 };
-// Per score CTA c (two words): the live groups [first, end) that its tile range
-// [T c / G, T (c + 1) / G) overlaps (first = end when the range is empty).
+// Per score CTA c (two words): the live groups [first, end) whose key tiles its range of the
+// sequence overlaps (first = end when it overlaps none).
 constexpr int kCtaWords = 2;
 
 struct MetaLayout {

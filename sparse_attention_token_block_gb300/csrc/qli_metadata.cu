@@ -6,12 +6,13 @@
 //   * per batch: live query rows Sq_b, key tokens Sk_b, compressed keys Lc_b, first output row,
 //     validity, query-group count and first group index (what the top-k reads per row);
 //   * one record per live query group -- group_tokens consecutive live rows of one batch whose last
-//     row sees at least one key -- with the batch's fields, the group's first tile in the
-//     concatenated tile sequence of all live groups, and its tile count ceil(n_last / 128), n_last
-//     being the visible-key count of its last row (the largest in the group under either mask);
-//   * per score CTA c ("each core's start point"): the range [first, end) of live groups that its
-//     tile range [T c / G, T (c + 1) / G) overlaps.  A score CTA derives its units -- (group,
-//     tile range) pairs -- from these records alone.
+//     row sees at least one key -- with the batch's fields, its tile count ceil(n_last / 128), n_last
+//     being the visible-key count of its last row (the largest in the group under either mask), and
+//     the position of its first tile in the sequence the split cuts: every live group, in order,
+//     as kUnitCost virtual tiles (its query load) followed by its key tiles, T positions in all;
+//   * per score CTA c ("each core's start point"): the range [first, end) of live groups whose key
+//     tiles its range [split_start(c), split_start(c + 1)) of the sequence overlaps.  A score CTA
+//     derives its units -- (group, tile range) pairs -- from these records alone.
 //
 // The work is a handful of block-wide passes: per-batch extents (one read of the lengths), a scan
 // of the groups per batch, one pass over the groups with a scan of the (live, tiles) pairs that
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
         for (int64_t g = g_lo; g < g_hi; ++g) {
             b = advance(b, g);
             const int64_t t = tiles_of(b, g, &r0);
-            if (t > 0) mine += (uint64_t(1) << 32) + (uint64_t)t;
+            if (t > 0) mine += (uint64_t(1) << 32) + (uint64_t)(t + kUnitCost);
         }
     }
     uint64_t tot;
@@ -200,23 +201,25 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
             if (t == 0) continue;
             int4* r = reinterpret_cast<int4*>(rec + li * kGroupWords);
             r[0] = make_int4((int32_t)b, (int32_t)r0, v_fr[b] + (int32_t)r0, v_sq[b]);
-            r[1] = make_int4(v_sk[b], v_lc[b], (int32_t)tile, (int32_t)t);
-            if (sl) v_tb[li] = (int32_t)tile;
+            r[1] = make_int4(v_sk[b], v_lc[b], (int32_t)(tile + kUnitCost), (int32_t)t);
+            if (sl) v_tb[li] = (int32_t)(tile + kUnitCost);
             ++li;
-            tile += t;
+            tile += t + kUnitCost;
         }
     }
     if (!sl) __threadfence_block();
     __syncthreads();
 
-    // ---- the split: CTA c owns tiles [split_start(c), split_start(c + 1)); its live groups are those from
-    // the one holding its first tile up to (excluding) the first that starts at or after its end
+    // ---- the split: CTA c owns positions [split_start(c), split_start(c + 1)) of the sequence; its
+    // live groups run from the one whose block (virtual tiles, then key tiles) holds its first
+    // position to (excluding) the first whose key tiles start at or after its end -- each of them
+    // has key tiles inside the range, and first = end when the range holds only virtual tiles
     for (int c = tid; c < G; c += kMetaThreads) {
         const int64_t t0 = split_start(T, G, G1, c), t1 = split_start(T, G, G1, c + 1);
         int32_t first = 0, end = 0;
         if (t1 > t0) {
-            first = (int32_t)last_at_most(v_tb, live, t0);
-            end = (int32_t)first_at_least(v_tb, live, t1);
+            first = (int32_t)last_at_most(v_tb, live, t0 + kUnitCost);
+            end = (int32_t)max((int64_t)first, first_at_least(v_tb, live, t1));
         }
         reinterpret_cast<int2*>(cta)[c] = make_int2(first, end);
     }
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
         int4* h = reinterpret_cast<int4*>(meta);
         h[0] = make_int4(kMetaMagic, G, (int32_t)live, (int32_t)T);
         h[1] = make_int4((int32_t)s_err, p.batch, p.rows, (int32_t)total_groups);
-        h[2] = make_int4(p.hash, G1, 0, 0);
+        h[2] = make_int4(p.hash, G1, kUnitCost, 0);
     }
 }
 

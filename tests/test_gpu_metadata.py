@@ -3,11 +3,12 @@ definition (needs a GB300).
 
 Definition (the metadata call: the cores used and each core's start point): query groups of
 group_tokens consecutive live rows per batch; a group's tiles are ceil(n / 128), n the visible keys
-of its last row; live groups (at least one tile) are listed in batch and row order with their first
-tile in the concatenated tile sequence of T tiles; score CTA c of G owns tiles
-[T W(c) / W(G), T W(c + 1) / W(G)) and the live groups that range overlaps, where W(c) weighs the
-first G1 CTAs (the first to arrive on their SM) 12 and the others 11.  Groups hold one token when a
-sequence has one query token, else up to three."""
+of its last row; live groups (at least one tile) are listed in batch and row order.  The split cuts
+a sequence of T positions in which every live group occupies U virtual positions (its query load)
+followed by its tiles; a record holds the position of the group's first tile.  Score CTA c of G
+owns positions [T W(c) / W(G), T W(c + 1) / W(G)) and the live groups whose tiles that range
+overlaps, where W(c) weighs the first G1 CTAs (the first to arrive on their SM) 12 and the others
+11.  Groups hold one token when a sequence has one query token, else up to three."""
 import numpy as np
 import pytest
 
@@ -43,7 +44,7 @@ def qli():
     return Q
 
 
-def derive(case, G, G1, gt):
+def derive(case, G, G1, gt, U):
     """Header fields, batch entries, live group records and CTA ranges of the definition."""
     B = case.batch
     batches, records = [], []
@@ -84,8 +85,8 @@ def derive(case, G, G1, gt):
             n = oracle.visible(case, sq, sk, rl)
             tiles = -(-n // 128)
             if tiles:
-                records.append([b, r0, first + r0, sq, sk, lc, T, tiles])
-                T += tiles
+                records.append([b, r0, first + r0, sq, sk, lc, T + U, tiles])
+                T += U + tiles
         gbase += groups
     ctas = []
     starts = [rec[6] for rec in records]
@@ -94,8 +95,8 @@ def derive(case, G, G1, gt):
         if t1 <= t0:
             ctas.append((0, 0))
             continue
-        first = max(i for i, s in enumerate(starts) if s <= t0)
-        end = next((i for i, s in enumerate(starts) if s >= t1), len(starts))
+        first = max(i for i, s in enumerate(starts) if s - U <= t0)       # block holding t0
+        end = max(first, next((i for i, s in enumerate(starts) if s >= t1), len(starts)))
         ctas.append((first, end))
     return dict(live=len(records), T=T, err=err, groups=gbase, batches=batches, records=records, ctas=ctas)
 
@@ -128,9 +129,9 @@ def test_metadata_matches_definition(qli, name, make):
     d = W.to_device(case)
     qli.check(qli.metadata(p, d["seq_lens_q"], d["seq_lens_k"], meta), "metadata")
     m = meta.cpu().numpy()
-    G, G1 = int(m[1]), int(m[9])
-    assert m[0] == MAGIC and 1 <= G <= 1024 and 1 <= G1 <= G
-    ref = derive(case, G, G1, group_tokens(case))
+    G, G1, U = int(m[1]), int(m[9]), int(m[10])
+    assert m[0] == MAGIC and 1 <= G <= 1024 and 1 <= G1 <= G and U == 2
+    ref = derive(case, G, G1, group_tokens(case), U)
     assert int(m[2]) == ref["live"] and int(m[3]) == ref["T"]
     assert int(m[4]) == ref["err"] and int(m[5]) == case.batch and int(m[6]) == case.rows
     assert int(m[7]) == ref["groups"]
@@ -143,7 +144,8 @@ def test_metadata_matches_definition(qli, name, make):
     rec_off = (cta_off + 2 * 1024 + 3) & ~3
     recs = m[rec_off:rec_off + 8 * ref["live"]].reshape(-1, 8)
     assert np.array_equal(recs, np.array(ref["records"], dtype=np.int64).reshape(-1, 8))
-    # every live group's tiles are covered exactly once by the CTAs' (group, tile range) units
+    # every live group's tiles are covered exactly once by the CTAs' (group, tile range) units,
+    # each unit holds at least one tile, and no virtual position is covered
     cover = np.zeros(ref["T"], np.int64)
     for c in range(G):
         t0, t1 = split_start(ref["T"], G, G1, c), split_start(ref["T"], G, G1, c + 1)
@@ -153,4 +155,7 @@ def test_metadata_matches_definition(qli, name, make):
             lo, hi = max(t0, tb), min(t1, tb + tn)
             assert hi > lo
             cover[lo:hi] += 1
-    assert (cover == 1).all()
+    real = np.zeros(ref["T"], bool)
+    for r in recs:
+        real[r[6]:r[6] + r[7]] = True
+    assert (cover[real] == 1).all() and (cover[~real] == 0).all()
