@@ -696,12 +696,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
     int64_t pages = 0;
     int32_t pg_first = 0;
     bool bad = false;
-    // the row's place and its pages: every page the batch's rows can see must lie in the pool; the
-    // first entry per thread is loaded now and checked after the selection, the rest (rows of more
-    // than kThreads pages) at once
-    auto prepare = [&](int64_t row) {
+    auto read_header = [&]() {
+        meta_ok = __ldcg(a.meta + kMhMagic) == kMetaMagic && __ldcg(a.meta + kMhLayoutHash) == p.hash;
+    };
+    auto locate = [&](int64_t row) {
         ri = row_info(a, meta_ok, row);
         pages = ri.n > 0 ? ceil_div64(ri.lc, p.block_size) : 0;
+    };
+    // every page the batch's rows can see must lie in the pool: the first entry per thread is
+    // loaded here and checked after the selection, the rest (rows of more than kThreads pages) at
+    // once
+    auto load_pages = [&]() {
         const int32_t* table = a.block_table + (ri.b < 0 ? 0 : ri.b) * p.max_blocks_per_seq;
         pg_first = tid < pages ? __ldcg(table + tid) : 0;
         bad = false;
@@ -710,25 +715,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
             bad |= pg < 0 || pg >= p.num_blocks;
         }
     };
-    auto read_header = [&]() {
-        meta_ok = __ldcg(a.meta + kMhMagic) == kMetaMagic && __ldcg(a.meta + kMhLayoutHash) == p.hash;
-    };
-    if (a.early) {
+    // after the score kernel the first row's place and pages are read before the wait; a
+    // standalone launch reads them after it and loads the pages once the row's copy is issued
+    const bool early = a.early && blockIdx.x < p.rows;
+    if (early) {
         read_header();
-        if (blockIdx.x < p.rows) prepare(blockIdx.x);
+        locate(blockIdx.x);
+        load_pages();
     }
     // the score lines (and, for a standalone launch, the metadata) come from earlier kernels; the
     // next call may overwrite them only after this grid completes (it waits too)
     ptx::pdl_wait();
     ptx::pdl_launch_dependents();
-    if (!a.early) {
-        read_header();
-        if (blockIdx.x < p.rows) prepare(blockIdx.x);
-    }
+    if (!a.early) read_header();
 
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
         int32_t* out = a.out + row * k;
-        if (row != blockIdx.x) prepare(row);
+        const bool loaded = early && row == blockIdx.x;
+        if (!loaded) locate(row);
         const int64_t n = ri.n;
         const uint32_t* line = a.scores + row * p.ld;
         const int need = (int)(n < k ? n : k);
@@ -744,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
             }
         }
         __syncthreads();
+        if (!loaded) load_pages();
         bool copy_ok = true;
         if (cached) {
             copy_ok = wait_copy(S.bar, bar_parity);   // bounded wait for the line
