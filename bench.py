@@ -592,9 +592,10 @@ def time_workload(Q, case, dev, flush_l2, steps, warmup):
 
 
 def run_mma(args, rank, world, local):
-    """Rate of tcgen05.mma kind::f16 (M 128, K 16, fp32 accumulator in tensor memory) with A from
-    tensor memory -- the score kernel's form -- or from shared memory, N 64 .. 256: one CTA per SM
-    issuing MMAs back to back.  Prints one JSON line per (A source, N)."""
+    """Rate of tcgen05.mma kind::f16 (K 16, fp32 accumulators in tensor memory): M 128 with A from
+    tensor memory -- the score kernel's form -- or from shared memory, M 64 with A from shared
+    memory; N 64 .. 256; MMAs issued back to back by one thread per CTA into one accumulator or
+    cycled over several independent ones; one or two CTAs per SM.  Prints one JSON line."""
     import ctypes
     import torch
     from sparse_attention_token_block_gb300 import build as B
@@ -602,36 +603,42 @@ def run_mma(args, rank, world, local):
     dev = torch.device("cuda", local)
     B.build()
     L = ctypes.CDLL(B.PEAK_LIB)
-    L.qli_peak_mma_f16.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p] * 4
+    L.qli_peak_mma_f16.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p] * 4
     L.qli_peak_mma_f16.restype = ctypes.c_int
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
-    ns = torch.zeros(sms, dtype=torch.int64, device=dev)
+    cyc = torch.zeros(2 * sms, dtype=torch.int64, device=dev)
+    ns = torch.zeros(2 * sms, dtype=torch.int64, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
     tpeak, tkind = tensor_peak()
     iters = 8192
+    # (A from tensor memory, M, N, accumulators, CTAs per SM)
+    shapes = [(1, 128, n, 1, 1) for n in (64, 128, 192, 256)] + [(0, 128, n, 1, 1) for n in (64, 128, 192, 256)]
+    shapes += [(1, 128, 64, c, 1) for c in (2, 4, 6)] + [(1, 128, 128, c, 1) for c in (2, 3)]
+    shapes += [(1, 128, 64, c, 2) for c in (1, 2)] + [(0, 128, 64, 4, 1)]
+    shapes += [(0, 64, n, c, 1) for n in (64, 128) for c in (1, 2)] + [(0, 64, 256, 1, 1)]
     out = []
-    for a_tmem in (1, 0):
-        for n in (64, 128, 192, 256):
-            best = None
-            for _ in range(max(3, args.warmup)):
-                assert L.qli_peak_mma_f16(a_tmem, n, iters, sms, cyc.data_ptr(), ns.data_ptr(), err.data_ptr(),
-                                          stream) == 0
-                torch.cuda.synchronize()
-                assert int(err.item()) == 0, "a bounded wait gave up"
-                c = cyc.cpu().numpy().astype(np.float64)
-                t = ns.cpu().numpy().astype(np.float64)
-                flop = 2.0 * 128 * n * 16 * iters
-                tf = sms * flop / (t.max() * 1e-9) / 1e12
-                if best is None or tf > best["tflops"]:
-                    best = {"a_operand": "tensor memory" if a_tmem else "shared memory", "n": n,
-                            "tflops": tf, "frac_of_bf16_peak": tf / tpeak,
-                            "flop_per_sm_cycle": float(np.median(flop / c)),
-                            "sm_mhz_implied": float(np.median(c / t * 1e3))}
-            out.append(best)
+    for a_tmem, m, n, chains, per_sm in shapes:
+        ctas = per_sm * sms
+        best = None
+        for _ in range(max(3, args.warmup)):
+            assert L.qli_peak_mma_f16(a_tmem, m, n, chains, per_sm, iters, ctas, cyc.data_ptr(), ns.data_ptr(),
+                                      err.data_ptr(), stream) == 0
+            torch.cuda.synchronize()
+            assert int(err.item()) == 0, "a bounded wait gave up"
+            c = cyc[:ctas].cpu().numpy().astype(np.float64)
+            t = ns[:ctas].cpu().numpy().astype(np.float64)
+            flop = 2.0 * m * n * 16 * iters
+            tf = ctas * flop / (t.max() * 1e-9) / 1e12
+            if best is None or tf > best["tflops"]:
+                best = {"a_operand": "tensor memory" if a_tmem else "shared memory", "m": m, "n": n,
+                        "accumulators": chains, "ctas_per_sm": per_sm,
+                        "tflops": tf, "frac_of_bf16_peak": tf / tpeak,
+                        "cycles_per_mma_per_sm": float(np.median(c)) / (iters * per_sm),
+                        "sm_mhz_implied": float(np.median(c / t * 1e3))}
+        out.append(best)
     if rank == 0:
-        print(json.dumps({"metric": "tcgen05.mma kind::f16 rate, M 128 K 16, one CTA per SM", "unit": "TFLOP/s",
+        print(json.dumps({"metric": "tcgen05.mma kind::f16 rate, K 16", "unit": "TFLOP/s",
                           "bf16_peak": tpeak, "bf16_peak_source": tkind, "sms": sms, "iters_per_cta": iters,
                           "results": out}))
 

@@ -3,10 +3,11 @@
  *
  * Measures the rate of the tensor-core contraction the indexer's score kernel issues:
  * tcgen05.mma.cta_group::1.kind::f16 (fp16 operands, fp32 accumulator in tensor memory), M = 128
- * rows, K = 16 per instruction, N columns, with the A operand read from tensor memory (the score
- * kernel's form: A is the converted key tile) or from shared memory.  The README has no
- * counterpart; the figure is the denominator the score kernel's tensor utilisation is judged
- * against.
+ * (or 64) rows, K = 16 per instruction, N columns, with the A operand read from tensor memory (the
+ * score kernel's form: A is the converted key tile) or from shared memory, issued into one
+ * accumulator (each MMA depends on the one before) or cycled over several independent ones.  The
+ * README has no counterpart; the figures are the denominators the score kernel's tensor
+ * utilisation is judged against.
  */
 #ifndef QLI_PEAK_H
 #define QLI_PEAK_H
@@ -18,16 +19,20 @@ extern "C" {
 #endif
 
 /*
- * Launch `ctas` CTAs (one per SM: pass the SM count) of 128 threads; in each, one thread issues
- * `iters` back-to-back MMAs of shape 128 x n x 16 into one accumulator (n a multiple of 16 in
- * [16, 256]; a_from_tmem: 1 A from tensor memory, 0 from shared memory), then waits (bounded) for
- * their completion.  Per CTA it writes the elapsed SM cycles to cycles[c] and the elapsed
- * nanoseconds (globaltimer) to nanos[c]; *err (device, zeroed by the caller) receives 1 if a wait
- * gave up.  All pointers are device memory owned by the caller.  Enqueued on `stream`.
- * Returns 0, or a CUDA error code (non-zero) for a launch failure or bad arguments.
+ * Launch `ctas` CTAs of 128 threads, `ctas_per_sm` (1 or 2) resident per SM (pass that many times
+ * the SM count); each allocates 512 / ctas_per_sm tensor-memory columns.  In each CTA one thread
+ * issues `iters` back-to-back MMAs of shape m x n x 16, cycling over `chains` accumulators (the
+ * i-th MMA goes to accumulator i mod chains), then waits (bounded) for their completion.
+ * Shapes: m = 128 with n a multiple of 16 in [16, 256], A from tensor memory (a_from_tmem = 1) or
+ * shared memory (0); m = 64 with n a multiple of 8 in [8, 256], A from shared memory only.  The
+ * accumulators and A must fit the columns: 64 + chains * n <= 512 / ctas_per_sm.  Per CTA it
+ * writes the elapsed SM cycles to cycles[c] and the elapsed nanoseconds (globaltimer) to nanos[c];
+ * *err (device, zeroed by the caller) receives 1 if a wait gave up.  All pointers are device
+ * memory owned by the caller.  Enqueued on `stream`.  Returns 0, or a CUDA error code (non-zero)
+ * for a launch failure or bad arguments.
  */
-int qli_peak_mma_f16(int a_from_tmem, int n, int iters, int ctas, unsigned long long* cycles,
-                     unsigned long long* nanos, unsigned int* err, void* stream);
+int qli_peak_mma_f16(int a_from_tmem, int m, int n, int chains, int ctas_per_sm, int iters, int ctas,
+                     unsigned long long* cycles, unsigned long long* nanos, unsigned int* err, void* stream);
 
 #ifdef __cplusplus
 }

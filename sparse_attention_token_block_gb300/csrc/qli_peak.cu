@@ -1,7 +1,8 @@
 // qli_peak.cu -- rate of the score kernel's tensor-core contraction form (see include/qli_peak.h):
-// tcgen05.mma kind::f16, M = 128, K = 16, N columns, A from tensor memory or shared memory, fp32
-// accumulator in tensor memory.  One thread per CTA issues the MMAs back to back into one
-// accumulator, so the measured interval is the tensor pipe's own throughput for that shape.
+// tcgen05.mma kind::f16, M = 64 or 128, K = 16, N columns, A from tensor memory or shared memory,
+// fp32 accumulators in tensor memory.  One thread per CTA issues the MMAs back to back, cycling
+// over `chains` accumulators, so the measured interval is the tensor pipe's throughput for that
+// shape when each accumulator's MMAs depend on one another (chains = 1) or not (chains > 1).
 #include <cuda_runtime.h>
 
 #include "qli_peak.h"
@@ -15,14 +16,14 @@ constexpr int kThreads = 128;
 constexpr int kMaxN = 256;
 constexpr int kAbytes = 128 * 256;                 // A: 128 rows x 128 fp16, two 64-dim blocks
 constexpr int kBbytes = kMaxN * 256;               // B: N rows x 128 fp16, two 64-dim blocks
-// more than half of an SM's shared memory, so that exactly one CTA (holding all 512 tensor-memory
-// columns) runs per SM
-constexpr int kSmem = 120 * 1024;
-static_assert(kAbytes + kBbytes + 64 + 1024 <= kSmem, "shared-memory carve-up");
+// shared memory per CTA: more than half of an SM's for one CTA per SM, more than a third for two
+constexpr int kSmem1 = 120 * 1024;
+constexpr int kSmem2 = 100 * 1024;
+static_assert(kAbytes + kBbytes + 64 + 1024 <= kSmem2, "shared-memory carve-up");
 
 __global__ void __launch_bounds__(kThreads, 1)
-    mma_rate_kernel(int a_tmem, int n, int iters, unsigned long long* cycles, unsigned long long* nanos,
-                    unsigned int* err)
+    mma_rate_kernel(int a_tmem, int m, int n, int chains, uint32_t tmem_cols, int iters,
+                    unsigned long long* cycles, unsigned long long* nanos, unsigned int* err)
 {
     extern __shared__ uint8_t peak_smem[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(peak_smem) + 1023) & ~uintptr_t(1023));
@@ -39,7 +40,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
     }
     if (warp == 0) {
-        ptx::tmem_alloc(slot, 512);
+        ptx::tmem_alloc(slot, tmem_cols);
         ptx::tmem_relinquish();
     }
     ptx::fence_proxy_async_smem();
@@ -61,19 +62,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     if (tid == 0) {
-        const uint32_t idesc = ptx::idesc_f16_f32(128, (uint32_t)n);
-        const uint32_t d = tmem + 64;                       // D in columns [64, 64 + n)
+        const uint32_t idesc = ptx::idesc_f16_f32((uint32_t)m, (uint32_t)n);
         const uint32_t a0 = ptx::smem_addr(a_s), b0 = ptx::smem_addr(b_s);
         const unsigned long long c0 = clock64();
         const unsigned long long g0 = ptx::globaltimer();
+        int ch = 0, kk = 0;                                 // accumulator; K step of a 128-dim row
         for (int i = 0; i < iters; ++i) {
-            const int kk = i & 7;                           // the 8 K steps of a 128-dim row
+            const uint32_t d = tmem + 64 + ch * n;          // accumulator ch: columns [64 + ch n, +n)
             const uint64_t bd = ptx::sdesc_kmajor_sw128(b0 + (kk >> 2) * (n * 128) + (kk & 3) * 32);
+            const uint32_t acc = i >= chains ? 1u : 0u;
             if (a_tmem) {
-                ptx::mma_f16_ts(d, tmem + kk * 8, bd, idesc, i > 0 ? 1u : 0u);
+                ptx::mma_f16_ts(d, tmem + kk * 8, bd, idesc, acc);
             } else {
                 const uint64_t ad = ptx::sdesc_kmajor_sw128(a0 + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
-                ptx::mma_f16_ss(d, ad, bd, idesc, i > 0 ? 1u : 0u);
+                ptx::mma_f16_ss(d, ad, bd, idesc, acc);
+            }
+            if (++ch == chains) {
+                ch = 0;
+                kk = (kk + 1) & 7;
             }
         }
         ptx::mma_commit(bar);
@@ -93,19 +99,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == 0) ptx::tmem_dealloc(tmem, 512);
+    if (warp == 0) ptx::tmem_dealloc(tmem, tmem_cols);
 }
 
 }  // namespace
 
-extern "C" int qli_peak_mma_f16(int a_from_tmem, int n, int iters, int ctas, unsigned long long* cycles,
-                                unsigned long long* nanos, unsigned int* err, void* stream)
+extern "C" int qli_peak_mma_f16(int a_from_tmem, int m, int n, int chains, int ctas_per_sm, int iters, int ctas,
+                                unsigned long long* cycles, unsigned long long* nanos, unsigned int* err,
+                                void* stream)
 {
-    if (n < 16 || n > kMaxN || n % 16 != 0 || iters < 1 || ctas < 1 || !cycles || !nanos || !err)
+    const bool shape_ok = (m == 128 && n % 16 == 0 && n >= 16) || (m == 64 && !a_from_tmem && n % 8 == 0 && n >= 8);
+    if (!shape_ok || n > kMaxN || (ctas_per_sm != 1 && ctas_per_sm != 2) || chains < 1 ||
+        64 + chains * n > 512 / ctas_per_sm || iters < 1 || ctas < 1 || !cycles || !nanos || !err)
         return (int)cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    const int smem = ctas_per_sm == 1 ? kSmem1 : kSmem2;
+    cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
-    mma_rate_kernel<<<ctas, kThreads, kSmem, static_cast<cudaStream_t>(stream)>>>(a_from_tmem ? 1 : 0, n, iters,
-                                                                                  cycles, nanos, err);
+    mma_rate_kernel<<<ctas, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+        a_from_tmem ? 1 : 0, m, n, chains, 512u / (uint32_t)ctas_per_sm, iters, cycles, nanos, err);
     return (int)cudaGetLastError();
 }
