@@ -87,6 +87,71 @@ __device__ int64_t first_at_least(const View& a, int64_t n, int64_t key)
     return lo;
 }
 
+// Problems of at most kSmallMeta batches and query groups: the per-batch extents, the group scan
+// and the live-group records worked out by one warp with shuffles (lane i holds batch i, then group
+// i) instead of the block-wide passes below, which cost more in barriers and first-time code than
+// the work itself.  Writes the batch entries and records as those passes do, the live groups' first
+// key-tile positions to v_tb (shared memory), and (live groups, T, groups) to out[0..2].
+constexpr int kSmallMeta = 32;
+
+__device__ __noinline__ void small_phases(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                                          int32_t* be, int32_t* rec, int32_t* v_tb, int64_t* out, uint32_t* err)
+{
+    const uint32_t full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int B = p.batch, gt = p.group_tokens;
+    BatchExtent x{0, 0, 0, 0, false, false};
+    if (lane < B) x = batch_extent(p, seq_lens_q, seq_lens_k, lane);
+    if (__any_sync(full, lane < B && !x.ok) && lane == 0) atomicOr(err, kErrLength);
+    const bool tnd_bad = __any_sync(full, lane < B && x.tnd_bad);   // bad prefix sums invalidate every batch
+    const bool okb = lane < B && x.ok && !tnd_bad;
+    const int groups = okb ? (x.sq + gt - 1) / gt : 0;
+    int g_in = groups;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(full, g_in, o);
+        if (lane >= o) g_in += y;
+    }
+    const int gb = g_in - groups;                    // batch lane's first group
+    const int total = __shfl_sync(full, g_in, 31);
+    if (lane < B) {
+        int4* e = reinterpret_cast<int4*>(be + (int64_t)lane * kBatchWords);
+        e[0] = make_int4(x.sq, x.sk, x.lc, x.first);
+        e[1] = make_int4(okb ? 1 : 0, groups, gb, 0);
+    }
+    // group `lane`: its batch (the last batch whose first group is at or before it, as the block
+    // passes find it), first row and key tiles
+    int b = 0;
+    for (int j = 1; j < B; ++j)
+        if (__shfl_sync(full, gb, j) <= lane) b = j;
+    const int sq = __shfl_sync(full, x.sq, b), sk = __shfl_sync(full, x.sk, b);
+    const int lc = __shfl_sync(full, x.lc, b), fr = __shfl_sync(full, x.first, b);
+    const int r0 = (lane - __shfl_sync(full, gb, b)) * gt;
+    const int t = lane < total ? (int)group_tiles(p, sq, sk, lc, r0) : 0;
+    const bool live = t > 0;
+    const uint32_t lmask = __ballot_sync(full, live);
+    const int li = __popc(lmask & ((1u << lane) - 1));
+    int p_in = live ? t + kUnitCost : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(full, p_in, o);
+        if (lane >= o) p_in += y;
+    }
+    const int pos = p_in - t;                        // the group's first key tile in the sequence
+    if (live) {
+        int4* r = reinterpret_cast<int4*>(rec + (int64_t)li * kGroupWords);
+        r[0] = make_int4(b, r0, fr + r0, sq);
+        r[1] = make_int4(sk, lc, pos, t);
+        v_tb[li] = pos;
+    }
+    const int T = __shfl_sync(full, p_in, 31);
+    if (lane == 0) {
+        out[0] = __popc(lmask);
+        out[1] = T;
+        out[2] = total;
+    }
+}
+
 __global__ void __launch_bounds__(kMetaThreads, 1)
     metadata_kernel(Params p, const int32_t* __restrict__ seq_lens_q,
                     const int32_t* __restrict__ seq_lens_k, int32_t* __restrict__ meta, int G, int G1)
@@ -120,95 +185,108 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     ptx::pdl_launch_dependents();
     __syncthreads();
 
-    // ---- per-batch extents and validity
-    for (int b = tid; b < p.batch; b += kMetaThreads) {
-        const BatchExtent x = batch_extent(p, seq_lens_q, seq_lens_k, b);
-        if (x.tnd_bad) s_tnd_bad = 1;
-        if (!x.ok) atomicOr(&s_err, kErrLength);
-        int4* e = reinterpret_cast<int4*>(be + (int64_t)b * kBatchWords);
-        e[0] = make_int4(x.sq, x.sk, x.lc, x.first);
-        if (sb) {
-            v_sq[b] = x.sq;
-            v_sk[b] = x.sk;
-            v_lc[b] = x.lc;
-            v_ok[b] = x.ok ? 1 : 0;
-            v_fr[b] = x.first;
-        } else {
-            e[1].x = x.ok ? 1 : 0;     // kBeOk, read back below
-        }
-    }
-    __syncthreads();
-    const bool tnd_bad = s_tnd_bad != 0;   // bad prefix sums invalidate every batch
-
-    // ---- query groups per batch and their prefix (the batch's first group)
-    int64_t running = 0;
-    for (int base = 0; base < p.batch; base += kMetaThreads) {
-        const int b = base + tid;
-        uint32_t groups = 0;
-        const bool okb = b < p.batch && !tnd_bad && v_ok[b];
-        if (b < p.batch) groups = okb ? (uint32_t)((v_sq[b] + gt - 1) / gt) : 0u;
-        uint64_t tot;
-        const uint64_t ex = block_scan64(groups, &tot, scan_sh, parity);
-        if (b < p.batch) {
+    __shared__ int64_t s_small[3];       // the one-warp passes' live groups, T and groups
+    int64_t total_groups = 0, live = 0, T = 0;
+    bool sl = true;
+    View v_tb{msm + 6 * nb, 1};
+    if (p.batch <= kSmallMeta && p.meta.max_groups <= kSmallMeta) {
+        if (tid < 32) small_phases(p, seq_lens_q, seq_lens_k, be, rec, msm + 6 * nb, s_small, &s_err);
+        __syncthreads();
+        live = s_small[0];
+        T = s_small[1];
+        total_groups = s_small[2];
+    } else {
+        // ---- per-batch extents and validity
+        for (int b = tid; b < p.batch; b += kMetaThreads) {
+            const BatchExtent x = batch_extent(p, seq_lens_q, seq_lens_k, b);
+            if (x.tnd_bad) s_tnd_bad = 1;
+            if (!x.ok) atomicOr(&s_err, kErrLength);
             int4* e = reinterpret_cast<int4*>(be + (int64_t)b * kBatchWords);
-            e[1] = make_int4(okb ? 1 : 0, (int32_t)groups, (int32_t)(running + ex), 0);
+            e[0] = make_int4(x.sq, x.sk, x.lc, x.first);
             if (sb) {
-                v_gb[b] = (int32_t)(running + ex);
-                v_ok[b] = okb ? 1 : 0;
+                v_sq[b] = x.sq;
+                v_sk[b] = x.sk;
+                v_lc[b] = x.lc;
+                v_ok[b] = x.ok ? 1 : 0;
+                v_fr[b] = x.first;
+            } else {
+                e[1].x = x.ok ? 1 : 0;     // kBeOk, read back below
             }
         }
-        running += (int64_t)tot;
-    }
-    const int64_t total_groups = running;
-    __syncthreads();
+        __syncthreads();
+        const bool tnd_bad = s_tnd_bad != 0;   // bad prefix sums invalidate every batch
 
-    // ---- groups: each thread owns a contiguous run; a group's batch comes from one binary search
-    // for the run's first group, then by advancing.  One scan of (live, tiles) gives every live
-    // group its record index and first tile.
-    const int64_t per = (total_groups + kMetaThreads - 1) / kMetaThreads;
-    const int64_t g_lo = min((int64_t)tid * per, total_groups);
-    const int64_t g_hi = min(g_lo + per, total_groups);
-    auto tiles_of = [&](int64_t b, int64_t g, int64_t* r0) -> int64_t {
-        *r0 = (g - v_gb[b]) * gt;
-        return group_tiles(p, v_sq[b], v_sk[b], v_lc[b], *r0);
-    };
-    auto advance = [&](int64_t b, int64_t g) -> int64_t {   // batches without groups share their successor's base
-        while (b + 1 < p.batch && v_gb[b + 1] <= g) ++b;
-        return b;
-    };
-    const int64_t b_lo = g_lo < g_hi ? last_at_most(v_gb, p.batch, g_lo) : 0;
-    uint64_t mine = 0;     // live groups << 32 | tiles (T < 2^31: the host bounds rows x tiles)
-    {
-        int64_t b = b_lo, r0;
-        for (int64_t g = g_lo; g < g_hi; ++g) {
-            b = advance(b, g);
-            const int64_t t = tiles_of(b, g, &r0);
-            if (t > 0) mine += (uint64_t(1) << 32) + (uint64_t)(t + kUnitCost);
+        // ---- query groups per batch and their prefix (the batch's first group)
+        int64_t running = 0;
+        for (int base = 0; base < p.batch; base += kMetaThreads) {
+            const int b = base + tid;
+            uint32_t groups = 0;
+            const bool okb = b < p.batch && !tnd_bad && v_ok[b];
+            if (b < p.batch) groups = okb ? (uint32_t)((v_sq[b] + gt - 1) / gt) : 0u;
+            uint64_t tot;
+            const uint64_t ex = block_scan64(groups, &tot, scan_sh, parity);
+            if (b < p.batch) {
+                int4* e = reinterpret_cast<int4*>(be + (int64_t)b * kBatchWords);
+                e[1] = make_int4(okb ? 1 : 0, (int32_t)groups, (int32_t)(running + ex), 0);
+                if (sb) {
+                    v_gb[b] = (int32_t)(running + ex);
+                    v_ok[b] = okb ? 1 : 0;
+                }
+            }
+            running += (int64_t)tot;
         }
-    }
-    uint64_t tot;
-    const uint64_t pre = block_scan64(mine, &tot, scan_sh, parity);
-    const int64_t live = (int64_t)(tot >> 32);
-    const int64_t T = (int64_t)(tot & 0xFFFFFFFFull);
-    const bool sl = live <= kSmemLive;
-    const View v_tb = sl ? View{msm + 6 * nb, 1} : View{rec + kGrTile, kGroupWords};
-    {
-        int64_t li = (int64_t)(pre >> 32), tile = (int64_t)(pre & 0xFFFFFFFFull);
-        int64_t b = b_lo, r0;
-        for (int64_t g = g_lo; g < g_hi; ++g) {
-            b = advance(b, g);
-            const int64_t t = tiles_of(b, g, &r0);
-            if (t == 0) continue;
-            int4* r = reinterpret_cast<int4*>(rec + li * kGroupWords);
-            r[0] = make_int4((int32_t)b, (int32_t)r0, v_fr[b] + (int32_t)r0, v_sq[b]);
-            r[1] = make_int4(v_sk[b], v_lc[b], (int32_t)(tile + kUnitCost), (int32_t)t);
-            if (sl) v_tb[li] = (int32_t)(tile + kUnitCost);
-            ++li;
-            tile += t + kUnitCost;
+        total_groups = running;
+        __syncthreads();
+
+        // ---- groups: each thread owns a contiguous run; a group's batch comes from one binary search
+        // for the run's first group, then by advancing.  One scan of (live, tiles) gives every live
+        // group its record index and first tile.
+        const int64_t per = (total_groups + kMetaThreads - 1) / kMetaThreads;
+        const int64_t g_lo = min((int64_t)tid * per, total_groups);
+        const int64_t g_hi = min(g_lo + per, total_groups);
+        auto tiles_of = [&](int64_t b, int64_t g, int64_t* r0) -> int64_t {
+            *r0 = (g - v_gb[b]) * gt;
+            return group_tiles(p, v_sq[b], v_sk[b], v_lc[b], *r0);
+        };
+        auto advance = [&](int64_t b, int64_t g) -> int64_t {   // batches without groups share their successor's base
+            while (b + 1 < p.batch && v_gb[b + 1] <= g) ++b;
+            return b;
+        };
+        const int64_t b_lo = g_lo < g_hi ? last_at_most(v_gb, p.batch, g_lo) : 0;
+        uint64_t mine = 0;     // live groups << 32 | tiles (T < 2^31: the host bounds rows x tiles)
+        {
+            int64_t b = b_lo, r0;
+            for (int64_t g = g_lo; g < g_hi; ++g) {
+                b = advance(b, g);
+                const int64_t t = tiles_of(b, g, &r0);
+                if (t > 0) mine += (uint64_t(1) << 32) + (uint64_t)(t + kUnitCost);
+            }
         }
+        uint64_t tot;
+        const uint64_t pre = block_scan64(mine, &tot, scan_sh, parity);
+        live = (int64_t)(tot >> 32);
+        T = (int64_t)(tot & 0xFFFFFFFFull);
+        sl = live <= kSmemLive;
+        v_tb = sl ? View{msm + 6 * nb, 1} : View{rec + kGrTile, kGroupWords};
+        {
+            int64_t li = (int64_t)(pre >> 32), tile = (int64_t)(pre & 0xFFFFFFFFull);
+            int64_t b = b_lo, r0;
+            for (int64_t g = g_lo; g < g_hi; ++g) {
+                b = advance(b, g);
+                const int64_t t = tiles_of(b, g, &r0);
+                if (t == 0) continue;
+                int4* r = reinterpret_cast<int4*>(rec + li * kGroupWords);
+                r[0] = make_int4((int32_t)b, (int32_t)r0, v_fr[b] + (int32_t)r0, v_sq[b]);
+                r[1] = make_int4(v_sk[b], v_lc[b], (int32_t)(tile + kUnitCost), (int32_t)t);
+                if (sl) v_tb[li] = (int32_t)(tile + kUnitCost);
+                ++li;
+                tile += t + kUnitCost;
+            }
+        }
+        if (!sl) __threadfence_block();
+        __syncthreads();
+
     }
-    if (!sl) __threadfence_block();
-    __syncthreads();
 
     // ---- the split: CTA c owns positions [split_start(c), split_start(c + 1)) of the sequence; its
     // live groups run from the one whose block (virtual tiles, then key tiles) holds its first

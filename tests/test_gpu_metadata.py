@@ -115,6 +115,10 @@ CASES = [
     ("bad_length", lambda: W.make_case("m3", batch=3, s1=2, q_lens=[2, 3, 1],
                                        seq_lens_k=[300, 300, 5000], block_size=64,
                                        sparse_count=16, seed=3)),
+    # 31 batches of at most one row: rows without keys, batches without rows between live ones
+    ("small_gaps", lambda: W.make_case("m4", batch=31, s1=1, q_lens=[(i % 3 > 0) * 1 for i in range(31)],
+                                       seq_lens_k=[0 if i % 4 == 1 else 40 * i + 7 for i in range(31)],
+                                       block_size=32, sparse_count=64, sparse_mode=3, seed=4)),
 ]
 
 

@@ -93,3 +93,38 @@ def test_plan_rejects_bad_arguments_and_leaves_the_stream_usable(qli):
     out = ix.run(**d)                     # capture ended cleanly: ordinary calls still work
     torch.cuda.synchronize()
     assert (out[0, :64] >= 0).all()
+
+
+def _poison_score_lines(ix):
+    """Every score code in the workspace set to the largest value: a tile the score kernel skipped
+    would then win its row's top-k."""
+    import torch
+    ix.workspace.view(torch.uint8)[256:].fill_(0xFF)
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "page_decode", "long_decode", "fp8_compressed_decode",
+                                  "varlen_prefill", "mixed"])
+def test_plan_replay_rewrites_every_visible_score(qli, name):
+    """A replay must score every visible key again: after the score lines were poisoned, it returns
+    the stream call's indices and rewrites the same metadata."""
+    import torch
+    if name == "mixed":
+        # empty batches, short query runs and rows that see no key, two tokens per query group
+        case = W.make_case("mixed", batch=37, s1=3, q_lens=[(i * 7) % 4 for i in range(37)],
+                           seq_lens_k=[0 if i % 5 == 0 else 64 + 97 * i for i in range(37)], block_size=64,
+                           sparse_count=96, sparse_mode=3, seed=33)
+    else:
+        case = W.WORKLOADS[name]()
+    p, ix, d = _setup(qli, case)
+    ref = ix.run(**d).clone()
+    meta_ref = ix.meta.clone()
+    plan = ix.plan(**d)
+    for _ in range(2):
+        _poison_score_lines(ix)
+        ix.out.fill_(-7)
+        plan.launch()
+        torch.cuda.synchronize()
+        assert torch.equal(ix.out, ref)
+        assert torch.equal(ix.meta, meta_ref)
+        assert ix.device_error()[0] == 0
+    plan.close()
