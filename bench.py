@@ -594,7 +594,7 @@ def time_workload(Q, case, dev, flush_l2, steps, warmup):
 def run_mma(args, rank, world, local):
     """Rate of tcgen05.mma kind::f16 (K 16, fp32 accumulators in tensor memory): M 128 with A from
     tensor memory -- the score kernel's form -- or from shared memory, M 64 with A from shared
-    memory; N 64 .. 256; MMAs issued back to back by one thread per CTA into one accumulator or
+    memory; N 64 .. 256; MMAs issued back to back by one warp per CTA into one accumulator or
     cycled over several independent ones; one or two CTAs per SM.  Prints one JSON line."""
     import ctypes
     import torch

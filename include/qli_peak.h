@@ -20,9 +20,10 @@ extern "C" {
 
 /*
  * Launch `ctas` CTAs of 128 threads, `ctas_per_sm` (1 or 2) resident per SM (pass that many times
- * the SM count); each allocates 512 / ctas_per_sm tensor-memory columns.  In each CTA one thread
- * issues `iters` back-to-back MMAs of shape m x n x 16, cycling over `chains` accumulators (the
- * i-th MMA goes to accumulator i mod chains), then waits (bounded) for their completion.
+ * the SM count); each allocates 512 / ctas_per_sm tensor-memory columns.  In each CTA one warp
+ * issues `iters` (a multiple of 8) back-to-back MMAs of shape m x n x 16 in groups of eight (the K
+ * steps of one 128-dim key tile), the i-th group into accumulator i mod `chains`, then waits
+ * (bounded) for their completion.
  * Shapes: m = 128 with n a multiple of 16 in [16, 256], A from tensor memory (a_from_tmem = 1) or
  * shared memory (0); m = 64 with n a multiple of 8 in [8, 256], A from shared memory only.  The
  * accumulators and A must fit the columns: 64 + chains * n <= 512 / ctas_per_sm.  Per CTA it

@@ -1,8 +1,9 @@
 // qli_peak.cu -- rate of the score kernel's tensor-core contraction form (see include/qli_peak.h):
 // tcgen05.mma kind::f16, M = 64 or 128, K = 16, N columns, A from tensor memory or shared memory,
-// fp32 accumulators in tensor memory.  One thread per CTA issues the MMAs back to back, cycling
-// over `chains` accumulators, so the measured interval is the tensor pipe's throughput for that
-// shape when each accumulator's MMAs depend on one another (chains = 1) or not (chains > 1).
+// fp32 accumulators in tensor memory.  One warp per CTA issues the MMAs back to back (one elected
+// lane, warp-uniform operands), cycling over `chains` accumulators, so the measured interval is the
+// tensor pipe's throughput for that shape when each accumulator's MMAs depend on one another
+// (chains = 1) or not (chains > 1).
 #include <cuda_runtime.h>
 
 #include "qli_peak.h"
@@ -61,40 +62,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (tid == 0) {
+    if (warp == 0) {
+        // the whole warp runs the loop with warp-uniform operands and one elected lane issues (the
+        // score kernel's form; issued from a lone thread the same MMAs go out far slower)
+        const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
         const uint32_t idesc = ptx::idesc_f16_f32((uint32_t)m, (uint32_t)n);
-        const uint32_t a0 = ptx::smem_addr(a_s), b0 = ptx::smem_addr(b_s);
+        const uint64_t ad0 = ptx::sdesc_kmajor_sw128(ptx::smem_addr(a_s));
+        const uint64_t bd0 = ptx::sdesc_kmajor_sw128(ptx::smem_addr(b_s));
+        const bool leader = ptx::elect_one();
         const unsigned long long c0 = clock64();
         const unsigned long long g0 = ptx::globaltimer();
-        int ch = 0, kk = 0;                                 // accumulator; K step of a 128-dim row
-        for (int i = 0; i < iters; ++i) {
-            const uint32_t d = tmem + 64 + ch * n;          // accumulator ch: columns [64 + ch n, +n)
-            const uint64_t bd = ptx::sdesc_kmajor_sw128(b0 + (kk >> 2) * (n * 128) + (kk & 3) * 32);
-            const uint32_t acc = i >= chains ? 1u : 0u;
-            if (a_tmem) {
-                ptx::mma_f16_ts(d, tmem + kk * 8, bd, idesc, acc);
-            } else {
-                const uint64_t ad = ptx::sdesc_kmajor_sw128(a0 + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
-                ptx::mma_f16_ss(d, ad, bd, idesc, acc);
+        // groups of 8 MMAs (the K steps of a 128-dim row, offsets fixed at compile time), group i
+        // into accumulator i mod chains, as the score kernel issues one key tile
+        int ch = 0;
+        for (int i = 0; i < iters / 8; ++i) {
+            const uint32_t d = tm + 64 + ch * n;            // accumulator ch: columns [64 + ch n, +n)
+            const bool first = i < chains;
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    // K step kk: 32 bytes into the 128-byte swizzle row; dims 64..127 in the second block
+                    const uint64_t bd = bd0 + (uint64_t)((((kk >> 2) * (n * 128)) + (kk & 3) * 32) >> 4);
+                    const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                    if (a_tmem) {
+                        ptx::mma_f16_ts(d, tm + kk * 8, bd, idesc, acc);
+                    } else {
+                        const uint64_t ad = ad0 + (uint64_t)((((kk >> 2) * (128 * 128)) + (kk & 3) * 32) >> 4);
+                        ptx::mma_f16_ss(d, ad, bd, idesc, acc);
+                    }
+                }
             }
-            if (++ch == chains) {
-                ch = 0;
-                kk = (kk + 1) & 7;
-            }
+            if (++ch == chains) ch = 0;
         }
-        ptx::mma_commit(bar);
-        // bounded wait for every MMA to complete (about 1 s); on expiry record the error and wait
-        // once more, bounded, before the tensor memory is released
-        bool ok = false;
-        for (long long spin = 0; spin < (1ll << 26) && !ok; ++spin) ok = ptx::mbar_try_wait(bar, 0);
-        const unsigned long long c1 = clock64();
-        const unsigned long long g1 = ptx::globaltimer();
-        if (!ok) {
-            atomicOr(err, 1u);
+        if (leader) {
+            ptx::mma_commit(bar);
+            // bounded wait for every MMA to complete (about 1 s); on expiry record the error and
+            // wait once more, bounded, before the tensor memory is released
+            bool ok = false;
             for (long long spin = 0; spin < (1ll << 26) && !ok; ++spin) ok = ptx::mbar_try_wait(bar, 0);
+            const unsigned long long c1 = clock64();
+            const unsigned long long g1 = ptx::globaltimer();
+            if (!ok) {
+                atomicOr(err, 1u);
+                for (long long spin = 0; spin < (1ll << 26) && !ok; ++spin) ok = ptx::mbar_try_wait(bar, 0);
+            }
+            cycles[blockIdx.x] = c1 - c0;
+            nanos[blockIdx.x] = g1 - g0;
         }
-        cycles[blockIdx.x] = c1 - c0;
-        nanos[blockIdx.x] = g1 - g0;
+        __syncwarp();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -109,7 +124,7 @@ extern "C" int qli_peak_mma_f16(int a_from_tmem, int m, int n, int chains, int c
                                 void* stream)
 {
     const bool shape_ok = (m == 128 && n % 16 == 0 && n >= 16) || (m == 64 && !a_from_tmem && n % 8 == 0 && n >= 8);
-    if (!shape_ok || n > kMaxN || (ctas_per_sm != 1 && ctas_per_sm != 2) || chains < 1 ||
+    if (!shape_ok || n > kMaxN || (ctas_per_sm != 1 && ctas_per_sm != 2) || chains < 1 || iters % 8 != 0 ||
         64 + chains * n > 512 / ctas_per_sm || iters < 1 || ctas < 1 || !cycles || !nanos || !err)
         return (int)cudaErrorInvalidValue;
     const int smem = ctas_per_sm == 1 ? kSmem1 : kSmem2;
