@@ -746,6 +746,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
                 ptx::mbar_arrive_expect_tx(S.bar, bytes);
                 ptx::bulk_load(S.cache, line, bytes, S.bar);
             }
+            // the CTA's next row (many rows per CTA, e.g. a prefill's) comes from DRAM: ask for its
+            // line's first kCacheKeys codes now, so that its copy finds them in L2
+            if (row + gridDim.x < p.rows) {
+                const int64_t nb = (p.ld < kCacheKeys ? p.ld : kCacheKeys) * 4;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(line + gridDim.x * p.ld),
+                             "r"((uint32_t)nb)
+                             : "memory");
+            }
         }
         __syncthreads();
         if (!loaded) load_pages();
