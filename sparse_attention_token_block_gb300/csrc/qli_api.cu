@@ -331,10 +331,13 @@ qli_status topk_impl(const qli_problem* p, const int32_t* block_table, const int
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     // more rows than SMs, each of at most kTopkSmallRows keys (ld bounds every row's visible keys):
     // the two-per-SM form for throughput; few rows: the 1024-thread form for latency
-    auto launch = (P.ld <= kTopkSmallRows && P.rows > sms) ? launch_topk_small : launch_topk;
+    // (the two-per-SM form runs persistent: one CTA per resident slot, each striding over the rows,
+    // which saves a CTA's launch and set-up per row and lets a CTA ask for its next row early)
+    const bool small = P.ld <= kTopkSmallRows && P.rows > sms;
+    auto launch = small ? launch_topk_small : launch_topk;
     cudaError_t e = launch(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),
                            reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values, after_score,
-                           static_cast<cudaStream_t>(stream));
+                           small ? 2 * sms : 0, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
 

@@ -283,14 +283,15 @@ cudaError_t launch_score_multi(const Params& p, const void* tmap_key, const void
                                const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                                const int32_t* block_table, const int32_t* meta, uint32_t* scores,
                                uint32_t* err_word, int grid, cudaStream_t st);
+// (max_ctas > 0: at most that many CTAs, each striding over the rows; else one CTA per row)
 cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
                         const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
-                        bool after_score, cudaStream_t st);
+                        bool after_score, int max_ctas, cudaStream_t st);
 // the same top-k with half the threads and a row cache of kTopkSmallRows keys (two CTAs per SM)
 constexpr int kTopkSmallRows = 8192;
 cudaError_t launch_topk_small(const Params& p, const int32_t* block_table, const int32_t* meta,
                               const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
-                              bool after_score, cudaStream_t st);
+                              bool after_score, int max_ctas, cudaStream_t st);
 cudaError_t launch_quantize_vectors(const void* x_bf16, int64_t nvec, void* codes, void* scales, bool fp8,
                                     bool scale_f32, cudaStream_t st);
 cudaError_t launch_quantize_keys(const Params& p, const void* k_bf16, int64_t tokens, const int32_t* tok_batch,

@@ -630,6 +630,26 @@ __device__ __noinline__ Binning sample_bound(const uint32_t* src, int c, int nee
     return make_binning(L, smx);
 }
 
+// Rows of at most kRankKeys keys: each key's place in the order is the number of keys of the row
+// that sort before it (a higher code, or the same code and a lower index), counted against every
+// key of the row cache; the first `need` places receive their indices in S.outv.  One pass and
+// one barrier instead of the bins' passes, which cost more than this count on short rows.
+constexpr int kRankKeys = 256;   // n^2 comparisons: measured faster than the bins up to ~256 keys
+__device__ __noinline__ void rank_order(const uint32_t* src, int n, int need)
+{
+    const Smem S = smem_view();
+    for (int t = threadIdx.x; t < n; t += kThreads) {
+        const uint32_t ct = src[t];
+        uint32_t r = 0;
+#pragma unroll 8
+        for (int j = 0; j < t; ++j) r += src[j] >= ct ? 1u : 0u;       // lower index: ties sort first
+#pragma unroll 8
+        for (int j = t + 1; j < n; ++j) r += src[j] > ct ? 1u : 0u;
+        if (r < (uint32_t)need) S.outv[r] = (uint32_t)t;
+    }
+    __syncthreads();
+}
+
 // Exact fallback: the k-th largest sort key of the row (radix select), then exactly k keys at or
 // above it, ordered by the bitonic network; the ordered indices end in S.val.
 __device__ __noinline__ void exact_topk(const uint32_t* line, int64_t n, int k)
@@ -767,7 +787,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
             int st = kBinTooMany;
             if (cached) {
                 // bins over the whole range (short rows: every key is a candidate) or from a sample
-                if (n <= kCap) {
+                if (n <= kRankKeys) {
+                    rank_order(S.cache, (int)n, need);
+                    st = kBinOrdered;
+                } else if (n <= kCap) {
                     // every key is a candidate: bins over the row's whole code range, counted and
                     // scattered straight from the row cache
                     uint32_t hi = 0, lo = 0xFFFFFFFFu;
@@ -834,13 +857,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
 
 cudaError_t QLI_TOPK_LAUNCHER(const Params& p, const int32_t* block_table, const int32_t* meta,
                         const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
-                        bool after_score, cudaStream_t st)
+                        bool after_score, int max_ctas, cudaStream_t st)
 {
     if (p.rows == 0) return cudaSuccess;
     TopkArgs a{p, block_table, meta, scores, err_word, out, values, after_score ? 1 : 0};
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int grid = p.rows < (1 << 30) ? p.rows : (1 << 30);
+    // one CTA per row, or (max_ctas > 0) at most max_ctas CTAs that stride over the rows
+    int grid = p.rows < (1 << 30) ? p.rows : (1 << 30);
+    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
     return launch_pdl(topk_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, a);
 }
 

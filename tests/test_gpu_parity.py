@@ -228,6 +228,24 @@ def test_topk_few_distinct_scores(qli):
     assert np.array_equal(gpu_idx, ora_idx)     # exact ties resolve by index on both sides
 
 
+@pytest.mark.parametrize("k", [40, 300, 512])
+def test_topk_short_rows_with_ties(qli, k):
+    """Rows of at most 512 keys (up to 256 keys each key's place is counted against the whole row), with keys drawn
+    from 5 distinct rows so that runs of exact ties cross the k-th place; k below, inside and at
+    or above the rows' lengths (then every key, in order, then -1)."""
+    case = W.make_case("short_ties", batch=6, s1=2, seq_lens_k=[1, 2, 63, 256, 257, 512], block_size=64,
+                       sparse_count=k, sparse_mode=3, seed=12)
+    rng = np.random.default_rng(12)
+    pick = rng.integers(0, 5, size=case.key.shape[:2])
+    protos = case.key[0, :5, 0].copy()
+    case.key[:, :, 0] = protos[pick]
+    case.k_scale[:] = np.float16(1.0)
+    gpu_idx, _, st, _ = run_gpu(qli, case)
+    ora_idx, _, _ = oracle.score_topk(case)
+    assert st == 0
+    assert np.array_equal(gpu_idx, ora_idx)     # exact ties resolve by index on both sides
+
+
 # ---------------------------------------------------------------------------- sparse_values
 
 @pytest.mark.parametrize("name", ["page_decode", "fp8_compressed_decode", "long_decode"])
