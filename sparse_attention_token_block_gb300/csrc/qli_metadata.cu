@@ -292,8 +292,16 @@ __global__ void __launch_bounds__(kMetaThreads, 1)
     // live groups run from the one whose block (virtual tiles, then key tiles) holds its first
     // position to (excluding) the first whose key tiles start at or after its end -- each of them
     // has key tiles inside the range, and first = end when the range holds only virtual tiles
+    // split_start(T, G, G1, c) = T W(c) / W(G) in 32-bit divisions: with T = q W(G) + r it is
+    // q W(c) + (r W(c)) / W(G), exactly (W(G) < 2^14, so r W(c) < 2^28; T < 2^31)
+    const uint32_t WG = (uint32_t)split_weight(G1, G);
+    const uint32_t tq = (uint32_t)T / WG, tr = (uint32_t)T % WG;
+    auto start_of = [&](int64_t c) -> int64_t {
+        const uint32_t w = (uint32_t)split_weight(G1, c);
+        return (int64_t)tq * w + (tr * w) / WG;
+    };
     for (int c = tid; c < G; c += kMetaThreads) {
-        const int64_t t0 = split_start(T, G, G1, c), t1 = split_start(T, G, G1, c + 1);
+        const int64_t t0 = start_of(c), t1 = start_of(c + 1);
         int32_t first = 0, end = 0;
         if (t1 > t0) {
             first = (int32_t)last_at_most(v_tb, live, t0 + kUnitCost);
