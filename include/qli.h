@@ -96,7 +96,20 @@ typedef struct {
     int32_t mask_complete_blocks; /* sparse_mode 3 with cmp_ratio > 1: 0 = a compressed key is
                                    visible once its block has started, n = ceil((p + 1) / cmp);
                                    1 = only complete blocks, n = floor((p + 1) / cmp) */
+    int32_t split_topk;         /* qli_split_topk: how the top-k runs for one query token per
+                                   sequence (BSND, S1 = 1); the result is the same either way */
 } qli_problem;
+
+/*
+ * The top-k in two stages (README function section, step 3, done as a per-split selection and a
+ * cross-split merge).  ON: every score CTA keeps, for each part of its key range that lies in one
+ * aligned block of 4096 keys of a row, the exact top sparse_count keys of that part (by score
+ * descending, index ascending), and the top-k merges those candidates per row; OFF: the top-k
+ * reads each row's whole score line.  AUTO is OFF: on a GB300 the two-stage form measured slower
+ * at every size tried.  Problems with more than one query token per sequence always run OFF.  ON
+ * makes the workspace larger (qli_workspace_size).  The indices are the same either way.
+ */
+typedef enum { QLI_SPLIT_AUTO = 0, QLI_SPLIT_ON = 1, QLI_SPLIT_OFF = 2 } qli_split_topk;
 
 /* Fill `p` with the README's defaults (BSND, int8, fp16, mode 0, cmp 1, k 2048, reserved fields
  * at their only accepted values).  The caller then sets the sizes. */

@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "QLI_OK", 1: "QLI_ERR_INVALID_ARG", 2: "QLI_ERR_UNSUPPORTED",
 INT8, FP8_E4M3 = 0, 1
 F16, F32 = 0, 1
 BSND, TND = 0, 1
+SPLIT_AUTO, SPLIT_ON, SPLIT_OFF = 0, 1, 2       # qli_split_topk
 INT64_MAX = (1 << 63) - 1
 
 # symbols include/qli.h declares
@@ -50,7 +51,8 @@ class Problem(ctypes.Structure):
         "sparse_count", "sparse_mode", "cmp_ratio", "query_quant_mode", "key_quant_mode",
         "return_value")] + [("pre_tokens", ctypes.c_int64), ("next_tokens", ctypes.c_int64),
                             ("max_seqlen_q", ctypes.c_int32), ("max_seqlen_k", ctypes.c_int32),
-                            ("key_stride", ctypes.c_int32), ("mask_complete_blocks", ctypes.c_int32)]
+                            ("key_stride", ctypes.c_int32), ("mask_complete_blocks", ctypes.c_int32),
+                            ("split_topk", ctypes.c_int32)]
 
 
 def _load():
@@ -281,7 +283,7 @@ def check(st: int, what: str = "qli"):
 def make_problem(*, batch, layout_q=BSND, max_q_tokens=0, total_q_tokens=0, qk_dtype=INT8,
                  scale_dtype=F16, num_blocks, block_size, max_blocks_per_seq, sparse_count,
                  sparse_mode, cmp_ratio, max_seqlen_q, max_seqlen_k, return_value=0, key_stride=0,
-                 mask_complete_blocks=0) -> Problem:
+                 mask_complete_blocks=0, split_topk=0) -> Problem:
     p = problem_init()
     p.batch = batch
     p.layout_q = layout_q
@@ -300,6 +302,7 @@ def make_problem(*, batch, layout_q=BSND, max_q_tokens=0, total_q_tokens=0, qk_d
     p.return_value = return_value
     p.key_stride = key_stride
     p.mask_complete_blocks = mask_complete_blocks
+    p.split_topk = split_topk
     return p
 
 
@@ -361,6 +364,22 @@ class Indexer:
         neg = codes < 0x80000000
         bits = torch.where(neg, (~codes) & 0xFFFFFFFF, codes & 0x7FFFFFFF)
         return bits.to(torch.int32).view(torch.float32).reshape(self.rows, ld)
+
+    def split_candidates(self):
+        """With the split-local selection on: the last call's candidate codes and key indices
+        ([rows, ld] int32 each, valid where the tile words say) and tile words ([rows, ld / 128]
+        int32: count of the tile's candidates, top bit set when they are in the candidate lines
+        rather than the score line).  Debug/test aid."""
+        import torch
+        lc = -(-self.p.max_seqlen_k // self.p.cmp_ratio)
+        ld = max(128, -(-lc // 128) * 128)
+        line = self.rows * ld * 4
+        ws = self.workspace.view(torch.uint8)
+        o = 256 + line
+        code = ws[o:o + line].view(torch.int32).view(self.rows, ld)
+        idx = ws[o + line:o + 2 * line].view(torch.int32).view(self.rows, ld)
+        info = ws[o + 2 * line:o + 2 * line + line // 128].view(torch.int32).view(self.rows, ld // 128)
+        return code, idx, info
 
 
 class Plan:

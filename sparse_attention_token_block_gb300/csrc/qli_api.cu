@@ -74,6 +74,8 @@ qli_status check(const qli_problem* p, const char** why)
                QLI_ERR_INVALID_ARG);
     QLI_REJECT(p->key_stride != 0 && ((int64_t)p->key_stride < (int64_t)p->block_size * 128 || p->key_stride % 16 != 0),
                "key_stride must be 0 or a multiple of 16 of at least block_size * 128", QLI_ERR_INVALID_ARG);
+    QLI_REJECT(p->split_topk < QLI_SPLIT_AUTO || p->split_topk > QLI_SPLIT_OFF, "split_topk must be 0, 1 or 2",
+               QLI_ERR_INVALID_ARG);
 #undef QLI_REJECT
     if (why) *why = "ok";
     return QLI_OK;
@@ -85,6 +87,16 @@ int group_tokens_of(const qli_problem* p)
 {
     if (p->layout_q == QLI_BSND) return p->max_q_tokens <= 1 ? 1 : (p->max_q_tokens < kMultiTokens ? p->max_q_tokens : kMultiTokens);
     return kMultiTokens;
+}
+
+// Whether the indexer's top-k runs in two stages (split-local selection in the one-token score
+// kernel, then the merge): only on request.  Measured on GB300 it is slower than the one-stage
+// top-k at every size tried (32 rows of 8k-32k and of 64k-128k keys, k = 64 ... 2048): each chunk's
+// selection stalls its CTA's key stream for ~18k cycles (four warps that run alone on their
+// sub-partitions), more than the merge saves, so AUTO keeps one stage.
+bool split_topk_of(const qli_problem* p, int group_tokens)
+{
+    return group_tokens == 1 && p->split_topk == QLI_SPLIT_ON;
 }
 
 int64_t max_groups_of(const qli_problem* p)
@@ -124,6 +136,7 @@ Params params_of(const qli_problem* q)
     p.hash = problem_hash(p);
     p.complete_blocks = q->mask_complete_blocks;
     p.key_stride = q->key_stride ? q->key_stride : q->block_size * kDim;
+    p.split_topk = split_topk_of(q, p.group_tokens) ? 1 : 0;
 #ifdef QLI_TESTING
     // failure-detection test switch of the testing build only (no device fault involved): the
     // score kernel's producer issues no copies (1), or its converters consume nothing (2) so the
@@ -141,7 +154,16 @@ WsLayout ws_layout(const Params& p)
     WsLayout w;
     w.scores_off = kWsHeaderBytes;
     w.ld = p.ld;
-    w.total = w.scores_off + (size_t)p.rows * (size_t)p.ld * sizeof(uint32_t);
+    const size_t line = (size_t)p.rows * (size_t)p.ld * sizeof(uint32_t);
+    w.cand_code_off = w.scores_off + line;
+    w.cand_idx_off = w.cand_code_off;
+    w.info_off = w.cand_code_off;
+    w.total = w.scores_off + line;
+    if (p.split_topk) {
+        w.cand_idx_off = w.cand_code_off + line;
+        w.info_off = w.cand_idx_off + line;
+        w.total = w.info_off + line / kTileKeys;
+    }
     return w;
 }
 
@@ -283,6 +305,13 @@ qli_status check_call(const qli_problem* p, const int32_t* metadata, size_t meta
 
 namespace {
 
+// The split-local selection's buffers inside the workspace
+SplitBufs split_bufs(uint8_t* ws, const WsLayout& W)
+{
+    return SplitBufs{reinterpret_cast<uint32_t*>(ws + W.cand_code_off), reinterpret_cast<uint32_t*>(ws + W.cand_idx_off),
+                     reinterpret_cast<uint32_t*>(ws + W.info_off)};
+}
+
 // The score stage; *launched tells whether a kernel was enqueued
 qli_status score_impl(const qli_problem* p, const void* query, const void* key, const void* weights,
                       const void* q_scale, const void* k_scale, const int32_t* seq_lens_q,
@@ -305,10 +334,11 @@ qli_status score_impl(const qli_problem* p, const void* query, const void* key, 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     CUtensorMap tm;
     if (!encode_key_map(&tm, key, P)) return QLI_ERR_CUDA;
-    auto launch = P.group_tokens == 1 ? launch_score : launch_score_multi;
+    auto launch = P.group_tokens != 1 ? launch_score_multi : (P.split_topk ? launch_score_split : launch_score);
     cudaError_t e = launch(P, &tm, query, key, weights, q_scale, k_scale, seq_lens_q, seq_lens_k, block_table,
-                           metadata, reinterpret_cast<uint32_t*>(ws + W.scores_off), reinterpret_cast<uint32_t*>(ws),
-                           score_ctas(sms, P.group_tokens), static_cast<cudaStream_t>(stream));
+                           metadata, reinterpret_cast<uint32_t*>(ws + W.scores_off), split_bufs(ws, W),
+                           reinterpret_cast<uint32_t*>(ws), score_ctas(sms, P.group_tokens),
+                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return QLI_ERR_CUDA;
     *launched = true;
     return QLI_OK;
@@ -336,8 +366,8 @@ qli_status topk_impl(const qli_problem* p, const int32_t* block_table, const int
     const bool small = P.ld <= kTopkSmallRows && P.rows > sms;
     auto launch = small ? launch_topk_small : launch_topk;
     cudaError_t e = launch(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),
-                           reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values, after_score,
-                           small ? 2 * sms : 0, static_cast<cudaStream_t>(stream));
+                           split_bufs(ws, W), reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values,
+                           after_score, small ? 2 * sms : 0, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
 

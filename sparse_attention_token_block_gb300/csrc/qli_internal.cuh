@@ -48,6 +48,23 @@ inline int score_first_ctas(int sms, int gt)
 // Top-k: candidates held per row
 constexpr int kTopkCap = 4096;
 
+// Split-local selection (the indexer's top-k in two stages: per split of a row, then across the
+// splits).  With it on, each one-token score CTA cuts its share of a row into chunks -- the parts of
+// the row's aligned kChunkKeys-key blocks that fall in its range -- and, once a chunk's scores are
+// all in its shared memory, keeps the chunk's exact top min(k, chunk keys) by (score descending,
+// index ascending).  A chunk of more than k keys writes those k candidates, in index order, to the
+// candidate lines at the chunk's own first key; a shorter chunk keeps its keys where the score line
+// has them.  One word per 128-key tile of a row says how many candidates the tile's slots hold and
+// where (kTileFromCandidates set: the candidate lines; clear: the score line); every tile that has
+// visible keys is written on every call, so the top-k reads only current words.
+constexpr int kChunkKeys = 4096;
+constexpr uint32_t kTileFromCandidates = 0x80000000u;
+struct SplitBufs {
+    uint32_t* code;   // [rows, ld] candidate codes (ordered uint32 scores)
+    uint32_t* idx;    // [rows, ld] candidate key indices
+    uint32_t* info;   // [rows, ld / kTileKeys] tile words
+};
+
 // Device error bits (sticky word at the start of the workspace)
 constexpr uint32_t kErrLength = 1u;       // a length beyond its bound / non-monotone prefix sums
 constexpr uint32_t kErrPage = 2u;         // a block_table entry outside [0, num_blocks)
@@ -116,6 +133,9 @@ constexpr size_t kWsHeaderBytes = 256;
 struct WsLayout {
     size_t scores_off;     // uint32 ordered scores [rows, ld]
     int64_t ld;            // row stride in elements (max Lc rounded up to a tile)
+    size_t cand_code_off;  // split-local selection only: candidate codes [rows, ld]
+    size_t cand_idx_off;   //   candidate indices [rows, ld]
+    size_t info_off;       //   tile words [rows, ld / kTileKeys]
     size_t total;
 };
 
@@ -135,6 +155,7 @@ struct Params {
     int32_t complete_blocks;   // mode 3 visibility: 0 ceil((p + 1) / cmp), 1 floor((p + 1) / cmp)
     int32_t key_stride;        // elements between key pages
     int32_t group_tokens;      // query tokens per group (1, or up to kMultiTokens)
+    int32_t split_topk;        // 1: split-local selection (one-token groups only), then the merge
     int64_t ld;            // score line stride
     MetaLayout meta;
 };
@@ -273,25 +294,32 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Launchers (defined in the kernel translation units)
 cudaError_t launch_metadata(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                             int32_t* meta, int num_ctas, int first_ctas, cudaStream_t st);
+// (the score launchers share one signature; only launch_score_split writes `split`)
 cudaError_t launch_score(const Params& p, const void* tmap_key, const void* query, const void* key,
                          const void* weights, const void* q_scale, const void* k_scale,
                          const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                          const int32_t* block_table, const int32_t* meta, uint32_t* scores,
-                         uint32_t* err_word, int grid, cudaStream_t st);
+                         const SplitBufs& split, uint32_t* err_word, int grid, cudaStream_t st);
 cudaError_t launch_score_multi(const Params& p, const void* tmap_key, const void* query, const void* key,
                                const void* weights, const void* q_scale, const void* k_scale,
                                const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                                const int32_t* block_table, const int32_t* meta, uint32_t* scores,
-                               uint32_t* err_word, int grid, cudaStream_t st);
-// (max_ctas > 0: at most that many CTAs, each striding over the rows; else one CTA per row)
+                               const SplitBufs& split, uint32_t* err_word, int grid, cudaStream_t st);
+cudaError_t launch_score_split(const Params& p, const void* tmap_key, const void* query, const void* key,
+                               const void* weights, const void* q_scale, const void* k_scale,
+                               const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                               const int32_t* block_table, const int32_t* meta, uint32_t* scores,
+                               const SplitBufs& split, uint32_t* err_word, int grid, cudaStream_t st);
+// (max_ctas > 0: at most that many CTAs, each striding over the rows; else one CTA per row;
+// `split` is read when p.split_topk is set)
 cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
-                        const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
-                        bool after_score, int max_ctas, cudaStream_t st);
+                        const uint32_t* scores, const SplitBufs& split, uint32_t* err_word, int32_t* out,
+                        float* values, bool after_score, int max_ctas, cudaStream_t st);
 // the same top-k with half the threads and a row cache of kTopkSmallRows keys (two CTAs per SM)
 constexpr int kTopkSmallRows = 8192;
 cudaError_t launch_topk_small(const Params& p, const int32_t* block_table, const int32_t* meta,
-                              const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
-                              bool after_score, int max_ctas, cudaStream_t st);
+                              const uint32_t* scores, const SplitBufs& split, uint32_t* err_word, int32_t* out,
+                              float* values, bool after_score, int max_ctas, cudaStream_t st);
 cudaError_t launch_quantize_vectors(const void* x_bf16, int64_t nvec, void* codes, void* scales, bool fp8,
                                     bool scale_f32, cudaStream_t st);
 cudaError_t launch_quantize_keys(const Params& p, const void* k_bf16, int64_t tokens, const int32_t* tok_batch,

@@ -49,8 +49,16 @@ namespace qli {
 namespace {
 
 constexpr int kGT = QLI_SCORE_GT;                 // most query tokens per group
+#if QLI_SCORE_SPLIT
+constexpr bool kSplit = true;                     // split-local selection in the epilogue
+static_assert(QLI_SCORE_GT == 1, "split-local selection is built for one-token groups");
+#else
+constexpr bool kSplit = false;
+#endif
 constexpr int kCtasPerSm = kGT == 1 ? 2 : 1;      // resident score CTAs per SM
-constexpr int kStages = kGT == 1 ? 4 : 5;         // key ring depth
+// key ring depth: two to four stages run the one-token kernel equally fast (measured), and three
+// leave the call ~1 us shorter; the split build takes two to make room for its chunk
+constexpr int kStages = kSplit ? 2 : (kGT == 1 ? 3 : 5);
 constexpr int kScaleSlots = 10;                  // scale ring depth (released by the epilogue)
 constexpr int kGroups = 1;                       // converter groups; tile i -> i % groups
 // epilogue groups: tile i -> group i % kEpiGroups, which always drains D buffer i % kNumD.  Groups
@@ -101,9 +109,14 @@ enum {
     kBarDfull = kBarAempty + kNumA,
     kBarDempty = kBarDfull + kNumD,
     kBarDrain = kBarDempty + kNumD,      // the MMA thread's final commit (all its MMAs done)
-    kNumBars = kBarDrain + 1
+    kBarEpi = kBarDrain + 1,             // split build: the epilogue warps meet (4 arrivals)
+    kNumBars = kBarEpi + (kSplit ? 1 : 0)
 };
-constexpr int kOffMisc = kOffBars + kNumBars * 8;
+// split build: one chunk of scores, then the selection's histograms (two buffers of one 256-bin
+// histogram per epilogue warp) and 16 scratch words
+constexpr int kOffChunk = (kOffBars + kNumBars * 8 + 15) & ~15;
+constexpr int kOffSel = kOffChunk + (kSplit ? kChunkKeys * 4 : 0);
+constexpr int kOffMisc = kOffSel + (kSplit ? (2 * 4 * 256 + 16) * 4 : 0);
 static_assert(kOffKring % 1024 == 0 && kOffQbuf % 1024 == 0, "shared-memory alignment");
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;   // + slack to align the base to 1024
 static_assert(kSmemBytes <= (kCtasPerSm == 2 ? 113 : 226) * 1024, "the CTAs of an SM must fit in its shared memory");
@@ -123,6 +136,9 @@ struct ScoreArgs {
     const int32_t* seq_lens_k;
     uint32_t* scores;
     uint32_t* err;
+#if QLI_SCORE_SPLIT
+    SplitBufs split;
+#endif
 };
 
 struct Shared {
@@ -502,6 +518,234 @@ __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, Span s
     }
 }
 
+#if QLI_SCORE_SPLIT
+// ------------------------------------------------------------------------------------------------
+// Split-local selection (epilogue warps of the split build)
+// ------------------------------------------------------------------------------------------------
+// The four epilogue warps meet on an mbarrier (one arrival per warp) whose wait is bounded like
+// every other: a named barrier could not give up if a warp had left on an abort.  The waiters spin
+// on the non-blocking test (the other warps arrive within a few hundred cycles; a suspended
+// wait resumes far later) and look at the abort flag and the clock every 256 tests.
+__device__ __forceinline__ bool epi_sync(const Shared& S, uint32_t& par, uint32_t* err)
+{
+    __syncwarp();
+    uint64_t* bar = &S.bars[kBarEpi];
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
+    bool ok = true;
+    uint64_t t0 = 0;
+    for (uint32_t spin = 1; !ptx::mbar_test_wait(bar, par); ++spin) {
+        if ((spin & 255) == 0) {
+            if (*S.abort) {
+                ok = false;
+                break;
+            }
+            const uint64_t now = ptx::globaltimer();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kWaitLimitNs) {
+                *S.abort = 1;
+                atomicOr(err, kErrTimeout);
+                ok = false;
+                break;
+            }
+        }
+    }
+    par ^= 1u;
+    return ok;
+}
+
+// The chunk [c0, c1) of output row `row` has all its codes in the chunk buffer (position j mod
+// kChunkKeys).  A chunk of at most k keys keeps them in the score line; a longer one writes its
+// exact top k by (code descending, index ascending) to the candidate lines at [c0, c0 + k), in
+// index order.  Either way the chunk's tile words say where its candidates are.  Within a chunk
+// the index part of the sort key is fixed above bit 11, so the selection ranks the 44-bit keys
+// K = code << 12 | (4095 - position): a radix select from the highest bit in which the chunk's
+// keys differ, 8 bits a pass, until the digit that holds the k-th key holds exactly the keys still
+// needed; every key with K at or above the prefix found is kept.  Each epilogue warp runs alone on
+// its SM sub-partition here, so the loops take four keys a thread per 16-byte load and count into
+// a histogram per warp with plain shared atomics, and the histograms are double-buffered (the
+// next pass's is cleared while warp 0 scans this one).  False: the CTA is aborting.
+__device__ __noinline__ bool chunk_select(const ScoreArgs& a, int64_t row, int c0, int c1, uint32_t& par)
+{
+    const Shared S = shared_view();
+    const int tid = threadIdx.x - kEpiWarp0 * 32, lane = tid & 31, warp = tid >> 5;
+    const int L = c1 - c0, k = a.p.sparse_count;
+    uint32_t* info = a.split.info + row * (a.p.ld / kTileKeys);
+    const int t0 = c0 / kTileKeys, nt = (L + kTileKeys - 1) / kTileKeys;
+    if (L <= k) {
+        // every key is a candidate: the chunk's tiles point at the score line (no one reads the
+        // chunk buffer, so the next tiles may overwrite it at once)
+        if (tid < nt) info[t0 + tid] = (uint32_t)min(kTileKeys, L - tid * kTileKeys);
+        return true;
+    }
+    // c0 is a multiple of 128, so the chunk's 4-key vectors are 16-byte aligned and the last one
+    // ends inside the buffer
+    const uint4* buf4 = reinterpret_cast<const uint4*>(S.base + kOffChunk) + ((c0 & (kChunkKeys - 1)) >> 2);
+    const int nv = (L + 3) >> 2;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(S.base + kOffSel);    // [2][4 warps][256]
+    uint32_t* misc = hist + 2 * 4 * 256;                                // [16] scratch
+    const uint32_t p0 = (uint32_t)(kChunkKeys - 1 - (c0 & (kChunkKeys - 1)));   // 4095 - position of c0
+    if (!epi_sync(S, par, a.err)) return false;                         // every code is in place
+    // the highest bit in which the keys differ; the first histogram buffer is cleared meanwhile
+    uint32_t mx = 0, mn = 0xFFFFFFFFu;
+    for (int v = tid; v < nv; v += kGroupThreads) {
+        const uint4 q = buf4[v];
+        const uint32_t c[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (4 * v + e < L) {
+                mx = max(mx, c[e]);
+                mn = min(mn, c[e]);
+            }
+    }
+    for (int i = tid; i < 4 * 256; i += kGroupThreads) hist[i] = 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if (lane == 0) {
+        misc[warp] = mx;
+        misc[4 + warp] = mn;
+    }
+    if (!epi_sync(S, par, a.err)) return false;
+    mx = max(max(misc[0], misc[1]), max(misc[2], misc[3]));
+    mn = min(min(misc[4], misc[5]), min(misc[6], misc[7]));
+    // (L >= 2 keys: the positions of the first and last differ)
+    int hi = mx != mn ? 12 + 31 - __clz(mx ^ mn) : 31 - __clz(p0 ^ (p0 - (uint32_t)(L - 1)));
+    // every key shares the bits above hi (those of the first key): the prefix starts with them
+    uint64_t mask = ~((2ull << hi) - 1ull);
+    uint64_t prefix = (((uint64_t)mx << 12) | p0) & mask;
+    uint32_t rem = (uint32_t)k;
+    for (int ps = 0;; ++ps) {
+        const int lo = hi >= 7 ? hi - 7 : 0;
+        const uint32_t dmask = (2u << (hi - lo)) - 1u;
+        uint32_t* H = hist + (ps & 1) * 1024;
+        uint32_t* Hw = H + warp * 256;
+        // a chunk's leading digits take few values, so most lanes would add to one bin: the lanes
+        // whose digit is lane 0's add through one atomic, the others each through their own
+        for (int vw = warp * 32; vw < nv; vw += kGroupThreads) {       // warp-uniform trip count
+            const int v = vw + lane;
+            uint32_t c[4] = {0u, 0u, 0u, 0u};
+            if (v < nv) {
+                const uint4 q = buf4[v];
+                c[0] = q.x;
+                c[1] = q.y;
+                c[2] = q.z;
+                c[3] = q.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 4 * v + e;
+                const uint64_t K = ((uint64_t)c[e] << 12) | (p0 - (uint32_t)i);
+                const bool in = v < nv && i < L && (K & mask) == prefix;
+                const uint32_t d = in ? (uint32_t)(K >> lo) & dmask : 0xFFFFFFFFu;
+                const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+                const unsigned same = __ballot_sync(0xffffffffu, in && d == d0);
+                if (lane == 0 && same) atomicAdd(&Hw[d0], (uint32_t)__popc(same));
+                else if (in && d != d0) atomicAdd(&Hw[d], 1u);
+            }
+        }
+        if (!epi_sync(S, par, a.err)) return false;
+        if (warp == 0) {
+            // lane l sums digits 255 - 8l down to 248 - 8l over the four warps' histograms; the
+            // running count from the top finds the digit where it reaches rem
+            uint32_t c8[8], sum = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int d = 255 - 8 * lane - q;
+                c8[q] = H[d] + H[256 + d] + H[512 + d] + H[768 + d];
+                sum += c8[q];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, incl >= rem);
+            if (lane == __ffs(hit) - 1) {
+                uint32_t above = incl - sum;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (above + c8[q] >= rem) {
+                        misc[8] = 255 - 8 * lane - q;
+                        misc[9] = rem - above;
+                        misc[10] = c8[q] == rem - above ? 1u : 0u;
+                        break;
+                    }
+                    above += c8[q];
+                }
+            }
+        } else {
+            uint32_t* Hn = hist + ((ps + 1) & 1) * 1024;       // the next pass's histograms
+            for (int i = tid - 32; i < 1024; i += kGroupThreads - 32) Hn[i] = 0;
+        }
+        if (!epi_sync(S, par, a.err)) return false;
+        prefix |= (uint64_t)misc[8] << lo;
+        mask |= (uint64_t)dmask << lo;
+        rem = misc[9];
+        if (misc[10] != 0 || lo == 0) break;     // (all bits fixed: one key, rem = 1)
+        hi = lo - 1;
+    }
+    // the kept keys (K >= prefix) in index order: warp w takes vectors [w per, (w + 1) per), lane
+    // l the vector of its step at offset l; a scan of the lanes' counts places each key
+    uint32_t* out_code = a.split.code + row * a.p.ld + c0;
+    uint32_t* out_idx = a.split.idx + row * a.p.ld + c0;
+    const int per = (nv + 3) >> 2;
+    const int v0 = warp * per, v1 = min(nv, v0 + per);
+    auto takes = [&](int v, uint32_t (&c)[4]) -> uint32_t {    // bit e: key 4v + e is kept
+        uint32_t m = 0;
+        if (v < v1) {
+            const uint4 q = buf4[v];
+            c[0] = q.x;
+            c[1] = q.y;
+            c[2] = q.z;
+            c[3] = q.w;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 4 * v + e;
+                if (i < L && (((uint64_t)c[e] << 12) | (p0 - (uint32_t)i)) >= prefix) m |= 1u << e;
+            }
+        }
+        return m;
+    };
+    uint32_t cnt = 0;
+    for (int vs = v0; vs < v1; vs += 32) {
+        uint32_t c[4];
+        cnt += __popc(takes(vs + lane, c));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0) misc[12 + warp] = cnt;
+    if (!epi_sync(S, par, a.err)) return false;
+    uint32_t base = 0;
+    for (int w = 0; w < warp; ++w) base += misc[12 + w];
+    for (int vs = v0; vs < v1; vs += 32) {
+        uint32_t c[4];
+        const int v = vs + lane;
+        uint32_t m = takes(v, c);
+        const uint32_t n = __popc(m);
+        uint32_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        uint32_t pos = base + incl - n;
+        while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1;
+            out_code[pos] = c[e];
+            out_idx[pos] = (uint32_t)(c0 + 4 * v + e);
+            ++pos;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (tid < nt) info[t0 + tid] = kTileFromCandidates | (uint32_t)max(0, min(kTileKeys, k - tid * kTileKeys));
+    return epi_sync(S, par, a.err);               // the chunk buffer may be overwritten again
+}
+#endif
+
 // ------------------------------------------------------------------------------------------------
 // Epilogue warps
 // ------------------------------------------------------------------------------------------------
@@ -517,6 +761,9 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp
     const int key_lane = tid;
     const Params& p = a.p;
     uint32_t tile_i = 0;
+#if QLI_SCORE_SPLIT
+    uint32_t epi_par = 0;       // phase of the epilogue warps' meeting barrier
+#endif
     Unit xn = read_unit(a, sp.g0, sp);
     for (int64_t u = sp.g0; u < sp.g1; ++u) {
         const int uu = (int)(u - sp.g0);
@@ -612,6 +859,18 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp
             for (int tt = 0; tt < kGT; ++tt)
                 if (tt < x.q_cnt && j < nvis[tt])
                     a.scores[(int64_t)(x.row0 + tt) * p.ld + j] = ordered_code(score[tt]);
+#if QLI_SCORE_SPLIT
+            // the chunk buffer takes the code too; a chunk ends with the unit or at an aligned
+            // kChunkKeys boundary (the units of one-token groups hold visible keys only)
+            if (j < nvis[0]) reinterpret_cast<uint32_t*>(S.base + kOffChunk)[j & (kChunkKeys - 1)] = ordered_code(score[0]);
+            {
+                const int f = x.kb + t * kTileKeys;
+                if (t == x.ntiles - 1 || ((f + kTileKeys) & (kChunkKeys - 1)) == 0) {
+                    const int c0 = max(x.kb, f & ~(kChunkKeys - 1)), c1 = min(nvis[0], f + kTileKeys);
+                    if (!chunk_select(a, x.row0, c0, c1, epi_par)) return;
+                }
+            }
+#endif
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&S.bars[kBarQempty + qb]);
@@ -643,6 +902,7 @@ __device__ void init_barriers(const Shared& S)
         ptx::mbar_init(&S.bars[kBarDempty + i], 4);
     }
     ptx::mbar_init(&S.bars[kBarDrain], 1);
+    if (kSplit) ptx::mbar_init(&S.bars[kBarEpi], 4);
     ptx::fence_mbar_init();
 }
 
@@ -750,9 +1010,10 @@ cudaError_t QLI_SCORE_LAUNCHER(const Params& p, const void* tmap_key, const void
                          const void* weights, const void* q_scale, const void* k_scale,
                          const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                          const int32_t* block_table, const int32_t* meta, uint32_t* scores,
-                         uint32_t* err_word, int grid, cudaStream_t st)
+                         const SplitBufs& split, uint32_t* err_word, int grid, cudaStream_t st)
 {
     (void)key;
+    (void)split;
     ScoreArgs a;
     a.p = p;
     a.seq_lens_q = seq_lens_q;
@@ -765,6 +1026,9 @@ cudaError_t QLI_SCORE_LAUNCHER(const Params& p, const void* tmap_key, const void
     a.meta = meta;
     a.scores = scores;
     a.err = err_word;
+#if QLI_SCORE_SPLIT
+    a.split = split;
+#endif
     const CUtensorMap* tm = static_cast<const CUtensorMap*>(tmap_key);
     if (p.qk_fp8) {
         return p.scale_f32 ? launch_variant<true, true>(tm, a, grid, st)

@@ -25,6 +25,13 @@
 // kCap (heavy ties) an exact radix select on the 64-bit sort keys finds the k-th key and exactly k
 // keys are gathered; when a bin holds more than kBigBucket candidates, a block-wide bitonic sort
 // orders them instead of step 4.
+// With the split-local selection on, a row's candidates are the keys each chunk of the score
+// CTAs kept (see SplitBufs): the row's tile words give each 128-key tile's count and source, a scan
+// gives each tile its place, and the candidates are gathered into the row cache in index order;
+// the same steps then order them by position, which follows index order, and each position is
+// mapped back to its key index.  Rows whose candidates do not fit (more than kSplitKeys, or more
+// than kSplitTiles tiles) are ordered from the whole score line, which the score kernel still
+// writes.
 // The first min(k, n) indices are written, then -1 up to sparse_count.  Rows with no visible key,
 // rows of an invalid batch and rows whose batch's block_table names a page outside the pool are all
 // -1.
@@ -43,15 +50,24 @@ constexpr int kCtasPerSm = kThreads == 1024 ? 1 : 2;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSampleKeys = 1024;             // keys sampled to bound the candidates' codes
 constexpr int kCap = kTopkCap;                // candidates held in shared memory
-constexpr int kSamples = 2048;
+constexpr int kSamples = 8192;               // samples of an uncached row (held in the row cache)
 constexpr int kBins = QLI_TOPK_BINS;          // ordering bins
 constexpr int kBinsPerThread = kBins / kThreads;
 constexpr int kSampleBins = 2048;             // bins of the sample histogram
 constexpr int kBigBucket = 256;
 constexpr int kCacheKeys = QLI_TOPK_CACHE_KEYS;   // score lines up to this length are cached in smem
 static_assert(kCacheKeys >= 2 * kTopkCap, "the row cache doubles as the uncached rows' scatter target");
+static_assert(kCacheKeys >= kSamples, "the row cache holds an uncached row's samples");
 constexpr int kMiscWords = 128;               // scratch: [0, 64) block reductions, [100, 111) single values
 constexpr int kSmemBytes = (kCacheKeys + kBins + 3 * kCap + 256 + kMiscWords) * 4 + 16;
+// Split-local candidates: gathered into the row cache from word kSplitBase on (the sampled path
+// scatters into the first 2 kCap words), at most kSplitKeys of them; tile offsets for rows of up
+// to kSplitTiles tiles follow the rest of shared memory
+constexpr int kSplitBase = kCacheKeys >= 3 * kCap ? 2 * kCap : 0;
+constexpr int kSplitKeys = kSplitBase > 0 ? kCacheKeys - kSplitBase : kCap;
+constexpr int kSplitTiles = kThreads == 1024 ? 2048 : kCacheKeys / kTileKeys;
+constexpr int kSmemSplitBytes = kSmemBytes + (kSplitTiles + 1) * 4;
+static_assert(kSmemSplitBytes <= 227 * 1024, "shared memory");
 
 struct TopkArgs {
     Params p;
@@ -61,6 +77,7 @@ struct TopkArgs {
     uint32_t* err;
     int32_t* out;
     float* values;     // optional: the score of each index written, -inf beside -1
+    SplitBufs split;   // the split-local candidates (read by the merging build only)
     // 1 when this launch directly follows the library's score kernel in the stream: that kernel
     // lets its dependents start only after its own griddepcontrol.wait returned, i.e. after the
     // metadata kernel before it had completed, so the metadata and the (unchanged) block_table can
@@ -108,6 +125,7 @@ struct Smem {
     uint32_t* hist;   // [256] radix-select digits
     uint32_t* misc;   // [kMiscWords] reduction scratch
     uint64_t* bar;    // bulk-copy barrier
+    uint32_t* toff;   // merging build: [kSplitTiles + 1] tile offsets (kTileFromCandidates: source)
 };
 
 extern __shared__ __align__(16) uint8_t topk_smem[];
@@ -125,6 +143,7 @@ __device__ __forceinline__ Smem smem_view()
     S.hist = S.outv + kCap;
     S.misc = S.hist + 256;
     S.bar = reinterpret_cast<uint64_t*>(S.misc + kMiscWords);
+    S.toff = reinterpret_cast<uint32_t*>(topk_smem + kSmemBytes);
     return S;
 }
 
@@ -662,23 +681,94 @@ __device__ __noinline__ void exact_topk(const uint32_t* line, int64_t n, int k)
 
 // Uncached rows (longer than kCacheKeys): the keys at or above the rank-r largest of kSamples
 // evenly spaced keys of the line, r = 1.15 k S / n + 4 sqrt(k S / n) + 2, gathered from global
-// memory into S.key / S.val; returns their count.
+// memory into S.key / S.val; returns their count.  The samples go to the row cache, which such a
+// row does not use: with S = 8192 the count expected at k = 2048 stays near 1.5 k up to 2^17 keys
+// (about 4.4 standard deviations below kCap), where 2048 samples left it near kCap and the exact
+// fallback often ran.
 __device__ __noinline__ int gather_sampled(const uint32_t* line, int64_t n, int k)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
     for (int i = tid; i < kSamples; i += kThreads) {
         const int64_t j = ((int64_t)i * n) / kSamples;
-        S.key[i] = __ldg(line + j);
+        S.cache[i] = __ldg(line + j);
     }
     __syncthreads();
     const float lam = (float)k * (float)kSamples / (float)n;   // samples expected above the k-th
     int rank = (int)(1.15f * lam + 4.0f * sqrtf(lam) + 2.0f);
     rank = rank < 1 ? 1 : (rank > kSamples ? kSamples : rank);
-    const uint32_t* samp = S.key;
+    const uint32_t* samp = S.cache;
     const uint64_t t = radix_select(
         S, kSamples, rank, [&](int64_t i) { return static_cast<uint64_t>(samp[i]) << 32; }, 56);
     return gather(S, line, n, t & 0xFFFFFFFF00000000ull);
+}
+
+// Merging build: the row's tile words -> exclusive offsets (with the source bit) in S.toff[0,
+// ntile) and the total in S.toff[ntile]; returns the candidate count, or -1 when the row is to be
+// ordered from its score line instead (too many tiles or candidates, or fewer candidates than the
+// row needs, which only a failed score launch leaves).  Block-wide.
+__device__ __noinline__ int split_offsets(const TopkArgs& a, int64_t row, int64_t n, int need)
+{
+    const Smem S = smem_view();
+    const int tid = threadIdx.x;
+    const int64_t ntile = (n + kTileKeys - 1) / kTileKeys;
+    if (ntile > kSplitTiles) return -1;
+    const uint32_t* info = a.split.info + row * (a.p.ld / kTileKeys);
+    constexpr int kPer = (kSplitTiles + kThreads - 1) / kThreads;   // tiles per thread, contiguous
+    uint32_t w[kPer], sum = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int64_t t = (int64_t)tid * kPer + q;
+        w[q] = t < ntile ? __ldcg(info + t) : 0u;
+        sum += min(w[q] & ~kTileFromCandidates, (uint32_t)kTileKeys);
+    }
+    uint32_t total;
+    uint32_t off = block_excl_scan(sum, &total, S.misc);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int64_t t = (int64_t)tid * kPer + q;
+        if (t < ntile) S.toff[t] = off | (w[q] & kTileFromCandidates);
+        off += min(w[q] & ~kTileFromCandidates, (uint32_t)kTileKeys);
+    }
+    if (tid == 0) S.toff[ntile] = total;
+    __syncthreads();
+    return (total > (uint32_t)kSplitKeys || total < (uint32_t)need) ? -1 : (int)total;
+}
+
+// Merging build: the candidates of the row's tiles, in tile order, into dst[0, total) (a warp per
+// tile, four 32-key loads per lane)
+__device__ __noinline__ void split_gather(const TopkArgs& a, int64_t row, int64_t ntile, uint32_t* dst)
+{
+    const Smem S = smem_view();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t base = row * a.p.ld;
+    for (int64_t t = warp; t < ntile; t += kWarps) {
+        const uint32_t o0 = S.toff[t], o1 = S.toff[t + 1] & ~kTileFromCandidates;
+        const uint32_t off = o0 & ~kTileFromCandidates, c = o1 - off;
+        if (c == 0) continue;
+        const uint32_t* src = ((o0 & kTileFromCandidates) ? a.split.code : a.scores) + base + t * kTileKeys;
+        uint32_t v[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) v[m] = (uint32_t)(lane + 32 * m) < c ? __ldcg(src + lane + 32 * m) : 0u;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            if ((uint32_t)(lane + 32 * m) < c) dst[off + lane + 32 * m] = v[m];
+    }
+    __syncthreads();
+}
+
+// Merging build: the key index of candidate position q (the last tile whose offset is <= q holds it)
+__device__ __forceinline__ uint32_t split_key(const TopkArgs& a, int64_t row, int64_t ntile, uint32_t q)
+{
+    const Smem S = smem_view();
+    int64_t lo = 0, hi = ntile - 1;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if ((S.toff[mid] & ~kTileFromCandidates) <= q) lo = mid; else hi = mid - 1;
+    }
+    const uint32_t o = S.toff[lo], r = q - (o & ~kTileFromCandidates);
+    return (o & kTileFromCandidates) ? __ldcg(a.split.idx + row * a.p.ld + lo * kTileKeys + r)
+                                     : (uint32_t)(lo * kTileKeys + r);
 }
 
 // Bounded wait for the row cache's bulk copy (false: it did not land within about 2 s)
@@ -696,7 +786,9 @@ __device__ bool wait_copy(uint64_t* bar, uint32_t& parity)
     return __syncthreads_and(ok);
 }
 
-// One CTA per row (the grid strides over rows).
+// One CTA per row (the grid strides over rows).  kMerge: the rows' candidates come from the
+// split-local selection.
+template <bool kMerge>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid_constant__ TopkArgs a)
 {
     const Smem S = smem_view();
@@ -756,8 +848,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         const int64_t n = ri.n;
         const uint32_t* line = a.scores + row * p.ld;
         const int need = (int)(n < k ? n : k);
-        const bool cached = n > 0 && n <= kCacheKeys;
         __syncthreads();                           // the previous row is done with shared memory
+        int M = -1;                                // merging build: the row's candidates
+        if constexpr (kMerge) {
+            if (n > 0) M = split_offsets(a, row, n, need);
+        }
+        const bool cached = n > 0 && n <= kCacheKeys && M < 0;
         if (tid == 0) {
             s_bad = 0;
             if (cached) {
@@ -768,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
             }
             // the CTA's next row (many rows per CTA, e.g. a prefill's) comes from DRAM: ask for its
             // line's first kCacheKeys codes now, so that its copy finds them in L2
-            if (row + gridDim.x < p.rows) {
+            if (!kMerge && row + gridDim.x < p.rows) {
                 const int64_t nb = (p.ld < kCacheKeys ? p.ld : kCacheKeys) * 4;
                 asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(line + gridDim.x * p.ld),
                              "r"((uint32_t)nb)
@@ -783,9 +879,35 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
             if (!copy_ok && tid == 0) atomicOr(a.err, kErrTimeout);
         }
         const uint32_t* result = S.outv;           // ordered indices of this row
+        const uint32_t* msrc = S.cache + kSplitBase;   // merging: the gathered candidates
         if (n > 0 && copy_ok) {
             int st = kBinTooMany;
-            if (cached) {
+            if (kMerge && M >= 0) {
+                // the same orders over the candidates' positions (index order)
+                split_gather(a, row, (n + kTileKeys - 1) / kTileKeys, S.cache + kSplitBase);
+                if (M <= kRankKeys) {
+                    rank_order(msrc, M, need);
+                    st = kBinOrdered;
+                } else if (M <= kCap) {
+                    uint32_t hi = 0, lo = 0xFFFFFFFFu;
+                    for (int i = tid; i < M; i += kThreads) {
+                        hi = max(hi, msrc[i]);
+                        lo = min(lo, msrc[i]);
+                    }
+                    block_max_min(&hi, &lo, S.misc);
+                    const Binning g = make_binning(lo, hi);
+                    count_bins(msrc, M, g);
+                    st = order_bins(msrc, nullptr, M, need, g, S.key, S.val);
+                } else if (kSplitBase > 0) {
+                    const Binning g = sample_bound(msrc, M, need);
+                    const int m = compact_and_count(msrc, M, g, true);
+                    st = order_bins(S.key, S.val, m, need, g, S.cache, S.cache + kCap);
+                }
+                if (st == kBinTooMany) {
+                    exact_topk(msrc, M, need);
+                    result = S.val;
+                }
+            } else if (cached) {
                 // bins over the whole range (short rows: every key is a candidate) or from a sample
                 if (n <= kRankKeys) {
                     rank_order(S.cache, (int)n, need);
@@ -837,14 +959,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         __syncthreads();
         const bool blank = n <= 0 || !copy_ok || s_bad;
         if (tid == 0 && s_bad) atomicOr(a.err, kErrPage);
-        for (int i = tid; i < k; i += kThreads) out[i] = (!blank && i < need) ? (int32_t)result[i] : -1;
+        const bool merged = kMerge && M >= 0;
+        const int64_t ntile = (n + kTileKeys - 1) / kTileKeys;
+        for (int i = tid; i < k; i += kThreads) {
+            int32_t v = -1;
+            if (!blank && i < need) v = merged ? (int32_t)split_key(a, row, ntile, result[i]) : (int32_t)result[i];
+            out[i] = v;
+        }
         if (a.values) {
-            // the written indices' scores, decoded from the row's score line (in L2)
+            // the written indices' scores, decoded from the row's score line (in L2) or, merging,
+            // from the gathered candidates
             float* val = a.values + row * k;
             for (int i = tid; i < k; i += kThreads) {
                 float v = -__int_as_float(0x7F800000);
                 if (!blank && i < need) {
-                    const uint32_t c = __ldg(line + result[i]);
+                    const uint32_t c = merged ? msrc[result[i]] : __ldg(line + result[i]);
                     v = __uint_as_float((c & 0x80000000u) ? (c & 0x7FFFFFFFu) : ~c);
                 }
                 val[i] = v;
@@ -856,17 +985,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
 }  // namespace
 
 cudaError_t QLI_TOPK_LAUNCHER(const Params& p, const int32_t* block_table, const int32_t* meta,
-                        const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
-                        bool after_score, int max_ctas, cudaStream_t st)
+                        const uint32_t* scores, const SplitBufs& split, uint32_t* err_word, int32_t* out,
+                        float* values, bool after_score, int max_ctas, cudaStream_t st)
 {
     if (p.rows == 0) return cudaSuccess;
-    TopkArgs a{p, block_table, meta, scores, err_word, out, values, after_score ? 1 : 0};
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    TopkArgs a{p, block_table, meta, scores, err_word, out, values, split, after_score ? 1 : 0};
+    auto kernel = p.split_topk ? topk_kernel<true> : topk_kernel<false>;
+    const int smem = p.split_topk ? kSmemSplitBytes : kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // one CTA per row, or (max_ctas > 0) at most max_ctas CTAs that stride over the rows
     int grid = p.rows < (1 << 30) ? p.rows : (1 << 30);
     if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-    return launch_pdl(topk_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, a);
+    return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, st, a);
 }
 
 }  // namespace qli

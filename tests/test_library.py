@@ -70,7 +70,8 @@ def test_validate_accepts_readme_example(Q):
     ("sparse_mode", 1, 1), ("cmp_ratio", 3, 1), ("cmp_ratio", 256, 1), ("query_quant_mode", 1, 1),
     ("key_quant_mode", 1, 1), ("pre_tokens", 5, 1), ("next_tokens", 0, 1), ("qk_dtype", 2, 1),
     ("scale_dtype", 7, 1), ("layout_q", 2, 1), ("max_blocks_per_seq", 3, 1),
-    ("return_value", 2, 1), ("num_blocks", 0, 1), ("batch", -1, 1),
+    ("return_value", 2, 1), ("num_blocks", 0, 1), ("batch", -1, 1), ("split_topk", 3, 1),
+    ("split_topk", -1, 1),
 ])
 def test_validate_rejects(Q, field, value, status):
     p = _ok_problem(Q)
@@ -78,6 +79,24 @@ def test_validate_rejects(Q, field, value, status):
     st, why = Q.validate(p)
     assert st == status, (field, why)
     assert Q.metadata_words(p) == 0 and Q.workspace_size(p) == 0
+
+
+def test_split_topk_workspace_and_auto_rule(Q):
+    """The two-stage top-k needs two more [rows, ld] lines and one word per tile in the
+    workspace; it runs only on request (AUTO keeps one stage), and a request for it is ignored when
+    S1 > 1."""
+    kw = dict(batch=4, max_q_tokens=1, num_blocks=600, block_size=64, max_blocks_per_seq=150,
+              max_seqlen_q=1, max_seqlen_k=9000)
+    rows, ld = 4, 9088
+    lines = 256 + rows * ld * 4
+    split = lines + 2 * rows * ld * 4 + rows * (ld // 128) * 4
+    size = lambda **o: Q.workspace_size(_ok_problem(Q, **dict(kw, **o)))
+    for k in (1, 64, 512, 2048):
+        assert size(sparse_count=k, split_topk=Q.SPLIT_OFF) == lines
+        assert size(sparse_count=k, split_topk=Q.SPLIT_AUTO) == lines
+        assert size(sparse_count=k, split_topk=Q.SPLIT_ON) == split
+    # query groups of several tokens: one stage whatever is asked
+    assert size(sparse_count=64, max_q_tokens=2, max_seqlen_q=2, split_topk=Q.SPLIT_ON) == 256 + 2 * (lines - 256)
 
 
 def test_invalid_calls_enqueue_nothing(Q):
