@@ -24,7 +24,9 @@ constexpr int kMaxSparse = 2048;
 // (MMA N = 64 * tokens).  One query token per sequence (decode): groups of one token, two score CTAs
 // per SM (separate CTAs keep more key copies in flight than one CTA with twice the resources).
 // Several tokens per sequence: groups of up to kMultiTokens tokens, one CTA per SM with all of the
-// SM's tensor memory, each converted key tile serving every token of the group.
+// SM's tensor memory, each converted key tile serving every token of the group (groups of two for
+// decodes of two or four tokens per sequence, which measured faster with a third accumulator
+// buffer; groups of three otherwise).
 constexpr int kTileKeys = 128;
 constexpr int kMultiTokens = 3;
 constexpr int kMaxCtas = 1024;            // bound on the split's CTA count (GB300 has 152 SMs)
@@ -305,6 +307,11 @@ cudaError_t launch_score_multi(const Params& p, const void* tmap_key, const void
                                const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                                const int32_t* block_table, const int32_t* meta, uint32_t* scores,
                                const SplitBufs& split, uint32_t* err_word, int grid, cudaStream_t st);
+cudaError_t launch_score_pair(const Params& p, const void* tmap_key, const void* query, const void* key,
+                              const void* weights, const void* q_scale, const void* k_scale,
+                              const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+                              const int32_t* block_table, const int32_t* meta, uint32_t* scores,
+                              const SplitBufs& split, uint32_t* err_word, int grid, cudaStream_t st);
 cudaError_t launch_score_split(const Params& p, const void* tmap_key, const void* query, const void* key,
                                const void* weights, const void* q_scale, const void* k_scale,
                                const int32_t* seq_lens_q, const int32_t* seq_lens_k,

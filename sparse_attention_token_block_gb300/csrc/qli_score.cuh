@@ -61,12 +61,14 @@ constexpr int kCtasPerSm = kGT == 1 ? 2 : 1;      // resident score CTAs per SM
 constexpr int kStages = kSplit ? 2 : (kGT == 1 ? 3 : 5);
 constexpr int kScaleSlots = 10;                  // scale ring depth (released by the epilogue)
 constexpr int kGroups = 1;                       // converter groups; tile i -> i % groups
-// epilogue groups: tile i -> group i % kEpiGroups, which always drains D buffer i % kNumD.  Groups
-// of several tokens give each tile kGT times the epilogue work, so that build has two groups.
+// epilogue groups: tile i -> group i % kEpiGroups, which drains D buffer i % kNumD.  Groups of
+// several tokens give each tile kGT times the epilogue work, so those builds have two groups.
+// Groups of two tokens (N = 128) leave tensor memory for a third D buffer, whose use lets the MMAs
+// of a tile start before the same group has drained its previous one; a buffer's phases then go
+// to the two groups in turn (each phase is drained by one group's four warps).
 constexpr int kEpiGroups = kGT == 1 ? 1 : 2;
 constexpr int kNumA = 2;                         // A buffers in tensor memory
-constexpr int kNumD = 2;                         // D buffers in tensor memory
-static_assert(kNumD % kEpiGroups == 0, "an epilogue group owns its D buffers");
+constexpr int kNumD = kGT == 2 ? 3 : 2;          // D buffers in tensor memory
 constexpr int kGroupThreads = 128;               // 4 warps, one key (TMEM lane) per thread
 constexpr int kConvWarp0 = 0;                    // converter group g: warps 4g .. 4g+3
 constexpr int kEpiWarp0 = 4 * kGroups;           // epilogue group g: warps kEpiWarp0 + 4g ..

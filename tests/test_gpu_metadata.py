@@ -27,9 +27,12 @@ def split_start(T, G, G1, c):
 
 
 def group_tokens(case):
-    """Query tokens per group: one for one query token per sequence, else up to three."""
+    """Query tokens per group: one for one query token per sequence, two for two or four, else up
+    to three."""
     if case.layout_q == "BSND":
-        return 1 if case.s1 <= 1 else min(case.s1, 3)
+        if case.s1 <= 1:
+            return 1
+        return 2 if case.s1 in (2, 4) else min(case.s1, 3)
     return 3
 
 
