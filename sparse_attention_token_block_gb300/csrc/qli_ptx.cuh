@@ -40,6 +40,14 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
     return r;
 }
 
+// x * s clamped to [0, 1], NaN to +0 (mul.sat runs on the FMA pipe, fmax on the half-rate ALU pipe)
+__device__ __forceinline__ float mul_sat(float x, float s)
+{
+    float r;
+    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(s));
+    return r;
+}
+
 __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
 {
     uint64_t r;

@@ -125,6 +125,14 @@ static_assert(kSmemBytes <= (kCtasPerSm == 2 ? 113 : 226) * 1024, "the CTAs of a
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// The epilogue's ReLU as a saturating multiply (FMA pipe) instead of a maximum (half-rate ALU
+// pipe): every head dot has |dot| <= 2^25 (int8: 128 * 128^2 = 2^21; e4m3: 128 * 448^2 < 2^25),
+// so sat(dot * 2^-25) = ReLU(dot) * 2^-25 exactly, and with the folded weight W|sQ| scaled by 2^25
+// (exact) each fma adds the same product W|sQ| ReLU(dot) as before, rounded the same way.  sat
+// also sends a NaN dot (an e4m3 NaN code) to 0, as the maximum did.
+constexpr float kReluUp = 0x1p25f;
+constexpr float kReluDown = 0x1p-25f;
+
 
 struct ScoreArgs {
     Params p;
@@ -446,7 +454,7 @@ __device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, Span s
             for (int i = tid; i < x.q_cnt * kHeads; i += kGroupThreads) {
                 const float w = load_scale(wraw, i, kScaleF32);
                 const float sq = load_scale(sqraw, i, kScaleF32);
-                wq[i] = w * fabsf(sq);
+                wq[i] = w * fabsf(sq) * kReluUp;
                 sgn[i] = sq < 0.0f ? 0x80008000u : 0u;
             }
             ptx::named_bar_sync(1 + grp, kGroupThreads);
@@ -798,19 +806,21 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp
                     const float4* w4 = reinterpret_cast<const float4*>(wq + tt * kHeads);
                     // heads h, h+1 in acc0 and h+2, h+3 in acc1 (packed pairs: four fma chains)
                     uint64_t acc0 = 0, acc1 = 0;
-                    // the weighted ReLU (min for a negative sK) sum of heads [h0, h0 + len)
+                    // the weighted ReLU sum of heads [h0, h0 + len): W|sQ| 2^25 times
+                    // sat(dot 2^-25), i.e. ReLU(dot) for sK >= 0 and ReLU(-dot) = -min(dot, 0)
+                    // for sK < 0 (whose sum then takes |sK|)
                     auto accumulate = [&](const uint32_t* d, int h0, int len) {
                         if (sk >= 0.0f) {
 #pragma unroll
                             for (int h = 0; h < len; h += 4) {
                                 const float4 w = w4[(h0 + h) >> 2];
                                 acc0 = ptx::fma2(ptx::pack2(w.x, w.y),
-                                                 ptx::pack2(fmaxf(__uint_as_float(d[h]), 0.0f),
-                                                            fmaxf(__uint_as_float(d[h + 1]), 0.0f)),
+                                                 ptx::pack2(ptx::mul_sat(__uint_as_float(d[h]), kReluDown),
+                                                            ptx::mul_sat(__uint_as_float(d[h + 1]), kReluDown)),
                                                  acc0);
                                 acc1 = ptx::fma2(ptx::pack2(w.z, w.w),
-                                                 ptx::pack2(fmaxf(__uint_as_float(d[h + 2]), 0.0f),
-                                                            fmaxf(__uint_as_float(d[h + 3]), 0.0f)),
+                                                 ptx::pack2(ptx::mul_sat(__uint_as_float(d[h + 2]), kReluDown),
+                                                            ptx::mul_sat(__uint_as_float(d[h + 3]), kReluDown)),
                                                  acc1);
                             }
                         } else {
@@ -818,12 +828,12 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp
                             for (int h = 0; h < len; h += 4) {
                                 const float4 w = w4[(h0 + h) >> 2];
                                 acc0 = ptx::fma2(ptx::pack2(w.x, w.y),
-                                                 ptx::pack2(fminf(__uint_as_float(d[h]), 0.0f),
-                                                            fminf(__uint_as_float(d[h + 1]), 0.0f)),
+                                                 ptx::pack2(ptx::mul_sat(__uint_as_float(d[h]), -kReluDown),
+                                                            ptx::mul_sat(__uint_as_float(d[h + 1]), -kReluDown)),
                                                  acc0);
                                 acc1 = ptx::fma2(ptx::pack2(w.z, w.w),
-                                                 ptx::pack2(fminf(__uint_as_float(d[h + 2]), 0.0f),
-                                                            fminf(__uint_as_float(d[h + 3]), 0.0f)),
+                                                 ptx::pack2(ptx::mul_sat(__uint_as_float(d[h + 2]), -kReluDown),
+                                                            ptx::mul_sat(__uint_as_float(d[h + 3]), -kReluDown)),
                                                  acc1);
                             }
                         }
@@ -848,7 +858,7 @@ __device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp
                     float a0, a1, a2, a3;
                     ptx::unpack2(acc0, a0, a1);
                     ptx::unpack2(acc1, a2, a3);
-                    score[tt] = sk * ((a0 + a2) + (a1 + a3));
+                    score[tt] = fabsf(sk) * ((a0 + a2) + (a1 + a3));
                 }
             }
             ptx::tc_fence_before();
