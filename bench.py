@@ -539,14 +539,15 @@ def score_roofline(stats, score_us, traffic=None):
             "algorithmic_bytes_per_launch": stats["score_bytes"], "traffic": traffic}
 
 
-def time_workload(Q, case, dev, flush_l2, steps, warmup):
+def time_workload(Q, case, dev, flush_l2, steps, warmup, split_topk=0):
     """One workload's indexer call timed like the headline step (the execution plan replayed, L2
     flushed between calls, events on the launching stream), plus a pass with events between the
-    three kernels for the per-stage times.  Returns the workload's summary for the JSON line."""
+    three kernels for the per-stage times.  Returns the workload's summary for the JSON line.
+    ``split_topk``: the problem's qli_split_topk (the two-stage top-k when ON)."""
     import torch
     stream = torch.cuda.current_stream(dev)
     stats = workload_stats(case)
-    p = Q.make_problem(**W.problem_kwargs(case))
+    p = Q.make_problem(**W.problem_kwargs(case), split_topk=split_topk)
     ix = Q.Indexer(p, device=dev)
     d = W.to_device(case, dev)
     plan = ix.plan(**d)
@@ -584,7 +585,8 @@ def time_workload(Q, case, dev, flush_l2, steps, warmup):
              "score": 1e3 * statistics.mean(e[1].elapsed_time(e[2]) for e in sev),
              "topk": 1e3 * statistics.mean(e[2].elapsed_time(e[3]) for e in sev)}
     peak, _ = peaks()
-    return {"config": config_of(case, None, 1)["workload"], "steps": steps,
+    return {"config": config_of(case, None, 1)["workload"] + (", two-stage top-k" if split_topk else ""),
+            "steps": steps,
             "us_per_call": us, "gops": stats["pairs"] * OPS_PER_PAIR / (us * 1e-6) / 1e9,
             "keys_scored_per_s": stats["pairs"] / (us * 1e-6), "stage_us": stage,
             "call_hbm_frac": stats["total_bytes"] / (us * 1e-6) / 1e9 / peak,
@@ -872,6 +874,11 @@ def main():
                 continue
             others[name] = time_workload(Q, make_workload(name, 0, rank), dev, flush_l2,
                                          max(3, min(args.steps, 30)), args.warmup)
+        if args.workload == "long_decode":
+            # the same call with the top-k in two stages (split-local selection in the score
+            # kernel, then the merge): opt-in, measured beside the default
+            others["long_decode_split_topk"] = time_workload(Q, case, dev, flush_l2, max(3, min(args.steps, 30)),
+                                                             args.warmup, split_topk=Q.SPLIT_ON)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case)
