@@ -249,31 +249,38 @@ __device__ uint64_t radix_select(const Smem& S, int64_t n, int k, Get get, int t
 }
 
 // Gather (unordered) into key/val the keys j < n of `line` (shared or global memory) whose sort
-// key is >= t64; returns how many (only the first kCap are stored).
+// key is >= t64; returns how many (only the first kCap are stored).  Each thread loads its kGatherU
+// keys of a stretch before testing any: over a score line in global memory one load at a time
+// left the loop waiting on each load's latency (a 2^17-key row: ~130 loads in a row per thread).
+constexpr int kGatherU = 8;
 __device__ int gather(const Smem& S, const uint32_t* line, int64_t n, uint64_t t64)
 {
     const int tid = threadIdx.x, lane = tid & 31;
     uint32_t* s_cnt = S.misc + 104;
     if (tid == 0) *s_cnt = 0;
     __syncthreads();
-    for (int64_t j0 = 0; j0 < n; j0 += kThreads) {
-        const int64_t j = j0 + tid;
-        uint32_t c = 0;
-        bool take = false;
-        if (j < n) {
-            c = line[j];
-            take = sort_key(c, (uint32_t)j) >= t64;
+    for (int64_t j0 = 0; j0 < n; j0 += (int64_t)kThreads * kGatherU) {
+        uint32_t c[kGatherU];
+#pragma unroll
+        for (int u = 0; u < kGatherU; ++u) {
+            const int64_t j = j0 + u * kThreads + tid;
+            c[u] = j < n ? line[j] : 0u;
         }
-        const unsigned bal = __ballot_sync(0xffffffffu, take);
-        if (bal) {
-            uint32_t base = 0;
-            if (lane == 0) base = atomicAdd(s_cnt, (uint32_t)__popc(bal));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (take) {
-                const uint32_t pos = base + __popc(bal & ((1u << lane) - 1u));
-                if (pos < (uint32_t)kCap) {
-                    S.key[pos] = c;
-                    S.val[pos] = (uint32_t)j;
+#pragma unroll
+        for (int u = 0; u < kGatherU; ++u) {
+            const int64_t j = j0 + u * kThreads + tid;
+            const bool take = j < n && sort_key(c[u], (uint32_t)j) >= t64;
+            const unsigned bal = __ballot_sync(0xffffffffu, take);
+            if (bal) {
+                uint32_t base = 0;
+                if (lane == 0) base = atomicAdd(s_cnt, (uint32_t)__popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                if (take) {
+                    const uint32_t pos = base + __popc(bal & ((1u << lane) - 1u));
+                    if (pos < (uint32_t)kCap) {
+                        S.key[pos] = c[u];
+                        S.val[pos] = (uint32_t)j;
+                    }
                 }
             }
         }
