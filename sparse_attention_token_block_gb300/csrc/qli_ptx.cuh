@@ -162,6 +162,25 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t
         : "memory");
 }
 
+// As tma_load_3d, with an L2 cache policy (createpolicy) for the loaded lines
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 uint64_t* bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// An L2 policy that marks every line it covers to be evicted first
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t x, int32_t y,
                                             uint64_t* bar)
 {

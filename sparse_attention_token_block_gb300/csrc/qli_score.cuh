@@ -278,6 +278,7 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs
     const int cpt = 1 << lgc;
     const int tpb = 32 >> lgc;                       // tiles per batch
     const int bs = p.block_size;
+    const uint64_t key_policy = ptx::policy_evict_first();   // keys are read once: leave L2 to the rest
     if (p.test_stall == 1) return;   // test switch: nothing arrives, the consumers' waits run out
     // this lane's chunk of tile t0 + lane / cpt of unit y: its first key's page (x) and its row in
     // the scale pool, page * bs + slot (y); y = -1 past the unit's keys (a page outside the pool is
@@ -341,8 +342,8 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs
                 if (c == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nch * R * kDim));
                 __syncwarp();
                 if (c >= 0 && c < nch)      // the key pool is [pages, bs, 128] with a page stride
-                    ptx::tma_load_3d(S.base + kOffKring + s * kKstageBytes + c * R * kDim, tmap, 0,
-                                     rows - pages * bs, pages, bar);
+                    ptx::tma_load_3d_hint(S.base + kOffKring + s * kKstageBytes + c * R * kDim, tmap, 0,
+                                          rows - pages * bs, pages, bar, key_policy);
             }
         }
     }
