@@ -704,10 +704,50 @@ __device__ __noinline__ int gather_sampled(const uint32_t* line, int64_t n, int 
     const float lam = (float)k * (float)kSamples / (float)n;   // samples expected above the k-th
     int rank = (int)(1.15f * lam + 4.0f * sqrtf(lam) + 2.0f);
     rank = rank < 1 ? 1 : (rank > kSamples ? kSamples : rank);
-    const uint32_t* samp = S.cache;
-    const uint64_t t = radix_select(
-        S, kSamples, rank, [&](int64_t i) { return static_cast<uint64_t>(samp[i]) << 32; }, 56);
-    return gather(S, line, n, t & 0xFFFFFFFF00000000ull);
+    // the bound: the lowest code of the histogram bin (kSampleBins over the samples' range) that
+    // holds the rank-th largest sample -- one counting pass instead of a radix select's four
+    constexpr int kPer = kSamples / kThreads;
+    static_assert(kPer * kThreads == kSamples, "whole samples per thread");
+    uint32_t x[kPer], smx = 0, smn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        x[q] = S.cache[tid + q * kThreads];
+        smx = max(smx, x[q]);
+        smn = min(smn, x[q]);
+    }
+    block_max_min(&smx, &smn, S.misc);
+    int s1 = 0;
+    while (s1 < 32 && ((smx - smn) >> s1) >= (uint32_t)kSampleBins) ++s1;
+    uint32_t* sb = S.bins;
+    for (int b = tid; b < kSampleBins; b += kThreads) sb[b] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) atomicAdd(&sb[(smx - x[q]) >> s1], 1u);
+    __syncthreads();
+    constexpr int bpt = kSampleBins / kThreads;     // sample bins per thread
+    uint32_t cnt[bpt], sum = 0;
+#pragma unroll
+    for (int q = 0; q < bpt; ++q) {
+        cnt[q] = sb[bpt * tid + q];
+        sum += cnt[q];
+    }
+    uint32_t total;
+    const uint32_t before = block_excl_scan(sum, &total, S.misc);
+    uint32_t* s_b = S.misc + 110;
+    if (before < (uint32_t)rank && before + sum >= (uint32_t)rank) {
+        uint32_t run = before;
+#pragma unroll
+        for (int q = 0; q < bpt; ++q) {
+            if (run < (uint32_t)rank && run + cnt[q] >= (uint32_t)rank) *s_b = bpt * tid + q;
+            run += cnt[q];
+        }
+    }
+    __syncthreads();
+    const uint32_t b1 = *s_b;
+    __syncthreads();
+    const uint64_t span = ((uint64_t)b1 + 1) << s1;
+    const uint32_t L = span > (uint64_t)(smx - smn) ? smn : (uint32_t)(smx - span + 1);
+    return gather(S, line, n, (uint64_t)L << 32);
 }
 
 // Merging build: the row's tile words -> exclusive offsets (with the source bit) in S.toff[0,
