@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libqli.so")
 # failure-detection test switch of include/qli_testing.h); the product library has no switch
 TEST_LIB = os.path.join(HERE, "libqli_testing.so")
 PEAK_LIB = os.path.join(HERE, "libqli_peak.so")
-SOURCES = ["qli_api.cu", "qli_metadata.cu", "qli_score.cu", "qli_score_multi.cu", "qli_score_pair.cu", "qli_score_split.cu", "qli_topk.cu", "qli_topk_small.cu", "qli_noalloc.cu", "qli_plan.cu", "qli_quant.cu", "qli_gather.cu"]
+SOURCES = ["qli_api.cu", "qli_metadata.cu", "qli_score.cu", "qli_score_multi.cu", "qli_score_pair.cu", "qli_score_split.cu", "qli_topk.cu", "qli_topk_small.cu", "qli_topk_cluster.cu", "qli_noalloc.cu", "qli_plan.cu", "qli_quant.cu", "qli_gather.cu"]
 HEADERS = ["qli_internal.cuh", "qli_ptx.cuh", "qli_score.cuh", "qli_topk.cuh"]
 TEST_SOURCE = "qli_api.cu"
 # the tensor-core rate micro-benchmark (include/qli_peak.h), a library of its own

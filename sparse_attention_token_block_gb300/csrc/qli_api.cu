@@ -371,6 +371,14 @@ qli_status topk_impl(const qli_problem* p, const int32_t* block_table, const int
     // the two-per-SM form for throughput; few rows: the 1024-thread form for latency
     // (the two-per-SM form runs persistent: one CTA per resident slot, each striding over the rows,
     // which saves a CTA's launch and set-up per row and lets a CTA ask for its next row early)
+    // rows longer than one CTA's row cache (and at most four times it), one stage: a cluster of
+    // four CTAs per row, each holding a quarter of the row
+    if (!P.split_topk && P.ld > kTopkCacheRows && P.ld <= (int64_t)kTopkClusterParts * kTopkCacheRows) {
+        cudaError_t e = launch_topk_cluster(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),
+                                            reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values,
+                                            static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+    }
     const bool small = P.ld <= kTopkSmallRows && P.rows > sms;
     auto launch = small ? launch_topk_small : launch_topk;
     cudaError_t e = launch(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),

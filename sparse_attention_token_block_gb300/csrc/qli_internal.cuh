@@ -322,6 +322,13 @@ cudaError_t launch_score_split(const Params& p, const void* tmap_key, const void
 cudaError_t launch_topk(const Params& p, const int32_t* block_table, const int32_t* meta,
                         const uint32_t* scores, const SplitBufs& split, uint32_t* err_word, int32_t* out,
                         float* values, bool after_score, int max_ctas, cudaStream_t st);
+// the one-stage top-k for rows longer than the 1024-thread form's row cache (kTopkCacheRows keys) and
+// at most kTopkClusterParts times it: a cluster of that many CTAs per row
+constexpr int kTopkCacheRows = 32768;
+constexpr int kTopkClusterParts = 4;
+cudaError_t launch_topk_cluster(const Params& p, const int32_t* block_table, const int32_t* meta,
+                                const uint32_t* scores, uint32_t* err_word, int32_t* out, float* values,
+                                cudaStream_t st);
 // the same top-k with half the threads and a row cache of kTopkSmallRows keys (two CTAs per SM)
 constexpr int kTopkSmallRows = 8192;
 cudaError_t launch_topk_small(const Params& p, const int32_t* block_table, const int32_t* meta,

@@ -833,6 +833,7 @@ __device__ bool wait_copy(uint64_t* bar, uint32_t& parity)
     return __syncthreads_and(ok);
 }
 
+#ifndef QLI_TOPK_HELPERS_ONLY
 // One CTA per row (the grid strides over rows).  kMerge: the rows' candidates come from the
 // split-local selection.
 template <bool kMerge>
@@ -1029,8 +1030,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
     }
 }
 
+#endif  // QLI_TOPK_HELPERS_ONLY
+
 }  // namespace
 
+#ifndef QLI_TOPK_HELPERS_ONLY
 cudaError_t QLI_TOPK_LAUNCHER(const Params& p, const int32_t* block_table, const int32_t* meta,
                         const uint32_t* scores, const SplitBufs& split, uint32_t* err_word, int32_t* out,
                         float* values, bool after_score, int max_ctas, cudaStream_t st)
@@ -1046,5 +1050,6 @@ cudaError_t QLI_TOPK_LAUNCHER(const Params& p, const int32_t* block_table, const
     if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
     return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, st, a);
 }
+#endif  // QLI_TOPK_HELPERS_ONLY
 
 }  // namespace qli

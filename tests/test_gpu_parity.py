@@ -332,6 +332,12 @@ LONG_ROWS = [
     ("long_fp8_k777", dict(batch=2, s1=1, qk_dtype=W.FP8, scale_dtype=W.F32,
                            seq_lens_k=[50001, 32769], block_size=256, sparse_count=777,
                            sparse_mode=3)),
+    # rows of every length in one problem: quarters of a cluster left empty, rows of at most 4096
+    # keys (every key a candidate), a single key
+    ("long_mixed", dict(batch=6, s1=1, seq_lens_k=[131072, 40001, 4096, 4097, 257, 1], block_size=64,
+                        sparse_count=2048, sparse_mode=0)),
+    ("long_mixed_k64", dict(batch=4, s1=1, seq_lens_k=[100000, 3, 70000, 33000], block_size=128,
+                            sparse_count=64, sparse_mode=3)),
 ]
 
 
@@ -340,6 +346,29 @@ def test_rows_beyond_row_cache(qli, name, kw):
     case = W.make_case(name, seed=zlib.crc32(name.encode()) % 1000, **kw)
     assert case.max_seqlen_k > 32768
     assert_parity(qli, case)
+
+
+def test_sparse_values_of_long_rows(qli):
+    """return_value = 1 on rows beyond one CTA's row cache: each written index's score, read from
+    the score line, and -inf beside -1."""
+    import torch
+    case = W.make_case("long_vals", batch=3, s1=1, seq_lens_k=[90000, 50000, 1000], block_size=64,
+                       sparse_count=512, sparse_mode=3, seed=64)
+    p = qli.make_problem(**W.problem_kwargs(case), return_value=1)
+    ix = qli.Indexer(p)
+    idx = ix.run(**W.to_device(case)).cpu().numpy()
+    vals = ix.values.cpu().numpy()
+    lines = ix.score_lines().cpu().numpy()
+    torch.cuda.synchronize()
+    assert ix.device_error()[0] == 0
+    ora_idx, ora_scores, err = oracle.score_topk(case, with_scores=True)
+    assert err == 0
+    exact, checked, fails = check(idx, ora_idx, ora_scores, visible_counts(case, oracle), case.sparse_count)
+    assert not fails, fails[:5]
+    for r in range(case.rows):
+        live = idx[r] >= 0
+        assert np.array_equal(vals[r][live], lines[r][idx[r][live]])
+        assert np.isneginf(vals[r][~live]).all()
 
 
 def test_tnd_sequence_beyond_row_cache(qli):
