@@ -65,6 +65,14 @@ def test_fp8_compressed_decode_full_size(qli):
     assert_parity(qli, case)
 
 
+def test_long_context_decode_sampled_rows(qli):
+    """The long-context decode timed beside the workloads (32 rows of 64k-128k keys, the top-k's
+    cluster form) at full size, checked on 8 of its rows (the oracle on all 3 M pairs takes
+    minutes)."""
+    case = W.long_context_decode()
+    assert_parity(qli, case, rows=[0, 3, 7, 12, 18, 23, 27, 31])
+
+
 def test_varlen_prefill_sampled_rows(qli):
     case = W.varlen_prefill()
     rng = np.random.default_rng(0)

@@ -323,3 +323,19 @@ def test_bad_tnd_prefix_sums_blank_every_row():
     case.seq_lens_q = np.array([5, 3], np.int32)     # decreasing
     idx, _, err = oracle.score_topk(case)
     assert err & oracle.ERR_LENGTH and (idx == -1).all()
+
+
+def test_fast_int8_draw_has_the_readme_distribution():
+    """The integer draw used for the long-context pool gives the distribution of the README-style
+    truncated uniform draw: -127..126 at 1/255 each, 0 at 2/255, never -128 or 127."""
+    rng = np.random.default_rng(5)
+    n = 4_000_000
+    fast = np.bincount(W._int8_like_readme_fast(rng, (n,)).astype(np.int16) + 128, minlength=256) / n
+    slow = np.bincount(W._int8_like_readme(np.random.default_rng(6).uniform(-128, 127, n)).astype(np.int16) + 128,
+                       minlength=256) / n
+    expect = np.zeros(256)
+    expect[1:255] = 1 / 255
+    expect[128] = 2 / 255
+    for h in (fast, slow):
+        assert h[0] == 0 and h[255] == 0
+        assert np.max(np.abs(h - expect)) < 6 * np.sqrt(2 / 255 / n)

@@ -88,6 +88,15 @@ def _int8_like_readme(draw: np.ndarray) -> np.ndarray:
     return np.trunc(draw).astype(np.int8)
 
 
+def _int8_like_readme_fast(rng, shape) -> np.ndarray:
+    """The distribution of _int8_like_readme(U(-128, 127)) drawn as integers: -127 .. 126 with
+    probability 1/255 each and 0 with 2/255 (the draws in (-1, 1) truncate to 0), i.e. a uniform
+    draw over -127 .. 127 with 127 sent to 0 -- without a float array of the whole shape."""
+    v = rng.integers(-127, 128, size=shape, dtype=np.int8)
+    v[v == 127] = 0
+    return v
+
+
 def _fp8_codes(x: np.ndarray) -> np.ndarray:
     import torch  # the float8 cast is a library routine; only used here for input drawing
 
@@ -134,8 +143,9 @@ def paged_layout(seq_lens_k, cmp_ratio, block_size, rng, permute=True, extra_pag
 def make_case(name, *, layout_q="BSND", qk_dtype=INT8, scale_dtype=F16, batch=1, s1=1,
               q_lens=None, seq_lens_k=(256,), block_size=128, sparse_count=64, sparse_mode=0,
               cmp_ratio=1, seed=0, permute=True, pass_seq_lens_q=False, extra_pages=0,
-              table_width=None) -> Case:
-    """General seeded case.
+              table_width=None, fast_draw=False) -> Case:
+    """General seeded case.  ``fast_draw``: int8 codes by _int8_like_readme_fast (same distribution,
+    another stream of draws; for pools of hundreds of MB).
 
     BSND: ``batch`` x ``s1`` query rows; ``q_lens`` (optional) gives
     actual_seq_lengths_query per batch.  TND: ``q_lens`` is the per-sequence
@@ -164,7 +174,10 @@ def make_case(name, *, layout_q="BSND", qk_dtype=INT8, scale_dtype=F16, batch=1,
         s1 = 0
     q_shape = rows_shape + (HEAD_DIM,)
     k_shape = (num_blocks, block_size, NUM_HEADS_K, HEAD_DIM)
-    if qk_dtype == INT8:
+    if qk_dtype == INT8 and fast_draw:
+        key = _int8_like_readme_fast(rng, k_shape)
+        query = _int8_like_readme_fast(rng, q_shape)
+    elif qk_dtype == INT8:
         key = _int8_like_readme(rng.uniform(-128, 127, k_shape))
         query = _int8_like_readme(rng.uniform(-128, 127, q_shape))
     else:
@@ -222,6 +235,16 @@ def long_decode(seed: int = 3, batch: int = 32) -> Case:
     return make_case("long_decode", batch=batch, s1=1, seq_lens_k=lens, block_size=64,
                      sparse_count=2048, sparse_mode=3, cmp_ratio=1, seed=seed + 100,
                      permute=True, pass_seq_lens_q=True)
+
+
+def long_context_decode(seed: int = 9, batch: int = 32) -> Case:
+    """B=32, one query token each, S_k ~ U{65536..131072}, 64-key pages, k=2048, causal: rows longer
+    than one top-k CTA's row cache (not one of the five workloads; timed beside them)."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(65536, 131072, size=batch, endpoint=True).astype(np.int32)
+    return make_case("long_context_decode", batch=batch, s1=1, seq_lens_k=lens, block_size=64,
+                     sparse_count=2048, sparse_mode=3, cmp_ratio=1, seed=seed + 100,
+                     permute=True, pass_seq_lens_q=True, fast_draw=True)
 
 
 def fp8_compressed_decode(seed: int = 4, batch: int = 16) -> Case:
