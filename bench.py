@@ -79,6 +79,8 @@ def make_workload(name, batch, rank):
         return fn(seed=3 + 1000 * rank, batch=batch or 32)
     if name == "fp8_compressed_decode":
         return fn(seed=4 + 1000 * rank, batch=batch or 16)
+    if name == "long_context_decode":
+        return fn(seed=9 + 1000 * rank, batch=batch or 32)
     return fn()
 
 
@@ -879,9 +881,7 @@ def main():
             # kernel, then the merge): opt-in, measured beside the default
             others["long_decode_split_topk"] = time_workload(Q, case, dev, flush_l2, max(3, min(args.steps, 30)),
                                                              args.warmup, split_topk=Q.SPLIT_ON)
-            # and a longer context (rows of 64k-128k keys: the top-k's cluster form)
-            others["long_context_decode"] = time_workload(Q, W.long_context_decode(seed=9 + 1000 * rank), dev,
-                                                          flush_l2, max(3, min(args.steps, 30)), args.warmup)
+
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case)

@@ -269,6 +269,7 @@ WORKLOADS = {
     "long_decode": long_decode,
     "fp8_compressed_decode": fp8_compressed_decode,
     "varlen_prefill": varlen_prefill,
+    "long_context_decode": long_context_decode,    # beside the five: rows beyond one CTA's cache
 }
 
 
