@@ -254,13 +254,13 @@ __host__ __device__ inline int32_t problem_hash(const Params& p)
 
 MetaLayout meta_layout(int64_t batch, int64_t max_groups);
 
-// The split of the T tiles over G score CTAs.  When two CTAs share each SM, the one that arrived
-// first (CTAs 0 .. G1 - 1) streams its tiles about 9 % faster than the other (measured: 0.91 against
-// 1.00 us per 128-key tile on the long decode), so their ranges are in proportion 12 : 11 and
-// both finish together; with G1 = G every range weighs the same.  W(c) is the weight of CTAs
-// 0 .. c - 1; CTA c owns tiles [T W(c) / W(G), T W(c + 1) / W(G)).  (T < 2^31 and W(G) < 2^14, so
-// the product fits.)
-constexpr int64_t kSplitFirst = 12, kSplitSecond = 11;
+// The split of the T tiles over G score CTAs: W(c) is the weight of CTAs 0 .. c - 1, and CTA c owns
+// tiles [T W(c) / W(G), T W(c + 1) / W(G)).  The CTAs that arrive first on their SM (0 .. G1 - 1)
+// may weigh kSplitFirst against the others' kSplitSecond; they weigh the same: with a three-stage
+// key ring the first and second CTA of an SM stream equally fast, and any skew (12 : 11, 13 : 11,
+// 11 : 12, 10 : 11 tried) left the long decode's score kernel ~2 us longer than equal ranges.
+// (T < 2^31 and W(G) < 2^14, so the product fits.)
+constexpr int64_t kSplitFirst = 1, kSplitSecond = 1;
 
 __host__ __device__ inline int64_t split_weight(int64_t G1, int64_t c)
 {

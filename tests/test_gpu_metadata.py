@@ -18,11 +18,14 @@ import workloads as W
 pytestmark = pytest.mark.gpu
 
 MAGIC = 0x514C4932
+# weights of the first-arriving score CTAs of an SM and of the others in the split (equal: the
+# library's kSplitFirst and kSplitSecond)
+FIRST, SECOND = 1, 1
 
 
 def split_start(T, G, G1, c):
     def w(x):
-        return x * 12 if x <= G1 else G1 * 12 + (x - G1) * 11
+        return x * FIRST if x <= G1 else G1 * FIRST + (x - G1) * SECOND
     return T * w(c) // w(G)
 
 
