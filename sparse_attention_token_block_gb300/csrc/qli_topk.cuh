@@ -1,11 +1,12 @@
 // qli_topk.cuh -- per-row top-k over the score lines (README function section, step 3: select the
-// top-k indices; parameter table: sparse_count, sparse_indices).  Included by two translation units
+// top-k indices; parameter table: sparse_count, sparse_indices).  Included by the translation units
 // that size the CTA:
-//   qli_topk.cu        1024 threads, rows of up to 32768 keys cached, 8192 ordering bins: one CTA
-//                      per SM (decode rows of up to 32k keys, latency first);
-//   qli_topk_small.cu  512 threads, rows of up to 8192 keys cached, 4096 bins, about 100 KB of
-//                      shared memory: two CTAs per SM (problems whose rows hold at most 8192 keys,
-//                      such as a prefill's many rows: throughput first).
+//   qli_topk.cu         1024 threads, rows of up to 32768 keys cached, 8192 ordering bins: one CTA
+//                       per SM (decode rows of up to 32k keys, latency first);
+//   qli_topk_small.cu   512 threads, rows of up to 8192 keys cached, 2048 bins, about 90 KB of
+//                       shared memory: two CTAs per SM (problems whose rows hold at most 8192 keys,
+//                       such as a prefill's many rows: throughput first);
+//   qli_topk_cluster.cu the helpers only, for its cluster kernel (rows of 32k to 128k keys).
 //
 // One CTA per output row.  Scores are held as order-preserving uint32 codes; a key's
 // full sort key is (code << 32) | (0xFFFFFFFF - index): score descending, then index ascending.
