@@ -59,7 +59,8 @@ constexpr int kBigBucket = 256;
 constexpr int kCacheKeys = QLI_TOPK_CACHE_KEYS;   // score lines up to this length are cached in smem
 static_assert(kCacheKeys >= 2 * kTopkCap, "the row cache doubles as the uncached rows' scatter target");
 static_assert(kCacheKeys >= kSamples, "the row cache holds an uncached row's samples");
-constexpr int kMiscWords = 128;               // scratch: [0, 64) block reductions, [100, 111) single values
+constexpr int kMiscWords = 128;               // scratch: [0, 64) block reductions, [100, 111) single values,
+                                              // [116, 124) the row places handed over
 constexpr int kSmemBytes = (kCacheKeys + kBins + 3 * kCap + 256 + kMiscWords) * 4 + 16;
 // Split-local candidates: gathered into the row cache from word kSplitBase on (the sampled path
 // scatters into the first 2 kCap words), at most kSplitKeys of them; tile offsets for rows of up
@@ -69,6 +70,9 @@ constexpr int kSplitKeys = kSplitBase > 0 ? kCacheKeys - kSplitBase : kCap;
 constexpr int kSplitTiles = kThreads == 1024 ? 2048 : kCacheKeys / kTileKeys;
 constexpr int kSmemSplitBytes = kSmemBytes + (kSplitTiles + 1) * 4;
 static_assert(kSmemSplitBytes <= 227 * 1024, "shared memory");
+// The two-per-SM build's CTAs take many rows each: their places are worked out ahead and each
+// next line is copied as soon as the row cache is free
+constexpr bool kPipe = kCtasPerSm == 2;
 
 struct TopkArgs {
     Params p;
@@ -876,6 +880,36 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
             bad |= pg < 0 || pg >= p.num_blocks;
         }
     };
+    // The two-per-SM build's CTAs take many rows each (a prefill's: ~50).  There the place of each
+    // row is worked out ahead -- thread t finds that of the CTA's (c kThreads + t)-th row when
+    // chunk c of its rows begins, one round of dependent loads instead of one per row -- and handed
+    // over through shared memory when the row comes up; and the next row's line is copied into
+    // the row cache as soon as the selection has left it, while the current row is written.  (A
+    // second line buffer, so that the next line could land during the selection, measured slower:
+    // 16 KB more shared memory per CTA.)
+    RowInfo mine{-1, 0, 0, 0};
+    auto fill = [&](int64_t it0) {
+        const int64_t r = blockIdx.x + (it0 + tid) * (int64_t)gridDim.x;
+        if (r < p.rows) mine = row_info(a, meta_ok, r);
+    };
+    int32_t* hand = reinterpret_cast<int32_t*>(S.misc + 116);   // [0, 4) this row, [4, 8) the next
+    auto publish = [&](int32_t* dst) {
+        dst[0] = (int32_t)mine.b;
+        dst[1] = (int32_t)mine.r;
+        dst[2] = (int32_t)mine.n;
+        dst[3] = (int32_t)mine.lc;
+    };
+    auto start_copy = [&](uint32_t* dst, const uint32_t* src, int64_t keys) {
+        ptx::fence_proxy_async_smem();
+        const uint32_t bytes = (uint32_t)(((keys * 4) + 15) & ~(int64_t)15);
+        ptx::mbar_arrive_expect_tx(S.bar, bytes);
+        ptx::bulk_load(dst, src, bytes, S.bar);
+    };
+    auto prefetch_line = [&](int64_t r) {
+        const int64_t nb = (p.ld < kCacheKeys ? p.ld : kCacheKeys) * 4;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.scores + r * p.ld), "r"((uint32_t)nb)
+                     : "memory");
+    };
     // after the score kernel the first row's place and pages are read before the wait; a
     // standalone launch reads them after it and loads the pages once the row's copy is issued
     const bool early = a.early && blockIdx.x < p.rows;
@@ -883,21 +917,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         read_header();
         locate(blockIdx.x);
         load_pages();
+        if constexpr (kPipe) fill(0);
     }
     // the score lines (and, for a standalone launch, the metadata) come from earlier kernels; the
     // next call may overwrite them only after this grid completes (it waits too)
     ptx::pdl_wait();
     ptx::pdl_launch_dependents();
-    if (!a.early) read_header();
+    if (!a.early) {
+        read_header();
+        if constexpr (kPipe) fill(0);
+    }
 
-    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+    bool copy_started = false;   // this row's line copy was issued during the previous row
+    int64_t it = 0;
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
         int32_t* out = a.out + row * k;
-        const bool loaded = early && row == blockIdx.x;
-        if (!loaded) locate(row);
+        const bool loaded = early && it == 0;
+        const bool ahead = kPipe && !kMerge && (it + 1) % kThreads != 0 && row + gridDim.x < p.rows;
+        if constexpr (kPipe) {
+            const int slot = (int)(it % kThreads);
+            if (slot == 0 && it > 0) fill(it);
+            if (tid == slot) publish(hand);
+            if (ahead && tid == slot + 1) publish(hand + 4);
+        } else if (!loaded) {
+            locate(row);
+        }
+        __syncthreads();                           // the previous row is done with shared memory
+        if (kPipe && !loaded) {
+            ri = RowInfo{hand[0], hand[1], hand[2], hand[3]};
+            pages = ri.n > 0 ? ceil_div64(ri.lc, p.block_size) : 0;
+        }
+        const int64_t nn = ahead ? hand[6] : 0;   // the next row's keys
         const int64_t n = ri.n;
         const uint32_t* line = a.scores + row * p.ld;
         const int need = (int)(n < k ? n : k);
-        __syncthreads();                           // the previous row is done with shared memory
         int M = -1;                                // merging build: the row's candidates
         if constexpr (kMerge) {
             if (n > 0) M = split_offsets(a, row, n, need);
@@ -905,20 +958,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         const bool cached = n > 0 && n <= kCacheKeys && M < 0;
         if (tid == 0) {
             s_bad = 0;
-            if (cached) {
-                ptx::fence_proxy_async_smem();
-                const uint32_t bytes = (uint32_t)(((n * 4) + 15) & ~(int64_t)15);
-                ptx::mbar_arrive_expect_tx(S.bar, bytes);
-                ptx::bulk_load(S.cache, line, bytes, S.bar);
-            }
-            // the CTA's next row (many rows per CTA, e.g. a prefill's) comes from DRAM: ask for its
-            // line's first kCacheKeys codes now, so that its copy finds them in L2
-            if (!kMerge && row + gridDim.x < p.rows) {
-                const int64_t nb = (p.ld < kCacheKeys ? p.ld : kCacheKeys) * 4;
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(line + gridDim.x * p.ld),
-                             "r"((uint32_t)nb)
-                             : "memory");
-            }
+            if (cached && !copy_started) start_copy(S.cache, line, n);
+            // the CTA's next row comes from DRAM: ask for its line's first kCacheKeys codes now,
+            // so that its copy finds them in L2 (asking two rows ahead measured slower)
+            if (!kMerge && row + gridDim.x < p.rows) prefetch_line(row + gridDim.x);
         }
         __syncthreads();
         if (!loaded) load_pages();
@@ -1006,6 +1049,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         bad |= tid < pages && (pg_first < 0 || pg_first >= p.num_blocks);
         if (bad) s_bad = 1;
         __syncthreads();
+        // the row cache is free: the next row's line lands there while this row is written
+        copy_started = copy_ok && nn > 0 && nn <= kCacheKeys;
+        if (tid == 0 && copy_started) start_copy(S.cache, line + gridDim.x * p.ld, nn);
         const bool blank = n <= 0 || !copy_ok || s_bad;
         if (tid == 0 && s_bad) atomicOr(a.err, kErrPage);
         const bool merged = kMerge && M >= 0;

@@ -132,6 +132,28 @@ def test_small_shapes(qli, name, kw):
     assert_parity(qli, case)
 
 
+# ---------------------------------------------------------------------------- many rows per CTA
+# Rows of at most 8192 keys and more rows than SMs: the two-per-SM top-k, each CTA taking every
+# 304th row.  Consecutive rows of a CTA here alternate between long (> 4096 keys), mid, short and
+# empty lines, so the next row's line is copied into either line buffer during a selection and
+# into the row cache after one.
+MANY = [
+    ("many_k2048", dict(layout_q="TND", q_lens=[400, 400, 400, 400], seq_lens_k=[8000, 3000, 200, 6000],
+                        block_size=128, sparse_count=2048, sparse_mode=3)),
+    ("many_k64", dict(layout_q="TND", q_lens=[350, 1, 0, 600, 300], seq_lens_k=[8192, 4096, 50, 4000, 4500],
+                      block_size=64, sparse_count=64, sparse_mode=3)),
+    ("many_bsnd_k300", dict(batch=100, s1=4, seq_lens_k=[(i * 2654435761) % 8192 for i in range(100)],
+                            block_size=64, sparse_count=300, sparse_mode=3)),
+]
+
+
+@pytest.mark.parametrize("name,kw", MANY, ids=[s[0] for s in MANY])
+def test_many_rows_per_cta(qli, name, kw):
+    case = W.make_case(name, seed=zlib.crc32(name.encode()) % 1000, **kw)
+    assert case.rows > 2 * 152
+    assert_parity(qli, case)
+
+
 def test_negative_scales_and_weights(qli):
     case = W.make_case("neg", batch=2, s1=2, seq_lens_k=[700, 300], block_size=64,
                        sparse_count=100, sparse_mode=3, seed=5, scale_dtype=W.F32)
