@@ -46,6 +46,15 @@ namespace {
 #if !defined(QLI_TOPK_THREADS) || !defined(QLI_TOPK_CACHE_KEYS) || !defined(QLI_TOPK_BINS) || !defined(QLI_TOPK_LAUNCHER)
 #error "include through qli_topk.cu or qli_topk_small.cu"
 #endif
+// The phases of the selection: out of line in the one-per-SM build (its decode rows measured
+// faster so), inlined in the two-per-SM build, whose 64 registers a thread otherwise went through
+// local memory at every call (prefill top-k 446 -> 430 us; long decode call 45.6 -> 46.1 us the
+// other way)
+#if QLI_TOPK_THREADS == 512
+#define QLI_TOPK_FN __forceinline__
+#else
+#define QLI_TOPK_FN __noinline__
+#endif
 constexpr int kThreads = QLI_TOPK_THREADS;
 constexpr int kCtasPerSm = kThreads == 1024 ? 1 : 2;
 constexpr int kWarps = kThreads / 32;
@@ -371,7 +380,7 @@ __device__ void bitonic_order(uint32_t* keys, uint32_t* vals, int c, uint64_t* s
 }
 
 // Rarely taken: heavy ties in one bin (or the exact fallback)
-__device__ __noinline__ void bitonic_any(uint32_t* keys, uint32_t* vals, int c, uint64_t* scratch)
+__device__ QLI_TOPK_FN void bitonic_any(uint32_t* keys, uint32_t* vals, int c, uint64_t* scratch)
 {
     constexpr int kMaxE = kCap / kThreads;          // c <= kCap
     static_assert(kMaxE * kThreads == kCap && kMaxE <= 16, "the network covers kCap keys");
@@ -436,7 +445,7 @@ __device__ Binning make_binning(uint32_t L, uint32_t top)
 // kCap are stored or counted).
 constexpr int kVecPerThread = kCacheKeys / (4 * kThreads);
 static_assert(kVecPerThread * 4 <= 32, "one pass bit per key in a 32-bit mask");
-__device__ __noinline__ int compact_and_count(const uint32_t* src, int c, Binning g, bool count)
+__device__ QLI_TOPK_FN int compact_and_count(const uint32_t* src, int c, Binning g, bool count)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
@@ -480,7 +489,7 @@ __device__ __noinline__ int compact_and_count(const uint32_t* src, int c, Binnin
 }
 
 // Bin counts of the m listed candidates lkey[0..m) (shared memory)
-__device__ __noinline__ void count_bins(const uint32_t* lkey, int m, Binning g)
+__device__ QLI_TOPK_FN void count_bins(const uint32_t* lkey, int m, Binning g)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
@@ -499,7 +508,7 @@ enum BinResult { kBinOrdered = 0, kBinTooMany = 1 };
 // first min(need, m) indices of the order go to S.outv.  A bin of more than kBigBucket candidates
 // sends them to the bitonic network instead.  kBinTooMany: fewer than `need` candidates or more
 // than kCap up to the threshold bin (nothing ordered).
-__device__ __noinline__ int order_bins(const uint32_t* lkey, const uint32_t* lval, int m, int need, Binning g,
+__device__ QLI_TOPK_FN int order_bins(const uint32_t* lkey, const uint32_t* lval, int m, int need, Binning g,
                                        uint32_t* tkey, uint32_t* tval)
 {
     const Smem S = smem_view();
@@ -605,7 +614,7 @@ __device__ __noinline__ int order_bins(const uint32_t* lkey, const uint32_t* lva
 // bound L for the candidates' codes from a sample of kSampleKeys evenly spaced keys -- the code of the rank-r largest sample,
 // r = 1.15 l + 4 sqrt(l) + 2 with l = need * kSampleKeys / c the samples expected above the
 // need-th key -- and the largest sample, the top of the bins.
-__device__ __noinline__ Binning sample_bound(const uint32_t* src, int c, int need)
+__device__ QLI_TOPK_FN Binning sample_bound(const uint32_t* src, int c, int need)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
@@ -666,7 +675,7 @@ __device__ __noinline__ Binning sample_bound(const uint32_t* src, int c, int nee
 // key of the row cache; the first `need` places receive their indices in S.outv.  One pass and
 // one barrier instead of the bins' passes, which cost more than this count on short rows.
 constexpr int kRankKeys = 256;   // n^2 comparisons: measured faster than the bins up to ~256 keys
-__device__ __noinline__ void rank_order(const uint32_t* src, int n, int need)
+__device__ QLI_TOPK_FN void rank_order(const uint32_t* src, int n, int need)
 {
     const Smem S = smem_view();
     for (int t = threadIdx.x; t < n; t += kThreads) {
@@ -683,7 +692,7 @@ __device__ __noinline__ void rank_order(const uint32_t* src, int n, int need)
 
 // Exact fallback: the k-th largest sort key of the row (radix select), then exactly k keys at or
 // above it, ordered by the bitonic network; the ordered indices end in S.val.
-__device__ __noinline__ void exact_topk(const uint32_t* line, int64_t n, int k)
+__device__ QLI_TOPK_FN void exact_topk(const uint32_t* line, int64_t n, int k)
 {
     const Smem S = smem_view();
     const uint64_t T = radix_select(S, n, k, [&](int64_t j) { return sort_key(line[j], (uint32_t)j); }, 56);
@@ -697,7 +706,7 @@ __device__ __noinline__ void exact_topk(const uint32_t* line, int64_t n, int k)
 // row does not use: with S = 8192 the count expected at k = 2048 stays near 1.5 k up to 2^17 keys
 // (about 4.4 standard deviations below kCap), where 2048 samples left it near kCap and the exact
 // fallback often ran.
-__device__ __noinline__ int gather_sampled(const uint32_t* line, int64_t n, int k)
+__device__ QLI_TOPK_FN int gather_sampled(const uint32_t* line, int64_t n, int k)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
@@ -759,7 +768,7 @@ __device__ __noinline__ int gather_sampled(const uint32_t* line, int64_t n, int 
 // ntile) and the total in S.toff[ntile]; returns the candidate count, or -1 when the row is to be
 // ordered from its score line instead (too many tiles or candidates, or fewer candidates than the
 // row needs, which only a failed score launch leaves).  Block-wide.
-__device__ __noinline__ int split_offsets(const TopkArgs& a, int64_t row, int64_t n, int need)
+__device__ QLI_TOPK_FN int split_offsets(const TopkArgs& a, int64_t row, int64_t n, int need)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
@@ -789,7 +798,7 @@ __device__ __noinline__ int split_offsets(const TopkArgs& a, int64_t row, int64_
 
 // Merging build: the candidates of the row's tiles, in tile order, into dst[0, total) (a warp per
 // tile, four 32-key loads per lane)
-__device__ __noinline__ void split_gather(const TopkArgs& a, int64_t row, int64_t ntile, uint32_t* dst)
+__device__ QLI_TOPK_FN void split_gather(const TopkArgs& a, int64_t row, int64_t ntile, uint32_t* dst)
 {
     const Smem S = smem_view();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

@@ -142,8 +142,8 @@ MANY = [
                         block_size=128, sparse_count=2048, sparse_mode=3)),
     ("many_k64", dict(layout_q="TND", q_lens=[350, 1, 0, 600, 300], seq_lens_k=[8192, 4096, 50, 4000, 4500],
                       block_size=64, sparse_count=64, sparse_mode=3)),
-    ("many_bsnd_k300", dict(batch=100, s1=4, seq_lens_k=[(i * 2654435761) % 8192 for i in range(100)],
-                            block_size=64, sparse_count=300, sparse_mode=3)),
+    ("many_bsnd_k301", dict(batch=100, s1=4, seq_lens_k=[(i * 2654435761) % 8192 for i in range(100)],
+                            block_size=64, sparse_count=301, sparse_mode=3)),
 ]
 
 
