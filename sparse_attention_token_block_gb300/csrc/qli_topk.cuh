@@ -504,7 +504,8 @@ enum BinResult { kBinOrdered = 0, kBinTooMany = 1 };
 // Steps 3-4 over the m listed candidates lkey / lval (lval null: a candidate's index is its
 // position; bins counted): the scan finds the bin where
 // the running count reaches need; the candidates of that bin and above are scattered into
-// tkey / tval (kCap each) and each takes its bin's start plus its rank among the bin's keys; the
+// tkey / tval (kCap words each, tval = tkey + kCap) and each takes its bin's start plus its rank
+// among the bin's keys; the
 // first min(need, m) indices of the order go to S.outv.  A bin of more than kBigBucket candidates
 // sends them to the bitonic network instead.  kBinTooMany: fewer than `need` candidates or more
 // than kCap up to the threshold bin (nothing ordered).
@@ -571,6 +572,50 @@ __device__ QLI_TOPK_FN int order_bins(const uint32_t* lkey, const uint32_t* lval
     big = __syncthreads_or(big);
     // 3. scatter the candidates up to the threshold bin
     constexpr int kPer = kCap / kThreads;           // m <= kCap: at most kPer per thread
+    if (big || !kPipe) {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = tid + q * kThreads;
+            if (i < m) {
+                const uint32_t x = lkey[i];
+                const uint32_t b = g(x);
+                if (b <= thr) {
+                    const uint32_t pos = atomicSub(&bins[b], 1u) - 1u;
+                    tkey[pos] = x;
+                    tval[pos] = lval ? lval[i] : (uint32_t)i;
+                }
+            }
+        }
+        __syncthreads();
+        if (big) {
+            bitonic_any(tkey, tval, cc, reinterpret_cast<uint64_t*>(S.bins));
+            for (int i = tid; i < need; i += kThreads) S.outv[i] = tval[i];
+            __syncthreads();
+            return kBinOrdered;
+        }
+        // 4. rank inside the bin (bins[b] is now the bin's start)
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = tid + q * kThreads;
+            if (i < cc) {
+                const uint32_t kc = tkey[i], kv = tval[i];
+                const uint64_t kk = sort_key(kc, kv);
+                const uint32_t b = g(kc);
+                const uint32_t s0 = bins[b];
+                const uint32_t e0 = b < thr ? bins[b + 1] : (uint32_t)cc;
+                uint32_t r = 0;
+                for (uint32_t j = s0; j < e0; ++j) r += sort_key(tkey[j], tval[j]) > kk ? 1u : 0u;
+                S.outv[s0 + r] = kv;
+            }
+        }
+        __syncthreads();
+        return kBinOrdered;
+    }
+    // The two-per-SM build scatters each candidate of small bins as its 64-bit sort key into the
+    // 2 kCap words from tkey on (tval follows tkey), so that the ranking reads one word pair per
+    // comparison (prefill top-k 428 -> 409 us; the one-per-SM build keeps two arrays: its long
+    // decode call measured 0.25 us slower with one)
+    uint64_t* tk = reinterpret_cast<uint64_t*>(tkey);
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
         const int i = tid + q * kThreads;
@@ -579,31 +624,24 @@ __device__ QLI_TOPK_FN int order_bins(const uint32_t* lkey, const uint32_t* lval
             const uint32_t b = g(x);
             if (b <= thr) {
                 const uint32_t pos = atomicSub(&bins[b], 1u) - 1u;
-                tkey[pos] = x;
-                tval[pos] = lval ? lval[i] : (uint32_t)i;
+                tk[pos] = sort_key(x, lval ? lval[i] : (uint32_t)i);
             }
         }
     }
     __syncthreads();
-    if (big) {
-        bitonic_any(tkey, tval, cc, reinterpret_cast<uint64_t*>(S.bins));
-        for (int i = tid; i < need; i += kThreads) S.outv[i] = tval[i];
-        __syncthreads();
-        return kBinOrdered;
-    }
-    // 4. rank inside the bin (bins[b] is now the bin's start)
+    // 4. rank inside the bin (bins[b] is now the bin's start); the index is the key's low word
+    // complemented
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
         const int i = tid + q * kThreads;
         if (i < cc) {
-            const uint32_t kc = tkey[i], kv = tval[i];
-            const uint64_t kk = sort_key(kc, kv);
-            const uint32_t b = g(kc);
+            const uint64_t kk = tk[i];
+            const uint32_t b = g((uint32_t)(kk >> 32));
             const uint32_t s0 = bins[b];
             const uint32_t e0 = b < thr ? bins[b + 1] : (uint32_t)cc;
             uint32_t r = 0;
-            for (uint32_t j = s0; j < e0; ++j) r += sort_key(tkey[j], tval[j]) > kk ? 1u : 0u;
-            S.outv[s0 + r] = kv;
+            for (uint32_t j = s0; j < e0; ++j) r += tk[j] > kk ? 1u : 0u;
+            S.outv[s0 + r] = ~(uint32_t)kk;
         }
     }
     __syncthreads();
