@@ -952,10 +952,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         ptx::mbar_arrive_expect_tx(S.bar, bytes);
         ptx::bulk_load(dst, src, bytes, S.bar);
     };
-    auto prefetch_line = [&](int64_t r) {
-        const int64_t nb = (p.ld < kCacheKeys ? p.ld : kCacheKeys) * 4;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.scores + r * p.ld), "r"((uint32_t)nb)
-                     : "memory");
+    // row r's line into L2: its first `keys` codes (at most kCacheKeys)
+    auto prefetch_line = [&](int64_t r, int64_t keys) {
+        const int64_t nb = ((min(keys, (int64_t)kCacheKeys) * 4) + 15) & ~(int64_t)15;
+        if (nb > 0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.scores + r * p.ld), "r"((uint32_t)nb)
+                         : "memory");
     };
     // after the score kernel the first row's place and pages are read before the wait; a
     // standalone launch reads them after it and loads the pages once the row's copy is issued
@@ -1006,9 +1008,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         if (tid == 0) {
             s_bad = 0;
             if (cached && !copy_started) start_copy(S.cache, line, n);
-            // the CTA's next row comes from DRAM: ask for its line's first kCacheKeys codes now,
-            // so that its copy finds them in L2 (asking two rows ahead measured slower)
-            if (!kMerge && row + gridDim.x < p.rows) prefetch_line(row + gridDim.x);
+            // the CTA's next row comes from DRAM: ask for its line now, so that its copy finds it
+            // in L2 (its keys where known, else the line's first kCacheKeys codes; asking two rows
+            // ahead measured slower)
+            if (!kMerge && row + gridDim.x < p.rows) prefetch_line(row + gridDim.x, ahead ? nn : p.ld);
         }
         __syncthreads();
         if (!loaded) load_pages();
