@@ -1,10 +1,11 @@
 /*
- * qli_testing.h -- entry point of the TESTING build of the library (libqli_testing.so) only.
+ * qli_testing.h -- entry points of the TESTING build of the library (libqli_testing.so) only.
  *
- * The product library (libqli.so) does not export this symbol and has no switch of any kind
+ * The product library (libqli.so) does not export these symbols and has no switch of any kind
  * that changes what its kernels do.  The testing build is the same library compiled with
  * QLI_TESTING; the failure-detection tests load it to make the score kernel's bounded waits run
- * out without faulting the GPU.  The README has no counterpart.
+ * out without faulting the GPU, and a top-k test to give its CTAs many rows each.  The README
+ * has no counterpart.
  */
 #ifndef QLI_TESTING_H
 #define QLI_TESTING_H
@@ -24,6 +25,15 @@ extern "C" {
  * memory before it exits, so the CUDA context stays usable.  Other values select 0.
  */
 void qli_testing_set_stall(int mode);
+
+/*
+ * Cap the grid of the persistent two-per-SM top-k (problems whose rows hold at most 8192 keys and
+ * outnumber the SMs) at `ctas` CTAs for the launches after this call (process-wide, host memory),
+ * so that a small problem gives each CTA hundreds of rows: the CTAs work their rows' places out
+ * in chunks of 512 rows, and the tests reach the chunk boundaries this way.  0 or less: no cap.
+ * The results are the same whatever the cap.
+ */
+void qli_testing_set_topk_ctas(int ctas);
 
 #ifdef __cplusplus
 }

@@ -63,6 +63,8 @@ def _load():
     if _lib_path == TESTING_LIB_PATH:
         L.qli_testing_set_stall.argtypes = [ctypes.c_int]
         L.qli_testing_set_stall.restype = None
+        L.qli_testing_set_topk_ctas.argtypes = [ctypes.c_int]
+        L.qli_testing_set_topk_ctas.restype = None
     vp, sz, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
     P = ctypes.POINTER(Problem)
     L.qli_problem_init.argtypes = [P]

@@ -28,6 +28,7 @@ namespace {
 
 #ifdef QLI_TESTING
 std::atomic<int> g_test_stall{0};
+std::atomic<int> g_test_topk_ctas{0};
 #endif
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -381,9 +382,14 @@ qli_status topk_impl(const qli_problem* p, const int32_t* block_table, const int
     }
     const bool small = P.ld <= kTopkSmallRows && P.rows > sms;
     auto launch = small ? launch_topk_small : launch_topk;
+    int max_ctas = small ? 2 * sms : 0;
+#ifdef QLI_TESTING
+    const int test_ctas = g_test_topk_ctas.load();
+    if (small && test_ctas > 0 && test_ctas < max_ctas) max_ctas = test_ctas;
+#endif
     cudaError_t e = launch(P, block_table, metadata, reinterpret_cast<const uint32_t*>(ws + W.scores_off),
                            split_bufs(ws, W), reinterpret_cast<uint32_t*>(ws), sparse_indices, sparse_values,
-                           after_score, small ? 2 * sms : 0, static_cast<cudaStream_t>(stream));
+                           after_score, max_ctas, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
 
@@ -541,6 +547,7 @@ int qli_version(void) { return 100; }
 
 #ifdef QLI_TESTING
 void qli_testing_set_stall(int mode) { g_test_stall.store(mode == 1 || mode == 2 ? mode : 0); }
+void qli_testing_set_topk_ctas(int ctas) { g_test_topk_ctas.store(ctas > 0 ? ctas : 0); }
 #endif
 
 }  // extern "C"
