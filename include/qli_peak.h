@@ -7,7 +7,7 @@
  * score kernel's form: A is the converted key tile) or from shared memory, issued into one
  * accumulator (each MMA depends on the one before) or cycled over several independent ones.  The
  * README has no counterpart; the figures are the denominators the score kernel's tensor
- * utilisation is judged against.
+ * utilisation is measured against.
  */
 #ifndef QLI_PEAK_H
 #define QLI_PEAK_H
