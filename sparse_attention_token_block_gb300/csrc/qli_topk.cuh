@@ -930,10 +930,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
     // The two-per-SM build's CTAs take many rows each (a prefill's: ~50).  There the place of each
     // row is worked out ahead -- thread t finds that of the CTA's (c kThreads + t)-th row when
     // chunk c of its rows begins, one round of dependent loads instead of one per row -- and handed
-    // over through shared memory when the row comes up; and the next row's line is copied into
-    // the row cache as soon as the selection has left it, while the current row is written.  (A
-    // second line buffer, so that the next line could land during the selection, measured slower:
-    // 16 KB more shared memory per CTA.)
+    // over through shared memory when the row comes up.  (Copying the next row's line earlier --
+    // while the current row is written, during its ranking, or into a second line buffer during
+    // its selection -- measured slower: a copy landing in shared memory slows the selection.)
     RowInfo mine{-1, 0, 0, 0};
     auto fill = [&](int64_t it0) {
         const int64_t r = blockIdx.x + (it0 + tid) * (int64_t)gridDim.x;
@@ -977,7 +976,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         if constexpr (kPipe) fill(0);
     }
 
-    bool copy_started = false;   // this row's line copy was issued during the previous row
     int64_t it = 0;
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
         int32_t* out = a.out + row * k;
@@ -1007,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         const bool cached = n > 0 && n <= kCacheKeys && M < 0;
         if (tid == 0) {
             s_bad = 0;
-            if (cached && !copy_started) start_copy(S.cache, line, n);
+            if (cached) start_copy(S.cache, line, n);
             // the CTA's next row comes from DRAM: ask for its line now, so that its copy finds it
             // in L2 (its keys where known, else the line's first kCacheKeys codes; asking two rows
             // ahead measured slower)
@@ -1099,9 +1097,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_kernel(const __grid
         bad |= tid < pages && (pg_first < 0 || pg_first >= p.num_blocks);
         if (bad) s_bad = 1;
         __syncthreads();
-        // the row cache is free: the next row's line lands there while this row is written
-        copy_started = copy_ok && nn > 0 && nn <= kCacheKeys;
-        if (tid == 0 && copy_started) start_copy(S.cache, line + gridDim.x * p.ld, nn);
         const bool blank = n <= 0 || !copy_ok || s_bad;
         if (tid == 0 && s_bad) atomicOr(a.err, kErrPage);
         const bool merged = kMerge && M >= 0;
