@@ -121,6 +121,15 @@ CASES = [
     ("bad_length", lambda: W.make_case("m3", batch=3, s1=2, q_lens=[2, 3, 1],
                                        seq_lens_k=[300, 300, 5000], block_size=64,
                                        sparse_count=16, seed=3)),
+    # 24 batches of two query groups (48 groups: the one-warp path's second half of groups)
+    ("page_decode", lambda: W.page_decode()),
+    # 32 batches x 2 groups = 64 groups, empty batches and rows without keys on both halves
+    ("two_halves", lambda: W.make_case("m5", batch=32, s1=4, q_lens=[(i * 7) % 5 for i in range(32)],
+                                       seq_lens_k=[0 if i % 6 == 2 else 50 * i + 3 for i in range(32)],
+                                       block_size=32, sparse_count=64, sparse_mode=3, seed=5)),
+    # 17 batches x 2 groups = 34 groups: two past the first half
+    ("just_over_half", lambda: W.make_case("m6", batch=17, s1=4, seq_lens_k=[300 + 17 * i for i in range(17)],
+                                           block_size=64, sparse_count=32, sparse_mode=0, seed=6)),
     # 31 batches of at most one row: rows without keys, batches without rows between live ones
     ("small_gaps", lambda: W.make_case("m4", batch=31, s1=1, q_lens=[(i % 3 > 0) * 1 for i in range(31)],
                                        seq_lens_k=[0 if i % 4 == 1 else 40 * i + 7 for i in range(31)],

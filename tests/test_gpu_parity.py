@@ -123,6 +123,11 @@ SMALL = [
                     sparse_mode=3)),
     ("identity_table", dict(batch=3, s1=2, seq_lens_k=[513, 1, 256], block_size=128,
                             sparse_count=300, permute=False)),
+    # 32 batches x 2 query groups = 64 groups (the metadata's one-warp path, both halves), empty
+    # batches and sequences without keys
+    ("groups64", dict(batch=32, s1=4, q_lens=[(i * 7) % 5 for i in range(32)],
+                      seq_lens_k=[0 if i % 6 == 2 else 97 * i + 3 for i in range(32)], block_size=64,
+                      sparse_count=96, sparse_mode=3)),
 ]
 
 
