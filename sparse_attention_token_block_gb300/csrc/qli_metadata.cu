@@ -91,10 +91,11 @@ __device__ int64_t first_at_least(const View& a, int64_t n, int64_t key)
 // and the live-group records worked out by one warp with shuffles (lane i holds batch i, then group
 // i) instead of the block-wide passes below, which cost more in barriers and first-time code than
 // the work itself.  Writes the batch entries and records as those passes do, the live groups' first
-// key-tile positions to v_tb (shared memory), and (live groups, T, groups) to out[0..2].
+// key-tile positions to v_tb (shared memory), and (live groups, T, groups) to out[0..2].  Inlined:
+// out of line, its first call fetched its code from DRAM after an L2 flush (~1 us of a decode call).
 constexpr int kSmallMeta = 32;
 
-__device__ __noinline__ void small_phases(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
+__device__ __forceinline__ void small_phases(const Params& p, const int32_t* seq_lens_q, const int32_t* seq_lens_k,
                                           int32_t* be, int32_t* rec, int32_t* v_tb, int64_t* out, uint32_t* err)
 {
     const uint32_t full = 0xffffffffu;

@@ -31,8 +31,10 @@
 //                    sum_h W[h] * ReLU(sQ[h] * sK * dot_h) -- and writes it as an order-preserving
 //                    uint32 into the row's score line when the key is visible under the mask.
 //
-// Tensor memory: A buffers in columns [0, 128), D buffers after them.  Each role is its own
-// non-inlined function so that its registers are allocated for it alone.  Every wait is bounded
+// Tensor memory: A buffers in columns [0, 128), D buffers after them.  The roles are inlined into
+// the kernel: as separate functions, each warp's first call fetched its role's code from DRAM
+// after the benchmark's L2 flush (long decode score kernel 27.0 -> 24.9 us inlined, prefill
+// 742 -> 717 us; ptxas fits every build in the same registers).  Every wait is bounded
 // (about two seconds of wall time); on expiry the kernel records kErrTimeout, raises a CTA-wide
 // abort flag and drains out instead of hanging.
 #ifndef QLI_SCORE_GT
@@ -194,7 +196,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 
 // Wait, bounded (about 0.2 s) and regardless of the abort flag, for an asynchronous operation this
 // CTA issued (a copy into its shared memory, its MMAs) before the CTA releases what it targets.
-__device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err)
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err)
 {
     const uint64_t t0 = ptx::globaltimer();
     while (!ptx::mbar_try_wait(bar, parity)) {
@@ -352,7 +354,7 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmap, const ScoreArgs
 }
 
 template <bool kScaleF32>
-__device__ __noinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, Span sp)
+__device__ __forceinline__ void producer(const CUtensorMap* tmap, const ScoreArgs& a, Span sp)
 {
     uint32_t tile_i = 0;        // tiles whose copies were issued
     int q_unit = -1;            // last unit whose query copies were issued
@@ -415,7 +417,7 @@ __device__ __forceinline__ void issue_mmas(const ScoreArgs& a, uint32_t tmem_any
     }
 }
 
-__device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, Span sp)
+__device__ __forceinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, Span sp)
 {
     issue_mmas(a, tmem, sp);
     // every MMA this warp issued has completed before tensor memory can be released
@@ -431,7 +433,7 @@ __device__ __noinline__ void mma_issuer(const ScoreArgs& a, uint32_t tmem, Span 
 // Converter warps: query group -> B operand; key tiles -> A operand in tensor memory
 // ------------------------------------------------------------------------------------------------
 template <bool kFp8, bool kScaleF32>
-__device__ __noinline__ void converter(const ScoreArgs& a, uint32_t tmem, Span sp)
+__device__ __forceinline__ void converter(const ScoreArgs& a, uint32_t tmem, Span sp)
 {
     const Shared S = shared_view();
     if (a.p.test_stall == 2) return;   // test switch: no tile is consumed; the copies wait in the ring
@@ -763,7 +765,7 @@ __device__ __noinline__ bool chunk_select(const ScoreArgs& a, int64_t row, int c
 // Epilogue warps
 // ------------------------------------------------------------------------------------------------
 template <bool kScaleF32>
-__device__ __noinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp)
+__device__ __forceinline__ void epilogue(const ScoreArgs& a, uint32_t tmem, Span sp)
 {
     const Shared S = shared_view();
     const int gtid = threadIdx.x - kEpiWarp0 * 32;
