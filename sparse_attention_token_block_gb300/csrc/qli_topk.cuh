@@ -46,10 +46,13 @@ namespace {
 #if !defined(QLI_TOPK_THREADS) || !defined(QLI_TOPK_CACHE_KEYS) || !defined(QLI_TOPK_BINS) || !defined(QLI_TOPK_LAUNCHER)
 #error "include through qli_topk.cu or qli_topk_small.cu"
 #endif
-// The phases of the selection: out of line in the one-per-SM build (its decode rows measured
-// faster so), inlined in the two-per-SM build, whose 64 registers a thread otherwise went through
-// local memory at every call (prefill top-k 446 -> 430 us; long decode call 45.6 -> 46.1 us the
-// other way)
+// The phases every ordered row runs (sampling, compaction, bin counts and order, the short rows'
+// ranking) are inlined in every build: out of line, each first call fetched its code from DRAM
+// after an L2 flush (long decode top-k 18.3 -> 17.0 us inlined, fp8 decode 18.1 -> 16.3 us).  The
+// rarer ones (the exact fallback, the bitonic network, the uncached rows' gather, the merge) stay
+// out of line in the one-per-SM build, whose decode call measured faster so, and are inlined in
+// the two-per-SM build, whose 64 registers a thread otherwise went through local memory at every
+// call (prefill top-k 446 -> 430 us)
 #if QLI_TOPK_THREADS == 512
 #define QLI_TOPK_FN __forceinline__
 #else
@@ -445,7 +448,7 @@ __device__ Binning make_binning(uint32_t L, uint32_t top)
 // kCap are stored or counted).
 constexpr int kVecPerThread = kCacheKeys / (4 * kThreads);
 static_assert(kVecPerThread * 4 <= 32, "one pass bit per key in a 32-bit mask");
-__device__ QLI_TOPK_FN int compact_and_count(const uint32_t* src, int c, Binning g, bool count)
+__device__ __forceinline__ int compact_and_count(const uint32_t* src, int c, Binning g, bool count)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
@@ -489,7 +492,7 @@ __device__ QLI_TOPK_FN int compact_and_count(const uint32_t* src, int c, Binning
 }
 
 // Bin counts of the m listed candidates lkey[0..m) (shared memory)
-__device__ QLI_TOPK_FN void count_bins(const uint32_t* lkey, int m, Binning g)
+__device__ __forceinline__ void count_bins(const uint32_t* lkey, int m, Binning g)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
@@ -509,7 +512,7 @@ enum BinResult { kBinOrdered = 0, kBinTooMany = 1 };
 // first min(need, m) indices of the order go to S.outv.  A bin of more than kBigBucket candidates
 // sends them to the bitonic network instead.  kBinTooMany: fewer than `need` candidates or more
 // than kCap up to the threshold bin (nothing ordered).
-__device__ QLI_TOPK_FN int order_bins(const uint32_t* lkey, const uint32_t* lval, int m, int need, Binning g,
+__device__ __forceinline__ int order_bins(const uint32_t* lkey, const uint32_t* lval, int m, int need, Binning g,
                                        uint32_t* tkey, uint32_t* tval)
 {
     const Smem S = smem_view();
@@ -652,7 +655,7 @@ __device__ QLI_TOPK_FN int order_bins(const uint32_t* lkey, const uint32_t* lval
 // bound L for the candidates' codes from a sample of kSampleKeys evenly spaced keys -- the code of the rank-r largest sample,
 // r = 1.15 l + 4 sqrt(l) + 2 with l = need * kSampleKeys / c the samples expected above the
 // need-th key -- and the largest sample, the top of the bins.
-__device__ QLI_TOPK_FN Binning sample_bound(const uint32_t* src, int c, int need)
+__device__ __forceinline__ Binning sample_bound(const uint32_t* src, int c, int need)
 {
     const Smem S = smem_view();
     const int tid = threadIdx.x;
@@ -713,7 +716,7 @@ __device__ QLI_TOPK_FN Binning sample_bound(const uint32_t* src, int c, int need
 // key of the row cache; the first `need` places receive their indices in S.outv.  One pass and
 // one barrier instead of the bins' passes, which cost more than this count on short rows.
 constexpr int kRankKeys = 256;   // n^2 comparisons: measured faster than the bins up to ~256 keys
-__device__ QLI_TOPK_FN void rank_order(const uint32_t* src, int n, int need)
+__device__ __forceinline__ void rank_order(const uint32_t* src, int n, int need)
 {
     const Smem S = smem_view();
     for (int t = threadIdx.x; t < n; t += kThreads) {
