@@ -59,10 +59,10 @@ constexpr bool kSplit = false;
 #endif
 constexpr int kCtasPerSm = kGT == 1 ? 2 : 1;      // resident score CTAs per SM
 // key ring depth (measured): the one-token kernel runs as fast with two, three or four stages and
-// three leave the call shortest; groups of three tokens run best with four (five to two: 755, 740,
-// 762, 765 us on the prefill), pairs keep five (seven: no change); the split build takes two to make
-// room for its chunk
-constexpr int kStages = kSplit ? 2 : (kGT == 1 ? 3 : (kGT == 3 ? 4 : 5));
+// three leave the call shortest; groups of three tokens run best with five (with the roles
+// inlined: three to five stages 720, 716, 707 us on the prefill), pairs keep five (seven: no
+// change); the split build takes two to make room for its chunk
+constexpr int kStages = kSplit ? 2 : (kGT == 1 ? 3 : 5);
 constexpr int kScaleSlots = 10;                  // scale ring depth (released by the epilogue)
 constexpr int kGroups = 1;                       // converter groups; tile i -> i % groups
 // epilogue groups: tile i -> group i % kEpiGroups, which drains D buffer i % kNumD.  Groups of
